@@ -1,0 +1,205 @@
+/*
+ * Reference oracle for the dense linear-layer GEMM  C[i,j] = sum_k A[i,k] * B[j,k].
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library calls, links or
+ * loads this file; only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg do.  It shares no code, header or table with the CUDA path.
+ *
+ * What it computes (plain definition, no blocking, no reordering):
+ *   - The product of a linear layer flattened to one GEMM: rows i of A are the
+ *     tokens (M = B*L), rows j of B are the weight rows W[d_ff, d_model], and
+ *     K = d_model is the shared inner dimension
+ *     ("GEMM analysis in TraceLens", sections "Linear layers in LLMs" and
+ *      "Flattening for GEMM": Y = X_flat @ W^T).
+ *   - The operand orientation A[M,K] x B[N,K]^T with B stored [N,K]
+ *     ("Gemm Optimization" guide, section 1.1 "Three-Level Tiling").
+ *   - For 8-bit inputs the accumulator is multiplied by a per-row scale of A
+ *     and a per-column scale of B ("Gemm Optimization" guide, section 7.1
+ *     "Direct Store": value = acc * scale_a * scale_b).
+ *
+ * Arithmetic: every input code is decoded exactly into a double, products and
+ * sums are formed in double in ascending k, one (i, j) at a time.  The sum of
+ * absolute products S[i,j] = sum_k |a_ik * b_jk| (times |sa_i * sb_j|) is
+ * returned beside the value for the tolerance test.
+ *
+ * Decoders are written from the format definitions:
+ *   bfloat16: 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits.
+ *   E4M3 (OCP "E4M3FN"): 1 sign bit, 4 exponent bits (bias 7), 3 fraction
+ *   bits, no infinities, S.1111.111 is NaN, largest finite 448.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stddef.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_BF16 0
+#define ORACLE_E4M3 1
+
+double oracle_decode_bf16(uint16_t bits)
+{
+    int sign = (bits >> 15) & 1;
+    int expo = (bits >> 7) & 0xFF;
+    int frac = bits & 0x7F;
+    double v;
+    if (expo == 0xFF) {
+        v = frac ? NAN : INFINITY;
+    } else if (expo == 0) {
+        /* subnormal: 0.fraction * 2^(1-127) */
+        v = ldexp((double)frac / 128.0, 1 - 127);
+    } else {
+        v = ldexp(1.0 + (double)frac / 128.0, expo - 127);
+    }
+    return sign ? -v : v;
+}
+
+double oracle_decode_e4m3(uint8_t code)
+{
+    int sign = (code >> 7) & 1;
+    int expo = (code >> 3) & 0xF;
+    int frac = code & 0x7;
+    double v;
+    if (expo == 0xF && frac == 0x7) {
+        v = NAN;
+    } else if (expo == 0) {
+        /* subnormal: 0.fraction * 2^(1-7) */
+        v = ldexp((double)frac / 8.0, 1 - 7);
+    } else {
+        v = ldexp(1.0 + (double)frac / 8.0, expo - 7);
+    }
+    return sign ? -v : v;
+}
+
+/*
+ * Round a double to the nearest bfloat16, ties to even, and return its bit
+ * pattern.  This is the rounding the output cast is read to use (the pages do
+ * not name one; round-to-nearest-even is the IEEE default).
+ */
+uint16_t oracle_round_bf16(double x)
+{
+    uint16_t sign = (uint16_t)(signbit(x) ? 0x8000 : 0);
+    if (isnan(x)) return (uint16_t)(sign | 0x7FC0);
+    double a = fabs(x);
+    if (isinf(a)) return (uint16_t)(sign | 0x7F80);
+    if (a == 0.0) return sign;
+    int e;
+    frexp(a, &e);                 /* a = f * 2^e, f in [0.5, 1) */
+    int unbiased = e - 1;         /* a = g * 2^unbiased, g in [1, 2) */
+    if (unbiased < -126) unbiased = -126;   /* subnormal range: fixed quantum */
+    /* quantum of the 7-bit fraction at this binade */
+    double q = ldexp(1.0, unbiased - 7);
+    double r = nearbyint(a / q);  /* current rounding mode: nearest, ties to even */
+    double v = r * q;
+    if (v == 0.0) return sign;    /* rounded below half the smallest subnormal */
+    /* rounding may carry into the next binade; re-derive the fields from v */
+    if (v >= ldexp(1.0, 128)) return (uint16_t)(sign | 0x7F80);
+    int ev;
+    frexp(v, &ev);
+    int ub = ev - 1;
+    uint16_t bits;
+    if (ub < -126) {
+        /* subnormal: v = frac * 2^-133 */
+        bits = (uint16_t)(int)nearbyint(v / ldexp(1.0, -133));
+    } else {
+        int frac = (int)nearbyint((v / ldexp(1.0, ub) - 1.0) * 128.0);
+        bits = (uint16_t)(((ub + 127) << 7) | frac);
+    }
+    return (uint16_t)(sign | bits);
+}
+
+/* Element-wise oracle_round_bf16 over an array. */
+void oracle_round_bf16_n(const double* x, int64_t count, uint16_t* out)
+{
+    for (int64_t t = 0; t < count; ++t) out[t] = oracle_round_bf16(x[t]);
+}
+
+static double load_code(int dtype, const void* base, int64_t idx)
+{
+    if (dtype == ORACLE_BF16)
+        return oracle_decode_bf16(((const uint16_t*)base)[idx]);
+    return oracle_decode_e4m3(((const uint8_t*)base)[idx]);
+}
+
+/* One output element, by the definition. */
+static void one_element(int dtype, const void* A, const void* B,
+                        const float* sa, const float* sb, int64_t K,
+                        int64_t i, int64_t j, double* c_out, double* s_out)
+{
+    double acc = 0.0, mag = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        double p = load_code(dtype, A, i * K + k) * load_code(dtype, B, j * K + k);
+        acc += p;
+        mag += fabs(p);
+    }
+    if (sa && sb) {
+        double s = (double)sa[i] * (double)sb[j];
+        acc *= s;
+        mag *= fabs(s);
+    }
+    *c_out = acc;
+    *s_out = mag;
+}
+
+/*
+ * Full product over the valid region.
+ *   A: m rows of K codes (row-major), B: n rows of K codes (row-major).
+ *   sa[m], sb[n]: fp32 scales, or both NULL for the unscaled product.
+ *   C_ref[m*n], S_abs[m*n]: row-major outputs (S_abs may be NULL).
+ * Returns 0, or -1 on a bad argument.
+ */
+int oracle_gemm(int dtype, const void* A, const void* B,
+                const float* sa, const float* sb,
+                int64_t m, int64_t n, int64_t K,
+                double* C_ref, double* S_abs)
+{
+    if ((dtype != ORACLE_BF16 && dtype != ORACLE_E4M3) || !A || !B || !C_ref ||
+        m < 0 || n < 0 || K < 0 || ((sa == NULL) != (sb == NULL)))
+        return -1;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < m; ++i) {
+        for (int64_t j = 0; j < n; ++j) {
+            double c, s;
+            one_element(dtype, A, B, sa, sb, K, i, j, &c, &s);
+            C_ref[i * n + j] = c;
+            if (S_abs) S_abs[i * n + j] = s;
+        }
+    }
+    return 0;
+}
+
+/*
+ * The same definition at a list of (row, col) points, for products too large
+ * to form in full.  rows[p] < m and cols[p] < n are the caller's contract;
+ * out-of-range points return -1 before any work.
+ */
+int oracle_gemm_points(int dtype, const void* A, const void* B,
+                       const float* sa, const float* sb,
+                       int64_t m, int64_t n, int64_t K,
+                       const int64_t* rows, const int64_t* cols, int64_t npts,
+                       double* C_ref, double* S_abs)
+{
+    if ((dtype != ORACLE_BF16 && dtype != ORACLE_E4M3) || !A || !B || !C_ref ||
+        !rows || !cols || npts < 0 || ((sa == NULL) != (sb == NULL)))
+        return -1;
+    for (int64_t p = 0; p < npts; ++p)
+        if (rows[p] < 0 || rows[p] >= m || cols[p] < 0 || cols[p] >= n) return -1;
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t p = 0; p < npts; ++p) {
+        double c, s;
+        one_element(dtype, A, B, sa, sb, K, rows[p], cols[p], &c, &s);
+        C_ref[p] = c;
+        if (S_abs) S_abs[p] = s;
+    }
+    return 0;
+}
+
+/* Threads an OpenMP region of this library uses (1 without OpenMP). */
+int oracle_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,120 @@
+"""The GEMM workloads, as seeded synthetic operands.
+
+Shapes and value distributions follow the linear-layer GEMMs the pages work
+with: the ragged-shape set of the FlyDSL RDNA3 pull request (decode batches of
+1/8/16 tokens, 48 tokens against K=48, 3402-token prefill, the 1024x50257x512
+lm_head, 2048x11007x1024, 4095^2x1024, 528^2x1024), the LLaMA-2-7B MLP up/gate
+projection shapes of "GEMM analysis in TraceLens" (section "Real-world
+example: LLaMA-2 7B": d_model 4096, d_ff 11008, prefill L=597, decode L=1),
+large squares for peak throughput, and an fp8 (E4M3) set with per-row scales
+on A and per-column scales on B.  No trained weights or datasets are involved:
+activations are N(0,1) and weights N(0, 0.02^2) draws.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+from .encode import to_bf16_codes, to_e4m3_codes
+from .rng import STREAM_A, STREAM_B, STREAM_SA, STREAM_SB, integers, normal, uniform
+
+# (m, n, K)
+SMALL_SQUARE = [(256, 256, 256)]
+RAGGED_SWEEP = [(1, 11008, 4096), (8, 4096, 4096), (16, 4096, 4096), (48, 4096, 48),
+                (333, 4096, 1024), (528, 528, 1024), (3402, 4096, 1024), (1024, 50257, 512),
+                (2048, 11007, 1024), (4095, 4095, 1024)]
+LLAMA_SHAPES = [(597, 11008, 4096), (1, 11008, 4096), (4, 11008, 4096), (16, 11008, 4096)]
+SQUARE_SHAPES = [(2048, 2048, 2048), (4096, 4096, 4096), (8192, 8192, 8192)]
+FP8_SHAPES = [(4096, 4096, 4096), (597, 11008, 4096), (16, 11008, 4096)]
+
+
+@dataclass
+class GemmCase:
+    """One GEMM problem: codes of A [m,K] and B [n,K], optional fp32 scales."""
+    dtype: str               # "bf16" or "fp8"
+    m: int
+    n: int
+    K: int
+    out: str                 # "bf16" or "f32"
+    dist: str                # recipe name
+    seed: int
+    A: np.ndarray = field(repr=False)   # uint16 (bf16 bits) or uint8 (E4M3 bits)
+    B: np.ndarray = field(repr=False)
+    sa: np.ndarray | None = field(default=None, repr=False)
+    sb: np.ndarray | None = field(default=None, repr=False)
+
+    @property
+    def name(self) -> str:
+        return f"{self.dtype}_{self.m}x{self.n}x{self.K}_{self.dist}_{self.out}"
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.m * self.n * self.K
+
+
+def make_case(dtype: str, m: int, n: int, K: int, *, out: str = "bf16",
+              dist: str = "normal", seed: int = 0,
+              a_std: float = 1.0, b_std: float = 0.02) -> GemmCase:
+    """Build one case.
+
+    dist:
+      "normal"   A ~ N(0, a_std^2), B ~ N(0, b_std^2)            (bf16)
+      "uniform"  A, B ~ U[-1, 1)                                 (bf16)
+      "int"      A, B integers in [-4, 4]; fp8 scales in {0.5, 1, 2}
+      "fp8"      x ~ N(0,1); sa, sb ~ U[0.5, 2); codes = e4m3(x / scale)
+    """
+    if dtype not in ("bf16", "fp8"):
+        raise ValueError(dtype)
+    sa = sb = None
+    if dist == "normal":
+        a = normal(seed, STREAM_A, (m, K), 0.0, a_std)
+        b = normal(seed, STREAM_B, (n, K), 0.0, b_std)
+    elif dist == "uniform":
+        a = uniform(seed, STREAM_A, (m, K), -1.0, 1.0)
+        b = uniform(seed, STREAM_B, (n, K), -1.0, 1.0)
+    elif dist == "int":
+        a = integers(seed, STREAM_A, (m, K), -4, 4)
+        b = integers(seed, STREAM_B, (n, K), -4, 4)
+        if dtype == "fp8":
+            pick = np.array([0.5, 1.0, 2.0], dtype=np.float32)
+            sa = pick[integers(seed, STREAM_SA, (m,), 0, 2).astype(np.int64)]
+            sb = pick[integers(seed, STREAM_SB, (n,), 0, 2).astype(np.int64)]
+    elif dist == "fp8":
+        if dtype != "fp8":
+            raise ValueError("the fp8 recipe makes E4M3 codes")
+        sa = uniform(seed, STREAM_SA, (m,), 0.5, 2.0).astype(np.float32)
+        sb = uniform(seed, STREAM_SB, (n,), 0.5, 2.0).astype(np.float32)
+        a = normal(seed, STREAM_A, (m, K)) / sa[:, None].astype(np.float64)
+        b = normal(seed, STREAM_B, (n, K)) / sb[:, None].astype(np.float64)
+    else:
+        raise ValueError(dist)
+    if dtype == "bf16":
+        A, B = to_bf16_codes(a), to_bf16_codes(b)
+    else:
+        A, B = to_e4m3_codes(a), to_e4m3_codes(b)
+        if sa is None:
+            sa = np.ones(m, dtype=np.float32)
+            sb = np.ones(n, dtype=np.float32)
+    return GemmCase(dtype, m, n, K, out, dist, seed, A, B, sa, sb)
+
+
+# name -> list of (dtype, m, n, K, out, dist)
+WORKLOADS = {
+    "square256": [("bf16", 256, 256, 256, "f32", "uniform"), ("bf16", 256, 256, 256, "f32", "int")],
+    "ragged": [("bf16", m, n, k, "bf16", "normal") for (m, n, k) in RAGGED_SWEEP],
+    "llama7b_mlp": [("bf16", m, n, k, "bf16", "normal") for (m, n, k) in LLAMA_SHAPES],
+    "square": [("bf16", m, n, k, "bf16", "square_normal") for (m, n, k) in SQUARE_SHAPES],
+    "fp8": [("fp8", m, n, k, "bf16", "fp8") for (m, n, k) in FP8_SHAPES],
+}
+
+
+def workload_shapes(name: str):
+    return list(WORKLOADS[name])
+
+
+def make_workload_case(entry, seed: int = 0) -> GemmCase:
+    dtype, m, n, k, out, dist = entry
+    if dist == "square_normal":
+        return make_case(dtype, m, n, k, out=out, dist="normal", seed=seed, a_std=1.0, b_std=1.0)
+    return make_case(dtype, m, n, k, out=out, dist=dist, seed=seed)

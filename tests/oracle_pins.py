@@ -1,0 +1,194 @@
+"""Checks that pin the oracle to facts other than itself.
+
+Each check takes an oracle library handle, so the same checks run against the
+oracle and against deliberately broken copies of it (tests/test_oracle_mutants.py).
+A check raises AssertionError when the oracle disagrees with:
+  - library decoders (torch bfloat16 / float8_e4m3fn -> float32) over every code,
+  - values fixed by the formats (E4M3 max 448, smallest subnormal 2^-9, NaN code),
+  - torch's float32 -> bfloat16 round-to-nearest-even,
+  - closed forms: identity and permutation products, rank-1 outer products,
+    all-ones, scaled rank-1,
+  - brute force in exact rational arithmetic on tiny shapes.
+"""
+from __future__ import annotations
+
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+import oracle
+from synthetic import integers, to_bf16_codes, to_e4m3_codes
+
+
+def _bf16(x):
+    return to_bf16_codes(np.asarray(x, dtype=np.float64))
+
+
+def check_bf16_decoder(lib):
+    codes = np.arange(1 << 16, dtype=np.uint16)
+    got = oracle.decode_bf16(codes, lib=lib)
+    want = torch.from_numpy(codes.view(np.int16).copy()).view(torch.bfloat16).float().numpy()
+    want = want.astype(np.float64)
+    same = (got == want) | (np.isnan(got) & np.isnan(want))
+    assert same.all(), f"bf16 decoder differs at codes {codes[~same][:8]}"
+
+
+def check_e4m3_decoder(lib):
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.decode_e4m3(codes, lib=lib)
+    want = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    same = (got == want) | (np.isnan(got) & np.isnan(want))
+    assert same.all(), f"e4m3 decoder differs at codes {codes[~same][:8]}"
+    # values the format fixes
+    assert got[0x7E] == 448.0 and got[0xFE] == -448.0
+    assert got[0x01] == 2.0 ** -9
+    assert got[0x08] == 2.0 ** -6
+    assert got[0x38] == 1.0
+    assert np.isnan(got[0x7F]) and np.isnan(got[0xFF])
+    assert np.isfinite(np.delete(got, [0x7F, 0xFF])).all()
+
+
+def check_round_bf16(lib):
+    rng = np.random.default_rng(1234)
+    # random float32 bit patterns over the finite range, plus exact ties
+    bits = rng.integers(0, 0x7F7FFFFF, size=200000, dtype=np.uint32)
+    x = bits.view(np.float32)
+    x = np.concatenate([x, -x])
+    ties = ((rng.integers(0x0080, 0x7F00, size=5000, dtype=np.uint32) << 16) | 0x8000).view(np.float32)
+    x = np.concatenate([x, ties, -ties, np.float32([0.0, -0.0, 1.0, 3.0e38])])
+    got = oracle.round_bf16(x.astype(np.float64), lib=lib)
+    want = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    bad = got != want
+    assert not bad.any(), f"round_bf16 differs for {x[bad][:4]}: {got[bad][:4]} vs {want[bad][:4]}"
+
+
+def check_identity(lib):
+    K, n = 24, 40
+    A = _bf16(np.eye(K))
+    Bv = integers(7, 1, (n, K), -100, 100) / 8.0
+    B = _bf16(Bv)
+    C, S = oracle.gemm(oracle.BF16, A, B, lib=lib)
+    assert C.shape == (K, n)
+    np.testing.assert_array_equal(C, Bv.T)   # every k/8 with |k| <= 100 is exact in bf16
+    np.testing.assert_array_equal(S, np.abs(Bv.T))
+
+
+def check_permutation(lib):
+    K, n, m = 16, 9, 12
+    rng = np.random.default_rng(5)
+    perm = rng.integers(0, K, size=m)
+    P = np.zeros((m, K))
+    P[np.arange(m), perm] = 1.0
+    Bv = integers(3, 1, (n, K), -50, 50) / 4.0
+    C, _ = oracle.gemm(oracle.BF16, _bf16(P), _bf16(Bv), lib=lib)
+    np.testing.assert_array_equal(C, Bv[:, perm].T)
+
+
+def check_rank1(lib):
+    m, n, K = 7, 11, 33
+    u = integers(11, 0, (m,), -3, 3)
+    v = integers(11, 1, (n,), -3, 3)
+    w = integers(11, 2, (K,), -4, 4)
+    w2 = integers(11, 3, (K,), -4, 4)
+    A = _bf16(np.outer(u, w))
+    B = _bf16(np.outer(v, w2))
+    C, _ = oracle.gemm(oracle.BF16, A, B, lib=lib)
+    np.testing.assert_array_equal(C, np.outer(u, v) * float(np.dot(w, w2)))
+
+
+def check_all_ones(lib):
+    for dt, enc in ((oracle.BF16, _bf16), (oracle.E4M3, to_e4m3_codes)):
+        m, n, K = 5, 6, 77
+        C, S = oracle.gemm(dt, enc(np.ones((m, K))), enc(np.ones((n, K))),
+                           *((np.ones(m, np.float32), np.ones(n, np.float32)) if dt == oracle.E4M3 else ()),
+                           lib=lib)
+        assert (C == K).all() and (S == K).all()
+
+
+def check_scaled_rank1_e4m3(lib):
+    m, n, K = 6, 10, 40
+    u = integers(21, 0, (m,), -4, 4)
+    v = integers(21, 1, (n,), -4, 4)
+    w = integers(21, 2, (K,), -4, 4)
+    w2 = integers(21, 3, (K,), -4, 4)
+    sa = np.float32([0.5, 1, 2, 0.25, 4, 1.5])
+    sb = np.linspace(0.5, 2.0, n).astype(np.float32)
+    A = to_e4m3_codes(np.outer(u, w))
+    B = to_e4m3_codes(np.outer(v, w2))
+    C, S = oracle.gemm(oracle.E4M3, A, B, sa, sb, lib=lib)
+    want = np.outer(u * sa.astype(np.float64), v * sb.astype(np.float64)) * float(np.dot(w, w2))
+    np.testing.assert_array_equal(C, want)
+    want_s = np.outer(np.abs(u) * sa, np.abs(v) * sb) * float(np.dot(np.abs(w), np.abs(w2)))
+    np.testing.assert_allclose(S, want_s, rtol=1e-15)
+
+
+def _exact_product(Av, Bv):
+    m, K = Av.shape
+    n = Bv.shape[0]
+    out = np.empty((m, n), dtype=object)
+    for i in range(m):
+        for j in range(n):
+            out[i, j] = sum((Fraction(float(Av[i, k])) * Fraction(float(Bv[j, k])) for k in range(K)),
+                            Fraction(0))
+    return out
+
+
+def check_brute_force(lib):
+    rng = np.random.default_rng(99)
+    for trial in range(12):
+        m, n, K = (int(x) for x in rng.integers(1, 9, size=3))
+        A = _bf16(rng.normal(size=(m, K)))
+        B = _bf16(rng.normal(size=(n, K)) * 3.0)
+        Av = torch.from_numpy(A.view(np.int16)).view(torch.bfloat16).double().numpy()
+        Bv = torch.from_numpy(B.view(np.int16)).view(torch.bfloat16).double().numpy()
+        C, S = oracle.gemm(oracle.BF16, A, B, lib=lib)
+        exact = _exact_product(Av, Bv)
+        # bf16 x bf16 products are exact in double; K <= 8 sums of them stay exact
+        for i in range(m):
+            for j in range(n):
+                assert Fraction(C[i, j]) == exact[i, j], (trial, i, j)
+        np.testing.assert_array_equal(S, (np.abs(Av)[:, None, :] * np.abs(Bv)[None, :, :]).sum(-1))
+    # e4m3 with scales
+    for trial in range(6):
+        m, n, K = (int(x) for x in rng.integers(1, 9, size=3))
+        A = to_e4m3_codes(rng.normal(size=(m, K)) * 4)
+        B = to_e4m3_codes(rng.normal(size=(n, K)))
+        sa = rng.uniform(0.5, 2, size=m).astype(np.float32)
+        sb = rng.uniform(0.5, 2, size=n).astype(np.float32)
+        Av = torch.from_numpy(A).view(torch.float8_e4m3fn).double().numpy()
+        Bv = torch.from_numpy(B).view(torch.float8_e4m3fn).double().numpy()
+        C, _ = oracle.gemm(oracle.E4M3, A, B, sa, sb, lib=lib)
+        exact = _exact_product(Av, Bv)
+        for i in range(m):
+            for j in range(n):
+                want = exact[i, j] * Fraction(float(sa[i])) * Fraction(float(sb[j]))
+                assert abs(Fraction(C[i, j]) - want) <= abs(want) * Fraction(1, 1 << 50), (trial, i, j)
+
+
+def check_points_match_full(lib):
+    m, n, K = 37, 29, 50
+    A = _bf16(integers(4, 0, (m, K), -4, 4))
+    B = _bf16(integers(4, 1, (n, K), -4, 4))
+    C, S = oracle.gemm(oracle.BF16, A, B, lib=lib)
+    rows = np.array([0, m - 1, 5, 36, 17])
+    cols = np.array([0, n - 1, 28, 3, 11])
+    Cp, Sp = oracle.gemm_points(oracle.BF16, A, B, rows, cols, lib=lib)
+    np.testing.assert_array_equal(Cp, C[rows, cols])
+    np.testing.assert_array_equal(Sp, S[rows, cols])
+
+
+ALL_CHECKS = [check_bf16_decoder, check_e4m3_decoder, check_round_bf16, check_identity,
+              check_permutation, check_rank1, check_all_ones, check_scaled_rank1_e4m3,
+              check_brute_force, check_points_match_full]
+
+
+def run_all(lib):
+    """Run every check; return the names of those that failed."""
+    failed = []
+    for chk in ALL_CHECKS:
+        try:
+            chk(lib)
+        except AssertionError:
+            failed.append(chk.__name__)
+    return failed

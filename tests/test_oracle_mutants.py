@@ -1,0 +1,60 @@
+"""Plant plausible mistakes in copies of the oracle (on the CPU) and check the pins catch each.
+
+Each mutant is the oracle's C source with one textual edit, compiled into a
+temporary library.  A mutant that every pin accepts would mean the pins cannot
+tell that mistake from the real oracle.
+"""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from tests import oracle_pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "gemm_oracle.c")
+
+MUTANTS = {
+    # a dropped term: the first k is skipped
+    "drop_first_k": ("for (int64_t k = 0; k < K; ++k)", "for (int64_t k = 1; k < K; ++k)"),
+    # a dropped term: the last k is skipped
+    "drop_last_k": ("for (int64_t k = 0; k < K; ++k)", "for (int64_t k = 0; k + 1 < K; ++k)"),
+    # a wrong sign in the accumulation
+    "wrong_sign": ("acc += p;", "acc -= p;"),
+    # a wrong index on B: k runs backwards along the row
+    "reversed_k_on_B": ("load_code(dtype, B, j * K + k)", "load_code(dtype, B, j * K + (K - 1 - k))"),
+    # a transposed operand read: B taken as [K, N] with the same buffer
+    "b_as_column_major": ("load_code(dtype, B, j * K + k)", "load_code(dtype, B, (k * K + j) % (K * (j + 1)))"),
+    # a dropped scale
+    "drop_sb": ("double s = (double)sa[i] * (double)sb[j];", "double s = (double)sa[i];"),
+    # scales applied by the wrong index
+    "sa_by_col": ("double s = (double)sa[i] * (double)sb[j];", "double s = (double)sa[j % (i + 1)] * (double)sb[j];"),
+    # decoder mistakes
+    "bf16_bias": ("ldexp(1.0 + (double)frac / 128.0, expo - 127)", "ldexp(1.0 + (double)frac / 128.0, expo - 126)"),
+    "e4m3_bias": ("ldexp(1.0 + (double)frac / 8.0, expo - 7)", "ldexp(1.0 + (double)frac / 8.0, expo - 8)"),
+    "e4m3_subnormal": ("v = ldexp((double)frac / 8.0, 1 - 7);", "v = ldexp(1.0 + (double)frac / 8.0, -7);"),
+    "e4m3_no_nan": ("if (expo == 0xF && frac == 0x7) {", "if (0) {"),
+    # rounding mistakes
+    "round_truncates": ("double r = nearbyint(a / q);", "double r = floor(a / q);"),
+    "round_half_up": ("double r = nearbyint(a / q);", "double r = floor(a / q + 0.5);"),
+    # magnitude sum wrong
+    "mag_signed": ("mag += fabs(p);", "mag += p;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_mutant(tmp_path, name):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    mutant_src = tmp_path / f"{name}.c"
+    mutant_src.write_text(src.replace(old, new))
+    lib_path = str(tmp_path / f"lib{name}.so")
+    subprocess.run(["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-std=c11", "-o", lib_path,
+                    str(mutant_src), "-lm"], check=True)
+    failed = oracle_pins.run_all(oracle.load(lib_path))
+    assert failed, f"mutant {name} passes every pin"
+
+
+def test_real_oracle_passes_every_pin():
+    assert oracle_pins.run_all(oracle.load()) == []
