@@ -1,0 +1,222 @@
+"""GB300 (sm_103a) dense linear-layer GEMM: C = A . B^T in bf16 and E4M3.
+
+Python binding of the C ABI in ``include/dgl.h``.  Functions named ``dgl_*``
+marshal plain integers/pointers into the library one to one; the ``gemm_*``
+helpers take torch CUDA tensors, allocate the output with torch when none is
+given, and call the same entry points on torch's current stream.  Every step
+of the computation runs in the library's CUDA kernels; if the library is
+missing, loading raises instead of falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import metrics  # noqa: F401  (pure-Python metric helpers)
+
+_PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG_DIR, "_build", "libdgl.so")
+
+DGL_OK = 0
+DGL_ERR_ARG = -1
+DGL_ERR_ALIGN = -2
+DGL_ERR_SHAPE = -3
+DGL_ERR_UNSUPPORTED = -4
+DGL_ERR_CUDA = -5
+DGL_ERR_TIMEOUT = -6
+
+OUT_BF16 = 0
+OUT_F32 = 1
+DTYPE_BF16 = 0
+DTYPE_E4M3 = 1
+PATH_TC = 0
+PATH_DECODE = 1
+PATH_EMPTY = 2
+
+EXPORTED = ["dgl_gemm_bf16", "dgl_gemm_fp8", "dgl_gemm_planned", "dgl_plan", "dgl_tile_metrics",
+            "dgl_device_status", "dgl_status_string", "dgl_version"]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int32), ("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32),
+                ("tile_k", ctypes.c_int32), ("stages", ctypes.c_int32), ("cta_group", ctypes.c_int32),
+                ("grid", ctypes.c_int32), ("num_tiles", ctypes.c_int32), ("tile_eff", ctypes.c_double),
+                ("wq_eff", ctypes.c_double), ("dim_eff", ctypes.c_double), ("est_us", ctypes.c_double)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+class DglError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+_lib = None
+
+
+def load_library(path: str | None = None):
+    """Load libdgl.so (build it first with ``_build.build()``); raises if absent."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise ImportError(f"{p} is missing: build it with dense_gemm_linear_gb300._build.build()")
+    lib = ctypes.CDLL(p)
+    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+    lib.dgl_gemm_bf16.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i32, vp]
+    lib.dgl_gemm_bf16.restype = i32
+    lib.dgl_gemm_fp8.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i32, vp]
+    lib.dgl_gemm_fp8.restype = i32
+    lib.dgl_gemm_planned.argtypes = [i32, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i32,
+                                     ctypes.POINTER(PlanInfo), vp]
+    lib.dgl_gemm_planned.restype = i32
+    lib.dgl_plan.argtypes = [i32, i64, i64, i64, i32, i32, ctypes.POINTER(PlanInfo)]
+    lib.dgl_plan.restype = i32
+    lib.dgl_tile_metrics.argtypes = [i64, i64, i32, i32, i32, ctypes.POINTER(PlanInfo)]
+    lib.dgl_tile_metrics.restype = i32
+    lib.dgl_device_status.argtypes = [vp]
+    lib.dgl_device_status.restype = i32
+    lib.dgl_status_string.argtypes = [i32]
+    lib.dgl_status_string.restype = ctypes.c_char_p
+    lib.dgl_version.argtypes = []
+    lib.dgl_version.restype = i32
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load_library().dgl_status_string(status).decode()
+    except ImportError:
+        return "library not loaded"
+
+
+def _check(status: int, where: str):
+    if status != DGL_OK:
+        raise DglError(status, where)
+
+
+# ---------------------------------------------------------------- raw C-ABI calls
+def dgl_gemm_bf16(A, B, C, M, N, K, m_valid=0, n_valid=0, out_dtype=OUT_BF16, stream=0) -> int:
+    return load_library().dgl_gemm_bf16(A, B, C, M, N, K, m_valid, n_valid, out_dtype, stream)
+
+
+def dgl_gemm_fp8(A, B, sa, sb, C, M, N, K, m_valid=0, n_valid=0, out_dtype=OUT_BF16, stream=0) -> int:
+    return load_library().dgl_gemm_fp8(A, B, sa, sb, C, M, N, K, m_valid, n_valid, out_dtype, stream)
+
+
+def dgl_gemm_planned(dtype, A, B, sa, sb, C, M, N, K, m_valid, n_valid, out_dtype, plan: PlanInfo,
+                     stream=0) -> int:
+    return load_library().dgl_gemm_planned(dtype, A, B, sa, sb, C, M, N, K, m_valid, n_valid, out_dtype,
+                                           ctypes.byref(plan), stream)
+
+
+def dgl_plan(dtype, m, n, K, out_dtype=OUT_BF16, num_sms=0) -> PlanInfo:
+    info = PlanInfo()
+    _check(load_library().dgl_plan(dtype, m, n, K, out_dtype, num_sms, ctypes.byref(info)), "dgl_plan")
+    return info
+
+
+def dgl_tile_metrics(m, n, tile_m, tile_n, num_units) -> PlanInfo:
+    info = PlanInfo()
+    _check(load_library().dgl_tile_metrics(m, n, tile_m, tile_n, num_units, ctypes.byref(info)),
+           "dgl_tile_metrics")
+    return info
+
+
+def dgl_device_status(stream=0) -> int:
+    return load_library().dgl_device_status(stream)
+
+
+def dgl_version() -> int:
+    return load_library().dgl_version()
+
+
+# ---------------------------------------------------------------- torch helpers
+def _stream_handle(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _check_operand(t, name, dtype):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dim() != 2 or t.stride(1) != 1 or t.stride(0) != t.shape[1]:
+        raise ValueError(f"{name} must be a contiguous 2-D tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _out_tensor(out, m, n, out_dtype, device):
+    import torch
+    tdt = torch.float32 if out_dtype == OUT_F32 else torch.bfloat16
+    if out is None:
+        return torch.empty((m, n), dtype=tdt, device=device), n, m
+    if out.dtype != tdt or out.dim() != 2 or out.stride(1) != 1:
+        raise ValueError("out must be a 2-D row-major tensor of the output dtype")
+    if out.shape[0] < m or out.stride(0) < n:
+        raise ValueError("out is smaller than the valid region")
+    return out, out.stride(0), out.shape[0]
+
+
+def gemm_bf16(A, B, out=None, *, out_dtype=OUT_BF16, stream=None, plan: PlanInfo | None = None):
+    """C = A . B^T for bf16 A [m, K], B [n, K] (CUDA tensors); returns C [m, n] (or `out`)."""
+    import torch
+    _check_operand(A, "A", torch.bfloat16)
+    _check_operand(B, "B", torch.bfloat16)
+    m, K = A.shape
+    n, K2 = B.shape
+    if K != K2:
+        raise ValueError("inner dimensions differ")
+    C, ldc, rows = _out_tensor(out, m, n, out_dtype, A.device)
+    s = _stream_handle(stream)
+    if plan is None:
+        st = dgl_gemm_bf16(A.data_ptr(), B.data_ptr(), C.data_ptr(), rows, ldc, K, m, n, out_dtype, s)
+    else:
+        st = dgl_gemm_planned(DTYPE_BF16, A.data_ptr(), B.data_ptr(), None, None, C.data_ptr(), rows, ldc, K,
+                              m, n, out_dtype, plan, s)
+    _check(st, "dgl_gemm_bf16")
+    return C
+
+
+def gemm_fp8(A, B, sa, sb, out=None, *, out_dtype=OUT_BF16, stream=None, plan: PlanInfo | None = None):
+    """C = (A . B^T) * sa[:, None] * sb[None, :] for E4M3 A [m, K], B [n, K]; fp32 scales."""
+    import torch
+    _check_operand(A, "A", torch.float8_e4m3fn)
+    _check_operand(B, "B", torch.float8_e4m3fn)
+    m, K = A.shape
+    n, K2 = B.shape
+    if K != K2:
+        raise ValueError("inner dimensions differ")
+    for name, s_, length in (("sa", sa, m), ("sb", sb, n)):
+        if s_.dtype != torch.float32 or not s_.is_cuda or s_.numel() != length or not s_.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous fp32 CUDA tensor of length {length}")
+    C, ldc, rows = _out_tensor(out, m, n, out_dtype, A.device)
+    s = _stream_handle(stream)
+    if plan is None:
+        st = dgl_gemm_fp8(A.data_ptr(), B.data_ptr(), sa.data_ptr(), sb.data_ptr(), C.data_ptr(), rows, ldc, K,
+                          m, n, out_dtype, s)
+    else:
+        st = dgl_gemm_planned(DTYPE_E4M3, A.data_ptr(), B.data_ptr(), sa.data_ptr(), sb.data_ptr(),
+                              C.data_ptr(), rows, ldc, K, m, n, out_dtype, plan, s)
+    _check(st, "dgl_gemm_fp8")
+    return C
+
+
+def plan(dtype, m, n, K, out_dtype=OUT_BF16, num_sms=0) -> dict:
+    return dgl_plan(dtype, m, n, K, out_dtype, num_sms).as_dict()
+
+
+def device_status(stream=None) -> int:
+    return dgl_device_status(_stream_handle(stream))
+
+
+def build() -> str:
+    from ._build import build as _b
+    return _b()

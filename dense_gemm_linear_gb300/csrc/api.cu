@@ -1,0 +1,307 @@
+// C ABI: argument validation, per-device state, plan cache, TMA tensor maps
+// and kernel dispatch.  See include/dgl.h for the contract of each call.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <tuple>
+#include <unordered_map>
+
+#include "common.cuh"
+#include "dgl.h"
+#include "launch.h"
+#include "plan.h"
+
+namespace dgl {
+
+// Per-device status word: kernels OR timeout bits into it.
+__device__ int g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool ready = false;
+  int num_sms = 0;
+  int cc_major = 0, cc_minor = 0;
+  int smem_optin = 0;
+  int* status = nullptr;  // device address of g_status_word on this device
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+struct PlanKey {
+  int dev, dtype, out;
+  int64_t m, n, K;
+  bool operator==(const PlanKey& o) const {
+    return dev == o.dev && dtype == o.dtype && out == o.out && m == o.m && n == o.n && K == o.K;
+  }
+};
+struct PlanKeyHash {
+  size_t operator()(const PlanKey& k) const {
+    size_t h = std::hash<int64_t>()(k.m);
+    h = h * 1000003u ^ std::hash<int64_t>()(k.n);
+    h = h * 1000003u ^ std::hash<int64_t>()(k.K);
+    h = h * 1000003u ^ static_cast<size_t>(k.dev * 16 + k.dtype * 4 + k.out);
+    return h;
+  }
+};
+std::unordered_map<PlanKey, dgl_plan_info, PlanKeyHash> g_plans;
+
+dgl_status get_device(int* dev_out, DeviceState** st_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DGL_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return DGL_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    if (cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&st.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&st.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&st.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return DGL_ERR_CUDA;
+    if (st.cc_major != 10 || st.cc_minor != 3) return DGL_ERR_UNSUPPORTED;
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&st.status), g_status_word) != cudaSuccess)
+      return DGL_ERR_CUDA;
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return DGL_ERR_CUDA;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    st.ready = true;
+  }
+  *dev_out = dev;
+  *st_out = &st;
+  return DGL_OK;
+}
+
+// 2-D tensor map over a row-major [rows, inner] matrix with a 128-byte-wide
+// box of box_rows rows and the 128-byte swizzle.  Reads outside
+// [0, inner) x [0, rows) return zeros.
+bool encode_operand_map(CUtensorMap* map, const void* base, bool e4m3, int64_t inner, int64_t rows,
+                        int box_rows) {
+  const CUtensorMapDataType dt = e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int64_t esize = e4m3 ? 1 : 2;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner * esize)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+struct Problem {
+  int dtype, out;
+  const void *A, *B;
+  const float *sa, *sb;
+  void* C;
+  int64_t M, N, K, m, n;
+};
+
+dgl_status validate(Problem& pr) {
+  if (pr.dtype != DGL_DTYPE_BF16 && pr.dtype != DGL_DTYPE_E4M3) return DGL_ERR_ARG;
+  if (pr.out != DGL_OUT_BF16 && pr.out != DGL_OUT_F32) return DGL_ERR_ARG;
+  if (pr.M < 0 || pr.N < 0 || pr.K < 0 || pr.m < 0 || pr.n < 0) return DGL_ERR_ARG;
+  if (pr.m == 0) pr.m = pr.M;
+  if (pr.n == 0) pr.n = pr.N;
+  if (pr.m > pr.M || pr.n > pr.N) return DGL_ERR_ARG;
+  if (pr.M > INT32_MAX || pr.N > INT32_MAX || pr.K > INT32_MAX) return DGL_ERR_SHAPE;
+  if (pr.m == 0 || pr.n == 0) return DGL_OK;  // empty product
+  if (!pr.C) return DGL_ERR_ARG;
+  if (!aligned(pr.C, pr.out == DGL_OUT_F32 ? 4 : 2)) return DGL_ERR_ALIGN;
+  if (pr.K == 0) return DGL_OK;  // empty sum: zero fill, operands unused
+  if (!pr.A || !pr.B) return DGL_ERR_ARG;
+  const int64_t esize = pr.dtype == DGL_DTYPE_E4M3 ? 1 : 2;
+  if ((pr.K * esize) % 16 != 0) return DGL_ERR_ALIGN;
+  if (!aligned(pr.A, 16) || !aligned(pr.B, 16)) return DGL_ERR_ALIGN;
+  if (pr.K * esize > INT32_MAX) return DGL_ERR_SHAPE;
+  if (pr.dtype == DGL_DTYPE_E4M3) {
+    if (!pr.sa || !pr.sb) return DGL_ERR_ARG;
+    if (!aligned(pr.sa, 4) || !aligned(pr.sb, 4)) return DGL_ERR_ALIGN;
+  }
+  return DGL_OK;
+}
+
+dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream) {
+  dgl_status st = validate(pr);
+  if (st != DGL_OK) return st;
+  if (pr.m == 0 || pr.n == 0) return DGL_OK;
+  int dev = 0;
+  DeviceState* ds = nullptr;
+  st = get_device(&dev, &ds);
+  if (st != DGL_OK) return st;
+  if (pr.K == 0) {
+    return launch_zero_fill(pr.out, pr.C, pr.N, static_cast<int>(pr.m), static_cast<int>(pr.n), stream) ==
+                   cudaSuccess
+               ? DGL_OK
+               : DGL_ERR_CUDA;
+  }
+
+  dgl_plan_info plan;
+  if (forced) {
+    if (forced->path == DGL_PATH_DECODE) {
+      if (pr.m > kDecodeMaxM) return DGL_ERR_UNSUPPORTED;
+      fill_decode_plan(pr.dtype, pr.out, pr.m, pr.n, pr.K, ds->num_sms, &plan);
+    } else if (forced->path == DGL_PATH_TC) {
+      if (!tc_supported_tile(forced->tile_m, forced->tile_n)) return DGL_ERR_UNSUPPORTED;
+      fill_tc_plan(pr.dtype, pr.out, pr.m, pr.n, pr.K, forced->tile_m, forced->tile_n, ds->num_sms, &plan);
+    } else {
+      return DGL_ERR_UNSUPPORTED;
+    }
+    if (forced->grid > 0) plan.grid = forced->grid;
+  } else {
+    PlanKey key{dev, pr.dtype, pr.out, pr.m, pr.n, pr.K};
+    std::lock_guard<std::mutex> lock(g_mu);
+    auto it = g_plans.find(key);
+    if (it == g_plans.end()) {
+      choose_plan(pr.dtype, pr.out, pr.m, pr.n, pr.K, ds->num_sms, &plan);
+      g_plans.emplace(key, plan);
+    } else {
+      plan = it->second;
+    }
+  }
+
+  const bool e4m3 = pr.dtype == DGL_DTYPE_E4M3;
+  const int esize = e4m3 ? 1 : 2;
+  if (plan.path == DGL_PATH_DECODE) {
+    DecodeParams p;
+    p.A = static_cast<const uint8_t*>(pr.A);
+    p.B = static_cast<const uint8_t*>(pr.B);
+    p.sa = pr.sa;
+    p.sb = pr.sb;
+    p.C = pr.C;
+    p.ldc = pr.N;
+    p.m = static_cast<int>(pr.m);
+    p.n = static_cast<int>(pr.n);
+    p.row_bytes = static_cast<int>(pr.K * esize);
+    const int grid = plan.grid > 0 ? plan.grid : decode_grid(pr.n, ds->num_sms);
+    return launch_decode(pr.dtype, pr.out, p, grid, stream) == cudaSuccess ? DGL_OK : DGL_ERR_CUDA;
+  }
+
+  CUtensorMap ta, tb;
+  if (!encode_operand_map(&ta, pr.A, e4m3, pr.K, pr.m, plan.tile_m) ||
+      !encode_operand_map(&tb, pr.B, e4m3, pr.K, pr.n, plan.tile_n))
+    return DGL_ERR_CUDA;
+  TcParams p;
+  p.C = pr.C;
+  p.ldc = pr.N;
+  p.m = static_cast<int>(pr.m);
+  p.n = static_cast<int>(pr.n);
+  p.K = static_cast<int>(pr.K);
+  p.sa = pr.sa;
+  p.sb = pr.sb;
+  p.tiles_m = static_cast<int>((pr.m + plan.tile_m - 1) / plan.tile_m);
+  p.tiles_n = static_cast<int>((pr.n + plan.tile_n - 1) / plan.tile_n);
+  p.num_tiles = p.tiles_m * p.tiles_n;
+  p.num_kb = static_cast<int>((pr.K * esize + 127) / 128);
+  p.group_m = 16;
+  p.status = ds->status;
+  const int grid = plan.grid > 0 ? (plan.grid < p.num_tiles ? plan.grid : p.num_tiles) : p.num_tiles;
+  if (tc_smem_bytes(plan.tile_n, e4m3) > ds->smem_optin) return DGL_ERR_UNSUPPORTED;
+  const cudaError_t e = e4m3 ? launch_tc_e4m3(pr.out, plan.tile_n, ta, tb, p, grid, stream)
+                             : launch_tc_bf16(pr.out, plan.tile_n, ta, tb, p, grid, stream);
+  return e == cudaSuccess ? DGL_OK : DGL_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace dgl
+
+using namespace dgl;
+
+extern "C" {
+
+dgl_status dgl_gemm_bf16(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t m_valid,
+                         int64_t n_valid, int32_t out_dtype, void* stream) {
+  Problem pr{DGL_DTYPE_BF16, out_dtype, A, B, nullptr, nullptr, C, M, N, K, m_valid, n_valid};
+  return run(pr, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+dgl_status dgl_gemm_fp8(const void* A, const void* B, const float* sa, const float* sb, void* C, int64_t M,
+                        int64_t N, int64_t K, int64_t m_valid, int64_t n_valid, int32_t out_dtype, void* stream) {
+  Problem pr{DGL_DTYPE_E4M3, out_dtype, A, B, sa, sb, C, M, N, K, m_valid, n_valid};
+  return run(pr, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+dgl_status dgl_gemm_planned(int32_t dtype, const void* A, const void* B, const float* sa, const float* sb, void* C,
+                            int64_t M, int64_t N, int64_t K, int64_t m_valid, int64_t n_valid, int32_t out_dtype,
+                            const dgl_plan_info* plan, void* stream) {
+  if (!plan) return DGL_ERR_ARG;
+  Problem pr{dtype, out_dtype, A, B, dtype == DGL_DTYPE_E4M3 ? sa : nullptr,
+             dtype == DGL_DTYPE_E4M3 ? sb : nullptr, C, M, N, K, m_valid, n_valid};
+  return run(pr, plan, static_cast<cudaStream_t>(stream));
+}
+
+dgl_status dgl_plan(int32_t dtype, int64_t m, int64_t n, int64_t K, int32_t out_dtype, int32_t num_sms,
+                    dgl_plan_info* out) {
+  if (!out) return DGL_ERR_ARG;
+  if (dtype != DGL_DTYPE_BF16 && dtype != DGL_DTYPE_E4M3) return DGL_ERR_ARG;
+  if (out_dtype != DGL_OUT_BF16 && out_dtype != DGL_OUT_F32) return DGL_ERR_ARG;
+  if (m < 0 || n < 0 || K < 0) return DGL_ERR_ARG;
+  if (m > INT32_MAX || n > INT32_MAX || K > INT32_MAX) return DGL_ERR_SHAPE;
+  if (num_sms <= 0) {
+    int dev = 0;
+    DeviceState* ds = nullptr;
+    const dgl_status st = get_device(&dev, &ds);
+    if (st != DGL_OK) return st;
+    num_sms = ds->num_sms;
+  }
+  choose_plan(dtype, out_dtype, m, n, K, num_sms, out);
+  return DGL_OK;
+}
+
+dgl_status dgl_tile_metrics(int64_t m, int64_t n, int32_t tile_m, int32_t tile_n, int32_t num_units,
+                            dgl_plan_info* out) {
+  if (!out || m < 0 || n < 0 || tile_m <= 0 || tile_n <= 0 || num_units <= 0) return DGL_ERR_ARG;
+  *out = dgl_plan_info{};
+  out->tile_m = tile_m;
+  out->tile_n = tile_n;
+  tile_metrics(m, n, tile_m, tile_n, num_units, out);
+  return DGL_OK;
+}
+
+dgl_status dgl_device_status(void* stream) {
+  int dev = 0;
+  DeviceState* ds = nullptr;
+  dgl_status st = get_device(&dev, &ds);
+  if (st != DGL_OK) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DGL_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, ds->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return DGL_ERR_CUDA;
+  if (word != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(ds->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return DGL_ERR_CUDA;
+    return DGL_ERR_TIMEOUT;
+  }
+  return DGL_OK;
+}
+
+const char* dgl_status_string(int32_t status) {
+  switch (status) {
+    case DGL_OK: return "ok";
+    case DGL_ERR_ARG: return "invalid argument";
+    case DGL_ERR_ALIGN: return "misaligned pointer or K not a multiple of 16 bytes";
+    case DGL_ERR_SHAPE: return "extent out of range";
+    case DGL_ERR_UNSUPPORTED: return "unsupported device or plan";
+    case DGL_ERR_CUDA: return "CUDA error";
+    case DGL_ERR_TIMEOUT: return "a kernel wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int32_t dgl_version(void) { return 100; }
+
+}  // extern "C"

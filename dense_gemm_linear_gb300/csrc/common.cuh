@@ -1,0 +1,51 @@
+// Parameters shared by the host launcher and the kernels.
+#pragma once
+
+#include <cstdint>
+
+namespace dgl {
+
+// Bits OR-ed into the device status word when a bounded wait gives up.
+enum : int {
+  STATUS_TIMEOUT_PRODUCER = 1,
+  STATUS_TIMEOUT_MMA = 2,
+  STATUS_TIMEOUT_EPILOGUE = 4,
+  STATUS_TIMEOUT_DRAIN = 8,
+};
+
+// Persistent tcgen05 tile kernel: problem and schedule.
+struct TcParams {
+  void* C;              // output, row pitch ldc elements
+  int64_t ldc;
+  int m, n, K;          // valid rows of A/C, valid rows of B (= columns of C), inner extent
+  const float* sa;      // E4M3 only: per-row scale of A (m entries)
+  const float* sb;      // E4M3 only: per-row scale of B (n entries)
+  int tiles_m, tiles_n, num_tiles, num_kb;
+  int group_m;          // tile raster: group_m row-tiles share each column sweep
+  int* status;          // device status word
+};
+
+// Decode (m <= 16) kernel parameters.
+struct DecodeParams {
+  const uint8_t* A;     // m rows, row pitch row_bytes
+  const uint8_t* B;     // n rows, row pitch row_bytes
+  const float* sa;
+  const float* sb;
+  void* C;
+  int64_t ldc;
+  int m, n;
+  int row_bytes;        // K * element size
+};
+
+__host__ __device__ inline void tile_coords(int tile, int tiles_m, int tiles_n, int group_m, int& mb, int& nb) {
+  const int per_group = group_m * tiles_n;
+  const int g = tile / per_group;
+  const int first_m = g * group_m;
+  const int rest = tiles_m - first_m;
+  const int gsize = rest < group_m ? rest : group_m;
+  const int r = tile - g * per_group;
+  mb = first_m + r % gsize;
+  nb = r / gsize;
+}
+
+}  // namespace dgl

@@ -1,0 +1,46 @@
+// Instantiations of the decode-shape kernel, plus the K = 0 zero fill.
+#include "decode_gemm.cuh"
+#include "launch.h"
+
+namespace dgl {
+
+namespace {
+
+template <bool FP8, bool OUT_F32>
+cudaError_t launch_one(const DecodeParams& p, int grid, cudaStream_t stream) {
+  auto kern = decode_gemm_kernel<FP8, OUT_F32>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DEC_SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, DEC_THREADS, DEC_SMEM_BYTES, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <typename T>
+__global__ void zero_fill_kernel(T* C, int64_t ldc, int m, int n) {
+  const int64_t total = static_cast<int64_t>(m) * n;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t i = idx / n, j = idx - i * n;
+    C[i * ldc + j] = T(0.0f);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decode(int dtype, int out, const DecodeParams& p, int grid, cudaStream_t stream) {
+  const bool f32 = out == 1;
+  if (dtype == 1) return f32 ? launch_one<true, true>(p, grid, stream) : launch_one<true, false>(p, grid, stream);
+  return f32 ? launch_one<false, true>(p, grid, stream) : launch_one<false, false>(p, grid, stream);
+}
+
+cudaError_t launch_zero_fill(int out, void* C, int64_t ldc, int m, int n, cudaStream_t stream) {
+  const int64_t total = static_cast<int64_t>(m) * n;
+  const int grid = static_cast<int>(total / 256 + 1 < 4096 ? total / 256 + 1 : 4096);
+  if (out == 1)
+    zero_fill_kernel<float><<<grid, 256, 0, stream>>>(static_cast<float*>(C), ldc, m, n);
+  else
+    zero_fill_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(static_cast<__nv_bfloat16*>(C), ldc, m, n);
+  return cudaGetLastError();
+}
+
+}  // namespace dgl

@@ -1,0 +1,164 @@
+// Host-side planner: path selection, the tile ladder, the padding screen and
+// a cost model built on tile- and wave-quantisation efficiency.  Pure host
+// code (no CUDA calls), so it runs and is tested without a GPU.
+//
+//  * Tile/wave quantisation: "GEMM analysis in TraceLens", section "GEMM
+//    dimension efficiency" (tile_eff, wq_eff, dim_eff; "Split-K or Stream-K
+//    are not yet modeled" there, and are not here either).
+//  * Padding screen: FlyDSL pull request 1303 (autotuner): reject a tile whose
+//    padded output area exceeds 1.25x the real area, unless nothing passes.
+//  * Ranking: that change's fallback weighs occupancy and last-round fill
+//    against work per byte of operand traffic; here the same quantities enter
+//    an explicit time estimate (waves x per-tile time, per-tile time = max of
+//    tensor-core time and operand-load time).
+//  * Decode: m <= 16 goes to the memory-bound path ("Gemm Optimization"
+//    guide, section 8.3: small M is bandwidth-bound).
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+
+#include "dgl.h"
+#include "plan.h"
+
+namespace dgl {
+
+namespace {
+
+// Machine model (per SM per SM clock), GB300.
+constexpr double kClockGHz = 1.9;               // sustained SM clock under load
+constexpr double kBf16FlopsPerClk = 8192.0;     // dense bf16 tcgen05 rate per SM
+constexpr double kOperandBytesPerClk = 64.0;    // L2 -> SM operand bandwidth per SM
+constexpr double kStoreBytesPerClk = 32.0;      // epilogue store rate per SM
+constexpr double kTileOverheadClk = 400.0;      // per-tile pipeline fill not hidden by the ring
+constexpr double kLaunchUs = 3.0;               // launch + prologue
+constexpr double kHbmGBs = 6500.0;              // achievable HBM bandwidth
+
+struct Rung {
+  int tile_m, tile_n;
+};
+constexpr Rung kLadder[] = {{128, 64}, {128, 128}, {128, 256}};
+
+}  // namespace
+
+void tile_metrics(int64_t m, int64_t n, int tile_m, int tile_n, int units, dgl_plan_info* out) {
+  const int64_t tiles_m = (m + tile_m - 1) / tile_m;
+  const int64_t tiles_n = (n + tile_n - 1) / tile_n;
+  const int64_t tiles = tiles_m * tiles_n;
+  const int64_t rounds = (tiles + units - 1) / units;
+  out->num_tiles = static_cast<int32_t>(std::min<int64_t>(tiles, INT32_MAX));
+  out->tile_eff = static_cast<double>(m) * static_cast<double>(n) /
+                  (static_cast<double>(tiles_m * tile_m) * static_cast<double>(tiles_n * tile_n));
+  out->wq_eff = rounds > 0 ? static_cast<double>(tiles) / static_cast<double>(rounds * units) : 0.0;
+  out->dim_eff = out->tile_eff * out->wq_eff;
+}
+
+double operand_bytes(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K) {
+  const double e = dtype == DGL_DTYPE_E4M3 ? 1.0 : 2.0;
+  const double o = out_dtype == DGL_OUT_F32 ? 4.0 : 2.0;
+  double bytes = (static_cast<double>(m) * K + static_cast<double>(n) * K) * e + static_cast<double>(m) * n * o;
+  if (dtype == DGL_DTYPE_E4M3) bytes += 4.0 * static_cast<double>(m + n);
+  return bytes;
+}
+
+static double tc_estimate_us(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int tile_m, int tile_n,
+                             int num_sms, int* grid_out) {
+  const double esize = dtype == DGL_DTYPE_E4M3 ? 1.0 : 2.0;
+  const double osize = out_dtype == DGL_OUT_F32 ? 4.0 : 2.0;
+  const int64_t tiles = ((m + tile_m - 1) / tile_m) * ((n + tile_n - 1) / tile_n);
+  const int64_t grid = std::min<int64_t>(tiles, num_sms);
+  const int64_t waves = (tiles + grid - 1) / grid;
+  const double num_kb = std::ceil(static_cast<double>(K) * esize / 128.0);
+  const double flops_per_clk = kBf16FlopsPerClk * (dtype == DGL_DTYPE_E4M3 ? 2.0 : 1.0);
+  const double k_per_stage = 128.0 / esize;
+  const double mma_clk = 2.0 * tile_m * tile_n * k_per_stage / flops_per_clk;
+  const double load_clk = (tile_m + tile_n) * 128.0 / kOperandBytesPerClk;
+  const double main_clk = num_kb * std::max(mma_clk, load_clk) + kTileOverheadClk;
+  const double epi_clk = tile_m * tile_n * osize / kStoreBytesPerClk;
+  const double tile_clk = std::max(main_clk, epi_clk);
+  const double us = (static_cast<double>(waves) * tile_clk + epi_clk) / (kClockGHz * 1e3);
+  const double hbm_us = operand_bytes(dtype, out_dtype, m, n, K) / (kHbmGBs * 1e3);
+  if (grid_out) *grid_out = static_cast<int>(grid);
+  return std::max(us, hbm_us) + kLaunchUs;
+}
+
+int tc_tile_k(int dtype) { return dtype == DGL_DTYPE_E4M3 ? 128 : 64; }
+
+int tc_stages(int tile_n) { return tile_n == 64 ? 8 : (tile_n == 128 ? 6 : 4); }
+
+bool tc_supported_tile(int tile_m, int tile_n) {
+  for (const Rung& r : kLadder)
+    if (r.tile_m == tile_m && r.tile_n == tile_n) return true;
+  return false;
+}
+
+void fill_tc_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int tile_m, int tile_n, int num_sms,
+                  dgl_plan_info* out) {
+  *out = dgl_plan_info{};
+  out->path = DGL_PATH_TC;
+  out->tile_m = tile_m;
+  out->tile_n = tile_n;
+  out->tile_k = tc_tile_k(dtype);
+  out->stages = tc_stages(tile_n);
+  out->cta_group = 1;
+  tile_metrics(m, n, tile_m, tile_n, num_sms, out);
+  int grid = 0;
+  out->est_us = tc_estimate_us(dtype, out_dtype, m, n, K, tile_m, tile_n, num_sms, &grid);
+  out->grid = grid;
+}
+
+int decode_grid(int64_t n, int num_sms) {
+  const int64_t groups = (n + 7) / 8;
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(groups, num_sms)));
+}
+
+void fill_decode_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int num_sms, dgl_plan_info* out) {
+  *out = dgl_plan_info{};
+  out->path = DGL_PATH_DECODE;
+  out->tile_m = 16;
+  out->tile_n = 8;
+  out->tile_k = dtype == DGL_DTYPE_E4M3 ? 64 : 32;
+  out->stages = 1;
+  out->cta_group = 1;
+  out->grid = decode_grid(n, num_sms);
+  out->num_tiles = static_cast<int32_t>(std::min<int64_t>((n + 7) / 8, INT32_MAX));
+  out->tile_eff = static_cast<double>(m) / 16.0;
+  out->wq_eff = 1.0;
+  out->dim_eff = out->tile_eff;
+  out->est_us = operand_bytes(dtype, out_dtype, m, n, K) / (kHbmGBs * 1e3) + kLaunchUs;
+}
+
+void choose_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int num_sms, dgl_plan_info* out) {
+  if (m <= 0 || n <= 0) {
+    *out = dgl_plan_info{};
+    out->path = DGL_PATH_EMPTY;
+    return;
+  }
+  if (m <= kDecodeMaxM) {
+    fill_decode_plan(dtype, out_dtype, m, n, K, num_sms, out);
+    return;
+  }
+  const double area = static_cast<double>(m) * static_cast<double>(n);
+  bool any_pass = false;
+  for (const Rung& r : kLadder) {
+    const double padded = std::ceil(static_cast<double>(m) / r.tile_m) * r.tile_m *
+                          std::ceil(static_cast<double>(n) / r.tile_n) * r.tile_n;
+    if (padded <= 1.25 * area) any_pass = true;
+  }
+  bool have = false;
+  dgl_plan_info best{};
+  for (const Rung& r : kLadder) {
+    const double padded = std::ceil(static_cast<double>(m) / r.tile_m) * r.tile_m *
+                          std::ceil(static_cast<double>(n) / r.tile_n) * r.tile_n;
+    if (any_pass && padded > 1.25 * area) continue;
+    dgl_plan_info cand;
+    fill_tc_plan(dtype, out_dtype, m, n, K, r.tile_m, r.tile_n, num_sms, &cand);
+    // ties go to the larger tile (later rungs are larger)
+    if (!have || cand.est_us <= best.est_us * (1.0 + 1e-9)) {
+      best = cand;
+      have = true;
+    }
+  }
+  *out = best;
+}
+
+}  // namespace dgl

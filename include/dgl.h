@@ -1,0 +1,162 @@
+/*
+ * dgl.h -- C ABI of the GB300 (sm_103a) dense linear-layer GEMM library.
+ *
+ * The operation.  Every compute entry point evaluates, for the valid region
+ * 0 <= i < m_valid, 0 <= j < n_valid,
+ *
+ *     C[i, j] = sum_{k < K} A[i, k] * B[j, k]                   (bf16 inputs)
+ *     C[i, j] = (sa[i] * sb[j]) applied to that sum              (E4M3 inputs)
+ *
+ * with fp32 accumulation.  This is a linear layer Y = X W^T flattened to one
+ * GEMM: A = X_flat [M = B*L tokens, K = d_model], B = W [N = d_ff, K]
+ * ("GEMM analysis in TraceLens", sections "Linear layers in LLMs",
+ * "Flattening for GEMM" and "Linear layer: Y = X @ W^T", which is the BLAS
+ * (T, N) call on row-major data).  The operand orientation C[M,N] = A[M,K] x
+ * B[N,K]^T, and the epilogue value = acc * scale_a * scale_b, follow the
+ * "Gemm Optimization" guide (sections 1.1 "Three-Level Tiling" and 7.1
+ * "Direct Store").  m_valid / n_valid are the real extents behind a tiled
+ * problem, as in FlyDSL pull request 1303 (RDNA3 WMMA GEMM: "m_valid/n_valid
+ * parameters: build over whole tiles and tell the kernel how much of the last
+ * one is real"); passing 0 selects the full extent, the old behaviour.
+ *
+ * Layout (all row-major, last dimension contiguous -- flattening is free only
+ * when it is, "GEMM analysis in TraceLens", section "Edge cases"):
+ *   A  at least m_valid rows of K elements, row pitch K elements.
+ *   B  at least n_valid rows of K elements, row pitch K elements.
+ *   C  M rows, row pitch N elements (so N is C's leading dimension).  Only
+ *      the valid region [0, m_valid) x [0, n_valid) is written; every other
+ *      element of C is left untouched.
+ *   sa m_valid fp32 scales (row i of A), sb n_valid fp32 scales (row j of B).
+ * Element types: bf16 (A, B), OCP E4M3 "e4m3fn" (A, B of dgl_gemm_fp8),
+ * fp32 scales; C is bf16 (rounded to nearest even) or fp32 by `out_dtype`.
+ *
+ * Memory and ownership: A, B, C, sa, sb are DEVICE pointers owned by the
+ * caller, on the current CUDA device.  The library allocates no device memory
+ * on these paths, never copies to or from the host, and keeps only a small
+ * per-device plan cache.  Calls are asynchronous with respect to the host:
+ * work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ * stream) and buffers must stay valid until it completes.
+ *
+ * Errors: arguments are validated on the host before any launch; a failed
+ * check returns an error code and enqueues nothing.  Nothing is printed and
+ * nothing is thrown.  Kernel waits are bounded: a wait that times out sets a
+ * per-device status word that dgl_device_status() reports.  There is no CPU
+ * fallback; a device that is not sm_103 returns DGL_ERR_UNSUPPORTED.
+ */
+#ifndef DGL_H_
+#define DGL_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DGL_OK = 0,
+  DGL_ERR_ARG = -1,         /* null pointer, bad enum, negative extent, m_valid > M, n_valid > N */
+  DGL_ERR_ALIGN = -2,       /* A/B/scales not 16/4-byte aligned, K not a multiple of 16 bytes */
+  DGL_ERR_SHAPE = -3,       /* an extent beyond 2^31 - 1 */
+  DGL_ERR_UNSUPPORTED = -4, /* device is not sm_103, or a forced plan the library cannot run */
+  DGL_ERR_CUDA = -5,        /* a CUDA runtime/driver call failed */
+  DGL_ERR_TIMEOUT = -6      /* a kernel's bounded wait gave up (see dgl_device_status) */
+} dgl_status;
+
+typedef enum { DGL_OUT_BF16 = 0, DGL_OUT_F32 = 1 } dgl_out_t;
+typedef enum { DGL_DTYPE_BF16 = 0, DGL_DTYPE_E4M3 = 1 } dgl_dtype_t;
+typedef enum { DGL_PATH_TC = 0, DGL_PATH_DECODE = 1, DGL_PATH_EMPTY = 2 } dgl_path_t;
+
+/*
+ * A launch plan: the path, the tile of the tile ladder, and the cost-model
+ * quantities behind the choice.  tile_eff, wq_eff and dim_eff are the tile-
+ * and wave-quantisation efficiencies of "GEMM analysis in TraceLens"
+ * (section "GEMM dimension efficiency": tile_eff = M N / (M_pad N_pad),
+ * wq_eff = tiles / (ceil(tiles / units) units), dim_eff = their product).
+ */
+typedef struct {
+  int32_t path;       /* dgl_path_t */
+  int32_t tile_m;     /* rows of C per tile (tcgen05 path: 128) */
+  int32_t tile_n;     /* columns of C per tile (tcgen05 path: 64, 128 or 256) */
+  int32_t tile_k;     /* K elements per pipeline stage (64 bf16, 128 E4M3) */
+  int32_t stages;     /* shared-memory ring depth */
+  int32_t cta_group;  /* CTAs sharing one MMA (1) */
+  int32_t grid;       /* CTAs launched (persistent: at most one per SM) */
+  int32_t num_tiles;  /* output tiles (tcgen05 path) or 8-row groups (decode path) */
+  double tile_eff;
+  double wq_eff;
+  double dim_eff;
+  double est_us;      /* cost-model estimate of the kernel time, microseconds */
+} dgl_plan_info;
+
+/*
+ * bf16 GEMM.  A [m_valid, K] bf16, B [n_valid, K] bf16, C [M, ldc = N].
+ * M, N: C's rows and row pitch (elements); m_valid <= M, n_valid <= N, 0 = full.
+ * K: inner extent; K * 2 bytes must be a multiple of 16 (K % 8 == 0).
+ * A, B 16-byte aligned; C aligned to its element size.
+ * out_dtype: DGL_OUT_BF16 or DGL_OUT_F32.  stream: cudaStream_t.
+ * M == 0 or N == 0 is an empty product (DGL_OK, nothing enqueued); K == 0
+ * writes zeros to the valid region (the empty sum).
+ */
+dgl_status dgl_gemm_bf16(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                         int64_t m_valid, int64_t n_valid, int32_t out_dtype, void* stream);
+
+/*
+ * E4M3 GEMM with per-row scales sa on A and per-column scales sb on B
+ * (fp32, 4-byte aligned, m_valid and n_valid entries):
+ *   C[i, j] = (acc * sa[i]) * sb[j], acc = fp32 sum of A[i, k] * B[j, k].
+ * K must be a multiple of 16.  Otherwise as dgl_gemm_bf16.
+ */
+dgl_status dgl_gemm_fp8(const void* A, const void* B, const float* sa, const float* sb, void* C, int64_t M,
+                        int64_t N, int64_t K, int64_t m_valid, int64_t n_valid, int32_t out_dtype, void* stream);
+
+/*
+ * Either GEMM with a caller-chosen plan instead of the planner's choice: the
+ * forced-tile sweep of FlyDSL pull request 1303 ("a second test runs every
+ * tile of both ladders against a shape that divides none of them").
+ * dtype: dgl_dtype_t (sa/sb ignored for bf16).  plan->path, tile_n and grid
+ * are honoured (grid <= 0 picks one); other fields are ignored.  A plan the
+ * library has no kernel for returns DGL_ERR_UNSUPPORTED.
+ */
+dgl_status dgl_gemm_planned(int32_t dtype, const void* A, const void* B, const float* sa, const float* sb,
+                            void* C, int64_t M, int64_t N, int64_t K, int64_t m_valid, int64_t n_valid,
+                            int32_t out_dtype, const dgl_plan_info* plan, void* stream);
+
+/*
+ * The plan the library would use for a problem of m x n x K (valid extents)
+ * on a device with num_sms SMs (num_sms <= 0: query the current device).
+ * Pure host logic when num_sms > 0: needs no GPU.
+ * Rule: m <= 16 takes the decode path; otherwise the tcgen05 tile ladder is
+ * screened by padded output area (rejecting a tile whose padded area exceeds
+ * 1.25x the real one unless none passes, as in FlyDSL pull request 1303's
+ * autotuner) and the survivor with the lowest cost-model time is chosen.
+ */
+dgl_status dgl_plan(int32_t dtype, int64_t m, int64_t n, int64_t K, int32_t out_dtype, int32_t num_sms,
+                    dgl_plan_info* out);
+
+/*
+ * Tile- and wave-quantisation metrics of an m x n output on tile_m x tile_n
+ * tiles spread over num_units parallel units ("GEMM analysis in TraceLens",
+ * section "How it's calculated").  Fills num_tiles, tile_eff, wq_eff and
+ * dim_eff of *out (other fields zero).  Pure host logic.
+ */
+dgl_status dgl_tile_metrics(int64_t m, int64_t n, int32_t tile_m, int32_t tile_n, int32_t num_units,
+                            dgl_plan_info* out);
+
+/*
+ * Synchronise `stream`, then report and clear the current device's status
+ * word: DGL_ERR_TIMEOUT if any kernel's bounded wait gave up since the last
+ * call, DGL_ERR_CUDA if synchronisation failed, else DGL_OK.
+ */
+dgl_status dgl_device_status(void* stream);
+
+/* Static description of a status code (never NULL). */
+const char* dgl_status_string(int32_t status);
+
+/* Library ABI version (major * 100 + minor). */
+int32_t dgl_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DGL_H_ */

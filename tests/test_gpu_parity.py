@@ -1,0 +1,183 @@
+"""CUDA path vs the oracle, element by element, through the C ABI.
+
+Small cases are compared in full; every case also checks that nothing outside
+the valid region of C was written (guard rows and a padded row pitch filled
+with NaN canaries, the guard-band idea of FlyDSL pull request 1303's tests).
+Tolerances: |C - C_ref| <= 1e-4 * sum_k |a_ik b_jk| + 1e-6 for fp32 output,
+plus 1e-2 |C_ref| for bf16 output; integer-valued inputs must match exactly.
+"""
+import numpy as np
+import pytest
+
+import dense_gemm_linear_gb300 as dgl
+from synthetic import make_case
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+def _full(case, **kw):
+    Cbuf, intact = gu.run(case, **kw)
+    assert intact, f"{case.name}: wrote outside the valid region"
+    C = gu.host_valid(case, Cbuf)
+    gu.assert_close_full(case, C)
+    return C
+
+
+# -------------------------------------------------------------- the 256^3 case
+def test_square256_uniform_f32():
+    _full(make_case("bf16", 256, 256, 256, out="f32", dist="uniform"))
+
+
+def test_square256_integer_bit_exact():
+    case = make_case("bf16", 256, 256, 256, out="f32", dist="int")
+    Cbuf, intact = gu.run(case)
+    assert intact
+    gu.assert_exact(case, gu.host_valid(case, Cbuf))
+
+
+# -------------------------------------------------------------- structure pins on the GPU path
+def test_identity_gives_transpose():
+    """A = I_K: C = B^T exactly, so any layout mistake shows as a permutation."""
+    K, n = 128, 192
+    case = make_case("bf16", K, n, K, out="f32", dist="int")
+    eye = np.eye(K)
+    from synthetic import to_bf16_codes
+    case.A = to_bf16_codes(eye)
+    Cbuf, intact = gu.run(case)
+    assert intact
+    C = gu.host_valid(case, Cbuf)
+    Bv = gu.oracle.decode_bf16(case.B)
+    np.testing.assert_array_equal(C, Bv.T)
+
+
+SMALL_RAGGED = [(130, 200, 72), (1, 37, 64), (17, 300, 136), (129, 257, 200), (255, 65, 8),
+                (300, 513, 1000), (16, 64, 4096), (33, 1000, 48), (500, 129, 2056)]
+
+
+@pytest.mark.parametrize("m,n,k", SMALL_RAGGED)
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_small_ragged_bf16(m, n, k, out):
+    _full(make_case("bf16", m, n, k, out=out), guard_rows=3, pad_cols=5)
+
+
+@pytest.mark.parametrize("m,n,k", SMALL_RAGGED)
+def test_small_ragged_e4m3(m, n, k):
+    if k % 16:
+        pytest.skip("E4M3 rows must be a multiple of 16 bytes")
+    _full(make_case("fp8", m, n, k, out="bf16", dist="fp8"), guard_rows=2, pad_cols=3)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("m", [1, 5, 16, 40, 200])
+def test_integer_bit_exact_all_paths(dtype, m):
+    case = make_case(dtype, m, 300, 512, out="f32", dist="int")
+    Cbuf, intact = gu.run(case, guard_rows=1, pad_cols=2)
+    assert intact
+    gu.assert_exact(case, gu.host_valid(case, Cbuf))
+
+
+# -------------------------------------------------------------- every ladder rung, forced
+LADDER = [(dgl.PATH_TC, 128, 64), (dgl.PATH_TC, 128, 128), (dgl.PATH_TC, 128, 256)]
+
+
+@pytest.mark.parametrize("path,tm,tn", LADDER, ids=lambda v: str(v))
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_forced_tile_on_shape_no_tile_divides(path, tm, tn, dtype, out):
+    """Each rung on a shape none of them divides (ragged in M, N and K)."""
+    case = make_case(dtype, 333, 517, 336, out=out, dist="fp8" if dtype == "fp8" else "normal")
+    plan = dgl.PlanInfo(path=path, tile_m=tm, tile_n=tn)
+    _full(case, plan=plan, guard_rows=4, pad_cols=7)
+
+
+@pytest.mark.parametrize("grid", [1, 3, 7])
+def test_persistent_tile_loop_small_grid(grid):
+    """Fewer CTAs than tiles: each CTA walks many tiles through both accumulators."""
+    case = make_case("bf16", 700, 900, 264, out="f32")
+    plan = dgl.PlanInfo(path=dgl.PATH_TC, tile_m=128, tile_n=128, grid=grid)
+    _full(case, plan=plan)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("m", [1, 3, 8, 16])
+@pytest.mark.parametrize("n", [1, 7, 8, 9, 1000, 2049])
+def test_decode_path(dtype, m, n):
+    case = make_case(dtype, m, n, 256, out="bf16", dist="fp8" if dtype == "fp8" else "normal")
+    assert dgl.dgl_plan(0 if dtype == "bf16" else 1, m, n, 256).path == dgl.PATH_DECODE
+    _full(case, guard_rows=2, pad_cols=3)
+
+
+@pytest.mark.parametrize("k", [16, 48, 272, 4104, 8192])
+def test_decode_k_extents(k):
+    _full(make_case("bf16", 7, 300, k, out="f32"))
+
+
+def test_decode_many_rows_per_cta():
+    """n large enough that each CTA reduces several 128-row blocks."""
+    case = make_case("bf16", 4, 50257, 64, out="bf16")
+    Cbuf, intact = gu.run(case, pad_cols=1)
+    assert intact
+    gu.assert_close_full(case, gu.host_valid(case, Cbuf))
+
+
+def test_forced_decode_vs_tile_same_result():
+    """m <= 16 through both paths: both within tolerance of the oracle."""
+    case = make_case("bf16", 12, 640, 512, out="f32")
+    _full(case, plan=dgl.PlanInfo(path=dgl.PATH_TC, tile_m=128, tile_n=128))
+    _full(case, plan=dgl.PlanInfo(path=dgl.PATH_DECODE))
+
+
+def test_deterministic_repeat():
+    case = make_case("bf16", 600, 700, 1024, out="f32")
+    ops = gu.to_device(case)
+    a, _ = gu.run(case, dev_ops=ops)
+    b, _ = gu.run(case, dev_ops=ops)
+    assert bool((a == b).all().item())
+
+
+# -------------------------------------------------------------- degenerate cases and errors
+def test_k_zero_writes_zeros():
+    import torch
+    C = gu.canary_buffer(5, 9, "f32")
+    A = torch.zeros(8, dtype=torch.bfloat16, device="cuda")
+    st = dgl.dgl_gemm_bf16(A.data_ptr(), A.data_ptr(), C.data_ptr(), 5, 9, 0, 4, 7, dgl.OUT_F32, 0)
+    assert st == dgl.DGL_OK
+    torch.cuda.synchronize()
+    c = C.cpu().numpy()
+    assert (c[:4, :7] == 0).all()
+    assert np.isnan(c[4, :]).all() and np.isnan(c[:, 7:]).all()
+
+
+def test_empty_product_is_noop():
+    assert dgl.dgl_gemm_bf16(None, None, None, 0, 10, 64, 0, 0, dgl.OUT_BF16, 0) == dgl.DGL_OK
+    assert dgl.dgl_gemm_bf16(None, None, None, 10, 0, 64, 0, 0, dgl.OUT_BF16, 0) == dgl.DGL_OK
+
+
+def test_argument_errors():
+    import torch
+    A = torch.zeros(64, 64, dtype=torch.bfloat16, device="cuda")
+    C = torch.zeros(64, 64, dtype=torch.bfloat16, device="cuda")
+    p = A.data_ptr()
+    assert dgl.dgl_gemm_bf16(p, p, C.data_ptr(), 64, 64, 60, 0, 0, 0, 0) == dgl.DGL_ERR_ALIGN  # K % 8
+    assert dgl.dgl_gemm_bf16(p + 2, p, C.data_ptr(), 64, 64, 64, 0, 0, 0, 0) == dgl.DGL_ERR_ALIGN
+    assert dgl.dgl_gemm_bf16(p, p, C.data_ptr(), 64, 64, 64, 65, 0, 0, 0) == dgl.DGL_ERR_ARG
+    assert dgl.dgl_gemm_bf16(None, p, C.data_ptr(), 64, 64, 64, 0, 0, 0, 0) == dgl.DGL_ERR_ARG
+    assert dgl.dgl_gemm_bf16(p, p, C.data_ptr(), 64, 64, 64, 0, 0, 7, 0) == dgl.DGL_ERR_ARG
+    assert dgl.dgl_gemm_fp8(p, p, None, None, C.data_ptr(), 64, 64, 64, 0, 0, 0, 0) == dgl.DGL_ERR_ARG
+    assert dgl.dgl_gemm_bf16(p, p, C.data_ptr(), 64, 64, 1 << 31, 0, 0, 0, 0) == dgl.DGL_ERR_SHAPE
+    bad = dgl.PlanInfo(path=dgl.PATH_TC, tile_m=128, tile_n=96)
+    assert dgl.dgl_gemm_planned(0, p, p, None, None, C.data_ptr(), 64, 64, 64, 0, 0, 0, bad, 0) == \
+        dgl.DGL_ERR_UNSUPPORTED
+    assert dgl.dgl_device_status(0) == dgl.DGL_OK
+
+
+def test_torch_helpers_and_streams():
+    import torch
+    case = make_case("bf16", 200, 300, 128, out="bf16")
+    A, B, _, _ = gu.to_device(case)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        C = dgl.gemm_bf16(A, B)
+    s.synchronize()
+    gu.assert_close_full(case, C.double().cpu().numpy())
