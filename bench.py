@@ -1,0 +1,450 @@
+"""Benchmark: dense linear-layer GEMM throughput on GB300 through the C ABI.
+
+One step = one pass over a workload's GEMMs (default: the bf16 ragged-shape
+set -- decode batches of 1/8/16 tokens, 48x4096x48, 333/528/3402-token
+prefill shapes, the 1024x50257x512 lm_head, 2048x11007x1024, 4095^2x1024 --
+with N(0,1) activations, N(0,0.02) weights and bf16 C).  Prints one JSON line.
+
+  python bench.py [--gpus N --steps K --warmup W] [--workload ragged|llama7b_mlp|square|fp8|square256]
+  python bench.py --impl reference      # the fp64 CPU oracle, timed on the host cores
+
+value = 2*m*n*K summed over the step's GEMMs (valid extents only) / step time,
+TFLOP/s, summed over ranks (each rank runs the workload independently).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s (2MNK/t) & % GB300 tensor peak; decode GB/s vs HBM"
+WORKLOAD_TEXT = {
+    "ragged": "bf16 ragged-shape sweep, fp32 accumulate, bf16 C: (1,11008,4096) (8,4096,4096) (16,4096,4096) "
+              "(48,4096,48) (333,4096,1024) (528,528,1024) (3402,4096,1024) (1024,50257,512) "
+              "(2048,11007,1024) (4095,4095,1024); A~N(0,1), B~N(0,0.02)",
+    "llama7b_mlp": "LLaMA-2-7B MLP up/gate shapes, bf16: (597,11008,4096) prefill, decode M in {1,4,16}",
+    "square": "bf16 squares M=N=K in {2048,4096,8192}, A,B~N(0,1), bf16 C",
+    "fp8": "E4M3 with per-row/per-column fp32 scales, bf16 C: (4096,4096,4096) (597,11008,4096) (16,11008,4096)",
+    "square256": "bf16 256^3, fp32 C: uniform[-1,1] and integer [-4,4] variants",
+}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="dgl", choices=["dgl", "reference"])
+    ap.add_argument("--workload", default="ragged", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--shape", default=None,
+                    help="single GEMM m,n,k[,bf16|fp8[,bf16|f32]] instead of a workload (profiling)")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-macs", type=float, default=4e9,
+                    help="multiply-adds of the bounded CPU-oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+def oracle_sample_run(cases, mac_budget):
+    """Time the oracle on a bounded band of rows of every case; returns (flops, seconds, threads, text)."""
+    import oracle
+    lib = oracle.load()
+    per_case = mac_budget / max(1, len(cases))
+    flops, secs, parts = 0.0, 0.0, []
+    for c in cases:
+        rows = int(max(1, min(c.m, per_case // max(1, c.n * c.K))))
+        dt = oracle.BF16 if c.dtype == "bf16" else oracle.E4M3
+        sa = c.sa[:rows] if c.sa is not None else None
+        t0 = time.perf_counter()
+        oracle.gemm(dt, c.A[:rows], c.B, sa, c.sb, lib=lib)
+        secs += time.perf_counter() - t0
+        flops += 2.0 * rows * c.n * c.K
+        parts.append(f"{rows}x{c.n}x{c.K}")
+    return flops, secs, oracle.threads(lib), "first rows of each GEMM: " + ", ".join(parts)
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from synthetic import WORKLOADS, make_workload_case
+    entries = WORKLOADS[args.workload] if args.shape is None else [shape_entry(args.shape)]
+    cases = [make_workload_case(e) for e in entries]
+    # each step: a bounded band of one GEMM (round robin), sized so the whole run stays within minutes
+    total_steps = args.steps + args.warmup
+    budget_macs = min(args.cpu_macs, 3e10 / max(1, total_steps)) if total_steps else args.cpu_macs
+    import oracle
+    lib = oracle.load()
+    flops_t, secs_t = 0.0, 0.0
+    desc = []
+    for s in range(total_steps):
+        c = cases[s % len(cases)]
+        rows = int(max(1, min(c.m, budget_macs // max(1, c.n * c.K))))
+        dt = oracle.BF16 if c.dtype == "bf16" else oracle.E4M3
+        sa = c.sa[:rows] if c.sa is not None else None
+        t0 = time.perf_counter()
+        oracle.gemm(dt, c.A[:rows], c.B, sa, c.sb, lib=lib)
+        el = time.perf_counter() - t0
+        if s >= args.warmup:
+            flops_t += 2.0 * rows * c.n * c.K
+            secs_t += el
+            if len(desc) < len(cases):
+                desc.append(f"{rows}x{c.n}x{c.K}")
+    value = flops_t / secs_t / 1e12 if secs_t > 0 else 0.0
+    cores = oracle.threads(lib)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs_t / max(1, args.steps) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_text(args), "sample": "one GEMM per step, round robin"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": "per step: first rows of one GEMM: " + ", ".join(desc)},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def shape_entry(text):
+    parts = text.split(",")
+    m, n, k = (int(v) for v in parts[:3])
+    dtype = parts[3] if len(parts) > 3 else "bf16"
+    out = parts[4] if len(parts) > 4 else "bf16"
+    return (dtype, m, n, k, out, "fp8" if dtype == "fp8" else "normal")
+
+
+def workload_text(args):
+    if args.shape is not None:
+        dtype, m, n, k, out, dist = shape_entry(args.shape)
+        return f"single GEMM {m}x{n}x{k} {dtype} inputs, {out} C ({dist} draws)"
+    return WORKLOAD_TEXT[args.workload]
+
+
+# ------------------------------------------------------------------ GPU arm
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import numpy as np
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    import dense_gemm_linear_gb300 as dgl
+    from dense_gemm_linear_gb300 import _build
+    if not os.path.exists(dgl.LIB_PATH):
+        _build.build()
+    lib = dgl.load_library()
+    from synthetic import WORKLOADS, make_workload_case
+
+    entries = WORKLOADS[args.workload] if args.shape is None else [shape_entry(args.shape)]
+    cases = [make_workload_case(e) for e in entries]
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream(dev)
+    s_handle = stream.cuda_stream
+
+    ops = []
+    for c in cases:
+        if c.dtype == "bf16":
+            A = torch.from_numpy(c.A.view(np.int16)).to(dev)
+            B = torch.from_numpy(c.B.view(np.int16)).to(dev)
+            sa = sb = None
+        else:
+            A = torch.from_numpy(c.A).to(dev)
+            B = torch.from_numpy(c.B).to(dev)
+            sa = torch.from_numpy(c.sa).to(dev)
+            sb = torch.from_numpy(c.sb).to(dev)
+        out_dtype = dgl.OUT_F32 if c.out == "f32" else dgl.OUT_BF16
+        C = torch.empty((c.m, c.n), dtype=torch.float32 if c.out == "f32" else torch.bfloat16, device=dev)
+        ops.append((c, A, B, sa, sb, C, out_dtype))
+
+    def make_call(c, A, B, sa, sb, C, out_dtype):
+        if c.dtype == "bf16":
+            args_ = (A.data_ptr(), B.data_ptr(), C.data_ptr(), c.m, c.n, c.K, c.m, c.n, out_dtype, s_handle)
+            fn = lib.dgl_gemm_bf16
+        else:
+            args_ = (A.data_ptr(), B.data_ptr(), sa.data_ptr(), sb.data_ptr(), C.data_ptr(), c.m, c.n, c.K, c.m,
+                     c.n, out_dtype, s_handle)
+            fn = lib.dgl_gemm_fp8
+
+        def call():
+            st = fn(*args_)
+            if st != 0:
+                raise RuntimeError(f"GEMM {c.name} failed: {dgl.status_string(st)}")
+        return call
+
+    calls = [make_call(*o) for o in ops]
+    plans = [dgl.dgl_plan(0 if c.dtype == "bf16" else 1, c.m, c.n, c.K,
+                          dgl.OUT_F32 if c.out == "f32" else dgl.OUT_BF16) for c in cases]
+
+    def kernel_name(c, p):
+        if p.path == dgl.PATH_DECODE:
+            return f"decode_gemm_kernel<{c.dtype}>"
+        return f"tc_gemm_kernel<{c.dtype}, 128x{p.tile_n}>"
+
+    knames = [kernel_name(c, p) for c, p in zip(cases, plans)]
+    flops = [2.0 * c.m * c.n * c.K for c in cases]
+    nbytes = []
+    for c in cases:
+        e = 2 if c.dtype == "bf16" else 1
+        o = 4 if c.out == "f32" else 2
+        nbytes.append(c.m * c.K * e + c.n * c.K * e + c.m * c.n * o + (4 * (c.m + c.n) if c.dtype == "fp8" else 0))
+
+    # warm-up
+    for _ in range(args.warmup):
+        for f in calls:
+            f()
+    torch.cuda.synchronize()
+    st = lib.dgl_device_status(s_handle)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {dgl.status_string(st)}")
+
+    # ---------------------------------------------------------- device-timed region
+    K_steps = args.steps
+    ncall = len(calls)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(ncall + 1)] for _ in range(K_steps)]
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s in range(K_steps):
+        ev = evs[s]
+        ev[0].record(stream)
+        for i, f in enumerate(calls):
+            f()
+            ev[i + 1].record(stream)
+    t_end.record(stream)
+    barrier()
+    clocks = sampler.stop()
+    st = lib.dgl_device_status(s_handle)
+    if st != 0:
+        raise RuntimeError(f"device status after timed region: {dgl.status_string(st)}")
+    total_ms = t_start.elapsed_time(t_end)
+    ms_per_step = total_ms / K_steps
+    per_call_ms = [0.0] * ncall
+    for s in range(K_steps):
+        for i in range(ncall):
+            per_call_ms[i] += evs[s][i].elapsed_time(evs[s][i + 1])
+    per_call_ms = [v / K_steps for v in per_call_ms]
+
+    step_flops = sum(flops)
+    if dist is not None:
+        t = torch.tensor([ms_per_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    else:
+        ms_max = ms_per_step
+    value = step_flops * world / (ms_max * 1e-3) / 1e12
+
+    # ---------------------------------------------------------- roofline of the dominant kernel
+    pk, pk_src = peaks()
+    by_kernel = {}
+    for i, kn in enumerate(knames):
+        d = by_kernel.setdefault(kn, {"ms": 0.0, "flops": 0.0, "bytes": 0.0, "launches": 0})
+        d["ms"] += per_call_ms[i]
+        d["flops"] += flops[i]
+        d["bytes"] += nbytes[i]
+        d["launches"] += 1
+    dominant = max(by_kernel, key=lambda k: by_kernel[k]["ms"])
+    dk = by_kernel[dominant]
+    if dominant.startswith("tc_gemm"):
+        peak_tf = pk["bf16_tflops"] * (2.0 if "fp8" in dominant else 1.0)
+        achieved = dk["flops"] / (dk["ms"] * 1e-3) / 1e12
+        roofline = {"kernel": dominant, "bound": "tensor", "achieved": achieved, "peak": peak_tf,
+                    "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": None,
+                    "peak_source": f"{pk_src} bf16 burst" + (" x2 (fp8 nominal ratio)" if "fp8" in dominant else ""),
+                    "launches_per_step": dk["launches"], "avg_launch_us": dk["ms"] * 1e3 / dk["launches"],
+                    "algorithmic_flops_per_launch": dk["flops"] / dk["launches"]}
+    else:
+        achieved = dk["bytes"] / (dk["ms"] * 1e-3) / 1e9
+        roofline = {"kernel": dominant, "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                    "frac": achieved / pk["hbm_gbs"], "traffic": None, "peak_source": f"{pk_src} hbm copy",
+                    "launches_per_step": dk["launches"], "avg_launch_us": dk["ms"] * 1e3 / dk["launches"],
+                    "algorithmic_bytes_per_launch": dk["bytes"] / dk["launches"]}
+    kernels = {k: {"launches_per_step": v["launches"], "us_per_step": v["ms"] * 1e3,
+                   "share": v["ms"] / sum(x["ms"] for x in by_kernel.values())} for k, v in by_kernel.items()}
+    dec = {k: v for k, v in by_kernel.items() if k.startswith("decode")}
+    roofline_decode = None
+    if dec:
+        db = sum(v["bytes"] for v in dec.values())
+        dm = sum(v["ms"] for v in dec.values())
+        roofline_decode = {"bound": "hbm", "achieved": db / (dm * 1e-3) / 1e9, "peak": pk["hbm_gbs"],
+                           "unit": "GB/s", "frac": db / (dm * 1e-3) / 1e9 / pk["hbm_gbs"],
+                           "peak_source": f"{pk_src} hbm copy"}
+    per_shape = []
+    for i, c in enumerate(cases):
+        t = per_call_ms[i] * 1e-3
+        per_shape.append({"shape": [c.m, c.n, c.K], "dtype": c.dtype, "out": c.out, "kernel": knames[i],
+                          "us": per_call_ms[i] * 1e3, "tflops": flops[i] / t / 1e12,
+                          "gbs": nbytes[i] / t / 1e9, "tile_eff": round(plans[i].tile_eff, 4),
+                          "wq_eff": round(plans[i].wq_eff, 4), "grid": plans[i].grid})
+
+    # ---------------------------------------------------------- end to end through host buffers
+    e2e = None
+    if args.e2e_steps > 0:
+        host = []
+        h2d = d2h = 0
+        for (c, A, B, sa, sb, C, _o) in ops:
+            hA = torch.empty(A.shape, dtype=A.dtype, pin_memory=True).copy_(A.cpu())
+            hB = torch.empty(B.shape, dtype=B.dtype, pin_memory=True).copy_(B.cpu())
+            hsa = sa.cpu().pin_memory() if sa is not None else None
+            hsb = sb.cpu().pin_memory() if sb is not None else None
+            hC = torch.empty(C.shape, dtype=C.dtype, pin_memory=True)
+            host.append((hA, hB, hsa, hsb, hC))
+            h2d += hA.numel() * hA.element_size() + hB.numel() * hB.element_size()
+            if hsa is not None:
+                h2d += 4 * (hsa.numel() + hsb.numel())
+            d2h += hC.numel() * hC.element_size()
+
+        def e2e_step():
+            for (c, A, B, sa, sb, C, _o), (hA, hB, hsa, hsb, hC), f in zip(ops, host, calls):
+                A.copy_(hA, non_blocking=True)
+                B.copy_(hB, non_blocking=True)
+                if sa is not None:
+                    sa.copy_(hsa, non_blocking=True)
+                    sb.copy_(hsb, non_blocking=True)
+                f()
+                hC.copy_(C, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+        if dist is not None:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": step_flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+               "steps": args.e2e_steps}
+
+    # ---------------------------------------------------------- CPU oracle baseline (rank 0, N = 1)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        f_, s_, cores, text = oracle_sample_run(cases, args.cpu_macs)
+        cpu = {"value": f_ / s_ / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": text, "seconds": s_}
+
+    if rank == 0:
+        l2_mb = torch.cuda.get_device_properties(dev).L2_cache_size / 2**20
+        ws = sum(nbytes) / 2**20
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K_steps,
+            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if all(c.dtype == "bf16" for c in cases) else "e4m3",
+            "data": "synthetic (seeded SplitMix64 draws; no datasets or trained weights)",
+            "config": {"workload": workload_text(args), "gemms_per_step": ncall,
+                       "parallelism": "replicas" if world > 1 else "single GPU",
+                       "l2": f"inputs larger than L2: each step touches {ws:.0f} MiB of A/B/C against a "
+                             f"{l2_mb:.0f} MiB L2, so every GEMM's operands were last read a full step earlier"},
+            "roofline": roofline, "roofline_decode": roofline_decode, "kernels": kernels, "per_shape": per_shape,
+            "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": K_steps * ncall, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -102,6 +102,22 @@ bool encode_operand_map(CUtensorMap* map, const void* base, bool e4m3, int64_t i
   return r == CUDA_SUCCESS;
 }
 
+// 2-D tensor map over C [rows, cols] (row pitch ldc elements) for 32 x 32
+// TMA stores from the epilogue's swizzled staging tile.  Writes outside
+// [0, cols) x [0, rows) are dropped.
+bool encode_output_map(CUtensorMap* map, void* base, bool f32, int64_t cols, int64_t rows, int64_t ldc) {
+  const CUtensorMapDataType dt = f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int64_t esize = f32 ? 4 : 2;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldc * esize)};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 struct Problem {
@@ -192,10 +208,14 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream) {
     return launch_decode(pr.dtype, pr.out, p, grid, stream) == cudaSuccess ? DGL_OK : DGL_ERR_CUDA;
   }
 
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tc;
   if (!encode_operand_map(&ta, pr.A, e4m3, pr.K, pr.m, plan.tile_m) ||
       !encode_operand_map(&tb, pr.B, e4m3, pr.K, pr.n, plan.tile_n))
     return DGL_ERR_CUDA;
+  const bool f32 = pr.out == DGL_OUT_F32;
+  const bool c_tma = aligned(pr.C, 16) && (pr.N * (f32 ? 4 : 2)) % 16 == 0;
+  std::memset(&tc, 0, sizeof(tc));
+  if (c_tma && !encode_output_map(&tc, pr.C, f32, pr.n, pr.m, pr.N)) return DGL_ERR_CUDA;
   TcParams p;
   p.C = pr.C;
   p.ldc = pr.N;
@@ -209,11 +229,13 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream) {
   p.num_tiles = p.tiles_m * p.tiles_n;
   p.num_kb = static_cast<int>((pr.K * esize + 127) / 128);
   p.group_m = 16;
+  p.c_tma = c_tma ? 1 : 0;
   p.status = ds->status;
   const int grid = plan.grid > 0 ? (plan.grid < p.num_tiles ? plan.grid : p.num_tiles) : p.num_tiles;
-  if (tc_smem_bytes(plan.tile_n, e4m3) > ds->smem_optin) return DGL_ERR_UNSUPPORTED;
-  const cudaError_t e = e4m3 ? launch_tc_e4m3(pr.out, plan.tile_n, ta, tb, p, grid, stream)
-                             : launch_tc_bf16(pr.out, plan.tile_n, ta, tb, p, grid, stream);
+  if (ds->smem_optin < 232448) return DGL_ERR_UNSUPPORTED;  // every variant is sized for 227 KB
+  const bool row_staging = !c_tma && !f32;
+  const cudaError_t e = e4m3 ? launch_tc_e4m3(pr.out, plan.tile_n, row_staging, ta, tb, tc, p, grid, stream)
+                             : launch_tc_bf16(pr.out, plan.tile_n, row_staging, ta, tb, tc, p, grid, stream);
   return e == cudaSuccess ? DGL_OK : DGL_ERR_CUDA;
 }
 

@@ -22,6 +22,7 @@ struct TcParams {
   const float* sb;      // E4M3 only: per-row scale of B (n entries)
   int tiles_m, tiles_n, num_tiles, num_kb;
   int group_m;          // tile raster: group_m row-tiles share each column sweep
+  int c_tma;            // 1: C is written by TMA tensor stores (16-byte aligned pitch and base)
   int* status;          // device status word
 };
 

@@ -1,38 +1,12 @@
 // E4M3 x E4M3 -> fp32 accumulate instantiations of the tcgen05 tile kernel,
 // with the per-row / per-column scale epilogue.
-#include "launch.h"
-#include "tc_gemm.cuh"
+#include "tc_launch.cuh"
 
 namespace dgl {
 
-namespace {
-
-template <int BN, bool OUT_F32>
-cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const TcParams& p, int grid,
-                       cudaStream_t stream) {
-  using Cfg = TcConfig<BN, tc_stages_for(BN), true, OUT_F32>;
-  auto kern = tc_gemm_kernel<Cfg>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(ta, tb, p);
-  return cudaGetLastError();
-}
-
-}  // namespace
-
-cudaError_t launch_tc_e4m3(int out, int tile_n, const CUtensorMap& ta, const CUtensorMap& tb, const TcParams& p,
-                           int grid, cudaStream_t stream) {
-  const bool f32 = out == 1;
-  switch (tile_n) {
-    case 64:
-      return f32 ? launch_one<64, true>(ta, tb, p, grid, stream) : launch_one<64, false>(ta, tb, p, grid, stream);
-    case 128:
-      return f32 ? launch_one<128, true>(ta, tb, p, grid, stream) : launch_one<128, false>(ta, tb, p, grid, stream);
-    case 256:
-      return f32 ? launch_one<256, true>(ta, tb, p, grid, stream) : launch_one<256, false>(ta, tb, p, grid, stream);
-    default:
-      return cudaErrorInvalidValue;
-  }
+cudaError_t launch_tc_e4m3(int out, int tile_n, bool row_staging, const CUtensorMap& ta, const CUtensorMap& tb,
+                           const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t stream) {
+  return tc_launch<true>(out, tile_n, row_staging, ta, tb, tc, p, grid, stream);
 }
 
 }  // namespace dgl

@@ -7,19 +7,31 @@
 //              each k-stage.  The tensor maps are bounded at the valid rows
 //              and at K, so rows past m or n and the k tail beyond K arrive as
 //              zeros and the k-loop carries no predicate (the descriptor-bound
-//              edge of "FlyDSL pull request 1303", changes to the RDNA3 GEMM).
+//              M edge of FlyDSL pull request 1303, applied to every extent).
 //   warp 1     allocates tensor memory, then one thread issues tcgen05.mma
 //              (four K=16 bf16 or K=32 E4M3 steps per 128-byte stage) into one
 //              of two TMEM accumulators and commits each stage back to the
 //              producer's "empty" barrier.
-//   warps 2-5  epilogue: tcgen05.ld of the finished accumulator (one row per
-//              thread), per-row / per-column scales for E4M3 ("Gemm
-//              Optimization" guide, section 7.1: acc * scale_a * scale_b),
-//              round to bf16 or keep fp32, then a transpose through shared
-//              memory so each warp store covers 32 consecutive columns of one
-//              row, with the column predicate j < n and row predicate i < m
-//              paid once per tile, outside the k-loop (section 7.2's
-//              CShuffle idea; the C-store predicate of the FlyDSL change).
+//   warps 2-9  epilogue, two warps per TMEM lane quarter, each taking every
+//              other 32-column chunk of its 32 rows.  A warp reads all of its
+//              chunks out of TMEM at once and releases the accumulator, then
+//              per chunk: E4M3 row/column scales ("Gemm Optimization" guide,
+//              section 7.1: acc * scale_a * scale_b), round to bf16 (or keep
+//              fp32), vector stores into a swizzled staging tile, and
+//                - a TMA tensor store of the 32 x 32 tile when C's row pitch
+//                  is 16-byte aligned (clipped at m and n by the tensor map:
+//                  the C-descriptor bound of the FlyDSL change), or
+//                - otherwise predicated stores from the staging tile with the
+//                  row predicate i < m and column predicate j < n paid once
+//                  per tile, outside the k-loop (that change's C-store
+//                  predicate).
+//              For bf16 C whose rows are not 16-byte aligned (N = 50257,
+//              11007, 4095, ...) the quarter's two warps instead stage whole
+//              tile rows, each shifted by its own misalignment, so every row's
+//              16-byte-aligned body leaves in one bulk copy and only its
+//              head and tail bytes take narrow stores.
+//              The staging transpose is section 7.2's "CShuffle" idea: re-map
+//              threads so each store covers contiguous columns of a row.
 // The two accumulators let the epilogue of tile t overlap the main loop of
 // tile t+1.
 #pragma once
@@ -32,13 +44,24 @@
 
 namespace dgl {
 
-template <int BN_, int STAGES_, bool FP8_, bool OUT_F32_>
+// Shared-memory ring depth for a tile width: about 192 KB of stages when the
+// epilogue stages 32 x 32 tiles, fewer when it stages whole rows.
+constexpr int tc_ring_stages(int bn, bool row_staging) {
+  return row_staging ? (bn == 64 ? 8 : (bn == 128 ? 5 : 3)) : (bn == 64 ? 8 : (bn == 128 ? 6 : 4));
+}
+
+template <int BN_, bool FP8_, bool OUT_F32_, bool ROWSTG_>
 struct TcConfig {
   static constexpr int BM = 128;
   static constexpr int BN = BN_;
-  static constexpr int STAGES = STAGES_;
   static constexpr bool FP8 = FP8_;
   static constexpr bool OUT_F32 = OUT_F32_;
+  // ROWSTG: bf16 C whose rows are not 16-byte aligned.  The epilogue stages
+  // whole tile rows, shifted by each row's misalignment, so the aligned body
+  // of every row leaves in one bulk copy.
+  static constexpr bool ROWSTG = ROWSTG_;
+  static_assert(!(ROWSTG && OUT_F32), "row staging is the bf16-output path");
+  static constexpr int STAGES = tc_ring_stages(BN, ROWSTG);
   static constexpr int ROW_BYTES = 128;                 // one 128-byte swizzle span of K per stage
   static constexpr int BK = FP8 ? 128 : 64;             // K elements per stage
   static constexpr int MMA_K_BYTES = 32;                // K=16 bf16 or K=32 E4M3 per instruction
@@ -46,36 +69,73 @@ struct TcConfig {
   static constexpr int A_STAGE_BYTES = BM * ROW_BYTES;
   static constexpr int B_STAGE_BYTES = BN * ROW_BYTES;
   static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-  static constexpr int EPI_WARPS = 4;
-  static constexpr int STG_PITCH = 33;                  // floats; odd pitch keeps the transpose conflict-free
-  static constexpr int STG_FLOATS = 32 * STG_PITCH;
+  static constexpr int EPI_WARPS = 8;
+  static constexpr int CHUNKS = BN / 32;                // 32-column chunks per tile row
+  static constexpr int CHUNKS_PER_WARP = CHUNKS / 2;    // two warps share a lane quarter
+  static constexpr int OUT_BYTES = OUT_F32 ? 4 : 2;
+  static constexpr int STG_ROW = 32 * OUT_BYTES;        // 32 x 32 staging row: 64 B (bf16) or 128 B (fp32)
+  // whole-row staging: BN bf16 + 16 bytes of shift room; the pitch is an odd
+  // multiple of 16 bytes so rows spread over the banks
+  static constexpr int ROW_PITCH = BN * 2 + 16;
+  static constexpr int STG_TOTAL = ROWSTG ? 4 * 32 * ROW_PITCH : EPI_WARPS * 4096;
   static constexpr int THREADS = 64 + EPI_WARPS * 32;
   static constexpr int TMEM_COLS = 2 * BN;              // two fp32 accumulators of BN columns
-  static constexpr int BAR_BYTES = 8 * (2 * STAGES + 5) + 8;
-  static constexpr int SMEM_BYTES =
-      1024 /* alignment slack */ + STAGES * STAGE_BYTES + EPI_WARPS * STG_FLOATS * 4 + BAR_BYTES;
-  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "UMMA N for M=128 must be a multiple of 16, <= 256");
-  static_assert(TMEM_COLS == 64 || TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512,
-                "TMEM allocation must be a power of two >= 32 columns");
+  static constexpr int BAR_BYTES = 8 * (2 * STAGES + 5) + 8 + 32;
+  static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + STAGES * STAGE_BYTES + STG_TOTAL + BAR_BYTES;
+  static_assert(BN == 64 || BN == 128 || BN == 256, "tile widths of the ladder");
+  static_assert((ROW_PITCH / 16) % 2 == 1, "row pitch: odd multiple of 16 bytes");
+  static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation: power of two");
   static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
 };
+
+// Byte offset of 16-byte unit `c16` of staging row `r`, in the layout a TMA
+// store with the 64-byte (bf16 rows) or 128-byte (fp32 rows) swizzle reads.
+template <int STG_ROW>
+__device__ __forceinline__ uint32_t stg_offset(int r, int c16) {
+  if constexpr (STG_ROW == 64)
+    return static_cast<uint32_t>(r * 64 + ((c16 ^ ((r >> 1) & 3)) << 4));
+  else
+    return static_cast<uint32_t>(r * 128 + ((c16 ^ (r & 7)) << 4));
+}
+
+// Copy bytes [lo, hi) of a staged row to global memory with the widest
+// naturally aligned stores (2, 4 or 8 bytes; the span is under 16 bytes).
+// The staged copy and the global row share their alignment modulo 16.
+__device__ __forceinline__ void store_row_pieces(uint8_t* g, uint32_t s, int lo, int hi) {
+  while (lo < hi) {
+    const uintptr_t ga = reinterpret_cast<uintptr_t>(g + lo);
+    const int left = hi - lo;
+    if ((ga & 7) == 0 && left >= 8) {
+      const uint2 v = lds_v2(s + lo);
+      *reinterpret_cast<uint2*>(g + lo) = v;
+      lo += 8;
+    } else if ((ga & 3) == 0 && left >= 4) {
+      *reinterpret_cast<uint32_t*>(g + lo) = lds_u32(s + lo);
+      lo += 4;
+    } else {
+      *reinterpret_cast<uint16_t*>(g + lo) = static_cast<uint16_t>(lds_u16(s + lo));
+      lo += 2;
+    }
+  }
+}
 
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const TcParams p) {
+                   const __grid_constant__ CUtensorMap tmC, const TcParams p) {
   constexpr int BM = Cfg::BM, BN = Cfg::BN, STAGES = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = sA + STAGES * Cfg::A_STAGE_BYTES;
-  float* stg = reinterpret_cast<float*>(sB + STAGES * Cfg::B_STAGE_BYTES);
-  uint64_t* full = reinterpret_cast<uint64_t*>(stg + Cfg::EPI_WARPS * Cfg::STG_FLOATS);
+  uint8_t* sStg = sB + STAGES * Cfg::B_STAGE_BYTES;      // 1024-aligned: stage sizes are multiples of 8 KB
+  uint64_t* full = reinterpret_cast<uint64_t*>(sStg + Cfg::STG_TOTAL);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* qflag = reinterpret_cast<volatile int*>(tmem_slot + 1);  // 8 epilogue-warp flags
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -96,6 +156,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (p.c_tma) tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
@@ -190,14 +251,28 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lanes 32q .. 32q+31 are reachable from this warp
-    float* my_stg = stg + (warp - 2) * Cfg::STG_FLOATS;
+    const int e = warp - 2;                 // 0..7
+    const int q = warp & 3;                 // TMEM lanes 32q .. 32q+31 are reachable from this warp
+    const int half = e >> 2;                // this warp takes chunks [half * CPW, (half + 1) * CPW)
+    constexpr int CPW = Cfg::CHUNKS_PER_WARP;
+    uint8_t* stg = Cfg::ROWSTG ? sStg + q * 32 * Cfg::ROW_PITCH : sStg + e * 4096;
+    const uint32_t stg_addr = smem_u32(stg);
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
       int mb, nb;
       tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, mb, nb);
       // all lanes decide together: tcgen05.ld below is warp-collective
-      const bool ready = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase));
+      bool ready = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase));
+      if constexpr (Cfg::ROWSTG) {
+        // The quarter's two warps meet at named barriers below, so they must
+        // also agree on giving up.  This barrier also orders the previous
+        // tile's bulk copies (finished reading the staging rows) before the
+        // rows are rewritten.
+        if (half == 0) bulk_wait_read0();
+        if (lane == 0) qflag[2 * q + half] = ready ? 1 : 0;
+        named_bar_sync(1 + q, 64);
+        ready = qflag[2 * q] != 0 && qflag[2 * q + 1] != 0;
+      }
       if (!ready) {
         fail = STATUS_TIMEOUT_EPILOGUE;
         break;
@@ -205,47 +280,137 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       tc_fence_after_sync();
       const int row0 = mb * BM + q * 32;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-      float row_scale = 1.0f;
-      if constexpr (Cfg::FP8) row_scale = (row0 + lane < p.m) ? p.sa[row0 + lane] : 0.0f;
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(t_row + c * 32, r);
-        tmem_ld_wait();
-        if (c == BN / 32 - 1) {
-          // accumulator fully read: hand it back to the MMA warp
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&tempty[acc]);
-        }
-        const int col0 = nb * BN + c * 32;
-        float col_scale = 1.0f;
-        if constexpr (Cfg::FP8) col_scale = (col0 + lane < p.n) ? p.sb[col0 + lane] : 0.0f;
+
+      // Read this warp's whole share of the accumulator, then hand it back.
+      uint32_t r[CPW][32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          float v = __uint_as_float(r[j]);
-          if constexpr (Cfg::FP8) v = (v * row_scale) * __shfl_sync(0xffffffffu, col_scale, j);
-          my_stg[lane * Cfg::STG_PITCH + j] = v;
+      for (int u = 0; u < CPW; ++u) tmem_ld_32x32b_x32(t_row + (half * CPW + u) * 32, r[u]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int u = 0; u < CPW; ++u) reg_fence(r[u]);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+
+      if constexpr (Cfg::FP8) {
+        const float row_scale = (row0 + lane < p.m) ? p.sa[row0 + lane] : 0.0f;
+#pragma unroll
+        for (int u = 0; u < CPW; ++u) {
+          const int col0 = nb * BN + (half * CPW + u) * 32;
+          const float col_scale = (col0 + lane < p.n) ? p.sb[col0 + lane] : 0.0f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            r[u][j] = __float_as_uint((__uint_as_float(r[u][j]) * row_scale) *
+                                      __shfl_sync(0xffffffffu, col_scale, j));
         }
-        __syncwarp();
-        const int col = col0 + lane;
-        if (col < p.n) {
-#pragma unroll 4
-          for (int rr = 0; rr < 32; ++rr) {
-            const int row = row0 + rr;
-            if (row >= p.m) break;
-            const float v = my_stg[rr * Cfg::STG_PITCH + lane];
-            if constexpr (Cfg::OUT_F32)
-              static_cast<float*>(p.C)[static_cast<int64_t>(row) * p.ldc + col] = v;
-            else
-              static_cast<__nv_bfloat16*>(p.C)[static_cast<int64_t>(row) * p.ldc + col] = __float2bfloat16_rn(v);
+      }
+
+      if constexpr (Cfg::ROWSTG) {
+        // ---- bf16 C, rows not 16-byte aligned: stage whole rows, shifted
+        const int row = row0 + lane;                     // this thread's row
+        const int ncols = min(BN, p.n - nb * BN);
+        const int L = row < p.m ? 2 * ncols : 0;         // valid bytes of this row's segment
+        uint8_t* rowp = row < p.m ? reinterpret_cast<uint8_t*>(static_cast<__nv_bfloat16*>(p.C) +
+                                                           static_cast<int64_t>(row) * p.ldc + nb * BN)
+                                  : nullptr;
+        const int delta = static_cast<int>(reinterpret_cast<uintptr_t>(rowp) & 15);
+        const uint32_t srow = stg_addr + lane * Cfg::ROW_PITCH + delta;  // staged byte 0 of the segment
+#pragma unroll
+        for (int u = 0; u < CPW; ++u) {
+          uint32_t w[16];
+#pragma unroll
+          for (int t = 0; t < 16; ++t) {
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(r[u][2 * t]), __uint_as_float(r[u][2 * t + 1]));
+            w[t] = *reinterpret_cast<uint32_t*>(&h2);
+          }
+          const uint32_t base = srow + 64 * (half * CPW + u);
+          if ((delta & 2) == 0) {
+#pragma unroll
+            for (int t = 0; t < 16; ++t) sts_u32(base + 4 * t, w[t]);
+          } else {
+            sts_u16(base, w[0] & 0xFFFFu);
+#pragma unroll
+            for (int t = 0; t < 15; ++t) sts_u32(base + 2 + 4 * t, __byte_perm(w[t], w[t + 1], 0x5432));
+            sts_u16(base + 62, w[15] >> 16);
           }
         }
-        __syncwarp();
+        fence_proxy_async_shared();
+        named_bar_sync(1 + q, 64);
+        if (L > 0) {
+          const int head = min(L, (16 - delta) & 15);
+          const int body = ((L - head) >> 4) << 4;
+          if (half == 0) {
+            if (body > 0) {
+              bulk_store_1d(rowp + head, srow + head, static_cast<uint32_t>(body));
+              bulk_commit();
+            }
+          } else {
+            store_row_pieces(rowp, srow, 0, head);
+            store_row_pieces(rowp, srow, head + body, L);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < CPW; ++u) {
+          const int col0 = nb * BN + (half * CPW + u) * 32;
+          // the previous chunk's TMA store must have read the staging tile
+          if (p.c_tma && lane == 0) bulk_wait_read0();
+          __syncwarp();
+          // this thread's row (lane) of the 32 x 32 chunk -> staging, 16 bytes at a time
+          if constexpr (Cfg::OUT_F32) {
+#pragma unroll
+            for (int c16 = 0; c16 < 8; ++c16)
+              sts_v4(stg_addr + stg_offset<Cfg::STG_ROW>(lane, c16), r[u][4 * c16], r[u][4 * c16 + 1],
+                     r[u][4 * c16 + 2], r[u][4 * c16 + 3]);
+          } else {
+#pragma unroll
+            for (int c16 = 0; c16 < 4; ++c16) {
+              uint32_t w[4];
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(r[u][8 * c16 + 2 * t]),
+                                                          __uint_as_float(r[u][8 * c16 + 2 * t + 1]));
+                w[t] = *reinterpret_cast<uint32_t*>(&h2);
+              }
+              sts_v4(stg_addr + stg_offset<Cfg::STG_ROW>(lane, c16), w[0], w[1], w[2], w[3]);
+            }
+          }
+          // A TMA store writes whole 16-byte units of a row, so a chunk that
+          // ends inside one (n * element size not a multiple of 16) takes the
+          // predicated path instead.
+          const bool tma_ok = p.c_tma && (col0 + 32 <= p.n || (p.n * Cfg::OUT_BYTES) % 16 == 0);
+          if (tma_ok) {
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0 && row0 < p.m && col0 < p.n) {
+              tma_store_2d(&tmC, stg, col0, row0);
+              bulk_commit();
+            }
+          } else {
+            __syncwarp();
+            // one row per step, a column per lane
+            const int col = col0 + lane;
+#pragma unroll 4
+            for (int rr = 0; rr < 32; ++rr) {
+              const int row = row0 + rr;
+              if (row < p.m && col < p.n) {
+                if constexpr (Cfg::OUT_F32) {
+                  const float v = *reinterpret_cast<const float*>(stg + stg_offset<128>(rr, lane >> 2) + (lane & 3) * 4);
+                  static_cast<float*>(p.C)[static_cast<int64_t>(row) * p.ldc + col] = v;
+                } else {
+                  const uint16_t v = *reinterpret_cast<const uint16_t*>(stg + stg_offset<64>(rr, lane >> 3) + (lane & 7) * 2);
+                  reinterpret_cast<uint16_t*>(p.C)[static_cast<int64_t>(row) * p.ldc + col] = v;
+                }
+              }
+            }
+            __syncwarp();
+          }
+        }
       }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
+    if ((Cfg::ROWSTG ? half == 0 : (p.c_tma && lane == 0))) bulk_wait0();
   }
 
   if (fail) atomicOr(p.status, fail);

@@ -1,0 +1,41 @@
+// Host-side dispatch of the tcgen05 kernel over its compile-time variants
+// (tile width, output type, whole-row staging), shared by the bf16 and E4M3
+// translation units.
+#pragma once
+
+#include "launch.h"
+#include "tc_gemm.cuh"
+
+namespace dgl {
+
+template <int BN, bool FP8, bool OUT_F32, bool ROWSTG>
+cudaError_t tc_launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const TcParams& p,
+                          int grid, cudaStream_t stream) {
+  using Cfg = TcConfig<BN, FP8, OUT_F32, ROWSTG>;
+  auto kern = tc_gemm_kernel<Cfg>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(ta, tb, tc, p);
+  return cudaGetLastError();
+}
+
+template <int BN, bool FP8>
+cudaError_t tc_launch_bn(int out, bool row_staging, const CUtensorMap& ta, const CUtensorMap& tb,
+                         const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t stream) {
+  if (out == 1) return tc_launch_one<BN, FP8, true, false>(ta, tb, tc, p, grid, stream);
+  if (row_staging) return tc_launch_one<BN, FP8, false, true>(ta, tb, tc, p, grid, stream);
+  return tc_launch_one<BN, FP8, false, false>(ta, tb, tc, p, grid, stream);
+}
+
+template <bool FP8>
+cudaError_t tc_launch(int out, int tile_n, bool row_staging, const CUtensorMap& ta, const CUtensorMap& tb,
+                      const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t stream) {
+  switch (tile_n) {
+    case 64: return tc_launch_bn<64, FP8>(out, row_staging, ta, tb, tc, p, grid, stream);
+    case 128: return tc_launch_bn<128, FP8>(out, row_staging, ta, tb, tc, p, grid, stream);
+    case 256: return tc_launch_bn<256, FP8>(out, row_staging, ta, tb, tc, p, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace dgl

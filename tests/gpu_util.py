@@ -31,13 +31,20 @@ def canary_buffer(rows, cols, out):
     return torch.full((rows, cols), CANARY_BF16, dtype=torch.int16, device=DEV).view(torch.bfloat16)
 
 
-def run(case, *, guard_rows=0, pad_cols=0, plan=None, dev_ops=None, stream=None):
+def run(case, *, guard_rows=0, pad_cols=0, plan=None, dev_ops=None, stream=None, base_offset=0):
     """Run the case through the C ABI.  C is a (m + guard_rows) x (n + pad_cols)
-    buffer prefilled with canaries; returns (device C buffer, canaries_intact)."""
+    buffer prefilled with canaries, starting base_offset elements into its
+    allocation; returns (device C buffer, canaries_intact)."""
     A, B, sa, sb = dev_ops if dev_ops is not None else to_device(case)
     m, n, K = case.m, case.n, case.K
     rows, ldc = m + guard_rows, n + pad_cols
-    Cbuf = canary_buffer(rows, ldc, case.out)
+    if base_offset:
+        flat = canary_buffer(1, rows * ldc + base_offset, case.out).view(-1)
+        lead = flat[:base_offset]
+        Cbuf = flat[base_offset:].view(rows, ldc)
+    else:
+        lead = None
+        Cbuf = canary_buffer(rows, ldc, case.out)
     out_dtype = dgl.OUT_F32 if case.out == "f32" else dgl.OUT_BF16
     s = (stream or torch.cuda.current_stream()).cuda_stream
     if plan is not None:
@@ -57,6 +64,9 @@ def run(case, *, guard_rows=0, pad_cols=0, plan=None, dev_ops=None, stream=None)
     bits = Cbuf.view(torch.int32) if case.out == "f32" else Cbuf.view(torch.int16)
     canary = CANARY_F32 if case.out == "f32" else CANARY_BF16
     intact = bool((bits[m:, :] == canary).all().item()) and bool((bits[:m, n:] == canary).all().item())
+    if lead is not None:
+        lb = lead.view(torch.int32) if case.out == "f32" else lead.view(torch.int16)
+        intact = intact and bool((lb == canary).all().item())
     return Cbuf, intact
 
 

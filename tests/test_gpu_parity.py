@@ -91,6 +91,19 @@ def test_forced_tile_on_shape_no_tile_divides(path, tm, tn, dtype, out):
     _full(case, plan=plan, guard_rows=4, pad_cols=7)
 
 
+@pytest.mark.parametrize("pad,base", [(0, 0), (8, 0), (3, 0), (1, 1), (0, 1), (5, 3)])
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+@pytest.mark.parametrize("tn", [64, 128, 256])
+def test_output_store_paths(pad, base, out, tn):
+    """C pitch and base alignment select the TMA-store or the predicated-store
+    epilogue; odd pitches alternate row alignment, an odd base shifts every row."""
+    case = make_case("bf16", 261, 328, 200, out=out)
+    plan = dgl.PlanInfo(path=dgl.PATH_TC, tile_m=128, tile_n=tn)
+    Cbuf, intact = gu.run(case, plan=plan, guard_rows=2, pad_cols=pad, base_offset=base)
+    assert intact, "wrote outside the valid region"
+    gu.assert_close_full(case, gu.host_valid(case, Cbuf))
+
+
 @pytest.mark.parametrize("grid", [1, 3, 7])
 def test_persistent_tile_loop_small_grid(grid):
     """Fewer CTAs than tiles: each CTA walks many tiles through both accumulators."""
