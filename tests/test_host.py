@@ -1,0 +1,183 @@
+"""Host-side checks that need no GPU: the C ABI library loads and exports
+every symbol include/dgl.h declares; the planner's metric helpers match the
+worked examples printed on the pages; planner rules; the input generator."""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dgl.h")
+
+
+@pytest.fixture(scope="module")
+def dgl():
+    import dense_gemm_linear_gb300 as d
+    from dense_gemm_linear_gb300 import _build
+    _build.build()
+    d.load_library()
+    return d
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dgl_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for must in ("dgl_gemm_bf16", "dgl_gemm_fp8", "dgl_gemm_planned", "dgl_plan", "dgl_tile_metrics",
+                 "dgl_device_status", "dgl_status_string", "dgl_version"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(dgl):
+    lib = ctypes.CDLL(dgl.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in dgl.h but not exported"
+    out = subprocess.run(["nm", "-D", "--defined-only", dgl.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\b(dgl_[a-z0-9_]+)\b", out))
+    assert set(declared_functions()) <= exported
+    assert set(dgl.EXPORTED) == set(declared_functions())
+
+
+def test_version_and_status_strings(dgl):
+    assert dgl.dgl_version() >= 100
+    for code in range(-6, 1):
+        assert dgl.status_string(code) not in ("", "unknown status")
+
+
+# ------------------------------------------------------------ TraceLens worked examples
+def test_tile_metrics_tracelens_example_1(dgl):
+    """M=10240, N=2048, tile 256x64, 304 CUs: 1280 tiles, tile_eff 1.0, 5 rounds, wq_eff 0.842."""
+    m = dgl.dgl_tile_metrics(10240, 2048, 256, 64, 304)
+    assert m.num_tiles == 1280
+    assert m.tile_eff == 1.0
+    assert round(m.wq_eff, 3) == 0.842 and round(m.dim_eff, 3) == 0.842
+
+
+def test_tile_metrics_tracelens_example_2(dgl):
+    """M=2048, N=10240, tile 256x144, 304 CUs: 576 tiles, tile_eff ~0.9877, wq_eff ~0.947, dim_eff ~0.935."""
+    m = dgl.dgl_tile_metrics(2048, 10240, 256, 144, 304)
+    assert m.num_tiles == 576
+    # the page prints these to three or four digits with "approximately"
+    assert abs(m.tile_eff - 0.9877) < 1e-4
+    assert abs(m.wq_eff - 0.947) < 1e-3
+    assert abs(m.dim_eff - 0.935) < 1e-3
+
+
+def test_tile_metrics_tracelens_output_example(dgl):
+    """The enhanced-output row: 2048x2048 on a 256x64 macro tile, 304 CUs -> 256 tiles, wq_eff 0.84."""
+    m = dgl.dgl_tile_metrics(2048, 2048, 256, 64, 304)
+    assert m.num_tiles == 256 and m.tile_eff == 1.0 and round(m.wq_eff, 2) == 0.84
+
+
+def test_tile_metrics_errors(dgl):
+    with pytest.raises(dgl.DglError):
+        dgl.dgl_tile_metrics(10, 10, 0, 64, 10)
+    with pytest.raises(dgl.DglError):
+        dgl.dgl_tile_metrics(10, 10, 64, 64, 0)
+
+
+# ------------------------------------------------------------ the guide's worked example (section 14)
+def test_guide_worked_example_flops_and_bytes():
+    """5120x5120x8320 FP8 with bf16 C and per-token scales: 436 GFLOP and 137.6 MB;
+    at ~500 TFLOP/s that is ~0.87 ms and ~158 GB/s."""
+    from dense_gemm_linear_gb300 import metrics
+    f = metrics.gemm_flops(5120, 5120, 8320)
+    b = metrics.gemm_bytes(5120, 5120, 8320, in_bytes=1, out_bytes=2, scaled=True)
+    assert round(f / 1e9) == 436
+    assert abs(b / 1e6 - 137.6) < 0.1          # 137.67 MB; the page truncates to 137.6
+    t = f / 500e12
+    assert round(t * 1e3, 2) == 0.87
+    assert round(b / t / 1e9) == 158
+
+
+def test_arithmetic_intensity_classification():
+    from dense_gemm_linear_gb300 import metrics
+    # decode is memory-bound, large squares compute-bound, on GB300's ~281 flop/byte crossover
+    assert metrics.arithmetic_intensity(1, 11008, 4096) < 2
+    assert metrics.arithmetic_intensity(4096, 4096, 4096) > 1000
+
+
+# ------------------------------------------------------------ planner rules
+def test_plan_decode_threshold(dgl):
+    for m in (1, 4, 16):
+        assert dgl.dgl_plan(0, m, 11008, 4096, num_sms=152).path == dgl.PATH_DECODE
+    assert dgl.dgl_plan(0, 17, 11008, 4096, num_sms=152).path == dgl.PATH_TC
+    assert dgl.dgl_plan(0, 0, 10, 10, num_sms=152).path == dgl.PATH_EMPTY
+
+
+@pytest.mark.parametrize("m,n,k", [(48, 4096, 48), (333, 4096, 1024), (528, 528, 1024), (3402, 4096, 1024),
+                                   (1024, 50257, 512), (2048, 11007, 1024), (4095, 4095, 1024),
+                                   (597, 11008, 4096), (4096, 4096, 4096), (8192, 8192, 8192), (17, 5, 64)])
+def test_plan_padding_screen(dgl, m, n, k):
+    """The chosen tile pads the output by at most 1.25x, unless no ladder tile can."""
+    p = dgl.dgl_plan(0, m, n, k, num_sms=152)
+    assert p.path == dgl.PATH_TC
+    padded = -(-m // p.tile_m) * p.tile_m * -(-n // p.tile_n) * p.tile_n
+    any_ok = any(-(-m // 128) * 128 * -(-n // tn) * tn <= 1.25 * m * n for tn in (64, 128, 256))
+    if any_ok:
+        assert padded <= 1.25 * m * n
+    assert p.grid == min(p.num_tiles, 152)
+    assert 0 < p.dim_eff <= 1.0 and p.est_us > 0
+
+
+def test_plan_argument_errors(dgl):
+    info = dgl.PlanInfo()
+    lib = dgl.load_library()
+    assert lib.dgl_plan(0, -1, 10, 10, 0, 152, ctypes.byref(info)) == dgl.DGL_ERR_ARG
+    assert lib.dgl_plan(5, 10, 10, 10, 0, 152, ctypes.byref(info)) == dgl.DGL_ERR_ARG
+    assert lib.dgl_plan(0, 10, 10, 10, 9, 152, ctypes.byref(info)) == dgl.DGL_ERR_ARG
+    assert lib.dgl_plan(0, 1 << 31, 10, 10, 0, 152, ctypes.byref(info)) == dgl.DGL_ERR_SHAPE
+    assert lib.dgl_plan(0, 10, 10, 10, 0, 152, None) == dgl.DGL_ERR_ARG
+
+
+def test_gemm_rejects_bad_arguments_before_any_device_call(dgl):
+    """Argument checks run before the library touches the GPU, so they work here."""
+    lib = dgl.load_library()
+    assert lib.dgl_gemm_bf16(16, 16, 16, 64, 64, 60, 0, 0, 0, None) == dgl.DGL_ERR_ALIGN      # K % 8
+    assert lib.dgl_gemm_bf16(18, 16, 16, 64, 64, 64, 0, 0, 0, None) == dgl.DGL_ERR_ALIGN      # A not 16 B aligned
+    assert lib.dgl_gemm_bf16(16, 16, 16, 64, 64, 64, 65, 0, 0, None) == dgl.DGL_ERR_ARG       # m_valid > M
+    assert lib.dgl_gemm_bf16(None, 16, 16, 64, 64, 64, 0, 0, 0, None) == dgl.DGL_ERR_ARG
+    assert lib.dgl_gemm_bf16(16, 16, 16, 64, 64, 64, 0, 0, 3, None) == dgl.DGL_ERR_ARG        # bad out dtype
+    assert lib.dgl_gemm_fp8(16, 16, None, None, 16, 64, 64, 64, 0, 0, 0, None) == dgl.DGL_ERR_ARG
+    assert lib.dgl_gemm_bf16(16, 16, 16, 64, 64, 1 << 31, 0, 0, 0, None) == dgl.DGL_ERR_SHAPE
+    assert lib.dgl_gemm_bf16(None, None, None, 0, 64, 64, 0, 0, 0, None) == dgl.DGL_OK        # empty
+    assert lib.dgl_gemm_planned(0, 16, 16, None, None, 16, 64, 64, 64, 0, 0, 0, None, None) == dgl.DGL_ERR_ARG
+
+
+# ------------------------------------------------------------ synthetic inputs
+def test_generator_is_counter_based():
+    from synthetic import STREAM_A, normal, splitmix64_stream, uniform
+    full = splitmix64_stream(0, STREAM_A, 0, 1000)
+    part = splitmix64_stream(0, STREAM_A, 400, 100)
+    assert np.array_equal(full[400:500], part)
+    a = uniform(3, 1, (5000,), -1, 1)
+    b = uniform(3, 1, (5000,), -1, 1)
+    assert np.array_equal(a, b) and a.min() >= -1 and a.max() < 1
+    x = normal(0, 0, (200000,))
+    assert abs(x.mean()) < 0.01 and abs(x.std() - 1) < 0.01
+
+
+def test_generator_known_splitmix64_values():
+    """SplitMix64 with state s: the first output for state 0 after one increment is
+    0xE220A8397B1DCDAF (the published reference sequence for seed 0)."""
+    from synthetic.rng import _GOLDEN, _mix64
+    z = np.array([0], dtype=np.uint64) + _GOLDEN
+    assert int(_mix64(z)[0]) == 0xE220A8397B1DCDAF
+
+
+def test_workload_shapes_and_encodings():
+    from synthetic import make_case
+    c = make_case("bf16", 3, 5, 8)
+    assert c.A.dtype == np.uint16 and c.A.shape == (3, 8) and c.B.shape == (5, 8)
+    c8 = make_case("fp8", 3, 5, 16, dist="fp8")
+    assert c8.A.dtype == np.uint8 and c8.sa.shape == (3,) and c8.sb.shape == (5,)
+    assert ((c8.sa >= 0.5) & (c8.sa < 2)).all()
+    ci = make_case("fp8", 4, 4, 16, dist="int")
+    assert set(np.unique(ci.sa)) <= {0.5, 1.0, 2.0}
