@@ -118,6 +118,63 @@ bool encode_output_map(CUtensorMap* map, void* base, bool f32, int64_t cols, int
   return r == CUDA_SUCCESS;
 }
 
+// Small direct-mapped cache of encoded tensor maps.  A map depends only on
+// the address, extents, pitch, box and element type, so a buffer reused from
+// call to call (weights, persistent activations) is encoded once.
+struct MapKey {
+  const void* base;
+  int64_t d0, d1, pitch;
+  int box_rows, kind;  // kind: 0 bf16 operand, 1 E4M3 operand, 2 bf16 output, 3 fp32 output
+  bool operator==(const MapKey& o) const {
+    return base == o.base && d0 == o.d0 && d1 == o.d1 && pitch == o.pitch && box_rows == o.box_rows &&
+           kind == o.kind;
+  }
+};
+struct MapSlot {
+  bool valid = false;
+  MapKey key{};
+  CUtensorMap map;
+};
+constexpr int kMapSlots = 512;
+std::mutex g_map_mu;
+MapSlot g_map_cache[kMapSlots];
+
+size_t map_slot(const MapKey& k) {
+  size_t h = reinterpret_cast<uintptr_t>(k.base) >> 4;
+  h = h * 0x9E3779B97F4A7C15ull ^ static_cast<size_t>(k.d0);
+  h = h * 0x9E3779B97F4A7C15ull ^ static_cast<size_t>(k.d1);
+  h = h * 0x9E3779B97F4A7C15ull ^ static_cast<size_t>(k.pitch * 131 + k.box_rows * 7 + k.kind);
+  return (h >> 17) % kMapSlots;
+}
+
+template <class Encode>
+bool cached_map(CUtensorMap* out, const MapKey& key, Encode encode) {
+  const size_t slot = map_slot(key);
+  {
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    if (g_map_cache[slot].valid && g_map_cache[slot].key == key) {
+      *out = g_map_cache[slot].map;
+      return true;
+    }
+  }
+  if (!encode(out)) return false;
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  g_map_cache[slot].valid = true;
+  g_map_cache[slot].key = key;
+  g_map_cache[slot].map = *out;
+  return true;
+}
+
+bool cached_operand_map(CUtensorMap* map, const void* base, bool e4m3, int64_t inner, int64_t rows, int box_rows) {
+  const MapKey key{base, inner, rows, inner, box_rows, e4m3 ? 1 : 0};
+  return cached_map(map, key, [&](CUtensorMap* m) { return encode_operand_map(m, base, e4m3, inner, rows, box_rows); });
+}
+
+bool cached_output_map(CUtensorMap* map, void* base, bool f32, int64_t cols, int64_t rows, int64_t ldc) {
+  const MapKey key{base, cols, rows, ldc, 32, f32 ? 3 : 2};
+  return cached_map(map, key, [&](CUtensorMap* m) { return encode_output_map(m, base, f32, cols, rows, ldc); });
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 struct Problem {
@@ -194,9 +251,15 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream) {
   const bool e4m3 = pr.dtype == DGL_DTYPE_E4M3;
   const int esize = e4m3 ? 1 : 2;
   if (plan.path == DGL_PATH_DECODE) {
+    const int parts = decode_parts(pr.n, ds->num_sms);
+    const int rows_lo = static_cast<int>(pr.n / parts);
+    const int rows_hi = static_cast<int>((pr.n + parts - 1) / parts);
+    CUtensorMap ta, tb_lo, tb_hi;
+    if (!cached_operand_map(&ta, pr.A, e4m3, pr.K, pr.m, static_cast<int>(pr.m)) ||
+        !cached_operand_map(&tb_lo, pr.B, e4m3, pr.K, pr.n, rows_lo) ||
+        !cached_operand_map(&tb_hi, pr.B, e4m3, pr.K, pr.n, rows_hi))
+      return DGL_ERR_CUDA;
     DecodeParams p;
-    p.A = static_cast<const uint8_t*>(pr.A);
-    p.B = static_cast<const uint8_t*>(pr.B);
     p.sa = pr.sa;
     p.sb = pr.sb;
     p.C = pr.C;
@@ -204,18 +267,36 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream) {
     p.m = static_cast<int>(pr.m);
     p.n = static_cast<int>(pr.n);
     p.row_bytes = static_cast<int>(pr.K * esize);
-    const int grid = plan.grid > 0 ? plan.grid : decode_grid(pr.n, ds->num_sms);
-    return launch_decode(pr.dtype, pr.out, p, grid, stream) == cudaSuccess ? DGL_OK : DGL_ERR_CUDA;
+    p.parts = parts;
+    p.rows_hi = rows_hi;
+    const int nk = static_cast<int>((pr.K * esize + 127) / 128);
+    int ks = decode_ksteps(rows_hi, nk);
+    if (forced && forced->tile_k > 0) {
+      // a forced plan may choose the stage width (K elements, a multiple of 128 bytes)
+      const int want = static_cast<int>(forced->tile_k * esize / 128);
+      if (want < 1 || want > 8 || forced->tile_k * esize % 128 != 0 || decode_stages(rows_hi, want) < 2)
+        return DGL_ERR_UNSUPPORTED;
+      ks = want;
+    }
+    p.ksteps = ks;
+    p.b_plane_bytes = decode_plane_bytes(rows_hi);
+    p.stage_bytes = decode_stage_bytes(rows_hi, ks);
+    p.stages = decode_stages(rows_hi, ks);
+    p.status = ds->status;
+    const int grid = forced && forced->grid > 0 ? (forced->grid < parts ? forced->grid : parts)
+                                                : decode_grid(pr.n, ds->num_sms);
+    return launch_decode(pr.dtype, pr.out, ta, tb_lo, tb_hi, p, grid, stream) == cudaSuccess ? DGL_OK
+                                                                                            : DGL_ERR_CUDA;
   }
 
   CUtensorMap ta, tb, tc;
-  if (!encode_operand_map(&ta, pr.A, e4m3, pr.K, pr.m, plan.tile_m) ||
-      !encode_operand_map(&tb, pr.B, e4m3, pr.K, pr.n, plan.tile_n))
+  if (!cached_operand_map(&ta, pr.A, e4m3, pr.K, pr.m, plan.tile_m) ||
+      !cached_operand_map(&tb, pr.B, e4m3, pr.K, pr.n, plan.tile_n))
     return DGL_ERR_CUDA;
   const bool f32 = pr.out == DGL_OUT_F32;
   const bool c_tma = aligned(pr.C, 16) && (pr.N * (f32 ? 4 : 2)) % 16 == 0;
   std::memset(&tc, 0, sizeof(tc));
-  if (c_tma && !encode_output_map(&tc, pr.C, f32, pr.n, pr.m, pr.N)) return DGL_ERR_CUDA;
+  if (c_tma && !cached_output_map(&tc, pr.C, f32, pr.n, pr.m, pr.N)) return DGL_ERR_CUDA;
   TcParams p;
   p.C = pr.C;
   p.ldc = pr.N;

@@ -26,16 +26,21 @@ struct TcParams {
   int* status;          // device status word
 };
 
-// Decode (m <= 16) kernel parameters.
+// Decode (m <= 16) kernel parameters.  A and B are read through tensor maps.
 struct DecodeParams {
-  const uint8_t* A;     // m rows, row pitch row_bytes
-  const uint8_t* B;     // n rows, row pitch row_bytes
   const float* sa;
   const float* sb;
   void* C;
   int64_t ldc;
   int m, n;
   int row_bytes;        // K * element size
+  int parts;            // B rows are cut into this many balanced parts
+  int rows_hi;          // ceil(n / parts): parts of this size use the second B map
+  int stages;           // ring depth
+  int ksteps;           // 128-byte K steps per stage
+  int b_plane_bytes;    // one B box: rows_hi rounded up to 8, x 128 bytes
+  int stage_bytes;      // ksteps x (A box (2 KB) + B box)
+  int* status;          // device status word
 };
 
 __host__ __device__ inline void tile_coords(int tile, int tiles_m, int tiles_n, int group_m, int& mb, int& nb) {

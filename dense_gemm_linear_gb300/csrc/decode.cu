@@ -7,11 +7,13 @@ namespace dgl {
 namespace {
 
 template <bool FP8, bool OUT_F32>
-cudaError_t launch_one(const DecodeParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb_lo, const CUtensorMap& tb_hi,
+                       const DecodeParams& p, int grid, cudaStream_t stream) {
   auto kern = decode_gemm_kernel<FP8, OUT_F32>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DEC_SMEM_BYTES);
+  static std::atomic<uint64_t> attr_done{0};  // one bit per device
+  cudaError_t e = set_smem_attr_once(kern, DEC_SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;
-  kern<<<grid, DEC_THREADS, DEC_SMEM_BYTES, stream>>>(p);
+  kern<<<grid, DEC_THREADS, DEC_SMEM_BYTES, stream>>>(ta, tb_lo, tb_hi, p);
   return cudaGetLastError();
 }
 
@@ -27,10 +29,14 @@ __global__ void zero_fill_kernel(T* C, int64_t ldc, int m, int n) {
 
 }  // namespace
 
-cudaError_t launch_decode(int dtype, int out, const DecodeParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_decode(int dtype, int out, const CUtensorMap& ta, const CUtensorMap& tb_lo,
+                          const CUtensorMap& tb_hi, const DecodeParams& p, int grid, cudaStream_t stream) {
   const bool f32 = out == 1;
-  if (dtype == 1) return f32 ? launch_one<true, true>(p, grid, stream) : launch_one<true, false>(p, grid, stream);
-  return f32 ? launch_one<false, true>(p, grid, stream) : launch_one<false, false>(p, grid, stream);
+  if (dtype == 1)
+    return f32 ? launch_one<true, true>(ta, tb_lo, tb_hi, p, grid, stream)
+               : launch_one<true, false>(ta, tb_lo, tb_hi, p, grid, stream);
+  return f32 ? launch_one<false, true>(ta, tb_lo, tb_hi, p, grid, stream)
+             : launch_one<false, false>(ta, tb_lo, tb_hi, p, grid, stream);
 }
 
 cudaError_t launch_zero_fill(int out, void* C, int64_t ldc, int m, int n, cudaStream_t stream) {

@@ -5,19 +5,26 @@
 // intensity is about m flop per byte of B ("Gemm Optimization" guide,
 // section 8.3: small M is memory-bound).
 //
-// Design: no tensor-memory pipeline at all.  Each CTA owns a contiguous,
-// balanced range of B rows (n / grid rows, any remainder spread one row at a
-// time) and all 16 warps split K.  A lane loads 16 bytes of one B row per
-// 64-byte chunk (8 rows x 64 bytes per warp load) with non-allocating
-// streaming loads, and feeds them to mma.sync (m16n8k16 bf16 or m16n8k32
-// E4M3, fp32 accumulate) with the m <= 16 rows of A as the 16-row operand.
-// Because a dot product may visit k in any order, the 16 bytes a lane holds
-// are assigned to the instruction's k slots by a fixed permutation, and the
-// lane's A fragment is loaded with the same permutation: the 16 bytes of A
-// rows g and g+8 at the same byte offset.  The per-warp partial sums of each
-// 8-row group are reduced across warps through shared memory in fixed warp
-// order (deterministic), then scaled (E4M3), rounded and stored with
-// consecutive threads on consecutive columns of C.
+// Design: a TMA streaming pipeline with the operand roles swapped.
+//   * B's rows are cut into P balanced parts (each floor(n/P) or ceil(n/P)
+//     rows, at most 128); a CTA walks parts blockIdx.x, +gridDim.x, ...
+//   * warp 0 streams each part through a shared-memory ring of ~192 KB.  A
+//     stage holds `ks` consecutive 128-byte steps of K ("planes"): per plane
+//     one TMA box of the part's B rows and one box of A's m rows (bytes past
+//     K arrive as zeros), both with the 128-byte swizzle.  The planes' loads
+//     go out back to back so adjacent pieces of each B row reach the memory
+//     system together.
+//   * warp 1 issues tcgen05.mma with the part's B rows as the 128-row operand
+//     and A's 16 rows as the N = 16 operand: D[row of B][row of A] accumulates
+//     in tensor memory (two 16-column buffers, alternating by part).  The MMA
+//     is asynchronous, so no warp waits on a chain of dependent products and
+//     the stream is limited only by memory.  Rows of either operand past its
+//     box (B rows past the part, A rows past m) read whatever the ring holds
+//     there; each feeds only its own row or column of D, which is never
+//     stored.
+//   * warps 2-5 read D (lane = row of B, 16 columns = rows of A), scale
+//     (E4M3), round and store C[i][j]: for each i the warp's 32 lanes write 32
+//     consecutive columns.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -28,116 +35,204 @@
 
 namespace dgl {
 
-constexpr int DEC_WARPS = 16;
-constexpr int DEC_THREADS = DEC_WARPS * 32;
-constexpr int DEC_BATCH = 8;        // 64-byte chunks per warp per batch (one 16-byte load per lane each)
-constexpr int DEC_BLOCK_GROUPS = 16;  // 8-row groups reduced per shared-memory pass (128 rows)
-constexpr int DEC_SMEM_BYTES = DEC_BLOCK_GROUPS * DEC_WARPS * 128 * 4;
+constexpr int DEC_MAX_ROWS = 128;                  // rows of B per part (the MMA's M)
+constexpr int DEC_THREADS = 192;                   // producer, MMA, 4 epilogue warps
+constexpr int DEC_MAX_STAGES = 32;
+constexpr int DEC_RING_BYTES = 196608;             // 192 KB of stages
+// The 128-row MMA operand of the ring's last plane reaches up to 16 KB past
+// that plane's start; the slack keeps every such read inside the allocation.
+constexpr int DEC_SLACK_BYTES = 16384;
+constexpr int DEC_SMEM_BYTES = 1024 + DEC_RING_BYTES + DEC_SLACK_BYTES + 8 * (2 * DEC_MAX_STAGES + 5) + 8;
+constexpr int DEC_A_BOX_BYTES = 16 * 128;
 
-__device__ __forceinline__ void mma_bf16_m16n8k16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                                  uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void mma_e4m3_m16n8k32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                                  uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+// Row range of part `part` of n rows cut into `parts` balanced pieces.
+__device__ __forceinline__ void part_rows(int part, int parts, int n, int& r0, int& r1) {
+  r0 = static_cast<int>(static_cast<int64_t>(part) * n / parts);
+  r1 = static_cast<int>(static_cast<int64_t>(part + 1) * n / parts);
 }
 
 template <bool FP8, bool OUT_F32>
-__global__ void __launch_bounds__(DEC_THREADS, 1) decode_gemm_kernel(const DecodeParams p) {
-  extern __shared__ float red[];  // [DEC_BLOCK_GROUPS][DEC_WARPS][16 rows of A][8 rows of B]
+__global__ void __launch_bounds__(DEC_THREADS, 1)
+    decode_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB_lo,
+                       const __grid_constant__ CUtensorMap tmB_hi, const DecodeParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + DEC_RING_BYTES + DEC_SLACK_BYTES);
+  uint64_t* empty = full + DEC_MAX_STAGES;
+  uint64_t* tfull = empty + DEC_MAX_STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  const int stages = p.stages;
+  const int stage_bytes = p.stage_bytes;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int g = lane >> 2;  // A row (and B row within the 8-row group)
-  const int t = lane & 3;   // 16-byte slot within a 64-byte chunk
 
-  const int64_t r_begin = static_cast<int64_t>(blockIdx.x) * p.n / gridDim.x;
-  const int64_t r_end = static_cast<int64_t>(blockIdx.x + 1) * p.n / gridDim.x;
-
-  const int nchunks = (p.row_bytes + 63) >> 6;
-  const int cpw = (nchunks + DEC_WARPS - 1) / DEC_WARPS;
-  const int c_begin = warp * cpw;
-  const int c_end = min(nchunks, c_begin + cpw);
-  const int nbatches = c_end > c_begin ? (c_end - c_begin + DEC_BATCH - 1) / DEC_BATCH : 0;
-
-  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  uint4 xa[DEC_BATCH], ya[DEC_BATCH];
-  auto load_a = [&](int cb) {
-#pragma unroll
-    for (int u = 0; u < DEC_BATCH; ++u) {
-      const int c = cb + u;
-      const int off = c * 64 + t * 16;
-      const bool ok = c < c_end && off < p.row_bytes;
-      xa[u] = (ok && g < p.m) ? ldg_v4(p.A + static_cast<int64_t>(g) * p.row_bytes + off) : zero;
-      ya[u] = (ok && g + 8 < p.m) ? ldg_v4(p.A + static_cast<int64_t>(g + 8) * p.row_bytes + off) : zero;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
     }
-  };
-  if (nbatches == 1) load_a(c_begin);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);
+    }
+    mbar_init(drain, 1);
+    fence_mbarrier_init();
+    fence_proxy_async_shared();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 32);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
 
-  for (int64_t blk = r_begin; blk < r_end; blk += 8 * DEC_BLOCK_GROUPS) {
-    const int64_t blk_end = min(r_end, blk + 8 * DEC_BLOCK_GROUPS);
-    const int ngroups = static_cast<int>((blk_end - blk + 7) >> 3);
-    for (int gi = 0; gi < ngroups; ++gi) {
-      const int64_t row = blk + gi * 8 + g;
-      const bool row_ok = row < blk_end;
-      const uint8_t* brow = p.B + row * p.row_bytes;
-      float acc0[4] = {0.f, 0.f, 0.f, 0.f};
-      float acc1[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int b = 0; b < nbatches; ++b) {
-        const int cb = c_begin + b * DEC_BATCH;
-        if (nbatches > 1) load_a(cb);
-        uint4 rb[DEC_BATCH];
-#pragma unroll
-        for (int u = 0; u < DEC_BATCH; ++u) {
-          const int c = cb + u;
-          const int off = c * 64 + t * 16;
-          rb[u] = (row_ok && c < c_end && off < p.row_bytes) ? ldg_stream_v4(brow + off) : zero;
-        }
-#pragma unroll
-        for (int u = 0; u < DEC_BATCH; ++u) {
-          float(&acc)[4] = (u & 1) ? acc1 : acc0;
-          if constexpr (FP8) {
-            mma_e4m3_m16n8k32(acc, xa[u].x, ya[u].x, xa[u].y, ya[u].y, rb[u].x, rb[u].y);
-            mma_e4m3_m16n8k32(acc, xa[u].z, ya[u].z, xa[u].w, ya[u].w, rb[u].z, rb[u].w);
-          } else {
-            mma_bf16_m16n8k16(acc, xa[u].x, ya[u].x, xa[u].y, ya[u].y, rb[u].x, rb[u].y);
-            mma_bf16_m16n8k16(acc, xa[u].z, ya[u].z, xa[u].w, ya[u].w, rb[u].z, rb[u].w);
+  const int nk = (p.row_bytes + 127) >> 7;   // 128-byte steps of K
+  const int ks = p.ksteps;                    // planes per stage
+  const int b_plane = p.b_plane_bytes;        // one B box, rows rounded up to 8, x 128 bytes
+  const int a_bytes = ks * DEC_A_BOX_BYTES;   // A planes first, then B planes
+  int fail = 0;
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB_lo);
+      tma_prefetch_desc(&tmB_hi);
+      const uint64_t pol_a = l2_policy_evict_last();
+      const uint64_t pol_b = l2_policy_evict_first();
+      const int kstep = FP8 ? 128 : 64;  // elements per 128 bytes
+      uint32_t stage = 0, phase = 0;
+      int64_t issued = 0;
+      for (int part = blockIdx.x; part < p.parts && !fail; part += gridDim.x) {
+        int r0, r1;
+        part_rows(part, p.parts, p.n, r0, r1);
+        const CUtensorMap* mb = (r1 - r0) == p.rows_hi ? &tmB_hi : &tmB_lo;
+        const uint32_t tx = (p.m + (r1 - r0)) * 128;  // A box of m rows + B box of the part's rows
+        for (int kb0 = 0; kb0 < nk; kb0 += ks) {
+          if (!mbar_wait(&empty[stage], phase ^ 1)) {
+            fail = STATUS_TIMEOUT_PRODUCER;
+            break;
+          }
+          const int planes = min(ks, nk - kb0);
+          uint8_t* sbase = ring + stage * stage_bytes;
+          mbar_arrive_expect_tx(&full[stage], tx * planes);
+          for (int j = 0; j < planes; ++j) {
+            tma_load_2d(sbase + j * DEC_A_BOX_BYTES, &tmA, &full[stage], (kb0 + j) * kstep, 0, pol_a);
+            tma_load_2d(sbase + a_bytes + j * b_plane, mb, &full[stage], (kb0 + j) * kstep, r0, pol_b);
+          }
+          ++issued;
+          if (++stage == static_cast<uint32_t>(stages)) {
+            stage = 0;
+            phase ^= 1;
           }
         }
       }
-      // accumulator fragment: d0 (g, 2t), d1 (g, 2t+1), d2 (g+8, 2t), d3 (g+8, 2t+1)
-      float* dst = red + (gi * DEC_WARPS + warp) * 128;
-      dst[g * 8 + 2 * t] = acc0[0] + acc1[0];
-      dst[g * 8 + 2 * t + 1] = acc0[1] + acc1[1];
-      dst[(g + 8) * 8 + 2 * t] = acc0[2] + acc1[2];
-      dst[(g + 8) * 8 + 2 * t + 1] = acc0[3] + acc1[3];
+      const int64_t first = issued > stages ? issued - stages : 0;
+      for (int64_t q = first; q < issued; ++q)
+        if (!mbar_wait(&full[q % stages], static_cast<uint32_t>((q / stages) & 1))) fail |= STATUS_TIMEOUT_DRAIN;
     }
-    __syncthreads();
-    const int ncols = static_cast<int>(blk_end - blk);
-    for (int idx = threadIdx.x; idx < p.m * ncols; idx += DEC_THREADS) {
-      const int i = idx / ncols;
-      const int c = idx - i * ncols;
-      const float* src = red + ((c >> 3) * DEC_WARPS) * 128 + i * 8 + (c & 7);
-      float s = 0.f;
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f32acc(FP8 ? 0u : 1u, 128, 16);
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool issued_any = false;
+      for (int part = blockIdx.x; part < p.parts && !fail; part += gridDim.x) {
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1)) {
+          fail = STATUS_TIMEOUT_MMA;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + acc * 16;
+        for (int kb0 = 0; kb0 < nk; kb0 += ks) {
+          if (!mbar_wait(&full[stage], phase)) {
+            fail = STATUS_TIMEOUT_MMA;
+            break;
+          }
+          tc_fence_after_sync();
+          const int planes = min(ks, nk - kb0);
+          const uint32_t sbase = smem_u32(ring + stage * stage_bytes);
+          for (int j = 0; j < planes; ++j) {
+            const uint32_t w_addr = sbase + a_bytes + j * b_plane;   // B rows: the 128-row operand
+            const uint32_t x_addr = sbase + j * DEC_A_BOX_BYTES;     // A rows: the 16-row operand
 #pragma unroll
-      for (int w = 0; w < DEC_WARPS; ++w) s += src[w * 128];
-      const int64_t col = blk + c;
-      if constexpr (FP8) s = (s * p.sa[i]) * p.sb[col];
-      if constexpr (OUT_F32)
-        static_cast<float*>(p.C)[i * p.ldc + col] = s;
-      else
-        static_cast<__nv_bfloat16*>(p.C)[i * p.ldc + col] = __float2bfloat16_rn(s);
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t wd = smem_desc_sw128(w_addr + 32 * k);
+              const uint64_t xd = smem_desc_sw128(x_addr + 32 * k);
+              const uint32_t accumulate = (kb0 | j | k) != 0;
+              if constexpr (FP8)
+                umma_e4m3(d_tmem, wd, xd, idesc, accumulate);
+              else
+                umma_bf16(d_tmem, wd, xd, idesc, accumulate);
+            }
+          }
+          issued_any = true;
+          umma_commit(&empty[stage]);
+          if (++stage == static_cast<uint32_t>(stages)) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (fail) break;
+        umma_commit(&tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      if (issued_any) {
+        umma_commit(drain);
+        if (!mbar_wait(drain, 0)) fail |= STATUS_TIMEOUT_DRAIN;
+      }
     }
-    __syncthreads();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lanes 32q .. 32q+31: rows 32q .. 32q+31 of the part
+    uint32_t acc = 0, acc_phase = 0;
+    for (int part = blockIdx.x; part < p.parts; part += gridDim.x) {
+      int r0, r1;
+      part_rows(part, p.parts, p.n, r0, r1);
+      const bool ready = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase));
+      if (!ready) {
+        fail = STATUS_TIMEOUT_EPILOGUE;
+        break;
+      }
+      tc_fence_after_sync();
+      uint32_t r[16];
+      tmem_ld_32x32b_x16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * 16, r);
+      tmem_ld_wait();
+      reg_fence16(r);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      const int col = r0 + q * 32 + lane;   // column of C = row of B
+      if (col < r1) {
+        float sbv = 1.0f;
+        if constexpr (FP8) sbv = p.sb[col];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          if (i < p.m) {
+            float v = __uint_as_float(r[i]);
+            if constexpr (FP8) v = (v * p.sa[i]) * sbv;
+            if constexpr (OUT_F32)
+              static_cast<float*>(p.C)[static_cast<int64_t>(i) * p.ldc + col] = v;
+            else
+              static_cast<__nv_bfloat16*>(p.C)[static_cast<int64_t>(i) * p.ldc + col] = __float2bfloat16_rn(v);
+          }
+        }
+      }
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+
+  if (fail) atomicOr(p.status, fail);
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, 32);
   }
 }
 

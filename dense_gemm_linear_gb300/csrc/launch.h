@@ -6,7 +6,22 @@
 
 #include "common.cuh"
 
+#include <atomic>
+
 namespace dgl {
+
+// Raise a kernel's dynamic shared-memory limit once per device.
+template <class Kernel>
+cudaError_t set_smem_attr_once(Kernel kern, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 // tcgen05 tile kernel.  out: 0 bf16, 1 fp32.  tile_n: 64, 128 or 256.
 // row_staging (bf16 output only): C rows are not 16-byte aligned, so the
@@ -16,7 +31,10 @@ cudaError_t launch_tc_bf16(int out, int tile_n, bool row_staging, const CUtensor
                            const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_tc_e4m3(int out, int tile_n, bool row_staging, const CUtensorMap& ta, const CUtensorMap& tb,
                            const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_decode(int dtype, int out, const DecodeParams& p, int grid, cudaStream_t stream);
+// Decode kernel: ta = A map (16-row box), tb_lo / tb_hi = B maps whose box
+// heights are the two part sizes floor(n/parts) and ceil(n/parts).
+cudaError_t launch_decode(int dtype, int out, const CUtensorMap& ta, const CUtensorMap& tb_lo,
+                          const CUtensorMap& tb_hi, const DecodeParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_zero_fill(int out, void* C, int64_t ldc, int m, int n, cudaStream_t stream);
 
 }  // namespace dgl

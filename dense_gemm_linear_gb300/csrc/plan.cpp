@@ -106,25 +106,49 @@ void fill_tc_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int
   out->grid = grid;
 }
 
-int decode_grid(int64_t n, int num_sms) {
-  const int64_t groups = (n + 7) / 8;
-  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(groups, num_sms)));
+int decode_parts(int64_t n, int num_sms) {
+  // balanced parts of at most 128 rows, a multiple of the SM count when n allows
+  const int64_t need = (n + 127) / 128;
+  const int64_t waves = (need + num_sms - 1) / num_sms;
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(n, waves * num_sms)));
 }
+
+int decode_grid(int64_t n, int num_sms) { return std::min(decode_parts(n, num_sms), num_sms); }
 
 void fill_decode_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int num_sms, dgl_plan_info* out) {
   *out = dgl_plan_info{};
   out->path = DGL_PATH_DECODE;
   out->tile_m = 16;
-  out->tile_n = 8;
-  out->tile_k = dtype == DGL_DTYPE_E4M3 ? 64 : 32;
-  out->stages = 1;
+  out->tile_n = static_cast<int32_t>((n + decode_parts(n, num_sms) - 1) / decode_parts(n, num_sms));
+  out->tile_k = dtype == DGL_DTYPE_E4M3 ? 128 : 64;
   out->cta_group = 1;
   out->grid = decode_grid(n, num_sms);
-  out->num_tiles = static_cast<int32_t>(std::min<int64_t>((n + 7) / 8, INT32_MAX));
+  out->num_tiles = decode_parts(n, num_sms);
+  const int nk = static_cast<int>((K * (dtype == DGL_DTYPE_E4M3 ? 1 : 2) + 127) / 128);
+  const int ks = decode_ksteps(out->tile_n, nk);
+  out->tile_k = ks * (dtype == DGL_DTYPE_E4M3 ? 128 : 64);
+  out->stages = decode_stages(out->tile_n, ks);
   out->tile_eff = static_cast<double>(m) / 16.0;
-  out->wq_eff = 1.0;
-  out->dim_eff = out->tile_eff;
+  out->wq_eff = static_cast<double>(out->num_tiles) /
+                (static_cast<double>((out->num_tiles + out->grid - 1) / out->grid) * out->grid);
+  out->dim_eff = out->tile_eff * out->wq_eff;
   out->est_us = operand_bytes(dtype, out_dtype, m, n, K) / (kHbmGBs * 1e3) + kLaunchUs;
+}
+
+int decode_plane_bytes(int rows_hi) { return (rows_hi + 7) / 8 * 8 * 128; }
+
+int decode_stage_bytes(int rows_hi, int ksteps) { return ksteps * (2048 + decode_plane_bytes(rows_hi)); }
+
+int decode_stages(int rows_hi, int ksteps) {
+  const int s = 196608 / decode_stage_bytes(rows_hi, ksteps);
+  return s < 32 ? s : 32;
+}
+
+int decode_ksteps(int rows_hi, int nk) {
+  // the widest stage that still leaves at least four in the ring
+  int ks = 8;
+  while (ks > 1 && decode_stages(rows_hi, ks) < 4) ks >>= 1;
+  return ks < nk ? ks : (nk > 0 ? nk : 1);
 }
 
 void choose_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int num_sms, dgl_plan_info* out) {

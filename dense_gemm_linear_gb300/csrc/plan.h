@@ -17,7 +17,12 @@ bool tc_supported_tile(int tile_m, int tile_n);
 void fill_tc_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int tile_m, int tile_n, int num_sms,
                   dgl_plan_info* out);
 void fill_decode_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int num_sms, dgl_plan_info* out);
+int decode_parts(int64_t n, int num_sms);
 int decode_grid(int64_t n, int num_sms);
+int decode_plane_bytes(int rows_hi);               // one B box: rows_hi rounded up to 8, x 128 bytes
+int decode_stage_bytes(int rows_hi, int ksteps);   // ksteps x (16-row A box + B box)
+int decode_stages(int rows_hi, int ksteps);        // ring depth in 192 KB, at most 32
+int decode_ksteps(int rows_hi, int nk);            // 128-byte K steps per stage
 void choose_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int num_sms, dgl_plan_info* out);
 
 }  // namespace dgl

@@ -3,6 +3,8 @@
 // translation units.
 #pragma once
 
+#include <atomic>
+
 #include "launch.h"
 #include "tc_gemm.cuh"
 
@@ -13,7 +15,8 @@ cudaError_t tc_launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CU
                           int grid, cudaStream_t stream) {
   using Cfg = TcConfig<BN, FP8, OUT_F32, ROWSTG>;
   auto kern = tc_gemm_kernel<Cfg>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+  static std::atomic<uint64_t> attr_done{0};  // one bit per device
+  cudaError_t e = set_smem_attr_once(kern, Cfg::SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;
   kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(ta, tb, tc, p);
   return cudaGetLastError();

@@ -121,6 +121,17 @@ def test_decode_path(dtype, m, n):
     _full(case, guard_rows=2, pad_cols=3)
 
 
+@pytest.mark.parametrize("ks", [1, 2, 4, 8])
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_decode_forced_stage_widths(ks, dtype):
+    """Every decode stage width (128-byte K steps per ring stage), with a K tail
+    that leaves the last stage partly filled."""
+    k = 1040 if dtype == "bf16" else 2080
+    case = make_case(dtype, 5, 777, k, out="f32", dist="fp8" if dtype == "fp8" else "normal")
+    kstep = 64 if dtype == "bf16" else 128
+    _full(case, plan=dgl.PlanInfo(path=dgl.PATH_DECODE, tile_k=ks * kstep), guard_rows=1, pad_cols=2)
+
+
 @pytest.mark.parametrize("k", [16, 48, 272, 4104, 8192])
 def test_decode_k_extents(k):
     _full(make_case("bf16", 7, 300, k, out="f32"))
