@@ -14,6 +14,7 @@ TFLOP/s, summed over ranks (each rank runs the workload independently).
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import os
 import statistics
@@ -47,6 +48,8 @@ def parse_args():
     ap.add_argument("--workload", default="ragged", choices=sorted(WORKLOAD_TEXT))
     ap.add_argument("--shape", default=None,
                     help="single GEMM m,n,k[,bf16|fp8[,bf16|f32]] instead of a workload (profiling)")
+    ap.add_argument("--tile", default=None,
+                    help="force the tcgen05 tile MxN (e.g. 256x256) instead of the planner's choice (profiling)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-macs", type=float, default=4e9,
                     help="multiply-adds of the bounded CPU-oracle sample")
@@ -248,8 +251,19 @@ def main():
         C = torch.empty((c.m, c.n), dtype=torch.float32 if c.out == "f32" else torch.bfloat16, device=dev)
         ops.append((c, A, B, sa, sb, C, out_dtype))
 
+    forced = None
+    if args.tile is not None:
+        tm_, tn_ = (int(v) for v in args.tile.lower().split("x"))
+        forced = dgl.PlanInfo(path=dgl.PATH_TC, tile_m=tm_, tile_n=tn_)
+
     def make_call(c, A, B, sa, sb, C, out_dtype):
-        if c.dtype == "bf16":
+        if forced is not None:
+            dt = dgl.DTYPE_BF16 if c.dtype == "bf16" else dgl.DTYPE_E4M3
+            args_ = (dt, A.data_ptr(), B.data_ptr(), sa.data_ptr() if sa is not None else None,
+                     sb.data_ptr() if sb is not None else None, C.data_ptr(), c.m, c.n, c.K, c.m, c.n, out_dtype,
+                     ctypes.byref(forced), s_handle)
+            fn = lib.dgl_gemm_planned
+        elif c.dtype == "bf16":
             args_ = (A.data_ptr(), B.data_ptr(), C.data_ptr(), c.m, c.n, c.K, c.m, c.n, out_dtype, s_handle)
             fn = lib.dgl_gemm_bf16
         else:
@@ -266,11 +280,13 @@ def main():
     calls = [make_call(*o) for o in ops]
     plans = [dgl.dgl_plan(0 if c.dtype == "bf16" else 1, c.m, c.n, c.K,
                           dgl.OUT_F32 if c.out == "f32" else dgl.OUT_BF16) for c in cases]
+    if forced is not None:
+        plans = [forced for _ in cases]
 
     def kernel_name(c, p):
         if p.path == dgl.PATH_DECODE:
             return f"decode_gemm_kernel<{c.dtype}>"
-        return f"tc_gemm_kernel<{c.dtype}, 128x{p.tile_n}>"
+        return f"tc_gemm_kernel<{c.dtype}, {p.tile_m}x{p.tile_n}>"
 
     knames = [kernel_name(c, p) for c, p in zip(cases, plans)]
     flops = [2.0 * c.m * c.n * c.K for c in cases]

@@ -290,8 +290,10 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream) {
   }
 
   CUtensorMap ta, tb, tc;
-  if (!cached_operand_map(&ta, pr.A, e4m3, pr.K, pr.m, plan.tile_m) ||
-      !cached_operand_map(&tb, pr.B, e4m3, pr.K, pr.n, plan.tile_n))
+  // each CTA of a pair loads its own 128 rows of A and half the tile's rows of B
+  const int cg = plan.cta_group == 2 ? 2 : 1;
+  if (!cached_operand_map(&ta, pr.A, e4m3, pr.K, pr.m, 128) ||
+      !cached_operand_map(&tb, pr.B, e4m3, pr.K, pr.n, plan.tile_n / cg))
     return DGL_ERR_CUDA;
   const bool f32 = pr.out == DGL_OUT_F32;
   const bool c_tma = aligned(pr.C, 16) && (pr.N * (f32 ? 4 : 2)) % 16 == 0;
@@ -312,11 +314,16 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream) {
   p.group_m = 16;
   p.c_tma = c_tma ? 1 : 0;
   p.status = ds->status;
-  const int grid = plan.grid > 0 ? (plan.grid < p.num_tiles ? plan.grid : p.num_tiles) : p.num_tiles;
+  // grid counts CTAs; a pair per tile when cg == 2
+  int grid = plan.grid > 0 ? plan.grid : p.num_tiles * cg;
+  if (grid > p.num_tiles * cg) grid = p.num_tiles * cg;
+  grid = grid / cg * cg;
+  if (grid < cg) grid = cg;
   if (ds->smem_optin < 232448) return DGL_ERR_UNSUPPORTED;  // every variant is sized for 227 KB
   const bool row_staging = !c_tma && !f32;
-  const cudaError_t e = e4m3 ? launch_tc_e4m3(pr.out, plan.tile_n, row_staging, ta, tb, tc, p, grid, stream)
-                             : launch_tc_bf16(pr.out, plan.tile_n, row_staging, ta, tb, tc, p, grid, stream);
+  const cudaError_t e =
+      e4m3 ? launch_tc_e4m3(pr.out, plan.tile_m, plan.tile_n, row_staging, ta, tb, tc, p, grid, stream)
+           : launch_tc_bf16(pr.out, plan.tile_m, plan.tile_n, row_staging, ta, tb, tc, p, grid, stream);
   return e == cudaSuccess ? DGL_OK : DGL_ERR_CUDA;
 }
 

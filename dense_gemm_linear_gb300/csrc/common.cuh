@@ -11,6 +11,7 @@ enum : int {
   STATUS_TIMEOUT_MMA = 2,
   STATUS_TIMEOUT_EPILOGUE = 4,
   STATUS_TIMEOUT_DRAIN = 8,
+  STATUS_TMEM_MISMATCH = 16,  // a CTA pair's tensor-memory allocations differ
 };
 
 // Persistent tcgen05 tile kernel: problem and schedule.

@@ -23,13 +23,15 @@ cudaError_t set_smem_attr_once(Kernel kern, int bytes, std::atomic<uint64_t>& do
   return e;
 }
 
-// tcgen05 tile kernel.  out: 0 bf16, 1 fp32.  tile_n: 64, 128 or 256.
+// tcgen05 tile kernel.  out: 0 bf16, 1 fp32.  tile_m: 128 (one CTA per tile)
+// or 256 (a CTA pair per tile, launched as clusters of two).  tile_n: 64, 128
+// or 256.
 // row_staging (bf16 output only): C rows are not 16-byte aligned, so the
 // epilogue stages whole rows and writes each row's aligned body in bulk.
 // tc: tensor map of C for TMA stores (used when p.c_tma is set).
-cudaError_t launch_tc_bf16(int out, int tile_n, bool row_staging, const CUtensorMap& ta, const CUtensorMap& tb,
+cudaError_t launch_tc_bf16(int out, int tile_m, int tile_n, bool row_staging, const CUtensorMap& ta, const CUtensorMap& tb,
                            const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_tc_e4m3(int out, int tile_n, bool row_staging, const CUtensorMap& ta, const CUtensorMap& tb,
+cudaError_t launch_tc_e4m3(int out, int tile_m, int tile_n, bool row_staging, const CUtensorMap& ta, const CUtensorMap& tb,
                            const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t stream);
 // Decode kernel: ta = A map (16-row box), tb_lo / tb_hi = B maps whose box
 // heights are the two part sizes floor(n/parts) and ceil(n/parts).

@@ -44,16 +44,20 @@
 
 namespace dgl {
 
-// Shared-memory ring depth for a tile width: about 192 KB of stages when the
-// epilogue stages 32 x 32 tiles, fewer when it stages whole rows.
-constexpr int tc_ring_stages(int bn, bool row_staging) {
-  return row_staging ? (bn == 64 ? 8 : (bn == 128 ? 5 : 3)) : (bn == 64 ? 8 : (bn == 128 ? 6 : 4));
+// Ring depth that fills the 227 KB per-CTA budget left by the epilogue's
+// staging area (at most 8 stages).
+constexpr int tc_ring_stages(int stage_bytes, int staging_bytes) {
+  const int s = (232448 - 1024 - staging_bytes - 512) / stage_bytes;
+  return s < 8 ? s : 8;
 }
 
-template <int BN_, bool FP8_, bool OUT_F32_, bool ROWSTG_>
+template <int BN_, bool FP8_, bool OUT_F32_, bool ROWSTG_, int CG_ = 1>
 struct TcConfig {
-  static constexpr int BM = 128;
-  static constexpr int BN = BN_;
+  static constexpr int CG = CG_;                        // CTAs per MMA: 1, or 2 for a CTA pair (M = 256)
+  static constexpr int BM = 128;                        // rows of C per CTA
+  static constexpr int TILE_M = BM * CG;                // rows of C per tile
+  static constexpr int BN = BN_;                        // columns of C per tile
+  static constexpr int B_ROWS = BN / CG;                // rows of B each CTA loads per stage
   static constexpr bool FP8 = FP8_;
   static constexpr bool OUT_F32 = OUT_F32_;
   // ROWSTG: bf16 C whose rows are not 16-byte aligned.  The epilogue stages
@@ -61,31 +65,35 @@ struct TcConfig {
   // of every row leaves in one bulk copy.
   static constexpr bool ROWSTG = ROWSTG_;
   static_assert(!(ROWSTG && OUT_F32), "row staging is the bf16-output path");
-  static constexpr int STAGES = tc_ring_stages(BN, ROWSTG);
+  static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair");
   static constexpr int ROW_BYTES = 128;                 // one 128-byte swizzle span of K per stage
   static constexpr int BK = FP8 ? 128 : 64;             // K elements per stage
   static constexpr int MMA_K_BYTES = 32;                // K=16 bf16 or K=32 E4M3 per instruction
   static constexpr int MMAS_PER_STAGE = ROW_BYTES / MMA_K_BYTES;
   static constexpr int A_STAGE_BYTES = BM * ROW_BYTES;
-  static constexpr int B_STAGE_BYTES = BN * ROW_BYTES;
+  static constexpr int B_STAGE_BYTES = B_ROWS * ROW_BYTES;
   static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
   static constexpr int EPI_WARPS = 8;
   static constexpr int CHUNKS = BN / 32;                // 32-column chunks per tile row
   static constexpr int CHUNKS_PER_WARP = CHUNKS / 2;    // two warps share a lane quarter
   static constexpr int OUT_BYTES = OUT_F32 ? 4 : 2;
   static constexpr int STG_ROW = 32 * OUT_BYTES;        // 32 x 32 staging row: 64 B (bf16) or 128 B (fp32)
+  static constexpr int STG_BYTES = 32 * STG_ROW;        // one 32 x 32 staging tile: 2 KB (bf16) or 4 KB (fp32)
   // whole-row staging: BN bf16 + 16 bytes of shift room; the pitch is an odd
   // multiple of 16 bytes so rows spread over the banks
   static constexpr int ROW_PITCH = BN * 2 + 16;
   static constexpr int STG_TOTAL = ROWSTG ? 4 * 32 * ROW_PITCH : EPI_WARPS * 4096;
+  static constexpr int STAGES = tc_ring_stages(STAGE_BYTES, STG_TOTAL);
   static constexpr int THREADS = 64 + EPI_WARPS * 32;
   static constexpr int TMEM_COLS = 2 * BN;              // two fp32 accumulators of BN columns
   static constexpr int BAR_BYTES = 8 * (2 * STAGES + 5) + 8 + 32;
   static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + STAGES * STAGE_BYTES + STG_TOTAL + BAR_BYTES;
   static_assert(BN == 64 || BN == 128 || BN == 256, "tile widths of the ladder");
+  static_assert(STAGES >= 3, "ring too shallow");
   static_assert((ROW_PITCH / 16) % 2 == 1, "row pitch: odd multiple of 16 bytes");
   static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation: power of two");
   static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
+  static_assert(B_STAGE_BYTES % 1024 == 0, "B stage tiles stay 1024-byte aligned");
 };
 
 // Byte offset of 16-byte unit `c16` of staging row `r`, in the layout a TMA
@@ -123,12 +131,12 @@ template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const TcParams p) {
-  constexpr int BM = Cfg::BM, BN = Cfg::BN, STAGES = Cfg::STAGES;
+  constexpr int BM = Cfg::BM, BN = Cfg::BN, STAGES = Cfg::STAGES, CG = Cfg::CG;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = sA + STAGES * Cfg::A_STAGE_BYTES;
-  uint8_t* sStg = sB + STAGES * Cfg::B_STAGE_BYTES;      // 1024-aligned: stage sizes are multiples of 8 KB
+  uint8_t* sStg = sB + STAGES * Cfg::B_STAGE_BYTES;      // 1024-aligned: stage sizes are multiples of 1 KB
   uint64_t* full = reinterpret_cast<uint64_t*>(sStg + Cfg::STG_TOTAL);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
@@ -139,15 +147,21 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // CTA pair: rank 0 (the leader) issues the MMAs and owns the barriers the
+  // MMA waits on; each CTA loads its own 128 rows of A and B_ROWS rows of B
+  // and stores its own 128 rows of C.
+  const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
+  const int cluster_id = blockIdx.x / CG;
+  const int num_clusters = gridDim.x / CG;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], 1);                // the (leader's) producer's expect-tx arrival
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], Cfg::EPI_WARPS);
+      mbar_init(&tempty[b], Cfg::EPI_WARPS * CG);
     }
     mbar_init(drain, 1);
     fence_mbarrier_init();
@@ -159,32 +173,65 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     if (p.c_tma) tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (CG == 2) {
+      tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before_sync();
-  __syncthreads();
+  if constexpr (CG == 2)
+    cluster_sync();  // barriers of both CTAs are initialised before either signals the other
+  else
+    __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
 
   int fail = 0;
+  if constexpr (CG == 2) {
+    // the leader's MMAs write this CTA's tensor memory at the leader's address
+    if (threadIdx.x == 0 && rank != 0) {
+      uint32_t leader_base;
+      asm volatile("ld.shared::cluster.u32 %0, [%1];"
+                   : "=r"(leader_base)
+                   : "r"(mapa_shared(smem_u32(tmem_slot), 0))
+                   : "memory");
+      if (leader_base != tmem_base) fail = STATUS_TMEM_MISMATCH;
+    }
+  }
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_last();
       uint32_t stage = 0, phase = 0;
       int64_t issued = 0;
-      for (int tile = blockIdx.x; tile < p.num_tiles && !fail; tile += gridDim.x) {
+      for (int tile = cluster_id; tile < p.num_tiles && !fail; tile += num_clusters) {
         int mb, nb;
         tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, mb, nb);
+        const int a_row = mb * Cfg::TILE_M + static_cast<int>(rank) * BM;
+        const int b_row = nb * BN + static_cast<int>(rank) * Cfg::B_ROWS;
         for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1)) {
+          const bool ok = mbar_wait(&empty[stage], phase ^ 1);
+          if (!ok) {
             fail = STATUS_TIMEOUT_PRODUCER;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
-          tma_load_2d(sA + stage * Cfg::A_STAGE_BYTES, &tmA, &full[stage], kb * Cfg::BK, mb * BM, pol);
-          tma_load_2d(sB + stage * Cfg::B_STAGE_BYTES, &tmB, &full[stage], kb * Cfg::BK, nb * BN, pol);
+          if constexpr (CG == 2) {
+            // Both CTAs' loads complete on the leader's barrier; the leader
+            // alone announces the pair's bytes.  A peer's bytes may land
+            // before that announcement: the transaction count goes negative
+            // for a moment and the phase still waits for the leader's arrival.
+            const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
+            if (rank == 0) mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES * CG);
+            tma_load_2d_pair(sA + stage * Cfg::A_STAGE_BYTES, &tmA, fb, kb * Cfg::BK, a_row, pol);
+            tma_load_2d_pair(sB + stage * Cfg::B_STAGE_BYTES, &tmB, fb, kb * Cfg::BK, b_row, pol);
+          } else {
+            mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
+            tma_load_2d(sA + stage * Cfg::A_STAGE_BYTES, &tmA, &full[stage], kb * Cfg::BK, a_row, pol);
+            tma_load_2d(sB + stage * Cfg::B_STAGE_BYTES, &tmB, &full[stage], kb * Cfg::BK, b_row, pol);
+          }
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -192,29 +239,35 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           }
         }
       }
-      // Copies still in flight land before this CTA may exit: wait for the
-      // completion of the last STAGES loads issued (already complete on the
-      // normal path).
+      // Copies still in flight land before this CTA may exit.  One CTA waits
+      // for the completion of its last STAGES loads; in a pair the loads land
+      // on the leader's barriers, so each producer waits instead for the MMA
+      // to have consumed its last STAGES stages (which implies they landed).
+      // Both are already complete on the normal path.
       const int64_t first = issued > STAGES ? issued - STAGES : 0;
       for (int64_t q = first; q < issued; ++q) {
-        if (!mbar_wait(&full[q % STAGES], static_cast<uint32_t>((q / STAGES) & 1))) fail |= STATUS_TIMEOUT_DRAIN;
+        const uint32_t par = static_cast<uint32_t>((q / STAGES) & 1);
+        const bool ok = CG == 2 ? mbar_wait(&empty[q % STAGES], par) : mbar_wait(&full[q % STAGES], par);
+        if (!ok) fail |= STATUS_TIMEOUT_DRAIN;
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f32acc(Cfg::FP8 ? 0u : 1u, BM, BN);
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc_f32acc(Cfg::FP8 ? 0u : 1u, Cfg::TILE_M, BN);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool issued_any = false;
-      for (int tile = blockIdx.x; tile < p.num_tiles && !fail; tile += gridDim.x) {
-        if (!mbar_wait(&tempty[acc], acc_phase ^ 1)) {
+      for (int tile = cluster_id; tile < p.num_tiles && !fail; tile += num_clusters) {
+        const bool ok = mbar_wait(&tempty[acc], acc_phase ^ 1);
+        if (!ok) {
           fail = STATUS_TIMEOUT_MMA;
           break;
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!mbar_wait(&full[stage], phase)) {
+          const bool ok2 = mbar_wait(&full[stage], phase);
+          if (!ok2) {
             fail = STATUS_TIMEOUT_MMA;
             break;
           }
@@ -226,26 +279,42 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             const uint64_t ad = smem_desc_sw128(a_addr + k * Cfg::MMA_K_BYTES);
             const uint64_t bd = smem_desc_sw128(b_addr + k * Cfg::MMA_K_BYTES);
             const uint32_t accumulate = (kb | k) != 0;
-            if constexpr (Cfg::FP8)
-              umma_e4m3(d_tmem, ad, bd, idesc, accumulate);
-            else
-              umma_bf16(d_tmem, ad, bd, idesc, accumulate);
+            if constexpr (CG == 2) {
+              if constexpr (Cfg::FP8)
+                umma_e4m3_pair(d_tmem, ad, bd, idesc, accumulate);
+              else
+                umma_bf16_pair(d_tmem, ad, bd, idesc, accumulate);
+            } else {
+              if constexpr (Cfg::FP8)
+                umma_e4m3(d_tmem, ad, bd, idesc, accumulate);
+              else
+                umma_bf16(d_tmem, ad, bd, idesc, accumulate);
+            }
           }
           issued_any = true;
-          umma_commit(&empty[stage]);
+          if constexpr (CG == 2)
+            umma_commit_pair_multicast(&empty[stage], 0x3);  // both CTAs' producers may refill
+          else
+            umma_commit(&empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (fail) break;
-        umma_commit(&tfull[acc]);
+        if constexpr (CG == 2)
+          umma_commit_pair_multicast(&tfull[acc], 0x3);  // both CTAs' epilogues
+        else
+          umma_commit(&tfull[acc]);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
       }
       // Every MMA this thread issued has finished before TMEM is released.
       if (issued_any) {
-        umma_commit(drain);
+        if constexpr (CG == 2)
+          umma_commit_pair_multicast(drain, 0x1);
+        else
+          umma_commit(drain);
         if (!mbar_wait(drain, 0)) fail |= STATUS_TIMEOUT_DRAIN;
       }
     }
@@ -258,7 +327,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     uint8_t* stg = Cfg::ROWSTG ? sStg + q * 32 * Cfg::ROW_PITCH : sStg + e * 4096;
     const uint32_t stg_addr = smem_u32(stg);
     uint32_t acc = 0, acc_phase = 0;
-    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+    for (int tile = cluster_id; tile < p.num_tiles; tile += num_clusters) {
       int mb, nb;
       tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, mb, nb);
       // all lanes decide together: tcgen05.ld below is warp-collective
@@ -278,7 +347,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         break;
       }
       tc_fence_after_sync();
-      const int row0 = mb * BM + q * 32;
+      const int row0 = mb * Cfg::TILE_M + static_cast<int>(rank) * BM + q * 32;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
 
       // Read this warp's whole share of the accumulator, then hand it back.
@@ -290,7 +359,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       for (int u = 0; u < CPW; ++u) reg_fence(r[u]);
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (lane == 0) {
+        if constexpr (CG == 2)
+          mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));  // the leader's MMA waits on it
+        else
+          mbar_arrive(&tempty[acc]);
+      }
 
       if constexpr (Cfg::FP8) {
         const float row_scale = (row0 + lane < p.m) ? p.sa[row0 + lane] : 0.0f;
@@ -350,17 +424,28 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           }
         }
       } else {
+        // bf16 chunks alternate between two 2 KB staging tiles, so a chunk's
+        // TMA store may still be reading one while the next chunk fills the
+        // other; fp32 chunks fill the whole 4 KB tile.
+        uint32_t buf = 0;
 #pragma unroll
         for (int u = 0; u < CPW; ++u) {
           const int col0 = nb * BN + (half * CPW + u) * 32;
-          // the previous chunk's TMA store must have read the staging tile
-          if (p.c_tma && lane == 0) bulk_wait_read0();
+          uint8_t* stg_u = stg + buf * Cfg::STG_BYTES;
+          const uint32_t stg_addr_u = stg_addr + buf * Cfg::STG_BYTES;
+          // the store that last used this staging tile has finished reading it
+          if (p.c_tma && lane == 0) {
+            if constexpr (Cfg::OUT_F32)
+              bulk_wait_read0();
+            else
+              bulk_wait_read1();
+          }
           __syncwarp();
           // this thread's row (lane) of the 32 x 32 chunk -> staging, 16 bytes at a time
           if constexpr (Cfg::OUT_F32) {
 #pragma unroll
             for (int c16 = 0; c16 < 8; ++c16)
-              sts_v4(stg_addr + stg_offset<Cfg::STG_ROW>(lane, c16), r[u][4 * c16], r[u][4 * c16 + 1],
+              sts_v4(stg_addr_u + stg_offset<Cfg::STG_ROW>(lane, c16), r[u][4 * c16], r[u][4 * c16 + 1],
                      r[u][4 * c16 + 2], r[u][4 * c16 + 3]);
           } else {
 #pragma unroll
@@ -372,7 +457,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                                                           __uint_as_float(r[u][8 * c16 + 2 * t + 1]));
                 w[t] = *reinterpret_cast<uint32_t*>(&h2);
               }
-              sts_v4(stg_addr + stg_offset<Cfg::STG_ROW>(lane, c16), w[0], w[1], w[2], w[3]);
+              sts_v4(stg_addr_u + stg_offset<Cfg::STG_ROW>(lane, c16), w[0], w[1], w[2], w[3]);
             }
           }
           // A TMA store writes whole 16-byte units of a row, so a chunk that
@@ -383,7 +468,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             fence_proxy_async_shared();
             __syncwarp();
             if (lane == 0 && row0 < p.m && col0 < p.n) {
-              tma_store_2d(&tmC, stg, col0, row0);
+              tma_store_2d(&tmC, stg_u, col0, row0);
               bulk_commit();
             }
           } else {
@@ -395,16 +480,17 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
               const int row = row0 + rr;
               if (row < p.m && col < p.n) {
                 if constexpr (Cfg::OUT_F32) {
-                  const float v = *reinterpret_cast<const float*>(stg + stg_offset<128>(rr, lane >> 2) + (lane & 3) * 4);
+                  const float v = *reinterpret_cast<const float*>(stg_u + stg_offset<128>(rr, lane >> 2) + (lane & 3) * 4);
                   static_cast<float*>(p.C)[static_cast<int64_t>(row) * p.ldc + col] = v;
                 } else {
-                  const uint16_t v = *reinterpret_cast<const uint16_t*>(stg + stg_offset<64>(rr, lane >> 3) + (lane & 7) * 2);
+                  const uint16_t v = *reinterpret_cast<const uint16_t*>(stg_u + stg_offset<64>(rr, lane >> 3) + (lane & 7) * 2);
                   reinterpret_cast<uint16_t*>(p.C)[static_cast<int64_t>(row) * p.ldc + col] = v;
                 }
               }
             }
             __syncwarp();
           }
+          if constexpr (!Cfg::OUT_F32) buf ^= 1u;
         }
       }
       acc ^= 1;
@@ -415,10 +501,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 
   if (fail) atomicOr(p.status, fail);
   tc_fence_before_sync();
-  __syncthreads();
+  if constexpr (CG == 2)
+    cluster_sync();  // neither CTA leaves while the other may still touch its memory
+  else
+    __syncthreads();
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    if constexpr (CG == 2)
+      tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
   }
 }
 

@@ -10,35 +10,62 @@
 
 namespace dgl {
 
-template <int BN, bool FP8, bool OUT_F32, bool ROWSTG>
+template <int BN, bool FP8, bool OUT_F32, bool ROWSTG, int CG>
 cudaError_t tc_launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const TcParams& p,
                           int grid, cudaStream_t stream) {
-  using Cfg = TcConfig<BN, FP8, OUT_F32, ROWSTG>;
+  using Cfg = TcConfig<BN, FP8, OUT_F32, ROWSTG, CG>;
   auto kern = tc_gemm_kernel<Cfg>;
   static std::atomic<uint64_t> attr_done{0};  // one bit per device
   cudaError_t e = set_smem_attr_once(kern, Cfg::SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;
-  kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(ta, tb, tc, p);
-  return cudaGetLastError();
+  if constexpr (CG == 1) {
+    kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(ta, tb, tc, p);
+    return cudaGetLastError();
+  } else {
+    // CTA pairs: a cluster of two CTAs per output tile
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CG;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, p);
+  }
 }
 
-template <int BN, bool FP8>
+template <int BN, bool FP8, int CG>
 cudaError_t tc_launch_bn(int out, bool row_staging, const CUtensorMap& ta, const CUtensorMap& tb,
                          const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t stream) {
-  if (out == 1) return tc_launch_one<BN, FP8, true, false>(ta, tb, tc, p, grid, stream);
-  if (row_staging) return tc_launch_one<BN, FP8, false, true>(ta, tb, tc, p, grid, stream);
-  return tc_launch_one<BN, FP8, false, false>(ta, tb, tc, p, grid, stream);
+  if (out == 1) return tc_launch_one<BN, FP8, true, false, CG>(ta, tb, tc, p, grid, stream);
+  if (row_staging) return tc_launch_one<BN, FP8, false, true, CG>(ta, tb, tc, p, grid, stream);
+  return tc_launch_one<BN, FP8, false, false, CG>(ta, tb, tc, p, grid, stream);
 }
 
 template <bool FP8>
-cudaError_t tc_launch(int out, int tile_n, bool row_staging, const CUtensorMap& ta, const CUtensorMap& tb,
+cudaError_t tc_launch(int out, int tile_m, int tile_n, bool row_staging, const CUtensorMap& ta, const CUtensorMap& tb,
                       const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t stream) {
-  switch (tile_n) {
-    case 64: return tc_launch_bn<64, FP8>(out, row_staging, ta, tb, tc, p, grid, stream);
-    case 128: return tc_launch_bn<128, FP8>(out, row_staging, ta, tb, tc, p, grid, stream);
-    case 256: return tc_launch_bn<256, FP8>(out, row_staging, ta, tb, tc, p, grid, stream);
-    default: return cudaErrorInvalidValue;
+  if (tile_m == 128) {
+    switch (tile_n) {
+      case 64: return tc_launch_bn<64, FP8, 1>(out, row_staging, ta, tb, tc, p, grid, stream);
+      case 128: return tc_launch_bn<128, FP8, 1>(out, row_staging, ta, tb, tc, p, grid, stream);
+      case 256: return tc_launch_bn<256, FP8, 1>(out, row_staging, ta, tb, tc, p, grid, stream);
+      default: return cudaErrorInvalidValue;
+    }
   }
+  if (tile_m == 256) {
+    switch (tile_n) {
+      case 128: return tc_launch_bn<128, FP8, 2>(out, row_staging, ta, tb, tc, p, grid, stream);
+      case 256: return tc_launch_bn<256, FP8, 2>(out, row_staging, ta, tb, tc, p, grid, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace dgl

@@ -78,7 +78,8 @@ def test_integer_bit_exact_all_paths(dtype, m):
 
 
 # -------------------------------------------------------------- every ladder rung, forced
-LADDER = [(dgl.PATH_TC, 128, 64), (dgl.PATH_TC, 128, 128), (dgl.PATH_TC, 128, 256)]
+LADDER = [(dgl.PATH_TC, 128, 64), (dgl.PATH_TC, 128, 128), (dgl.PATH_TC, 128, 256), (dgl.PATH_TC, 256, 128),
+          (dgl.PATH_TC, 256, 256)]
 
 
 @pytest.mark.parametrize("path,tm,tn", LADDER, ids=lambda v: str(v))
@@ -93,22 +94,22 @@ def test_forced_tile_on_shape_no_tile_divides(path, tm, tn, dtype, out):
 
 @pytest.mark.parametrize("pad,base", [(0, 0), (8, 0), (3, 0), (1, 1), (0, 1), (5, 3)])
 @pytest.mark.parametrize("out", ["bf16", "f32"])
-@pytest.mark.parametrize("tn", [64, 128, 256])
-def test_output_store_paths(pad, base, out, tn):
+@pytest.mark.parametrize("tm,tn", [(128, 64), (128, 128), (128, 256), (256, 128), (256, 256)])
+def test_output_store_paths(pad, base, out, tm, tn):
     """C pitch and base alignment select the TMA-store or the predicated-store
     epilogue; odd pitches alternate row alignment, an odd base shifts every row."""
     case = make_case("bf16", 261, 328, 200, out=out)
-    plan = dgl.PlanInfo(path=dgl.PATH_TC, tile_m=128, tile_n=tn)
+    plan = dgl.PlanInfo(path=dgl.PATH_TC, tile_m=tm, tile_n=tn)
     Cbuf, intact = gu.run(case, plan=plan, guard_rows=2, pad_cols=pad, base_offset=base)
     assert intact, "wrote outside the valid region"
     gu.assert_close_full(case, gu.host_valid(case, Cbuf))
 
 
-@pytest.mark.parametrize("grid", [1, 3, 7])
-def test_persistent_tile_loop_small_grid(grid):
-    """Fewer CTAs than tiles: each CTA walks many tiles through both accumulators."""
+@pytest.mark.parametrize("tm,grid", [(128, 1), (128, 3), (128, 7), (256, 2), (256, 6)])
+def test_persistent_tile_loop_small_grid(tm, grid):
+    """Fewer CTAs (or CTA pairs) than tiles: each walks many tiles through both accumulators."""
     case = make_case("bf16", 700, 900, 264, out="f32")
-    plan = dgl.PlanInfo(path=dgl.PATH_TC, tile_m=128, tile_n=128, grid=grid)
+    plan = dgl.PlanInfo(path=dgl.PATH_TC, tile_m=tm, tile_n=128, grid=grid)
     _full(case, plan=plan)
 
 
