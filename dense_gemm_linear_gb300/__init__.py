@@ -41,7 +41,8 @@ class PlanInfo(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32),
                 ("tile_k", ctypes.c_int32), ("stages", ctypes.c_int32), ("cta_group", ctypes.c_int32),
                 ("grid", ctypes.c_int32), ("num_tiles", ctypes.c_int32), ("tile_eff", ctypes.c_double),
-                ("wq_eff", ctypes.c_double), ("dim_eff", ctypes.c_double), ("est_us", ctypes.c_double)]
+                ("wq_eff", ctypes.c_double), ("dim_eff", ctypes.c_double), ("est_us", ctypes.c_double),
+                ("stream_k", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

@@ -6,6 +6,7 @@
 
 #include <cstdint>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <tuple>
 #include <unordered_map>
@@ -53,6 +54,45 @@ struct PlanKeyHash {
   }
 };
 std::unordered_map<PlanKey, dgl_plan_info, PlanKeyHash> g_plans;
+
+// Stream-K workspace, one per (device, stream): fp32 partial tiles and one
+// epoch flag per partial slot.  Launches on one stream run in order, so they
+// can share it; each launch gets a fresh epoch so stale flags never match.
+struct Workspace {
+  float* ws = nullptr;
+  size_t ws_bytes = 0;
+  int* flags = nullptr;
+  int nflags = 0;
+  int epoch = 0;
+};
+std::map<std::pair<int, cudaStream_t>, Workspace> g_workspaces;
+
+dgl_status acquire_workspace(int dev, cudaStream_t stream, size_t bytes, int nflags, float** ws, int** flags,
+                             int* epoch) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  Workspace& w = g_workspaces[std::make_pair(dev, stream)];
+  if (w.ws_bytes < bytes || w.nflags < nflags || w.epoch == INT32_MAX) {
+    // growing frees the old buffers, which waits for work still using them
+    if (w.ws) cudaFree(w.ws);
+    if (w.flags) cudaFree(w.flags);
+    w = Workspace{};
+    const size_t want = bytes > (size_t(24) << 20) ? bytes : (size_t(24) << 20);
+    const int want_flags = nflags > 512 ? nflags : 512;
+    if (cudaMalloc(reinterpret_cast<void**>(&w.ws), want) != cudaSuccess) return DGL_ERR_CUDA;
+    if (cudaMalloc(reinterpret_cast<void**>(&w.flags), sizeof(int) * want_flags) != cudaSuccess) {
+      cudaFree(w.ws);
+      w = Workspace{};
+      return DGL_ERR_CUDA;
+    }
+    if (cudaMemset(w.flags, 0, sizeof(int) * want_flags) != cudaSuccess) return DGL_ERR_CUDA;
+    w.ws_bytes = want;
+    w.nflags = want_flags;
+  }
+  *ws = w.ws;
+  *flags = w.flags;
+  *epoch = ++w.epoch;
+  return DGL_OK;
+}
 
 dgl_status get_device(int* dev_out, DeviceState** st_out) {
   int dev = 0;
@@ -231,7 +271,8 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream) {
       fill_decode_plan(pr.dtype, pr.out, pr.m, pr.n, pr.K, ds->num_sms, &plan);
     } else if (forced->path == DGL_PATH_TC) {
       if (!tc_supported_tile(forced->tile_m, forced->tile_n)) return DGL_ERR_UNSUPPORTED;
-      fill_tc_plan(pr.dtype, pr.out, pr.m, pr.n, pr.K, forced->tile_m, forced->tile_n, ds->num_sms, &plan);
+      fill_tc_plan(pr.dtype, pr.out, pr.m, pr.n, pr.K, forced->tile_m, forced->tile_n, ds->num_sms, &plan,
+                   forced->stream_k ? 1 : 0);
     } else {
       return DGL_ERR_UNSUPPORTED;
     }
@@ -316,9 +357,24 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream) {
   p.status = ds->status;
   // grid counts CTAs; a pair per tile when cg == 2
   int grid = plan.grid > 0 ? plan.grid : p.num_tiles * cg;
-  if (grid > p.num_tiles * cg) grid = p.num_tiles * cg;
+  if (!plan.stream_k && grid > p.num_tiles * cg) grid = p.num_tiles * cg;
+  if (grid > ds->num_sms) grid = ds->num_sms;
   grid = grid / cg * cg;
   if (grid < cg) grid = cg;
+  p.workers = grid / cg;
+  p.dp_tiles = p.num_tiles;
+  p.sk_units = 0;
+  p.ws = nullptr;
+  p.flags = nullptr;
+  p.epoch = 0;
+  if (plan.stream_k && p.num_tiles % p.workers != 0) {
+    p.dp_tiles = p.num_tiles / p.workers * p.workers;
+    p.sk_units = static_cast<int64_t>(p.num_tiles - p.dp_tiles) * p.num_kb;
+    const size_t slot_floats = static_cast<size_t>(128) * plan.tile_n;
+    const size_t bytes = sizeof(float) * slot_floats * static_cast<size_t>(grid);
+    const dgl_status wst = acquire_workspace(dev, stream, bytes, grid, &p.ws, &p.flags, &p.epoch);
+    if (wst != DGL_OK) return wst;
+  }
   if (ds->smem_optin < 232448) return DGL_ERR_UNSUPPORTED;  // every variant is sized for 227 KB
   const bool row_staging = !c_tma && !f32;
   const cudaError_t e =

@@ -12,6 +12,7 @@ enum : int {
   STATUS_TIMEOUT_EPILOGUE = 4,
   STATUS_TIMEOUT_DRAIN = 8,
   STATUS_TMEM_MISMATCH = 16,  // a CTA pair's tensor-memory allocations differ
+  STATUS_TIMEOUT_FIXUP = 32,  // a stream-K partial tile never arrived
 };
 
 // Persistent tcgen05 tile kernel: problem and schedule.
@@ -25,6 +26,18 @@ struct TcParams {
   int group_m;          // tile raster: group_m row-tiles share each column sweep
   int c_tma;            // 1: C is written by TMA tensor stores (16-byte aligned pitch and base)
   int* status;          // device status word
+  // Schedule.  `workers` CTAs (or CTA pairs) run at once.  Tiles below
+  // dp_tiles run whole, worker w taking w, w + workers, ...  The remaining
+  // tiles' k-stages ("units", tile-major) are split into `workers` equal
+  // contiguous ranges (stream-K): a worker whose range starts inside a tile
+  // writes its fp32 partial to its workspace slot and raises its flag; the
+  // worker holding a tile's first k-stage adds the partials and stores C.
+  int workers;
+  int dp_tiles;
+  int64_t sk_units;
+  float* ws;            // workers x CTAs-per-worker slots of 128 x BN fp32 partials
+  int* flags;           // one per slot: the epoch of the partial it holds
+  int epoch;            // differs from every earlier launch on this workspace
 };
 
 // Decode (m <= 16) kernel parameters.  A and B are read through tensor maps.
@@ -42,6 +55,56 @@ struct DecodeParams {
   int b_plane_bytes;    // one B box: rows_hi rounded up to 8, x 128 bytes
   int stage_bytes;      // ksteps x (A box (2 KB) + B box)
   int* status;          // device status word
+};
+
+// One piece of a worker's schedule: k-stages [kb0, kb1) of one tile.
+struct Segment {
+  int tile, kb0, kb1;
+};
+
+__host__ __device__ inline int64_t sk_range_start(int64_t units, int workers, int w) {
+  return units * w / workers;
+}
+
+// The worker whose stream-K range holds unit u.
+__host__ __device__ inline int sk_worker_of(int64_t units, int workers, int64_t u) {
+  int w = static_cast<int>(u * workers / units);
+  while (w + 1 < workers && sk_range_start(units, workers, w + 1) <= u) ++w;
+  while (w > 0 && sk_range_start(units, workers, w) > u) --w;
+  return w;
+}
+
+// Walks worker w's segments in order: its data-parallel tiles, then its
+// stream-K range.  Every role of a CTA walks the same sequence.
+struct SegmentIter {
+  int w, workers, nk, dp_tiles, next_dp;
+  int64_t u, u_end;
+  __host__ __device__ SegmentIter(int worker, int num_workers, int num_kb, int dp, int64_t units)
+      : w(worker), workers(num_workers), nk(num_kb), dp_tiles(dp), next_dp(worker), u(0), u_end(0) {
+    if (units > 0) {
+      u = sk_range_start(units, num_workers, worker);
+      u_end = sk_range_start(units, num_workers, worker + 1);
+    }
+  }
+  __host__ __device__ bool next(Segment& s) {
+    if (next_dp < dp_tiles) {
+      s.tile = next_dp;
+      s.kb0 = 0;
+      s.kb1 = nk;
+      next_dp += workers;
+      return true;
+    }
+    if (u < u_end) {
+      const int64_t t = u / nk;
+      s.tile = dp_tiles + static_cast<int>(t);
+      s.kb0 = static_cast<int>(u - t * nk);
+      const int64_t left = u_end - u;
+      s.kb1 = static_cast<int>(left < nk - s.kb0 ? s.kb0 + left : nk);
+      u += s.kb1 - s.kb0;
+      return true;
+    }
+    return false;
+  }
 };
 
 __host__ __device__ inline void tile_coords(int tile, int tiles_m, int tiles_n, int group_m, int& mb, int& nb) {

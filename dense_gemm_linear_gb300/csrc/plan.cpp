@@ -90,8 +90,10 @@ static const Rung* find_rung(int tile_m, int tile_n) {
   return nullptr;
 }
 
+constexpr double kFixupUs = 2.0;  // write + read of one fp32 partial tile per split tile
+
 static double tc_estimate_us(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int tile_m, int tile_n,
-                             int num_sms, int* grid_out) {
+                             int num_sms, bool stream_k, int* grid_out) {
   const Rung* r = find_rung(tile_m, tile_n);
   const int cg = tile_m == 256 ? 2 : 1;
   const double esize = dtype == DGL_DTYPE_E4M3 ? 1.0 : 2.0;
@@ -100,10 +102,27 @@ static double tc_estimate_us(int dtype, int out_dtype, int64_t m, int64_t n, int
   const int64_t groups = std::min<int64_t>(tiles, units);
   const int64_t waves = (tiles + groups - 1) / groups;
   const double k_stages = std::ceil(static_cast<double>(K) * esize / 128.0);
-  const double us = kLaunchUs + static_cast<double>(waves) * (k_stages * r->stage_us + r->tile_us);
+  const double tile_us = k_stages * r->stage_us + r->tile_us;
+  double us = kLaunchUs + static_cast<double>(waves) * tile_us;
+  if (stream_k) {
+    const int64_t full = tiles / units;                       // whole waves, data-parallel
+    const double tail_stages = static_cast<double>(tiles - full * units) * k_stages / units;
+    us = kLaunchUs + static_cast<double>(full) * tile_us + tail_stages * r->stage_us + kFixupUs + r->tile_us;
+  }
   const double hbm_us = operand_bytes(dtype, out_dtype, m, n, K) / (kHbmGBs * 1e3) + kLaunchUs;
-  if (grid_out) *grid_out = static_cast<int>(groups * cg);
+  if (grid_out) *grid_out = static_cast<int>((stream_k ? units : groups) * cg);
   return std::max(us, hbm_us);
+}
+
+// Stream-K pays when the last wave is partial and each worker gets at least
+// a few k-stages of the tail.
+bool stream_k_eligible(int64_t m, int64_t n, int64_t K, int dtype, int tile_m, int tile_n, int num_sms) {
+  const int cg = tile_m == 256 ? 2 : 1;
+  const int64_t tiles = ((m + tile_m - 1) / tile_m) * ((n + tile_n - 1) / tile_n);
+  const int64_t units = std::max(1, num_sms / cg);
+  const int64_t nk = (K * (dtype == DGL_DTYPE_E4M3 ? 1 : 2) + 127) / 128;
+  const int64_t tail = tiles % units;
+  return tail != 0 && tail * nk >= 4 * units;
 }
 
 int tc_tile_k(int dtype) { return dtype == DGL_DTYPE_E4M3 ? 128 : 64; }
@@ -118,7 +137,7 @@ int tc_stages(int tile_m, int tile_n) {
 bool tc_supported_tile(int tile_m, int tile_n) { return find_rung(tile_m, tile_n) != nullptr; }
 
 void fill_tc_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int tile_m, int tile_n, int num_sms,
-                  dgl_plan_info* out) {
+                  dgl_plan_info* out, int stream_k) {
   *out = dgl_plan_info{};
   out->path = DGL_PATH_TC;
   out->tile_m = tile_m;
@@ -127,9 +146,21 @@ void fill_tc_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int
   out->stages = tc_stages(tile_m, tile_n);
   out->cta_group = tile_m == 256 ? 2 : 1;
   tile_metrics(m, n, tile_m, tile_n, num_sms / out->cta_group, out);
+  // stream_k: 1 force on (if eligible), 0 force off, -1 let the model decide
+  const bool sk_ok = stream_k_eligible(m, n, K, dtype, tile_m, tile_n, num_sms);
   int grid = 0;
-  out->est_us = tc_estimate_us(dtype, out_dtype, m, n, K, tile_m, tile_n, num_sms, &grid);
+  out->est_us = tc_estimate_us(dtype, out_dtype, m, n, K, tile_m, tile_n, num_sms, false, &grid);
   out->grid = grid;
+  out->stream_k = 0;
+  if (sk_ok && stream_k != 0) {
+    int grid_sk = 0;
+    const double est_sk = tc_estimate_us(dtype, out_dtype, m, n, K, tile_m, tile_n, num_sms, true, &grid_sk);
+    if (stream_k == 1 || est_sk < 0.97 * out->est_us) {
+      out->est_us = est_sk;
+      out->grid = grid_sk;
+      out->stream_k = 1;
+    }
+  }
 }
 
 int decode_parts(int64_t n, int num_sms) {
@@ -189,7 +220,7 @@ void choose_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int 
   }
   for (const Pin& pin : kPins) {
     if (pin.dtype == dtype && pin.m == m && pin.n == n && pin.K == K) {
-      fill_tc_plan(dtype, out_dtype, m, n, K, pin.tile_m, pin.tile_n, num_sms, out);
+      fill_tc_plan(dtype, out_dtype, m, n, K, pin.tile_m, pin.tile_n, num_sms, out, 0);
       return;
     }
   }
@@ -207,7 +238,7 @@ void choose_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int 
                           std::ceil(static_cast<double>(n) / r.tile_n) * r.tile_n;
     if (any_pass && padded > 1.25 * area) continue;
     dgl_plan_info cand;
-    fill_tc_plan(dtype, out_dtype, m, n, K, r.tile_m, r.tile_n, num_sms, &cand);
+    fill_tc_plan(dtype, out_dtype, m, n, K, r.tile_m, r.tile_n, num_sms, &cand, 0);
     // ties go to the larger tile (later rungs are larger)
     if (!have || cand.est_us <= best.est_us * (1.0 + 1e-9)) {
       best = cand;

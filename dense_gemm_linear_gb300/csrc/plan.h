@@ -14,8 +14,10 @@ double operand_bytes(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K);
 int tc_tile_k(int dtype);
 int tc_stages(int tile_m, int tile_n);
 bool tc_supported_tile(int tile_m, int tile_n);
+// stream_k: 1 on (when eligible), 0 off, -1 the cost model decides.
 void fill_tc_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int tile_m, int tile_n, int num_sms,
-                  dgl_plan_info* out);
+                  dgl_plan_info* out, int stream_k);
+bool stream_k_eligible(int64_t m, int64_t n, int64_t K, int dtype, int tile_m, int tile_n, int num_sms);
 void fill_decode_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int num_sms, dgl_plan_info* out);
 int decode_parts(int64_t n, int num_sms);
 int decode_grid(int64_t n, int num_sms);

@@ -151,8 +151,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   // MMA waits on; each CTA loads its own 128 rows of A and B_ROWS rows of B
   // and stores its own 128 rows of C.
   const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
-  const int cluster_id = blockIdx.x / CG;
-  const int num_clusters = gridDim.x / CG;
+  const int cluster_id = blockIdx.x / CG;  // the worker index of the schedule (p.workers == gridDim.x / CG)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -207,12 +206,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       const uint64_t pol = l2_policy_evict_last();
       uint32_t stage = 0, phase = 0;
       int64_t issued = 0;
-      for (int tile = cluster_id; tile < p.num_tiles && !fail; tile += num_clusters) {
+      SegmentIter it(cluster_id, p.workers, p.num_kb, p.dp_tiles, p.sk_units);
+      Segment sg;
+      while (!fail && it.next(sg)) {
         int mb, nb;
-        tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, mb, nb);
+        tile_coords(sg.tile, p.tiles_m, p.tiles_n, p.group_m, mb, nb);
         const int a_row = mb * Cfg::TILE_M + static_cast<int>(rank) * BM;
         const int b_row = nb * BN + static_cast<int>(rank) * Cfg::B_ROWS;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
           const bool ok = mbar_wait(&empty[stage], phase ^ 1);
           if (!ok) {
             fail = STATUS_TIMEOUT_PRODUCER;
@@ -257,7 +258,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       constexpr uint32_t idesc = idesc_f32acc(Cfg::FP8 ? 0u : 1u, Cfg::TILE_M, BN);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool issued_any = false;
-      for (int tile = cluster_id; tile < p.num_tiles && !fail; tile += num_clusters) {
+      SegmentIter it(cluster_id, p.workers, p.num_kb, p.dp_tiles, p.sk_units);
+      Segment sg;
+      while (!fail && it.next(sg)) {
         const bool ok = mbar_wait(&tempty[acc], acc_phase ^ 1);
         if (!ok) {
           fail = STATUS_TIMEOUT_MMA;
@@ -265,7 +268,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
           const bool ok2 = mbar_wait(&full[stage], phase);
           if (!ok2) {
             fail = STATUS_TIMEOUT_MMA;
@@ -278,7 +281,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           for (int k = 0; k < Cfg::MMAS_PER_STAGE; ++k) {
             const uint64_t ad = smem_desc_sw128(a_addr + k * Cfg::MMA_K_BYTES);
             const uint64_t bd = smem_desc_sw128(b_addr + k * Cfg::MMA_K_BYTES);
-            const uint32_t accumulate = (kb | k) != 0;
+            const uint32_t accumulate = (kb != sg.kb0 || k != 0) ? 1u : 0u;
             if constexpr (CG == 2) {
               if constexpr (Cfg::FP8)
                 umma_e4m3_pair(d_tmem, ad, bd, idesc, accumulate);
@@ -327,9 +330,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     uint8_t* stg = Cfg::ROWSTG ? sStg + q * 32 * Cfg::ROW_PITCH : sStg + e * 4096;
     const uint32_t stg_addr = smem_u32(stg);
     uint32_t acc = 0, acc_phase = 0;
-    for (int tile = cluster_id; tile < p.num_tiles; tile += num_clusters) {
+    SegmentIter it(cluster_id, p.workers, p.num_kb, p.dp_tiles, p.sk_units);
+    Segment sg;
+    while (it.next(sg)) {
       int mb, nb;
-      tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, mb, nb);
+      tile_coords(sg.tile, p.tiles_m, p.tiles_n, p.group_m, mb, nb);
       // all lanes decide together: tcgen05.ld below is warp-collective
       bool ready = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase));
       if constexpr (Cfg::ROWSTG) {
@@ -349,6 +354,85 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       tc_fence_after_sync();
       const int row0 = mb * Cfg::TILE_M + static_cast<int>(rank) * BM + q * 32;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+
+      // ---- stream-K: a segment that does not hold the tile's first k-stage
+      // hands its partial sum over through the workspace; the one that does
+      // adds every partial into tensor memory before the usual epilogue.  Both
+      // walk the accumulator one 32-column chunk at a time, so neither holds
+      // more than two chunks in registers.  Workspace slot layout: float4
+      // (chunk c, column quad t, slab row e) at (c * 8 + t) * 128 + e, so each
+      // warp access covers 512 contiguous bytes.
+      if (sg.kb0 > 0 || sg.kb1 < p.num_kb) {
+        const int e_row = q * 32 + lane;  // row of this CTA's 128-row slab
+        if (sg.kb0 > 0) {
+          float4* slot = reinterpret_cast<float4*>(p.ws + (static_cast<int64_t>(cluster_id) * CG + rank) * (128 * BN));
+#pragma unroll 1
+          for (int u = 0; u < CPW; ++u) {
+            const int c = half * CPW + u;
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(t_row + c * 32, v);
+            tmem_ld_wait();
+            reg_fence(v);
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+              slot[(c * 8 + t) * 128 + e_row] = make_float4(__uint_as_float(v[4 * t]), __uint_as_float(v[4 * t + 1]),
+                                                            __uint_as_float(v[4 * t + 2]), __uint_as_float(v[4 * t + 3]));
+          }
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) {
+            if constexpr (CG == 2)
+              mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+            else
+              mbar_arrive(&tempty[acc]);
+          }
+          named_bar_sync(5, Cfg::EPI_WARPS * 32);  // every epilogue thread has written its part
+          if (warp == 2 && lane == 0) {
+            __threadfence();
+            st_release_gpu(p.flags + cluster_id * CG + rank, p.epoch);
+          }
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1;
+          continue;
+        }
+        // finisher: the workers whose ranges hold the tile's other k-stages
+        const int64_t t_rel = sg.tile - p.dp_tiles;
+        const int w_last = sk_worker_of(p.sk_units, p.workers, (t_rel + 1) * p.num_kb - 1);
+        if (warp == 2 && lane == 0) {
+          for (int wc = cluster_id + 1; wc <= w_last; ++wc) {
+            if (sk_range_start(p.sk_units, p.workers, wc) == sk_range_start(p.sk_units, p.workers, wc + 1))
+              continue;  // an empty range holds no k-stages of this tile
+            if (!wait_flag_gpu(p.flags + wc * CG + rank, p.epoch)) fail |= STATUS_TIMEOUT_FIXUP;
+          }
+        }
+        named_bar_sync(5, Cfg::EPI_WARPS * 32);
+#pragma unroll 1
+        for (int u = 0; u < CPW; ++u) {
+          const int c = half * CPW + u;
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(t_row + c * 32, v);
+          tmem_ld_wait();
+          reg_fence(v);
+#pragma unroll 1
+          for (int wc = cluster_id + 1; wc <= w_last; ++wc) {
+            if (sk_range_start(p.sk_units, p.workers, wc) == sk_range_start(p.sk_units, p.workers, wc + 1)) continue;
+            const float4* slot =
+                reinterpret_cast<const float4*>(p.ws + (static_cast<int64_t>(wc) * CG + rank) * (128 * BN));
+            float4 x[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) x[t] = ldg_cg_v4f(slot + (c * 8 + t) * 128 + e_row);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              v[4 * t] = __float_as_uint(__uint_as_float(v[4 * t]) + x[t].x);
+              v[4 * t + 1] = __float_as_uint(__uint_as_float(v[4 * t + 1]) + x[t].y);
+              v[4 * t + 2] = __float_as_uint(__uint_as_float(v[4 * t + 2]) + x[t].z);
+              v[4 * t + 3] = __float_as_uint(__uint_as_float(v[4 * t + 3]) + x[t].w);
+            }
+          }
+          tmem_st_32x32b_x32(t_row + c * 32, v);
+        }
+        tmem_st_wait();
+      }
 
       // Read this warp's whole share of the accumulator, then hand it back.
       uint32_t r[CPW][32];

@@ -31,11 +31,15 @@
  * fp32 scales; C is bf16 (rounded to nearest even) or fp32 by `out_dtype`.
  *
  * Memory and ownership: A, B, C, sa, sb are DEVICE pointers owned by the
- * caller, on the current CUDA device.  The library allocates no device memory
- * on these paths, never copies to or from the host, and keeps only a small
- * per-device plan cache.  Calls are asynchronous with respect to the host:
- * work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
- * stream) and buffers must stay valid until it completes.
+ * caller, on the current CUDA device.  The library never copies to or from the
+ * host.  It keeps a small per-device plan cache and, for plans with
+ * stream_k = 1, a per-(device, stream) workspace of fp32 partial tiles
+ * (about 20 MB), allocated with cudaMalloc on the first such call on that
+ * stream and kept until the process exits; that first call therefore must not
+ * be made while the stream is being captured into a CUDA graph.  Calls are
+ * asynchronous with respect to the host: work is enqueued on `stream` (a
+ * cudaStream_t; NULL = the legacy default stream) and buffers must stay
+ * valid until it completes.
  *
  * Errors: arguments are validated on the host before any launch; a failed
  * check returns an error code and enqueues nothing.  Nothing is printed and
@@ -75,17 +79,19 @@ typedef enum { DGL_PATH_TC = 0, DGL_PATH_DECODE = 1, DGL_PATH_EMPTY = 2 } dgl_pa
  */
 typedef struct {
   int32_t path;       /* dgl_path_t */
-  int32_t tile_m;     /* rows of C per tile (tcgen05 path: 128) */
+  int32_t tile_m;     /* rows of C per tile (tcgen05 path: 128, or 256 for a CTA pair) */
   int32_t tile_n;     /* columns of C per tile (tcgen05 path: 64, 128 or 256) */
   int32_t tile_k;     /* K elements per pipeline stage (64 bf16, 128 E4M3) */
   int32_t stages;     /* shared-memory ring depth */
-  int32_t cta_group;  /* CTAs sharing one MMA (1) */
+  int32_t cta_group;  /* CTAs sharing one MMA: 1, or 2 (a CTA pair, tile_m 256) */
   int32_t grid;       /* CTAs launched (persistent: at most one per SM) */
   int32_t num_tiles;  /* output tiles (tcgen05 path) or 8-row groups (decode path) */
   double tile_eff;
   double wq_eff;
   double dim_eff;
   double est_us;      /* cost-model estimate of the kernel time, microseconds */
+  int32_t stream_k;   /* 1: tiles of the last, partial wave are split along K across all workers */
+  int32_t reserved;   /* zero */
 } dgl_plan_info;
 
 /*
@@ -113,9 +119,11 @@ dgl_status dgl_gemm_fp8(const void* A, const void* B, const float* sa, const flo
  * Either GEMM with a caller-chosen plan instead of the planner's choice: the
  * forced-tile sweep of FlyDSL pull request 1303 ("a second test runs every
  * tile of both ladders against a shape that divides none of them").
- * dtype: dgl_dtype_t (sa/sb ignored for bf16).  plan->path, tile_n and grid
- * are honoured (grid <= 0 picks one); other fields are ignored.  A plan the
- * library has no kernel for returns DGL_ERR_UNSUPPORTED.
+ * dtype: dgl_dtype_t (sa/sb ignored for bf16).  plan->path, tile_m, tile_n,
+ * stream_k and grid are honoured (grid <= 0 picks one), and for the decode
+ * path tile_k (K elements per ring stage, a multiple of 128 bytes, 0 = pick);
+ * other fields are ignored.  A plan the library has no kernel for returns
+ * DGL_ERR_UNSUPPORTED.
  */
 dgl_status dgl_gemm_planned(int32_t dtype, const void* A, const void* B, const float* sa, const float* sb,
                             void* C, int64_t M, int64_t N, int64_t K, int64_t m_valid, int64_t n_valid,

@@ -113,6 +113,31 @@ def test_persistent_tile_loop_small_grid(tm, grid):
     _full(case, plan=plan)
 
 
+@pytest.mark.parametrize("tm,tn", [(128, 128), (128, 256), (256, 128), (256, 256)])
+@pytest.mark.parametrize("m,n,k", [(700, 900, 2048), (300, 520, 4096), (1030, 1000, 1024)])
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_stream_k_split_tiles(tm, tn, m, n, k, out):
+    """Stream-K: tiles of the partial last wave split along K across workers,
+    partials handed over through the workspace (guard bands on C)."""
+    case = make_case("bf16", m, n, k, out=out)
+    plan = dgl.PlanInfo(path=dgl.PATH_TC, tile_m=tm, tile_n=tn, stream_k=1)
+    _full(case, plan=plan, guard_rows=2, pad_cols=3)
+
+
+@pytest.mark.parametrize("tm,tn", [(128, 256), (256, 256)])
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_stream_k_integer_exact_and_repeatable(tm, tn, dtype):
+    """Integer inputs: split sums are exact in fp32, so stream-K must match the
+    exact result bit for bit, on back-to-back launches sharing the workspace."""
+    case = make_case(dtype, 900, 1100, 2048, out="f32", dist="int")
+    plan = dgl.PlanInfo(path=dgl.PATH_TC, tile_m=tm, tile_n=tn, stream_k=1)
+    ops = gu.to_device(case)
+    for _ in range(3):
+        Cbuf, intact = gu.run(case, plan=plan, dev_ops=ops)
+        assert intact
+        gu.assert_exact(case, gu.host_valid(case, Cbuf))
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "fp8"])
 @pytest.mark.parametrize("m", [1, 3, 8, 16])
 @pytest.mark.parametrize("n", [1, 7, 8, 9, 1000, 2049])
