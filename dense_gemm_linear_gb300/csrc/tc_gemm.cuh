@@ -86,7 +86,13 @@ struct TcConfig {
   static constexpr int STAGES = tc_ring_stages(STAGE_BYTES, STG_TOTAL);
   static constexpr int THREADS = 64 + EPI_WARPS * 32;
   static constexpr int TMEM_COLS = 2 * BN;              // two fp32 accumulators of BN columns
-  static constexpr int BAR_BYTES = 8 * (2 * STAGES + 5) + 8 + 32;
+  static constexpr int BAR_BYTES = 8 * (2 * STAGES + 6) + 8 + 32;
+  // stream-K: one CTA's fp32 partial tile, and how many fit in the ring
+  static constexpr int SLOT_BYTES = BM * BN * 4;
+  static constexpr int RING_SLOTS = STAGES * STAGE_BYTES / SLOT_BYTES;
+  // fix-up staging per epilogue warp: 2 KB pieces, two of them when room allows
+  static constexpr int FX_WARP_BYTES = ROWSTG ? 16 * ROW_PITCH : 4096;
+  static constexpr int FX_BUFS = FX_WARP_BYTES >= 4096 ? 2 : 1;
   static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + STAGES * STAGE_BYTES + STG_TOTAL + BAR_BYTES;
   static_assert(BN == 64 || BN == 128 || BN == 256, "tile widths of the ladder");
   static_assert(STAGES >= 3, "ring too shallow");
@@ -94,6 +100,8 @@ struct TcConfig {
   static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation: power of two");
   static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
   static_assert(B_STAGE_BYTES % 1024 == 0, "B stage tiles stay 1024-byte aligned");
+  static_assert(RING_SLOTS >= 1, "a partial tile fits in the ring");
+  static_assert(FX_WARP_BYTES >= 2048 && FX_WARP_BYTES % 16 == 0, "fix-up staging piece");
 };
 
 // Byte offset of 16-byte unit `c16` of staging row `r`, in the layout a TMA
@@ -142,7 +150,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* fixbar = drain + 1;                          // stream-K: partial tiles landed in the ring
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fixbar + 1);
   volatile int* qflag = reinterpret_cast<volatile int*>(tmem_slot + 1);  // 8 epilogue-warp flags
 
   const int warp = threadIdx.x >> 5;
@@ -163,6 +172,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       mbar_init(&tempty[b], Cfg::EPI_WARPS * CG);
     }
     mbar_init(drain, 1);
+    mbar_init(fixbar, 1);
     fence_mbarrier_init();
     fence_proxy_async_shared();
   }
@@ -329,7 +339,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     constexpr int CPW = Cfg::CHUNKS_PER_WARP;
     uint8_t* stg = Cfg::ROWSTG ? sStg + q * 32 * Cfg::ROW_PITCH : sStg + e * 4096;
     const uint32_t stg_addr = smem_u32(stg);
-    uint32_t acc = 0, acc_phase = 0;
+    uint32_t acc = 0, acc_phase = 0, fx_phase = 0;
     SegmentIter it(cluster_id, p.workers, p.num_kb, p.dp_tiles, p.sk_units);
     Segment sg;
     while (it.next(sg)) {
@@ -356,56 +366,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
 
       // ---- stream-K: a segment that does not hold the tile's first k-stage
-      // hands its partial sum over through the workspace; the one that does
-      // adds every partial into tensor memory before the usual epilogue.  Both
-      // walk the accumulator one 32-column chunk at a time, so neither holds
-      // more than two chunks in registers.  Workspace slot layout: float4
-      // (chunk c, column quad t, slab row e) at (c * 8 + t) * 128 + e, so each
-      // warp access covers 512 contiguous bytes.
-      if (sg.kb0 > 0 || sg.kb1 < p.num_kb) {
-        const int e_row = q * 32 + lane;  // row of this CTA's 128-row slab
-        if (sg.kb0 > 0) {
-          float4* slot = reinterpret_cast<float4*>(p.ws + (static_cast<int64_t>(cluster_id) * CG + rank) * (128 * BN));
-#pragma unroll 1
-          for (int u = 0; u < CPW; ++u) {
-            const int c = half * CPW + u;
-            uint32_t v[32];
-            tmem_ld_32x32b_x32(t_row + c * 32, v);
-            tmem_ld_wait();
-            reg_fence(v);
-#pragma unroll
-            for (int t = 0; t < 8; ++t)
-              slot[(c * 8 + t) * 128 + e_row] = make_float4(__uint_as_float(v[4 * t]), __uint_as_float(v[4 * t + 1]),
-                                                            __uint_as_float(v[4 * t + 2]), __uint_as_float(v[4 * t + 3]));
-          }
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) {
-            if constexpr (CG == 2)
-              mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
-            else
-              mbar_arrive(&tempty[acc]);
-          }
-          named_bar_sync(5, Cfg::EPI_WARPS * 32);  // every epilogue thread has written its part
-          if (warp == 2 && lane == 0) {
-            __threadfence();
-            st_release_gpu(p.flags + cluster_id * CG + rank, p.epoch);
-          }
-          acc ^= 1;
-          if (acc == 0) acc_phase ^= 1;
-          continue;
-        }
-        // finisher: the workers whose ranges hold the tile's other k-stages
-        const int64_t t_rel = sg.tile - p.dp_tiles;
-        const int w_last = sk_worker_of(p.sk_units, p.workers, (t_rel + 1) * p.num_kb - 1);
-        if (warp == 2 && lane == 0) {
-          for (int wc = cluster_id + 1; wc <= w_last; ++wc) {
-            if (sk_range_start(p.sk_units, p.workers, wc) == sk_range_start(p.sk_units, p.workers, wc + 1))
-              continue;  // an empty range holds no k-stages of this tile
-            if (!wait_flag_gpu(p.flags + wc * CG + rank, p.epoch)) fail |= STATUS_TIMEOUT_FIXUP;
-          }
-        }
-        named_bar_sync(5, Cfg::EPI_WARPS * 32);
+      // hands its fp32 partial tile over through the workspace; the segment
+      // that does adds every partial into tensor memory before the usual
+      // epilogue.  Slot layout (per CTA of the worker): float4 number
+      // ((c * 4 + q) * 8 + t) * 32 + lane holds columns 32c + 4t .. 32c + 4t + 3
+      // of slab row 32q + lane, so each warp's 32 x 32 chunk is 4 KB of
+      // contiguous memory, written and read with bulk copies.
+      if (sg.kb0 > 0) {
+        uint8_t* slot = reinterpret_cast<uint8_t*>(p.ws) + (static_cast<int64_t>(cluster_id) * CG + rank) * Cfg::SLOT_BYTES;
+        const uint32_t fx = Cfg::ROWSTG ? stg_addr + half * Cfg::FX_WARP_BYTES : stg_addr;
+        int piece = 0;
 #pragma unroll 1
         for (int u = 0; u < CPW; ++u) {
           const int c = half * CPW + u;
@@ -413,85 +383,254 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           tmem_ld_32x32b_x32(t_row + c * 32, v);
           tmem_ld_wait();
           reg_fence(v);
-#pragma unroll 1
-          for (int wc = cluster_id + 1; wc <= w_last; ++wc) {
-            if (sk_range_start(p.sk_units, p.workers, wc) == sk_range_start(p.sk_units, p.workers, wc + 1)) continue;
-            const float4* slot =
-                reinterpret_cast<const float4*>(p.ws + (static_cast<int64_t>(wc) * CG + rank) * (128 * BN));
-            float4 x[8];
 #pragma unroll
-            for (int t = 0; t < 8; ++t) x[t] = ldg_cg_v4f(slot + (c * 8 + t) * 128 + e_row);
+          for (int h = 0; h < 2; ++h, ++piece) {
+            const uint32_t buf = fx + (Cfg::FX_BUFS == 2 ? (piece & 1) * 2048 : 0);
+            // the copy that last read this buffer (or an earlier tile's store) is done with it
+            if (lane == 0) {
+              if (Cfg::FX_BUFS == 2 && piece > 0)
+                bulk_wait_read1();
+              else
+                bulk_wait_read0();
+            }
+            __syncwarp();
 #pragma unroll
-            for (int t = 0; t < 8; ++t) {
-              v[4 * t] = __float_as_uint(__uint_as_float(v[4 * t]) + x[t].x);
-              v[4 * t + 1] = __float_as_uint(__uint_as_float(v[4 * t + 1]) + x[t].y);
-              v[4 * t + 2] = __float_as_uint(__uint_as_float(v[4 * t + 2]) + x[t].z);
-              v[4 * t + 3] = __float_as_uint(__uint_as_float(v[4 * t + 3]) + x[t].w);
+            for (int tt = 0; tt < 4; ++tt) {
+              const int t = 4 * h + tt;
+              sts_v4(buf + (tt * 32 + lane) * 16, v[4 * t], v[4 * t + 1], v[4 * t + 2], v[4 * t + 3]);
+            }
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+              bulk_store_1d(slot + (c * 4 + q) * 4096 + h * 2048, buf, 2048);
+              bulk_commit();
             }
           }
-          tmem_st_32x32b_x32(t_row + c * 32, v);
         }
-        tmem_st_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (CG == 2)
+            mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+          else
+            mbar_arrive(&tempty[acc]);
+          bulk_wait0();  // this warp's pieces are in global memory
+          fence_proxy_async_global();
+          __threadfence();
+        }
+        named_bar_sync(5, Cfg::EPI_WARPS * 32);  // every epilogue warp's pieces are written
+        if (warp == 2 && lane == 0) st_release_gpu(p.flags + cluster_id * CG + rank, p.epoch);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+        continue;
+      }
+      if (sg.kb1 < p.num_kb) {
+        // Finisher: the tile's other k-stages belong to workers cluster_id + 1
+        // .. w_last (an empty range holds none).  This is the worker's last
+        // segment, so every MMA has finished and the operand ring is free:
+        // partial tiles are bulk-copied into it, RING_SLOTS at a time.
+        const int64_t t_rel = sg.tile - p.dp_tiles;
+        const int w_last = sk_worker_of(p.sk_units, p.workers, (t_rel + 1) * p.num_kb - 1);
+        auto nonempty = [&](int w) {
+          return sk_range_start(p.sk_units, p.workers, w) != sk_range_start(p.sk_units, p.workers, w + 1);
+        };
+        const uint32_t ring = smem_u32(sA);
+        int wc = cluster_id + 1;
+        while (true) {
+          while (wc <= w_last && !nonempty(wc)) ++wc;
+          if (wc > w_last) break;
+          const int w_first = wc;
+          int nb = 0;
+          for (; wc <= w_last && nb < Cfg::RING_SLOTS; ++wc)
+            if (nonempty(wc)) ++nb;
+          if (warp == 2 && lane == 0) {
+            int i = 0;
+            for (int w = w_first; w < wc; ++w) {
+              if (!nonempty(w)) continue;
+              if (!wait_flag_gpu(p.flags + w * CG + rank, p.epoch)) fail |= STATUS_TIMEOUT_FIXUP;
+              if (i == 0) {
+                fence_proxy_async_global();
+                fence_proxy_async_shared();
+                mbar_arrive_expect_tx(fixbar, static_cast<uint32_t>(nb * Cfg::SLOT_BYTES));
+              }
+              const uint8_t* src =
+                  reinterpret_cast<const uint8_t*>(p.ws) + (static_cast<int64_t>(w) * CG + rank) * Cfg::SLOT_BYTES;
+              for (int off = 0; off < Cfg::SLOT_BYTES; off += 32768)
+                bulk_load_1d(ring + i * Cfg::SLOT_BYTES + off, src + off, min(32768, Cfg::SLOT_BYTES - off), fixbar);
+              ++i;
+            }
+          }
+          if (!mbar_wait(fixbar, fx_phase)) fail |= STATUS_TIMEOUT_FIXUP;
+          fx_phase ^= 1;
+#pragma unroll 1
+          for (int u = 0; u < CPW; ++u) {
+            const int c = half * CPW + u;
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(t_row + c * 32, v);
+            tmem_ld_wait();
+            reg_fence(v);
+#pragma unroll 1
+            for (int i = 0; i < nb; ++i) {
+              const uint32_t src = ring + i * Cfg::SLOT_BYTES + ((c * 4 + q) * 8 * 32 + lane) * 16;
+#pragma unroll
+              for (int t = 0; t < 8; ++t) {
+                const float4 x = lds_v4f(src + t * 512);
+                v[4 * t] = __float_as_uint(__uint_as_float(v[4 * t]) + x.x);
+                v[4 * t + 1] = __float_as_uint(__uint_as_float(v[4 * t + 1]) + x.y);
+                v[4 * t + 2] = __float_as_uint(__uint_as_float(v[4 * t + 2]) + x.z);
+                v[4 * t + 3] = __float_as_uint(__uint_as_float(v[4 * t + 3]) + x.w);
+              }
+            }
+            tmem_st_32x32b_x32(t_row + c * 32, v);
+          }
+          tmem_st_wait();
+          named_bar_sync(5, Cfg::EPI_WARPS * 32);  // the ring is read before the next copies land in it
+        }
       }
 
-      // Read this warp's whole share of the accumulator, then hand it back.
-      uint32_t r[CPW][32];
+      // The warp's share of the accumulator is read G chunks at a time, which
+      // bounds the registers it holds; the buffer goes back to the MMA once
+      // the last chunk has been read.
+      constexpr int G = CPW > 2 ? 2 : CPW;
+      float row_scale = 0.0f;
+      if constexpr (Cfg::FP8) row_scale = (row0 + lane < p.m) ? p.sa[row0 + lane] : 0.0f;
+      // row staging (bf16 C, rows not 16-byte aligned): this thread's row
+      const int row = row0 + lane;
+      const int ncols = min(BN, p.n - nb * BN);
+      const int L = (Cfg::ROWSTG && row < p.m) ? 2 * ncols : 0;  // valid bytes of the row's segment
+      uint8_t* rowp = L > 0 ? reinterpret_cast<uint8_t*>(static_cast<__nv_bfloat16*>(p.C) +
+                                                         static_cast<int64_t>(row) * p.ldc + nb * BN)
+                            : nullptr;
+      const int delta = static_cast<int>(reinterpret_cast<uintptr_t>(rowp) & 15);
+      const uint32_t srow = stg_addr + lane * Cfg::ROW_PITCH + delta;  // staged byte 0 of the segment
+      uint32_t buf = 0;
 #pragma unroll
-      for (int u = 0; u < CPW; ++u) tmem_ld_32x32b_x32(t_row + (half * CPW + u) * 32, r[u]);
-      tmem_ld_wait();
+      for (int g0 = 0; g0 < CPW; g0 += G) {
+        uint32_t r[G][32];
 #pragma unroll
-      for (int u = 0; u < CPW; ++u) reg_fence(r[u]);
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) {
-        if constexpr (CG == 2)
-          mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));  // the leader's MMA waits on it
-        else
-          mbar_arrive(&tempty[acc]);
-      }
+        for (int uu = 0; uu < G; ++uu) tmem_ld_32x32b_x32(t_row + (half * CPW + g0 + uu) * 32, r[uu]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int uu = 0; uu < G; ++uu) reg_fence(r[uu]);
+        if (g0 + G == CPW) {
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) {
+            if constexpr (CG == 2)
+              mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));  // the leader's MMA waits on it
+            else
+              mbar_arrive(&tempty[acc]);
+          }
+        }
 
-      if constexpr (Cfg::FP8) {
-        const float row_scale = (row0 + lane < p.m) ? p.sa[row0 + lane] : 0.0f;
+        if constexpr (Cfg::FP8) {
 #pragma unroll
-        for (int u = 0; u < CPW; ++u) {
-          const int col0 = nb * BN + (half * CPW + u) * 32;
-          const float col_scale = (col0 + lane < p.n) ? p.sb[col0 + lane] : 0.0f;
+          for (int uu = 0; uu < G; ++uu) {
+            const int col0 = nb * BN + (half * CPW + g0 + uu) * 32;
+            const float col_scale = (col0 + lane < p.n) ? p.sb[col0 + lane] : 0.0f;
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            r[u][j] = __float_as_uint((__uint_as_float(r[u][j]) * row_scale) *
-                                      __shfl_sync(0xffffffffu, col_scale, j));
+            for (int j = 0; j < 32; ++j)
+              r[uu][j] = __float_as_uint((__uint_as_float(r[uu][j]) * row_scale) *
+                                         __shfl_sync(0xffffffffu, col_scale, j));
+          }
+        }
+
+        if constexpr (Cfg::ROWSTG) {
+          // ---- stage whole rows, shifted by each row's misalignment
+#pragma unroll
+          for (int uu = 0; uu < G; ++uu) {
+            uint32_t w[16];
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+              __nv_bfloat162 h2 =
+                  __floats2bfloat162_rn(__uint_as_float(r[uu][2 * t]), __uint_as_float(r[uu][2 * t + 1]));
+              w[t] = *reinterpret_cast<uint32_t*>(&h2);
+            }
+            const uint32_t base = srow + 64 * (half * CPW + g0 + uu);
+            if ((delta & 2) == 0) {
+#pragma unroll
+              for (int t = 0; t < 16; ++t) sts_u32(base + 4 * t, w[t]);
+            } else {
+              sts_u16(base, w[0] & 0xFFFFu);
+#pragma unroll
+              for (int t = 0; t < 15; ++t) sts_u32(base + 2 + 4 * t, __byte_perm(w[t], w[t + 1], 0x5432));
+              sts_u16(base + 62, w[15] >> 16);
+            }
+          }
+        } else {
+          // bf16 chunks alternate between two 2 KB staging tiles, so a chunk's
+          // TMA store may still be reading one while the next chunk fills the
+          // other; fp32 chunks fill the whole 4 KB tile.
+#pragma unroll
+          for (int uu = 0; uu < G; ++uu) {
+            const int col0 = nb * BN + (half * CPW + g0 + uu) * 32;
+            uint8_t* stg_u = stg + buf * Cfg::STG_BYTES;
+            const uint32_t stg_addr_u = stg_addr + buf * Cfg::STG_BYTES;
+            // the store that last used this staging tile has finished reading it
+            if (p.c_tma && lane == 0) {
+              if constexpr (Cfg::OUT_F32)
+                bulk_wait_read0();
+              else
+                bulk_wait_read1();
+            }
+            __syncwarp();
+            // this thread's row (lane) of the 32 x 32 chunk -> staging, 16 bytes at a time
+            if constexpr (Cfg::OUT_F32) {
+#pragma unroll
+              for (int c16 = 0; c16 < 8; ++c16)
+                sts_v4(stg_addr_u + stg_offset<Cfg::STG_ROW>(lane, c16), r[uu][4 * c16], r[uu][4 * c16 + 1],
+                       r[uu][4 * c16 + 2], r[uu][4 * c16 + 3]);
+            } else {
+#pragma unroll
+              for (int c16 = 0; c16 < 4; ++c16) {
+                uint32_t w[4];
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                  __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(r[uu][8 * c16 + 2 * t]),
+                                                            __uint_as_float(r[uu][8 * c16 + 2 * t + 1]));
+                  w[t] = *reinterpret_cast<uint32_t*>(&h2);
+                }
+                sts_v4(stg_addr_u + stg_offset<Cfg::STG_ROW>(lane, c16), w[0], w[1], w[2], w[3]);
+              }
+            }
+            // A TMA store writes whole 16-byte units of a row, so a chunk that
+            // ends inside one (n * element size not a multiple of 16) takes the
+            // predicated path instead.
+            const bool tma_ok = p.c_tma && (col0 + 32 <= p.n || (p.n * Cfg::OUT_BYTES) % 16 == 0);
+            if (tma_ok) {
+              fence_proxy_async_shared();
+              __syncwarp();
+              if (lane == 0 && row0 < p.m && col0 < p.n) {
+                tma_store_2d(&tmC, stg_u, col0, row0);
+                bulk_commit();
+              }
+            } else {
+              __syncwarp();
+              // one row per step, a column per lane
+              const int col = col0 + lane;
+#pragma unroll 4
+              for (int rr = 0; rr < 32; ++rr) {
+                const int grow = row0 + rr;
+                if (grow < p.m && col < p.n) {
+                  if constexpr (Cfg::OUT_F32) {
+                    const float v =
+                        *reinterpret_cast<const float*>(stg_u + stg_offset<128>(rr, lane >> 2) + (lane & 3) * 4);
+                    static_cast<float*>(p.C)[static_cast<int64_t>(grow) * p.ldc + col] = v;
+                  } else {
+                    const uint16_t v =
+                        *reinterpret_cast<const uint16_t*>(stg_u + stg_offset<64>(rr, lane >> 3) + (lane & 7) * 2);
+                    reinterpret_cast<uint16_t*>(p.C)[static_cast<int64_t>(grow) * p.ldc + col] = v;
+                  }
+                }
+              }
+              __syncwarp();
+            }
+            if constexpr (!Cfg::OUT_F32) buf ^= 1u;
+          }
         }
       }
 
       if constexpr (Cfg::ROWSTG) {
-        // ---- bf16 C, rows not 16-byte aligned: stage whole rows, shifted
-        const int row = row0 + lane;                     // this thread's row
-        const int ncols = min(BN, p.n - nb * BN);
-        const int L = row < p.m ? 2 * ncols : 0;         // valid bytes of this row's segment
-        uint8_t* rowp = row < p.m ? reinterpret_cast<uint8_t*>(static_cast<__nv_bfloat16*>(p.C) +
-                                                           static_cast<int64_t>(row) * p.ldc + nb * BN)
-                                  : nullptr;
-        const int delta = static_cast<int>(reinterpret_cast<uintptr_t>(rowp) & 15);
-        const uint32_t srow = stg_addr + lane * Cfg::ROW_PITCH + delta;  // staged byte 0 of the segment
-#pragma unroll
-        for (int u = 0; u < CPW; ++u) {
-          uint32_t w[16];
-#pragma unroll
-          for (int t = 0; t < 16; ++t) {
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(r[u][2 * t]), __uint_as_float(r[u][2 * t + 1]));
-            w[t] = *reinterpret_cast<uint32_t*>(&h2);
-          }
-          const uint32_t base = srow + 64 * (half * CPW + u);
-          if ((delta & 2) == 0) {
-#pragma unroll
-            for (int t = 0; t < 16; ++t) sts_u32(base + 4 * t, w[t]);
-          } else {
-            sts_u16(base, w[0] & 0xFFFFu);
-#pragma unroll
-            for (int t = 0; t < 15; ++t) sts_u32(base + 2 + 4 * t, __byte_perm(w[t], w[t + 1], 0x5432));
-            sts_u16(base + 62, w[15] >> 16);
-          }
-        }
         fence_proxy_async_shared();
         named_bar_sync(1 + q, 64);
         if (L > 0) {
@@ -506,75 +645,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             store_row_pieces(rowp, srow, 0, head);
             store_row_pieces(rowp, srow, head + body, L);
           }
-        }
-      } else {
-        // bf16 chunks alternate between two 2 KB staging tiles, so a chunk's
-        // TMA store may still be reading one while the next chunk fills the
-        // other; fp32 chunks fill the whole 4 KB tile.
-        uint32_t buf = 0;
-#pragma unroll
-        for (int u = 0; u < CPW; ++u) {
-          const int col0 = nb * BN + (half * CPW + u) * 32;
-          uint8_t* stg_u = stg + buf * Cfg::STG_BYTES;
-          const uint32_t stg_addr_u = stg_addr + buf * Cfg::STG_BYTES;
-          // the store that last used this staging tile has finished reading it
-          if (p.c_tma && lane == 0) {
-            if constexpr (Cfg::OUT_F32)
-              bulk_wait_read0();
-            else
-              bulk_wait_read1();
-          }
-          __syncwarp();
-          // this thread's row (lane) of the 32 x 32 chunk -> staging, 16 bytes at a time
-          if constexpr (Cfg::OUT_F32) {
-#pragma unroll
-            for (int c16 = 0; c16 < 8; ++c16)
-              sts_v4(stg_addr_u + stg_offset<Cfg::STG_ROW>(lane, c16), r[u][4 * c16], r[u][4 * c16 + 1],
-                     r[u][4 * c16 + 2], r[u][4 * c16 + 3]);
-          } else {
-#pragma unroll
-            for (int c16 = 0; c16 < 4; ++c16) {
-              uint32_t w[4];
-#pragma unroll
-              for (int t = 0; t < 4; ++t) {
-                __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(r[u][8 * c16 + 2 * t]),
-                                                          __uint_as_float(r[u][8 * c16 + 2 * t + 1]));
-                w[t] = *reinterpret_cast<uint32_t*>(&h2);
-              }
-              sts_v4(stg_addr_u + stg_offset<Cfg::STG_ROW>(lane, c16), w[0], w[1], w[2], w[3]);
-            }
-          }
-          // A TMA store writes whole 16-byte units of a row, so a chunk that
-          // ends inside one (n * element size not a multiple of 16) takes the
-          // predicated path instead.
-          const bool tma_ok = p.c_tma && (col0 + 32 <= p.n || (p.n * Cfg::OUT_BYTES) % 16 == 0);
-          if (tma_ok) {
-            fence_proxy_async_shared();
-            __syncwarp();
-            if (lane == 0 && row0 < p.m && col0 < p.n) {
-              tma_store_2d(&tmC, stg_u, col0, row0);
-              bulk_commit();
-            }
-          } else {
-            __syncwarp();
-            // one row per step, a column per lane
-            const int col = col0 + lane;
-#pragma unroll 4
-            for (int rr = 0; rr < 32; ++rr) {
-              const int row = row0 + rr;
-              if (row < p.m && col < p.n) {
-                if constexpr (Cfg::OUT_F32) {
-                  const float v = *reinterpret_cast<const float*>(stg_u + stg_offset<128>(rr, lane >> 2) + (lane & 3) * 4);
-                  static_cast<float*>(p.C)[static_cast<int64_t>(row) * p.ldc + col] = v;
-                } else {
-                  const uint16_t v = *reinterpret_cast<const uint16_t*>(stg_u + stg_offset<64>(rr, lane >> 3) + (lane & 7) * 2);
-                  reinterpret_cast<uint16_t*>(p.C)[static_cast<int64_t>(row) * p.ldc + col] = v;
-                }
-              }
-            }
-            __syncwarp();
-          }
-          if constexpr (!Cfg::OUT_F32) buf ^= 1u;
         }
       }
       acc ^= 1;
