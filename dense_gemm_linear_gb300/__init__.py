@@ -34,7 +34,7 @@ PATH_DECODE = 1
 PATH_EMPTY = 2
 
 EXPORTED = ["dgl_gemm_bf16", "dgl_gemm_fp8", "dgl_gemm_planned", "dgl_plan", "dgl_tile_metrics",
-            "dgl_device_status", "dgl_status_string", "dgl_version"]
+            "dgl_device_status", "dgl_status_string", "dgl_version", "dgl_gemm_noalloc"]
 
 
 class PlanInfo(ctypes.Structure):
@@ -74,6 +74,8 @@ def load_library(path: str | None = None):
     lib.dgl_gemm_planned.argtypes = [i32, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i32,
                                      ctypes.POINTER(PlanInfo), vp]
     lib.dgl_gemm_planned.restype = i32
+    lib.dgl_gemm_noalloc.argtypes = [i32, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i32, vp]
+    lib.dgl_gemm_noalloc.restype = i32
     lib.dgl_plan.argtypes = [i32, i64, i64, i64, i32, i32, ctypes.POINTER(PlanInfo)]
     lib.dgl_plan.restype = i32
     lib.dgl_tile_metrics.argtypes = [i64, i64, i32, i32, i32, ctypes.POINTER(PlanInfo)]
@@ -114,6 +116,11 @@ def dgl_gemm_planned(dtype, A, B, sa, sb, C, M, N, K, m_valid, n_valid, out_dtyp
                      stream=0) -> int:
     return load_library().dgl_gemm_planned(dtype, A, B, sa, sb, C, M, N, K, m_valid, n_valid, out_dtype,
                                            ctypes.byref(plan), stream)
+
+
+def dgl_gemm_noalloc(dtype, A, B, sa, sb, C, M, N, K, m_valid=0, n_valid=0, out_dtype=OUT_BF16, stream=0) -> int:
+    """The GEMM that allocates no device memory (stream-K partials in a fixed device array)."""
+    return load_library().dgl_gemm_noalloc(dtype, A, B, sa, sb, C, M, N, K, m_valid, n_valid, out_dtype, stream)
 
 
 def dgl_plan(dtype, m, n, K, out_dtype=OUT_BF16, num_sms=0) -> PlanInfo:

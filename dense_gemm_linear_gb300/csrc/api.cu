@@ -94,6 +94,25 @@ dgl_status acquire_workspace(int dev, cudaStream_t stream, size_t bytes, int nfl
   return DGL_OK;
 }
 
+// ---- scratch of dgl_gemm_noalloc: a fixed device array instead of cudaMalloc.
+// Layout: DGL_NOALLOC_SCRATCH_BYTES of fp32 partial tiles, then one epoch flag
+// per partial slot.  Every device that loads the library holds it until exit.
+constexpr int kNoallocFlags = 160;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[DGL_NOALLOC_SCRATCH_BYTES + kNoallocFlags * sizeof(int)];
+
+// The array as this device sees it.  Host code cannot use the array's name as
+// an address (it stands for a host-side shadow), so set-up asks the runtime
+// for the device address once per device, with that device current.
+struct StaticScratch {
+  bool ready = false;
+  float* ws = nullptr;
+  size_t ws_bytes = 0;
+  int* flags = nullptr;
+  int nflags = 0;
+  int epoch = 0;  // last epoch handed out; flags hold earlier epochs or zero
+};
+StaticScratch g_noalloc[kMaxDevices];
+
 dgl_status get_device(int* dev_out, DeviceState** st_out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return DGL_ERR_CUDA;
@@ -249,7 +268,7 @@ dgl_status validate(Problem& pr) {
   return DGL_OK;
 }
 
-dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream) {
+dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream, StaticScratch* fixed = nullptr) {
   dgl_status st = validate(pr);
   if (st != DGL_OK) return st;
   if (pr.m == 0 || pr.n == 0) return DGL_OK;
@@ -372,8 +391,22 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream) {
     p.sk_units = static_cast<int64_t>(p.num_tiles - p.dp_tiles) * p.num_kb;
     const size_t slot_floats = static_cast<size_t>(128) * plan.tile_n;
     const size_t bytes = sizeof(float) * slot_floats * static_cast<size_t>(grid);
-    const dgl_status wst = acquire_workspace(dev, stream, bytes, grid, &p.ws, &p.flags, &p.epoch);
-    if (wst != DGL_OK) return wst;
+    if (fixed) {
+      // the caller's problem needs more partial tiles than the array holds
+      if (bytes > fixed->ws_bytes || grid > fixed->nflags) return DGL_ERR_SHAPE;
+      std::lock_guard<std::mutex> lock(g_mu);
+      if (fixed->epoch == INT32_MAX) {
+        // epochs ran out: clear the flags so that counting can restart
+        if (cudaMemsetAsync(fixed->flags, 0, sizeof(int) * fixed->nflags, stream) != cudaSuccess) return DGL_ERR_CUDA;
+        fixed->epoch = 0;
+      }
+      p.ws = fixed->ws;
+      p.flags = fixed->flags;
+      p.epoch = ++fixed->epoch;
+    } else {
+      const dgl_status wst = acquire_workspace(dev, stream, bytes, grid, &p.ws, &p.flags, &p.epoch);
+      if (wst != DGL_OK) return wst;
+    }
   }
   if (ds->smem_optin < 232448) return DGL_ERR_UNSUPPORTED;  // every variant is sized for 227 KB
   const bool row_staging = !c_tma && !f32;
@@ -381,6 +414,29 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream) {
       e4m3 ? launch_tc_e4m3(pr.out, plan.tile_m, plan.tile_n, row_staging, ta, tb, tc, p, grid, stream)
            : launch_tc_bf16(pr.out, plan.tile_m, plan.tile_n, row_staging, ta, tb, tc, p, grid, stream);
   return e == cudaSuccess ? DGL_OK : DGL_ERR_CUDA;
+}
+
+// First use on a device: look up the array's device address and clear its
+// flags (synchronous; later calls enqueue work only).
+dgl_status noalloc_setup(int dev, StaticScratch** out) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  StaticScratch& sc = g_noalloc[dev];
+  if (!sc.ready) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return DGL_ERR_CUDA;
+    uint8_t* base = static_cast<uint8_t*>(ptr);
+    int* flags = reinterpret_cast<int*>(base + DGL_NOALLOC_SCRATCH_BYTES);
+    if (cudaMemset(flags, 0, sizeof(int) * kNoallocFlags) != cudaSuccess) return DGL_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return DGL_ERR_CUDA;
+    sc.ws = reinterpret_cast<float*>(base);
+    sc.ws_bytes = DGL_NOALLOC_SCRATCH_BYTES;
+    sc.flags = flags;
+    sc.nflags = kNoallocFlags;
+    sc.epoch = 0;
+    sc.ready = true;
+  }
+  *out = &sc;
+  return DGL_OK;
 }
 
 }  // namespace
@@ -453,6 +509,32 @@ dgl_status dgl_device_status(void* stream) {
     return DGL_ERR_TIMEOUT;
   }
   return DGL_OK;
+}
+
+dgl_status dgl_gemm_noalloc(int32_t dtype, const void* A, const void* B, const float* sa, const float* sb, void* C,
+                            int64_t M, int64_t N, int64_t K, int64_t m_valid, int64_t n_valid, int32_t out_dtype,
+                            void* stream) {
+  if (dtype != DGL_DTYPE_BF16 && dtype != DGL_DTYPE_E4M3) return DGL_ERR_ARG;
+  Problem pr{dtype, out_dtype, A, B, dtype == DGL_DTYPE_E4M3 ? sa : nullptr,
+             dtype == DGL_DTYPE_E4M3 ? sb : nullptr, C, M, N, K, m_valid, n_valid};
+  dgl_status st = validate(pr);
+  if (st != DGL_OK) return st;
+  if (pr.m == 0 || pr.n == 0) return DGL_OK;
+  int dev = 0;
+  DeviceState* ds = nullptr;
+  st = get_device(&dev, &ds);
+  if (st != DGL_OK) return st;
+  StaticScratch* sc = nullptr;
+  st = noalloc_setup(dev, &sc);
+  if (st != DGL_OK) return st;
+  // the planner's path and tile; on the tcgen05 path the last, partial wave
+  // is always split along K (when it has one)
+  dgl_plan_info plan;
+  choose_plan(pr.dtype, pr.out, pr.m, pr.n, pr.K, ds->num_sms, &plan);
+  plan.stream_k = plan.path == DGL_PATH_TC ? 1 : 0;
+  plan.grid = 0;
+  plan.tile_k = 0;
+  return run(pr, &plan, static_cast<cudaStream_t>(stream), sc);
 }
 
 const char* dgl_status_string(int32_t status) {

@@ -130,6 +130,45 @@ dgl_status dgl_gemm_planned(int32_t dtype, const void* A, const void* B, const f
                             int32_t out_dtype, const dgl_plan_info* plan, void* stream);
 
 /*
+ * Size in bytes of the fixed device array that dgl_gemm_noalloc uses for its
+ * fp32 partial tiles: 20 MiB, one 128 x 256 fp32 tile for each of 160 CTAs.
+ */
+#define DGL_NOALLOC_SCRATCH_BYTES (20u * 1024u * 1024u)
+
+/*
+ * GEMM that allocates no device memory.  No page behind this library
+ * describes it: it exists for callers that cannot call cudaMalloc while they
+ * run, such as a framework that hands every byte of device memory out from
+ * its own pool (an allocation outside the pool fails or breaks the pool's
+ * accounting) or a serving loop that forbids allocation after start-up
+ * (cudaMalloc may block on the whole device).
+ *
+ * It computes what dgl_gemm_bf16 (dtype = DGL_DTYPE_BF16; sa and sb ignored)
+ * or dgl_gemm_fp8 (dtype = DGL_DTYPE_E4M3) compute, with the same arguments,
+ * layouts, validation and error codes.  On the tcgen05 path it always splits
+ * the tiles of the last, partial wave along K across all CTAs (stream-K); the
+ * partial tiles go through a static device array of DGL_NOALLOC_SCRATCH_BYTES
+ * plus 160 flags that the library holds on every device that loads it, until
+ * the process exits.  A problem whose split would need more partial tiles
+ * than the array holds (more than DGL_NOALLOC_SCRATCH_BYTES, or more than 160
+ * CTAs) returns DGL_ERR_SHAPE and enqueues nothing.  Problems without a
+ * partial last wave, and those on the decode path (m_valid <= 16), run as
+ * dgl_gemm_bf16 / dgl_gemm_fp8 would and do not touch the array.
+ *
+ * Set-up: the first call on a device (the current device) looks the array's
+ * address up and clears its flags, synchronously; make that first call
+ * before any stream capture.  Later calls only enqueue work.
+ * The array is shared by every call on a device and keeps what the last call
+ * left in it (each call tags its flags with a new epoch, so stale contents
+ * are never taken for fresh ones).  Calls whose kernels overlap on the GPU,
+ * for example on two streams, race on it: order them, or use dgl_gemm_bf16 /
+ * dgl_gemm_fp8.
+ */
+dgl_status dgl_gemm_noalloc(int32_t dtype, const void* A, const void* B, const float* sa, const float* sb,
+                            void* C, int64_t M, int64_t N, int64_t K, int64_t m_valid, int64_t n_valid,
+                            int32_t out_dtype, void* stream);
+
+/*
  * The plan the library would use for a problem of m x n x K (valid extents)
  * on a device with num_sms SMs (num_sms <= 0: query the current device).
  * Pure host logic when num_sms > 0: needs no GPU.
