@@ -44,6 +44,12 @@ constexpr int DEC_RING_BYTES = 196608;             // 192 KB of stages
 constexpr int DEC_SLACK_BYTES = 16384;
 constexpr int DEC_SMEM_BYTES = 1024 + DEC_RING_BYTES + DEC_SLACK_BYTES + 8 * (2 * DEC_MAX_STAGES + 5) + 8;
 constexpr int DEC_A_BOX_BYTES = 16 * 128;
+// Independent accumulators per part: the four MMAs of a 128-byte K step go to
+// four separate 16-column TMEM accumulators, so consecutive MMAs do not wait
+// on one another's result; the epilogue adds the four.
+constexpr int DEC_NACC = 4;
+constexpr int DEC_ACC_COLS = 16 * DEC_NACC;         // one accumulator buffer (of two)
+constexpr int DEC_TMEM_COLS = 2 * DEC_ACC_COLS;
 
 // Row range of part `part` of n rows cut into `parts` balanced pieces.
 __device__ __forceinline__ void part_rows(int part, int parts, int n, int& r0, int& r1) {
@@ -82,7 +88,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     fence_proxy_async_shared();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, 32);
+    tmem_alloc(tmem_slot, DEC_TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before_sync();
@@ -146,7 +152,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
           break;
         }
         tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + acc * 16;
+        const uint32_t d_tmem = tmem_base + acc * DEC_ACC_COLS;
         for (int kb0 = 0; kb0 < nk; kb0 += ks) {
           if (!mbar_wait(&full[stage], phase)) {
             fail = STATUS_TIMEOUT_MMA;
@@ -162,11 +168,11 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
             for (int k = 0; k < 4; ++k) {
               const uint64_t wd = smem_desc_sw128(w_addr + 32 * k);
               const uint64_t xd = smem_desc_sw128(x_addr + 32 * k);
-              const uint32_t accumulate = (kb0 | j | k) != 0;
+              const uint32_t accumulate_k = (kb0 | j) != 0;  // accumulator k starts at the part's first plane
               if constexpr (FP8)
-                umma_e4m3(d_tmem, wd, xd, idesc, accumulate);
+                umma_e4m3(d_tmem + 16 * k, wd, xd, idesc, accumulate_k);
               else
-                umma_bf16(d_tmem, wd, xd, idesc, accumulate);
+                umma_bf16(d_tmem + 16 * k, wd, xd, idesc, accumulate_k);
             }
           }
           issued_any = true;
@@ -200,9 +206,21 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
       }
       tc_fence_after_sync();
       uint32_t r[16];
-      tmem_ld_32x32b_x16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * 16, r);
-      tmem_ld_wait();
-      reg_fence16(r);
+      {
+        uint32_t r2[32];
+        const uint32_t t = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * DEC_ACC_COLS;
+        tmem_ld_32x32b_x32(t, r2);           // accumulators 0 and 1
+        tmem_ld_wait();
+        reg_fence(r2);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r2[i]) + __uint_as_float(r2[16 + i]));
+        tmem_ld_32x32b_x32(t + 32, r2);      // accumulators 2 and 3
+        tmem_ld_wait();
+        reg_fence(r2);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          r[i] = __float_as_uint(__uint_as_float(r[i]) + (__uint_as_float(r2[i]) + __uint_as_float(r2[16 + i])));
+      }
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -232,7 +250,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, 32);
+    tmem_dealloc(tmem_base, DEC_TMEM_COLS);
   }
 }
 
