@@ -1,4 +1,5 @@
-"""Reference oracle for C = A . B^T (bf16 and E4M3 inputs, fp64 arithmetic).
+"""Reference oracle for C = A . B^T (bf16 and E4M3 inputs, fp64 arithmetic),
+and for the linear layer around it (bias, GELU / SiLU, gated up projection).
 
 TEST INFRASTRUCTURE ONLY.  The product library never imports this package;
 only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
@@ -26,6 +27,10 @@ _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 
 BF16 = 0
 E4M3 = 1
+
+ACT_NONE = 0
+ACT_GELU = 1
+ACT_SILU = 2
 
 _lock = threading.Lock()
 _lib = None
@@ -56,6 +61,14 @@ def _bind(lib):
     lib.oracle_gemm_points.argtypes = [ctypes.c_int, vp, vp, vp, vp, c_i64, c_i64, c_i64,
                                        vp, vp, c_i64, vp, vp]
     lib.oracle_gemm_points.restype = ctypes.c_int
+    lib.oracle_act.argtypes = [ctypes.c_int, ctypes.c_double]
+    lib.oracle_act.restype = ctypes.c_double
+    lib.oracle_linear.argtypes = [ctypes.c_int, vp, vp, vp, vp, vp, c_i64, c_i64, c_i64, ctypes.c_int,
+                                  ctypes.c_int, vp, vp]
+    lib.oracle_linear.restype = ctypes.c_int
+    lib.oracle_linear_points.argtypes = [ctypes.c_int, vp, vp, vp, vp, vp, c_i64, c_i64, c_i64, ctypes.c_int,
+                                         ctypes.c_int, vp, vp, c_i64, vp, vp]
+    lib.oracle_linear_points.restype = ctypes.c_int
     lib.oracle_threads.argtypes = []
     lib.oracle_threads.restype = ctypes.c_int
     return lib
@@ -137,6 +150,69 @@ def gemm_points(dtype, A, B, rows, cols, sa=None, sb=None, lib=None):
     if rc != 0:
         raise ValueError("oracle_gemm_points rejected its arguments")
     return C, S
+
+
+def _linear_inputs(dtype, A, B, sa, sb, bias, gated):
+    A = _codes(A, dtype)
+    B = _codes(B, dtype)
+    m, K = A.shape
+    rows_b, K2 = B.shape
+    if K != K2:
+        raise ValueError("inner dimensions differ")
+    if gated and rows_b % 2:
+        raise ValueError("a gated layer's B holds 2n rows")
+    n = rows_b // 2 if gated else rows_b
+    if (sa is None) != (sb is None):
+        raise ValueError("give both scales or neither")
+    if sa is not None:
+        sa = np.ascontiguousarray(sa, dtype=np.float32)
+        sb = np.ascontiguousarray(sb, dtype=np.float32)
+        if sa.shape != (m,) or sb.shape != (rows_b,):
+            raise ValueError("scale lengths must be m and the rows of B")
+    if bias is not None:
+        bias = np.ascontiguousarray(bias, dtype=np.float32)
+        if bias.shape != (rows_b,):
+            raise ValueError("bias length must be the rows of B")
+    return A, B, sa, sb, bias, m, n, K
+
+
+def linear(dtype, A, B, sa=None, sb=None, bias=None, act=ACT_NONE, gated=False, lib=None):
+    """Reference linear layer: act(A . B^T (* scales) + bias), or with gated=True
+    act(gate + b_gate) * (up + b_up) where B = [gate rows; up rows].
+    Returns (Y_ref, E_abs), float64 [m, n]."""
+    lib = lib or load()
+    A, B, sa, sb, bias, m, n, K = _linear_inputs(dtype, A, B, sa, sb, bias, gated)
+    Y = np.empty((m, n), dtype=np.float64)
+    E = np.empty((m, n), dtype=np.float64)
+    rc = lib.oracle_linear(dtype, _ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(bias), m, n, K, int(act),
+                           int(bool(gated)), _ptr(Y), _ptr(E))
+    if rc != 0:
+        raise ValueError("oracle_linear rejected its arguments")
+    return Y, E
+
+
+def linear_points(dtype, A, B, rows, cols, sa=None, sb=None, bias=None, act=ACT_NONE, gated=False, lib=None):
+    """Reference linear layer at the points (rows[p], cols[p]); returns (Y_ref, E_abs)."""
+    lib = lib or load()
+    A, B, sa, sb, bias, m, n, K = _linear_inputs(dtype, A, B, sa, sb, bias, gated)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    cols = np.ascontiguousarray(cols, dtype=np.int64)
+    if rows.shape != cols.shape:
+        raise ValueError("rows and cols differ in length")
+    Y = np.empty(rows.shape, dtype=np.float64)
+    E = np.empty(rows.shape, dtype=np.float64)
+    rc = lib.oracle_linear_points(dtype, _ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(bias), m, n, K, int(act),
+                                  int(bool(gated)), _ptr(rows), _ptr(cols), rows.size, _ptr(Y), _ptr(E))
+    if rc != 0:
+        raise ValueError("oracle_linear_points rejected its arguments")
+    return Y, E
+
+
+def act(kind, x, lib=None):
+    """The activation alone, elementwise over doubles."""
+    lib = lib or load()
+    x = np.asarray(x, dtype=np.float64)
+    return np.array([lib.oracle_act(int(kind), float(v)) for v in x.ravel()]).reshape(x.shape)
 
 
 def decode_bf16(bits, lib=None):

@@ -194,6 +194,129 @@ int oracle_gemm_points(int dtype, const void* A, const void* B,
     return 0;
 }
 
+/*
+ * ---- The linear layer around the product ------------------------------------
+ *
+ * A linear layer adds a bias per output feature to the product, Y = X W^T + b
+ * ("GEMM analysis in TraceLens", section "Backward pass GEMMs": the forward
+ * operation Y = X @ W^T + b, whose bias gradient db has shape [d_ff]; the
+ * trace's aten::addmm is that call).  A feed-forward block applies an
+ * activation to the first projection (Funlib GEMM issue, section
+ * "Description": XW1 -> GELU -> XW2), and the LLaMA MLP pairs an up and a gate
+ * projection of the same shape ("GEMM analysis in TraceLens", section
+ * "Real-world example: LLaMA-2 7B").
+ *
+ *   act 0: identity;  act 1: GELU(x) = x * Phi(x), Phi the standard normal
+ *   distribution function (the exact, erf form);  act 2: SiLU(x) = x * sigma(x),
+ *   sigma the logistic function.
+ *
+ *   plain:  Y[i,j] = act(c(i, j) + bias[j])
+ *   gated:  Y[i,j] = act(c(i, j) + bias[j]) * (c(i, n + j) + bias[n + j])
+ *           B holds 2n rows: the gate projection's n rows, then the up
+ *           projection's n rows; sb and bias hold 2n entries in the same order.
+ * where c(i, r) is the (scaled) product of row i of A with row r of B as
+ * above, and bias may be NULL (all zeros).
+ *
+ * E_abs is the error scale of the tolerance test: how far Y may move when
+ * each product moves by its own allowance (which scales with S + |bias|).
+ * Plain: L * (S + |b|), with L = 1.2 bounding |act'| (GELU' <= 1.13,
+ * SiLU' <= 1.10).  Gated: |act(g)| * (S_up + |b_up|) + L * |u| * (S_g + |b_g|),
+ * to first order in the allowances.
+ */
+#define ORACLE_ACT_NONE 0
+#define ORACLE_ACT_GELU 1
+#define ORACLE_ACT_SILU 2
+
+double oracle_act(int act, double x)
+{
+    switch (act) {
+    case ORACLE_ACT_GELU: return x * 0.5 * erfc(-x / sqrt(2.0));   /* Phi(x) = erfc(-x / sqrt 2) / 2 */
+    case ORACLE_ACT_SILU: return x / (1.0 + exp(-x));
+    default: return x;
+    }
+}
+
+static double act_slope_bound(int act)
+{
+    return act == ORACLE_ACT_NONE ? 1.0 : 1.2;
+}
+
+static void linear_element(int dtype, const void* A, const void* B,
+                           const float* sa, const float* sb, const float* bias,
+                           int64_t n, int64_t K, int act, int gated,
+                           int64_t i, int64_t j, double* y_out, double* e_out)
+{
+    double g, sg;
+    one_element(dtype, A, B, sa, sb, K, i, j, &g, &sg);
+    const double bg = bias ? (double)bias[j] : 0.0;
+    const double x = g + bg;
+    const double ax = oracle_act(act, x);
+    const double L = act_slope_bound(act);
+    if (!gated) {
+        *y_out = ax;
+        *e_out = L * (sg + fabs(bg));
+        return;
+    }
+    double u, su;
+    one_element(dtype, A, B, sa, sb, K, i, n + j, &u, &su);
+    const double bu = bias ? (double)bias[n + j] : 0.0;
+    const double v = u + bu;
+    *y_out = ax * v;
+    *e_out = fabs(ax) * (su + fabs(bu)) + L * fabs(v) * (sg + fabs(bg));
+}
+
+static int linear_args_ok(int dtype, const void* A, const void* B, const float* sa, const float* sb,
+                          int64_t m, int64_t n, int64_t K, int act, int gated, const double* Y)
+{
+    return (dtype == ORACLE_BF16 || dtype == ORACLE_E4M3) && A && B && Y && m >= 0 && n >= 0 &&
+           K >= 0 && (sa == NULL) == (sb == NULL) && act >= ORACLE_ACT_NONE && act <= ORACLE_ACT_SILU &&
+           (gated == 0 || gated == 1);
+}
+
+/*
+ * The linear layer over the valid region: Y_ref[m*n] and E_abs[m*n]
+ * (row-major; E_abs may be NULL).  B has n rows (2n when gated).
+ * Returns 0, or -1 on a bad argument.
+ */
+int oracle_linear(int dtype, const void* A, const void* B,
+                  const float* sa, const float* sb, const float* bias,
+                  int64_t m, int64_t n, int64_t K, int act, int gated,
+                  double* Y_ref, double* E_abs)
+{
+    if (!linear_args_ok(dtype, A, B, sa, sb, m, n, K, act, gated, Y_ref)) return -1;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < m; ++i) {
+        for (int64_t j = 0; j < n; ++j) {
+            double y, e;
+            linear_element(dtype, A, B, sa, sb, bias, n, K, act, gated, i, j, &y, &e);
+            Y_ref[i * n + j] = y;
+            if (E_abs) E_abs[i * n + j] = e;
+        }
+    }
+    return 0;
+}
+
+/* The linear layer at a list of (row, col) points; as oracle_gemm_points. */
+int oracle_linear_points(int dtype, const void* A, const void* B,
+                         const float* sa, const float* sb, const float* bias,
+                         int64_t m, int64_t n, int64_t K, int act, int gated,
+                         const int64_t* rows, const int64_t* cols, int64_t npts,
+                         double* Y_ref, double* E_abs)
+{
+    if (!linear_args_ok(dtype, A, B, sa, sb, m, n, K, act, gated, Y_ref) || !rows || !cols || npts < 0)
+        return -1;
+    for (int64_t p = 0; p < npts; ++p)
+        if (rows[p] < 0 || rows[p] >= m || cols[p] < 0 || cols[p] >= n) return -1;
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t p = 0; p < npts; ++p) {
+        double y, e;
+        linear_element(dtype, A, B, sa, sb, bias, n, K, act, gated, rows[p], cols[p], &y, &e);
+        Y_ref[p] = y;
+        if (E_abs) E_abs[p] = e;
+    }
+    return 0;
+}
+
 /* Threads an OpenMP region of this library uses (1 without OpenMP). */
 int oracle_threads(void)
 {

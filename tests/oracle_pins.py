@@ -8,7 +8,11 @@ A check raises AssertionError when the oracle disagrees with:
   - torch's float32 -> bfloat16 round-to-nearest-even,
   - closed forms: identity and permutation products, rank-1 outer products,
     all-ones, scaled rank-1,
-  - brute force in exact rational arithmetic on tiny shapes.
+  - brute force in exact rational arithmetic on tiny shapes,
+  - for the linear layer: library routines for the normal distribution
+    function and the logistic function, the symmetry act(x) - act(-x) = x,
+    printed values (Phi(1), sigma(ln 3) = 3/4), and one-hot rows of A that
+    turn the product into a lookup of B, so bias, gate and up terms are exact.
 """
 from __future__ import annotations
 
@@ -178,9 +182,119 @@ def check_points_match_full(lib):
     np.testing.assert_array_equal(Sp, S[rows, cols])
 
 
+# ------------------------------------------------------------ the linear layer around the product
+E4M3_ONE = 0x38  # 1.0 in E4M3: exponent field 7 (bias 7), fraction 0
+
+
+def _ndtr(x):
+    from scipy.special import ndtr  # standard normal distribution function, a library routine
+    return ndtr(x)
+
+
+def _expit(x):
+    from scipy.special import expit  # the logistic function, a library routine
+    return expit(x)
+
+
+def _act_lib(kind, x):
+    x = np.asarray(x, dtype=np.float64)
+    if kind == oracle.ACT_GELU:
+        return x * _ndtr(x)
+    if kind == oracle.ACT_SILU:
+        return x * _expit(x)
+    return x
+
+
+def check_act_closed_forms(lib):
+    xs = np.array([-6.0, -3.0, -1.0, -0.5, -1e-3, 0.0, 1e-3, 0.5, 1.0, 2.0, 3.0, 6.0])
+    for kind in (oracle.ACT_NONE, oracle.ACT_GELU, oracle.ACT_SILU):
+        got = oracle.act(kind, xs, lib=lib)
+        np.testing.assert_allclose(got, _act_lib(kind, xs), rtol=1e-13, atol=1e-300)
+        if kind != oracle.ACT_NONE:
+            # act(x) - act(-x) = x: Phi(x) + Phi(-x) = 1 and sigma(x) + sigma(-x) = 1
+            np.testing.assert_allclose(got - oracle.act(kind, -xs, lib=lib), xs, rtol=1e-13, atol=1e-15)
+    # printed table values: Phi(1) = 0.8413447..., sigma(ln 3) = 3/4 exactly
+    assert abs(oracle.act(oracle.ACT_GELU, [1.0], lib=lib)[0] - 0.8413447460685429) < 1e-12
+    ln3 = float(np.log(3.0))
+    assert abs(oracle.act(oracle.ACT_SILU, [ln3], lib=lib)[0] - 0.75 * ln3) < 1e-15
+
+
+def _one_hot_rows(m, K, seed):
+    """A's rows are one-hot: row i has a single 1 at column k_i."""
+    ks = integers(seed, 0, (m,), 0, K - 1).astype(np.int64)
+    A = np.zeros((m, K))
+    A[np.arange(m), ks] = 1.0
+    return A, ks
+
+
+def check_linear_bias_onehot(lib):
+    m, n, K = 9, 13, 11
+    A, ks = _one_hot_rows(m, K, 5)
+    Bv = integers(5, 1, (n, K), -4, 4)
+    bias = (integers(5, 2, (n,), -8, 8) / 4.0).astype(np.float32)  # exact quarters
+    for kind in (oracle.ACT_NONE, oracle.ACT_GELU, oracle.ACT_SILU):
+        Y, E = oracle.linear(oracle.BF16, _bf16(A), _bf16(Bv), bias=bias, act=kind, lib=lib)
+        X = Bv[:, ks].T + bias[None, :].astype(np.float64)  # X[i, j] = B[j, k_i] + bias[j]
+        np.testing.assert_allclose(Y, _act_lib(kind, X), rtol=1e-13, atol=1e-300)
+        L = 1.0 if kind == oracle.ACT_NONE else 1.2
+        np.testing.assert_allclose(E, L * (np.abs(Bv[:, ks].T) + np.abs(bias)[None, :]), rtol=1e-15)
+
+
+def check_linear_gated_onehot(lib):
+    m, n, K = 7, 10, 9
+    A, ks = _one_hot_rows(m, K, 6)
+    Bg = integers(6, 1, (n, K), -4, 4)
+    Bu = integers(6, 3, (n, K), -4, 4)
+    bias = (integers(6, 2, (2 * n,), -8, 8) / 4.0).astype(np.float32)
+    for kind in (oracle.ACT_GELU, oracle.ACT_SILU):
+        Y, E = oracle.linear(oracle.BF16, _bf16(A), _bf16(np.vstack([Bg, Bu])), bias=bias, act=kind,
+                             gated=True, lib=lib)
+        G = Bg[:, ks].T + bias[None, :n].astype(np.float64)
+        U = Bu[:, ks].T + bias[None, n:].astype(np.float64)
+        np.testing.assert_allclose(Y, _act_lib(kind, G) * U, rtol=1e-13, atol=1e-300)
+        want_E = (np.abs(_act_lib(kind, G)) * (np.abs(Bu[:, ks].T) + np.abs(bias[None, n:]))
+                  + 1.2 * np.abs(U) * (np.abs(Bg[:, ks].T) + np.abs(bias[None, :n])))
+        np.testing.assert_allclose(E, want_E, rtol=1e-13, atol=1e-300)
+
+
+def check_linear_gated_scaled_e4m3(lib):
+    """E4M3 with per-row and per-column scales: the up half takes the scales and
+    bias of rows n .. 2n-1 of B."""
+    m, n, K = 6, 8, 16
+    ks = integers(7, 0, (m,), 0, K - 1).astype(np.int64)
+    A = np.zeros((m, K), dtype=np.uint8)
+    A[np.arange(m), ks] = E4M3_ONE
+    Bg = integers(7, 1, (n, K), -4, 4)
+    Bu = integers(7, 3, (n, K), -4, 4)
+    B = to_e4m3_codes(np.vstack([Bg, Bu]))
+    pick = np.array([0.5, 1.0, 2.0], dtype=np.float32)
+    sa = pick[integers(7, 4, (m,), 0, 2).astype(np.int64)]
+    sb = pick[integers(7, 5, (2 * n,), 0, 2).astype(np.int64)]
+    bias = (integers(7, 2, (2 * n,), -8, 8) / 4.0).astype(np.float32)
+    Y, _ = oracle.linear(oracle.E4M3, A, B, sa, sb, bias=bias, act=oracle.ACT_SILU, gated=True, lib=lib)
+    s_a = sa.astype(np.float64)[:, None]
+    G = Bg[:, ks].T * s_a * sb[None, :n] + bias[None, :n]
+    U = Bu[:, ks].T * s_a * sb[None, n:] + bias[None, n:]
+    np.testing.assert_allclose(Y, _act_lib(oracle.ACT_SILU, G) * U, rtol=1e-13, atol=1e-300)
+
+
+def check_linear_points_match_full(lib):
+    m, n, K = 21, 17, 40
+    A = _bf16(integers(8, 0, (m, K), -4, 4))
+    B = _bf16(integers(8, 1, (2 * n, K), -4, 4))
+    bias = (integers(8, 2, (2 * n,), -8, 8) / 8.0).astype(np.float32)
+    Y, E = oracle.linear(oracle.BF16, A, B, bias=bias, act=oracle.ACT_GELU, gated=True, lib=lib)
+    rows = np.array([0, m - 1, 4, 13])
+    cols = np.array([0, n - 1, 16, 2])
+    Yp, Ep = oracle.linear_points(oracle.BF16, A, B, rows, cols, bias=bias, act=oracle.ACT_GELU, gated=True, lib=lib)
+    np.testing.assert_array_equal(Yp, Y[rows, cols])
+    np.testing.assert_array_equal(Ep, E[rows, cols])
+
+
 ALL_CHECKS = [check_bf16_decoder, check_e4m3_decoder, check_round_bf16, check_identity,
               check_permutation, check_rank1, check_all_ones, check_scaled_rank1_e4m3,
-              check_brute_force, check_points_match_full]
+              check_brute_force, check_points_match_full, check_act_closed_forms, check_linear_bias_onehot,
+              check_linear_gated_onehot, check_linear_gated_scaled_e4m3, check_linear_points_match_full]
 
 
 def run_all(lib):

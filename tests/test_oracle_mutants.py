@@ -39,6 +39,16 @@ MUTANTS = {
     "round_half_up": ("double r = nearbyint(a / q);", "double r = floor(a / q + 0.5);"),
     # magnitude sum wrong
     "mag_signed": ("mag += fabs(p);", "mag += p;"),
+    # linear layer: activation constants and signs
+    "gelu_half_not_root2": ("x * 0.5 * erfc(-x / sqrt(2.0))", "x * 0.5 * erfc(-x / 2.0)"),
+    "gelu_sign": ("x * 0.5 * erfc(-x / sqrt(2.0))", "x * 0.5 * erfc(x / sqrt(2.0))"),
+    "silu_sign": ("return x / (1.0 + exp(-x));", "return x / (1.0 + exp(x));"),
+    # linear layer: bias and gate / up indexing
+    "bias_dropped": ("const double x = g + bg;", "const double x = g;"),
+    "bias_up_index": ("const double bu = bias ? (double)bias[n + j] : 0.0;", "const double bu = bias ? (double)bias[j] : 0.0;"),
+    "up_row_is_gate_row": ("one_element(dtype, A, B, sa, sb, K, i, n + j, &u, &su);", "one_element(dtype, A, B, sa, sb, K, i, j, &u, &su);"),
+    "gate_and_up_swapped": ("*y_out = ax * v;", "*y_out = oracle_act(act, v) * x;"),
+    "error_scale_drops_bias": ("*e_out = L * (sg + fabs(bg));", "*e_out = L * sg;"),
 }
 
 
