@@ -36,6 +36,8 @@ WORKLOAD_TEXT = {
     "square": "bf16 squares M=N=K in {2048,4096,8192}, A,B~N(0,1), bf16 C",
     "fp8": "E4M3 with per-row/per-column fp32 scales, bf16 C: (4096,4096,4096) (597,11008,4096) (16,11008,4096)",
     "square256": "bf16 256^3, fp32 C: uniform[-1,1] and integer [-4,4] variants",
+    "linear": "linear layers with fused epilogues, bf16 C: GPT-3-XL forward addmm 10240x8192x2048 + bias + GELU; "
+              "LLaMA-2-7B prefill up/gate pair 597x(2x11008)x4096 as one gated SiLU call, bf16 and E4M3",
 }
 
 
@@ -149,6 +151,16 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ CPU oracle timing
+def oracle_band(oracle, lib, c, rows):
+    """The oracle on the first `rows` rows of case c (the GEMM, or the linear layer)."""
+    dt = oracle.BF16 if c.dtype == "bf16" else oracle.E4M3
+    sa = c.sa[:rows] if c.sa is not None else None
+    if c.linear:
+        oracle.linear(dt, c.A[:rows], c.B, sa, c.sb, bias=c.bias, act=c.act, gated=c.gated, lib=lib)
+    else:
+        oracle.gemm(dt, c.A[:rows], c.B, sa, c.sb, lib=lib)
+
+
 def oracle_sample_run(cases, mac_budget):
     """Time the oracle on a bounded band of rows of every case; returns (flops, seconds, threads, text)."""
     import oracle
@@ -156,14 +168,12 @@ def oracle_sample_run(cases, mac_budget):
     per_case = mac_budget / max(1, len(cases))
     flops, secs, parts = 0.0, 0.0, []
     for c in cases:
-        rows = int(max(1, min(c.m, per_case // max(1, c.n * c.K))))
-        dt = oracle.BF16 if c.dtype == "bf16" else oracle.E4M3
-        sa = c.sa[:rows] if c.sa is not None else None
+        rows = int(max(1, min(c.m, per_case // max(1, c.b_rows * c.K))))
         t0 = time.perf_counter()
-        oracle.gemm(dt, c.A[:rows], c.B, sa, c.sb, lib=lib)
+        oracle_band(oracle, lib, c, rows)
         secs += time.perf_counter() - t0
-        flops += 2.0 * rows * c.n * c.K
-        parts.append(f"{rows}x{c.n}x{c.K}")
+        flops += 2.0 * rows * c.b_rows * c.K
+        parts.append(f"{rows}x{c.b_rows}x{c.K}")
     return flops, secs, oracle.threads(lib), "first rows of each GEMM: " + ", ".join(parts)
 
 
@@ -183,17 +193,15 @@ def run_reference(args):
     desc = []
     for s in range(total_steps):
         c = cases[s % len(cases)]
-        rows = int(max(1, min(c.m, budget_macs // max(1, c.n * c.K))))
-        dt = oracle.BF16 if c.dtype == "bf16" else oracle.E4M3
-        sa = c.sa[:rows] if c.sa is not None else None
+        rows = int(max(1, min(c.m, budget_macs // max(1, c.b_rows * c.K))))
         t0 = time.perf_counter()
-        oracle.gemm(dt, c.A[:rows], c.B, sa, c.sb, lib=lib)
+        oracle_band(oracle, lib, c, rows)
         el = time.perf_counter() - t0
         if s >= args.warmup:
-            flops_t += 2.0 * rows * c.n * c.K
+            flops_t += 2.0 * rows * c.b_rows * c.K
             secs_t += el
             if len(desc) < len(cases):
-                desc.append(f"{rows}x{c.n}x{c.K}")
+                desc.append(f"{rows}x{c.b_rows}x{c.K}")
     value = flops_t / secs_t / 1e12 if secs_t > 0 else 0.0
     cores = oracle.threads(lib)
     line = {
@@ -275,15 +283,23 @@ def main():
             sb = torch.from_numpy(c.sb).to(dev)
         out_dtype = dgl.OUT_F32 if c.out == "f32" else dgl.OUT_BF16
         C = torch.empty((c.m, c.n), dtype=torch.float32 if c.out == "f32" else torch.bfloat16, device=dev)
-        ops.append((c, A, B, sa, sb, C, out_dtype))
+        bias = torch.from_numpy(c.bias).to(dev) if c.bias is not None else None
+        ops.append((c, A, B, sa, sb, C, out_dtype, bias))
 
     forced = None
     if args.tile is not None:
         tm_, tn_ = (int(v) for v in args.tile.lower().split("x"))
         forced = dgl.PlanInfo(path=dgl.PATH_TC, tile_m=tm_, tile_n=tn_)
 
-    def make_call(c, A, B, sa, sb, C, out_dtype):
-        if forced is not None:
+    def make_call(c, A, B, sa, sb, C, out_dtype, bias):
+        if c.linear:
+            dt = dgl.DTYPE_BF16 if c.dtype == "bf16" else dgl.DTYPE_E4M3
+            args_ = (dt, A.data_ptr(), B.data_ptr(), sa.data_ptr() if sa is not None else None,
+                     sb.data_ptr() if sb is not None else None, bias.data_ptr() if bias is not None else None,
+                     C.data_ptr(), c.m, c.n, c.K, c.m, c.n, out_dtype, c.act, int(c.gated),
+                     ctypes.byref(forced) if forced is not None else None, s_handle)
+            fn = lib.dgl_linear
+        elif forced is not None:
             dt = dgl.DTYPE_BF16 if c.dtype == "bf16" else dgl.DTYPE_E4M3
             args_ = (dt, A.data_ptr(), B.data_ptr(), sa.data_ptr() if sa is not None else None,
                      sb.data_ptr() if sb is not None else None, C.data_ptr(), c.m, c.n, c.K, c.m, c.n, out_dtype,
@@ -304,7 +320,9 @@ def main():
         return call
 
     calls = [make_call(*o) for o in ops]
-    plans = [dgl.dgl_plan(0 if c.dtype == "bf16" else 1, c.m, c.n, c.K,
+    plans = [dgl.dgl_plan_linear(0 if c.dtype == "bf16" else 1, c.m, c.n, c.K,
+                                 dgl.OUT_F32 if c.out == "f32" else dgl.OUT_BF16, int(c.gated)) if c.linear else
+             dgl.dgl_plan(0 if c.dtype == "bf16" else 1, c.m, c.n, c.K,
                           dgl.OUT_F32 if c.out == "f32" else dgl.OUT_BF16) for c in cases]
     if forced is not None:
         plans = [forced for _ in cases]
@@ -319,15 +337,17 @@ def main():
             store = "tma-store"
         else:
             store = "predicated" if c.out == "f32" else "row-staging"
-        return f"tc_gemm_kernel<{c.dtype}, {p.tile_m}x{p.tile_n}, {store}>"
+        epi = ", linear" if c.linear else ""
+        return f"tc_gemm_kernel<{c.dtype}, {p.tile_m}x{p.tile_n}, {store}{epi}>"
 
     knames = [kernel_name(c, p) for c, p in zip(cases, plans)]
-    flops = [2.0 * c.m * c.n * c.K for c in cases]
+    flops = [float(c.flops) for c in cases]
     nbytes = []
     for c in cases:
         e = 2 if c.dtype == "bf16" else 1
         o = 4 if c.out == "f32" else 2
-        nbytes.append(c.m * c.K * e + c.n * c.K * e + c.m * c.n * o + (4 * (c.m + c.n) if c.dtype == "fp8" else 0))
+        nbytes.append(c.m * c.K * e + c.b_rows * c.K * e + c.m * c.n * o +
+                      (4 * (c.m + c.b_rows) if c.dtype == "fp8" else 0) + (4 * c.b_rows if c.bias is not None else 0))
 
     # warm-up
     for _ in range(args.warmup):
@@ -422,6 +442,8 @@ def main():
     for i, c in enumerate(cases):
         t = per_call_ms[i] * 1e-3
         per_shape.append({"shape": [c.m, c.n, c.K], "dtype": c.dtype, "out": c.out, "kernel": knames[i],
+                          "epilogue": ({"act": ["none", "gelu", "silu"][c.act], "bias": c.bias is not None,
+                                        "gated": c.gated} if c.linear else None),
                           "us": per_call_ms[i] * 1e3, "tflops": flops[i] / t / 1e12,
                           "gbs": nbytes[i] / t / 1e9, "tile_eff": round(plans[i].tile_eff, 4),
                           "wq_eff": round(plans[i].wq_eff, 4), "grid": plans[i].grid})
@@ -431,22 +453,27 @@ def main():
     if args.e2e_steps > 0:
         host = []
         h2d = d2h = 0
-        for (c, A, B, sa, sb, C, _o) in ops:
+        for (c, A, B, sa, sb, C, _o, bias) in ops:
             hA = torch.empty(A.shape, dtype=A.dtype, pin_memory=True).copy_(A.cpu())
             hB = torch.empty(B.shape, dtype=B.dtype, pin_memory=True).copy_(B.cpu())
             hsa = sa.cpu().pin_memory() if sa is not None else None
             hsb = sb.cpu().pin_memory() if sb is not None else None
             hC = torch.empty(C.shape, dtype=C.dtype, pin_memory=True)
-            host.append((hA, hB, hsa, hsb, hC))
+            hbias = bias.cpu().pin_memory() if bias is not None else None
+            host.append((hA, hB, hsa, hsb, hC, hbias))
             h2d += hA.numel() * hA.element_size() + hB.numel() * hB.element_size()
+            if hbias is not None:
+                h2d += 4 * hbias.numel()
             if hsa is not None:
                 h2d += 4 * (hsa.numel() + hsb.numel())
             d2h += hC.numel() * hC.element_size()
 
         def e2e_step():
-            for (c, A, B, sa, sb, C, _o), (hA, hB, hsa, hsb, hC), f in zip(ops, host, calls):
+            for (c, A, B, sa, sb, C, _o, bias), (hA, hB, hsa, hsb, hC, hbias), f in zip(ops, host, calls):
                 A.copy_(hA, non_blocking=True)
                 B.copy_(hB, non_blocking=True)
+                if bias is not None:
+                    bias.copy_(hbias, non_blocking=True)
                 if sa is not None:
                     sa.copy_(hsa, non_blocking=True)
                     sb.copy_(hsb, non_blocking=True)

@@ -32,9 +32,13 @@ DTYPE_E4M3 = 1
 PATH_TC = 0
 PATH_DECODE = 1
 PATH_EMPTY = 2
+ACT_NONE = 0
+ACT_GELU = 1
+ACT_SILU = 2
 
 EXPORTED = ["dgl_gemm_bf16", "dgl_gemm_fp8", "dgl_gemm_planned", "dgl_plan", "dgl_tile_metrics",
-            "dgl_device_status", "dgl_status_string", "dgl_version", "dgl_gemm_noalloc"]
+            "dgl_device_status", "dgl_status_string", "dgl_version", "dgl_gemm_noalloc", "dgl_linear",
+            "dgl_plan_linear"]
 
 
 class PlanInfo(ctypes.Structure):
@@ -76,6 +80,11 @@ def load_library(path: str | None = None):
     lib.dgl_gemm_planned.restype = i32
     lib.dgl_gemm_noalloc.argtypes = [i32, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i32, vp]
     lib.dgl_gemm_noalloc.restype = i32
+    lib.dgl_linear.argtypes = [i32, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i32, i32, i32,
+                               ctypes.POINTER(PlanInfo), vp]
+    lib.dgl_linear.restype = i32
+    lib.dgl_plan_linear.argtypes = [i32, i64, i64, i64, i32, i32, i32, ctypes.POINTER(PlanInfo)]
+    lib.dgl_plan_linear.restype = i32
     lib.dgl_plan.argtypes = [i32, i64, i64, i64, i32, i32, ctypes.POINTER(PlanInfo)]
     lib.dgl_plan.restype = i32
     lib.dgl_tile_metrics.argtypes = [i64, i64, i32, i32, i32, ctypes.POINTER(PlanInfo)]
@@ -123,9 +132,23 @@ def dgl_gemm_noalloc(dtype, A, B, sa, sb, C, M, N, K, m_valid=0, n_valid=0, out_
     return load_library().dgl_gemm_noalloc(dtype, A, B, sa, sb, C, M, N, K, m_valid, n_valid, out_dtype, stream)
 
 
+def dgl_linear(dtype, A, B, sa, sb, bias, C, M, N, K, m_valid=0, n_valid=0, out_dtype=OUT_BF16, act=0, gated=0,
+               plan: PlanInfo | None = None, stream=0) -> int:
+    """Linear layer act(A . B^T + bias), or the gated form (see include/dgl.h)."""
+    return load_library().dgl_linear(dtype, A, B, sa, sb, bias, C, M, N, K, m_valid, n_valid, out_dtype, act, gated,
+                                     ctypes.byref(plan) if plan is not None else None, stream)
+
+
 def dgl_plan(dtype, m, n, K, out_dtype=OUT_BF16, num_sms=0) -> PlanInfo:
     info = PlanInfo()
     _check(load_library().dgl_plan(dtype, m, n, K, out_dtype, num_sms, ctypes.byref(info)), "dgl_plan")
+    return info
+
+
+def dgl_plan_linear(dtype, m, n, K, out_dtype=OUT_BF16, gated=0, num_sms=0) -> PlanInfo:
+    info = PlanInfo()
+    _check(load_library().dgl_plan_linear(dtype, m, n, K, out_dtype, int(gated), num_sms, ctypes.byref(info)),
+           "dgl_plan_linear")
     return info
 
 
@@ -228,3 +251,39 @@ def device_status(stream=None) -> int:
 def build() -> str:
     from ._build import build as _b
     return _b()
+
+
+def linear(A, B, bias=None, out=None, *, act=ACT_NONE, gated=False, sa=None, sb=None, out_dtype=OUT_BF16,
+           stream=None, plan: PlanInfo | None = None):
+    """Linear layer with a fused epilogue: act(A . B^T + bias), or with
+    gated=True act(A . Bg^T + bg) * (A . Bu^T + bu) for B = [Bg; Bu] (2n rows).
+
+    A [m, K] and B are bf16 (or E4M3 with fp32 scales sa [m], sb [rows of B]);
+    bias is fp32 with one entry per row of B, or None.  Returns C [m, n].
+    """
+    import torch
+    e4m3 = A.dtype == torch.float8_e4m3fn
+    want = torch.float8_e4m3fn if e4m3 else torch.bfloat16
+    _check_operand(A, "A", want)
+    _check_operand(B, "B", want)
+    m, K = A.shape
+    rows_b, K2 = B.shape
+    if K != K2:
+        raise ValueError("inner dimensions differ")
+    if gated and rows_b % 2:
+        raise ValueError("a gated layer's B holds 2n rows: gate rows, then up rows")
+    n = rows_b // 2 if gated else rows_b
+    vecs = [("bias", bias, rows_b)] + ([("sa", sa, m), ("sb", sb, rows_b)] if e4m3 else [])
+    for name, v, length in vecs:
+        if v is None and name == "bias":
+            continue
+        if v is None or v.dtype != torch.float32 or not v.is_cuda or v.numel() != length or not v.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous fp32 CUDA tensor of length {length}")
+    C, ldc, rows = _out_tensor(out, m, n, out_dtype, A.device)
+    st = dgl_linear(DTYPE_E4M3 if e4m3 else DTYPE_BF16, A.data_ptr(), B.data_ptr(),
+                    sa.data_ptr() if e4m3 else None, sb.data_ptr() if e4m3 else None,
+                    bias.data_ptr() if bias is not None else None, C.data_ptr(), rows, ldc, K, m, n, out_dtype,
+                    int(act), int(bool(gated)), plan, _stream_handle(stream))
+    _check(st, "dgl_linear")
+    return C
+

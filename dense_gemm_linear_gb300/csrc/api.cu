@@ -242,6 +242,10 @@ struct Problem {
   const float *sa, *sb;
   void* C;
   int64_t M, N, K, m, n;
+  // linear-layer epilogue (dgl_linear): bias per column, activation, gated up projection
+  const float* bias = nullptr;
+  int act = 0;
+  int gated = 0;
 };
 
 dgl_status validate(Problem& pr) {
@@ -251,7 +255,10 @@ dgl_status validate(Problem& pr) {
   if (pr.m == 0) pr.m = pr.M;
   if (pr.n == 0) pr.n = pr.N;
   if (pr.m > pr.M || pr.n > pr.N) return DGL_ERR_ARG;
+  if (pr.act < DGL_ACT_NONE || pr.act > DGL_ACT_SILU || (pr.gated != 0 && pr.gated != 1)) return DGL_ERR_ARG;
   if (pr.M > INT32_MAX || pr.N > INT32_MAX || pr.K > INT32_MAX) return DGL_ERR_SHAPE;
+  if (pr.gated && 2 * pr.n > INT32_MAX) return DGL_ERR_SHAPE;  // B holds 2 n rows
+  if (pr.bias && !aligned(pr.bias, 4)) return DGL_ERR_ALIGN;
   if (pr.m == 0 || pr.n == 0) return DGL_OK;  // empty product
   if (!pr.C) return DGL_ERR_ARG;
   if (!aligned(pr.C, pr.out == DGL_OUT_F32 ? 4 : 2)) return DGL_ERR_ALIGN;
@@ -283,19 +290,25 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream, Sta
                : DGL_ERR_CUDA;
   }
 
+  // The linear-layer epilogue runs in its own kernel variants (128- and
+  // 256-wide tiles, CTA pairs when gated) and on the decode path (not gated).
+  const bool linear = pr.act != 0 || pr.bias != nullptr || pr.gated != 0;
   dgl_plan_info plan;
   if (forced) {
     if (forced->path == DGL_PATH_DECODE) {
-      if (pr.m > kDecodeMaxM) return DGL_ERR_UNSUPPORTED;
+      if (pr.m > kDecodeMaxM || pr.gated) return DGL_ERR_UNSUPPORTED;
       fill_decode_plan(pr.dtype, pr.out, pr.m, pr.n, pr.K, ds->num_sms, &plan);
     } else if (forced->path == DGL_PATH_TC) {
       if (!tc_supported_tile(forced->tile_m, forced->tile_n)) return DGL_ERR_UNSUPPORTED;
-      fill_tc_plan(pr.dtype, pr.out, pr.m, pr.n, pr.K, forced->tile_m, forced->tile_n, ds->num_sms, &plan,
-                   forced->stream_k ? 1 : 0);
+      if (linear && !tc_supported_epi_tile(forced->tile_m, forced->tile_n, pr.gated != 0)) return DGL_ERR_UNSUPPORTED;
+      fill_tc_plan(pr.dtype, pr.out, pr.m, pr.gated ? 2 * pr.n : pr.n, pr.K, forced->tile_m, forced->tile_n,
+                   ds->num_sms, &plan, forced->stream_k ? 1 : 0);
     } else {
       return DGL_ERR_UNSUPPORTED;
     }
     if (forced->grid > 0) plan.grid = forced->grid;
+  } else if (linear) {
+    choose_linear_plan(pr.dtype, pr.out, pr.m, pr.n, pr.K, pr.gated != 0, ds->num_sms, &plan);
   } else {
     PlanKey key{dev, pr.dtype, pr.out, pr.m, pr.n, pr.K};
     std::lock_guard<std::mutex> lock(g_mu);
@@ -343,6 +356,8 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream, Sta
     p.stage_bytes = decode_stage_bytes(rows_hi, ks);
     p.stages = decode_stages(rows_hi, ks);
     p.status = ds->status;
+    p.bias = pr.bias;
+    p.act = pr.act;
     const int grid = forced && forced->grid > 0 ? (forced->grid < parts ? forced->grid : parts)
                                                 : decode_grid(pr.n, ds->num_sms);
     return launch_decode(pr.dtype, pr.out, ta, tb_lo, tb_hi, p, grid, stream) == cudaSuccess ? DGL_OK
@@ -352,8 +367,10 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream, Sta
   CUtensorMap ta, tb, tc;
   // each CTA of a pair loads its own 128 rows of A and half the tile's rows of B
   const int cg = plan.cta_group == 2 ? 2 : 1;
+  // a gated layer's B holds the gate rows, then the up rows
+  const int64_t b_rows = pr.gated ? 2 * pr.n : pr.n;
   if (!cached_operand_map(&ta, pr.A, e4m3, pr.K, pr.m, 128) ||
-      !cached_operand_map(&tb, pr.B, e4m3, pr.K, pr.n, plan.tile_n / cg))
+      !cached_operand_map(&tb, pr.B, e4m3, pr.K, b_rows, plan.tile_n / cg))
     return DGL_ERR_CUDA;
   const bool f32 = pr.out == DGL_OUT_F32;
   const bool c_tma = aligned(pr.C, 16) && (pr.N * (f32 ? 4 : 2)) % 16 == 0;
@@ -368,12 +385,18 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream, Sta
   p.sa = pr.sa;
   p.sb = pr.sb;
   p.tiles_m = static_cast<int>((pr.m + plan.tile_m - 1) / plan.tile_m);
-  p.tiles_n = static_cast<int>((pr.n + plan.tile_n - 1) / plan.tile_n);
+  // a gated tile's MMA covers tile_n rows of B: tile_n / 2 output columns
+  const int out_w = pr.gated ? plan.tile_n / 2 : plan.tile_n;
+  p.tiles_n = static_cast<int>((pr.n + out_w - 1) / out_w);
   p.num_tiles = p.tiles_m * p.tiles_n;
   p.num_kb = static_cast<int>((pr.K * esize + 127) / 128);
   p.group_m = 16;
   p.c_tma = c_tma ? 1 : 0;
   p.status = ds->status;
+  p.bias = pr.bias;
+  p.act = pr.act;
+  p.gated = pr.gated;
+  p.n_up = static_cast<int>(pr.n);
   // grid counts CTAs; a pair per tile when cg == 2
   int grid = plan.grid > 0 ? plan.grid : p.num_tiles * cg;
   if (!plan.stream_k && grid > p.num_tiles * cg) grid = p.num_tiles * cg;
@@ -410,9 +433,13 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream, Sta
   }
   if (ds->smem_optin < 232448) return DGL_ERR_UNSUPPORTED;  // every variant is sized for 227 KB
   const bool row_staging = !c_tma && !f32;
-  const cudaError_t e =
-      e4m3 ? launch_tc_e4m3(pr.out, plan.tile_m, plan.tile_n, row_staging, ta, tb, tc, p, grid, stream)
-           : launch_tc_bf16(pr.out, plan.tile_m, plan.tile_n, row_staging, ta, tb, tc, p, grid, stream);
+  cudaError_t e;
+  if (linear)
+    e = e4m3 ? launch_tc_e4m3_epi(pr.out, plan.tile_m, plan.tile_n, row_staging, ta, tb, tc, p, grid, stream)
+             : launch_tc_bf16_epi(pr.out, plan.tile_m, plan.tile_n, row_staging, ta, tb, tc, p, grid, stream);
+  else
+    e = e4m3 ? launch_tc_e4m3(pr.out, plan.tile_m, plan.tile_n, row_staging, ta, tb, tc, p, grid, stream)
+             : launch_tc_bf16(pr.out, plan.tile_m, plan.tile_n, row_staging, ta, tb, tc, p, grid, stream);
   return e == cudaSuccess ? DGL_OK : DGL_ERR_CUDA;
 }
 
@@ -467,6 +494,17 @@ dgl_status dgl_gemm_planned(int32_t dtype, const void* A, const void* B, const f
   return run(pr, plan, static_cast<cudaStream_t>(stream));
 }
 
+dgl_status dgl_linear(int32_t dtype, const void* A, const void* B, const float* sa, const float* sb,
+                      const float* bias, void* C, int64_t M, int64_t N, int64_t K, int64_t m_valid, int64_t n_valid,
+                      int32_t out_dtype, int32_t act, int32_t gated, const dgl_plan_info* plan, void* stream) {
+  Problem pr{dtype, out_dtype, A, B, dtype == DGL_DTYPE_E4M3 ? sa : nullptr,
+             dtype == DGL_DTYPE_E4M3 ? sb : nullptr, C, M, N, K, m_valid, n_valid};
+  pr.bias = bias;
+  pr.act = act;
+  pr.gated = gated;
+  return run(pr, plan, static_cast<cudaStream_t>(stream));
+}
+
 dgl_status dgl_plan(int32_t dtype, int64_t m, int64_t n, int64_t K, int32_t out_dtype, int32_t num_sms,
                     dgl_plan_info* out) {
   if (!out) return DGL_ERR_ARG;
@@ -482,6 +520,24 @@ dgl_status dgl_plan(int32_t dtype, int64_t m, int64_t n, int64_t K, int32_t out_
     num_sms = ds->num_sms;
   }
   choose_plan(dtype, out_dtype, m, n, K, num_sms, out);
+  return DGL_OK;
+}
+
+dgl_status dgl_plan_linear(int32_t dtype, int64_t m, int64_t n, int64_t K, int32_t out_dtype, int32_t gated,
+                           int32_t num_sms, dgl_plan_info* out) {
+  if (!out) return DGL_ERR_ARG;
+  if (dtype != DGL_DTYPE_BF16 && dtype != DGL_DTYPE_E4M3) return DGL_ERR_ARG;
+  if (out_dtype != DGL_OUT_BF16 && out_dtype != DGL_OUT_F32) return DGL_ERR_ARG;
+  if (m < 0 || n < 0 || K < 0 || (gated != 0 && gated != 1)) return DGL_ERR_ARG;
+  if (m > INT32_MAX || 2 * n > INT32_MAX || K > INT32_MAX) return DGL_ERR_SHAPE;
+  if (num_sms <= 0) {
+    int dev = 0;
+    DeviceState* ds = nullptr;
+    const dgl_status st = get_device(&dev, &ds);
+    if (st != DGL_OK) return st;
+    num_sms = ds->num_sms;
+  }
+  choose_linear_plan(dtype, out_dtype, m, n, K, gated != 0, num_sms, out);
   return DGL_OK;
 }
 

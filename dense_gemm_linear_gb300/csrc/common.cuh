@@ -38,6 +38,14 @@ struct TcParams {
   float* ws;            // workers x CTAs-per-worker slots of 128 x BN fp32 partials
   int* flags;           // one per slot: the epoch of the partial it holds
   int epoch;            // differs from every earlier launch on this workspace
+  // Linear-layer epilogue: y = act(acc (* scales) + bias[col]); gated (CTA
+  // pairs only): B holds the gate rows, then the up rows from row n_up, and
+  // y = act(gate + bias[col]) * (up + bias[n_up + col]).  sb and bias follow
+  // B's rows.  bias may be null.
+  const float* bias;
+  int act;              // 0 identity, 1 GELU (x * Phi(x)), 2 SiLU (x * sigma(x))
+  int gated;
+  int n_up;
 };
 
 // Decode (m <= 16) kernel parameters.  A and B are read through tensor maps.
@@ -55,7 +63,43 @@ struct DecodeParams {
   int b_plane_bytes;    // one B box: rows_hi rounded up to 8, x 128 bytes
   int stage_bytes;      // ksteps x (A box (2 KB) + B box)
   int* status;          // device status word
+  const float* bias;    // linear-layer epilogue: bias per column of C, or null
+  int act;              // 0 identity, 1 GELU, 2 SiLU
 };
+
+// The activations of the linear-layer epilogue.
+//   GELU(x) = x * Phi(x), Phi(x) = (1 + erf(x / sqrt 2)) / 2.  erf(z) for
+//   z >= 0 is evaluated with formula 7.1.26 of Abramowitz and Stegun,
+//   "Handbook of Mathematical Functions" (1964): with t = 1 / (1 + p z),
+//   erf(z) = 1 - (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) e^{-z^2}, with an
+//   absolute error below 1.5e-7; erf is odd, which gives z < 0.
+//   SiLU(x) = x * sigma(x) = x / (1 + e^-x).
+// Both use the hardware exponential and reciprocal: the epilogue evaluates
+// one activation per output element and must stay shorter than the next
+// tile's MMAs.
+__device__ __forceinline__ float gelu_as7126(float x) {
+  const float z = fabsf(x) * 0.70710678118654752f;
+  const float t = __fdividef(1.0f, fmaf(0.3275911f, z, 1.0f));
+  float poly = fmaf(1.061405429f, t, -1.453152027f);
+  poly = fmaf(poly, t, 1.421413741f);
+  poly = fmaf(poly, t, -0.284496736f);
+  poly = fmaf(poly, t, 0.254829592f);
+  poly *= t;
+  const float tail = 0.5f * poly * __expf(-z * z);  // (1 - erf(z)) / 2 = Phi(-|x|)
+  const float phi = x >= 0.0f ? 1.0f - tail : tail;
+  return x * phi;
+}
+
+__device__ __forceinline__ float silu_fast(float x) {
+  // e^-x overflows below x = -88; sigma(x) x is then below 1e-36 in size
+  return x < -80.0f ? 0.0f * x : __fdividef(x, 1.0f + __expf(-x));
+}
+
+__device__ __forceinline__ float apply_act(int act, float x) {
+  if (act == 1) return gelu_as7126(x);
+  if (act == 2) return silu_fast(x);
+  return x;
+}
 
 // One piece of a worker's schedule: k-stages [kb0, kb1) of one tile.
 struct Segment {

@@ -228,11 +228,13 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
       if (col < r1) {
         float sbv = 1.0f;
         if constexpr (FP8) sbv = p.sb[col];
+        const float bv = p.bias ? p.bias[col] : 0.0f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           if (i < p.m) {
             float v = __uint_as_float(r[i]);
             if constexpr (FP8) v = (v * p.sa[i]) * sbv;
+            v = apply_act(p.act, v + bv);
             if constexpr (OUT_F32)
               static_cast<float*>(p.C)[static_cast<int64_t>(i) * p.ldc + col] = v;
             else

@@ -33,6 +33,14 @@ cudaError_t launch_tc_bf16(int out, int tile_m, int tile_n, bool row_staging, co
                            const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_tc_e4m3(int out, int tile_m, int tile_n, bool row_staging, const CUtensorMap& ta, const CUtensorMap& tb,
                            const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t stream);
+// The same with the linear-layer epilogue compiled in (p.bias, p.act,
+// p.gated); tile_n 128 or 256 only.
+cudaError_t launch_tc_bf16_epi(int out, int tile_m, int tile_n, bool row_staging, const CUtensorMap& ta,
+                               const CUtensorMap& tb, const CUtensorMap& tc, const TcParams& p, int grid,
+                               cudaStream_t stream);
+cudaError_t launch_tc_e4m3_epi(int out, int tile_m, int tile_n, bool row_staging, const CUtensorMap& ta,
+                               const CUtensorMap& tb, const CUtensorMap& tc, const TcParams& p, int grid,
+                               cudaStream_t stream);
 // Decode kernel: ta = A map (16-row box), tb_lo / tb_hi = B maps whose box
 // heights are the two part sizes floor(n/parts) and ceil(n/parts).
 cudaError_t launch_decode(int dtype, int out, const CUtensorMap& ta, const CUtensorMap& tb_lo,

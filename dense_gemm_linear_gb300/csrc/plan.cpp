@@ -249,3 +249,34 @@ void choose_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int 
 }
 
 }  // namespace dgl
+
+namespace dgl {
+
+bool tc_supported_epi_tile(int tile_m, int tile_n, bool gated) {
+  if (!tc_supported_tile(tile_m, tile_n) || (tile_n != 128 && tile_n != 256)) return false;
+  return !gated || tile_m == 256;
+}
+
+void choose_linear_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, bool gated, int num_sms,
+                        dgl_plan_info* out) {
+  if (!gated) {
+    choose_plan(dtype, out_dtype, m, n, K, num_sms, out);
+    if (out->path == DGL_PATH_TC && !tc_supported_epi_tile(out->tile_m, out->tile_n, false))
+      fill_tc_plan(dtype, out_dtype, m, n, K, out->tile_m, 128, num_sms, out, 0);
+    return;
+  }
+  // gate and up rows side by side: a product with 2 n rows of B on CTA pairs
+  dgl_plan_info best{};
+  bool have = false;
+  for (int tile_n : {256, 128}) {
+    dgl_plan_info cand;
+    fill_tc_plan(dtype, out_dtype, m, 2 * n, K, 256, tile_n, num_sms, &cand, 0);
+    if (!have || cand.est_us < best.est_us * 0.97) {
+      best = cand;
+      have = true;
+    }
+  }
+  *out = best;
+}
+
+}  // namespace dgl

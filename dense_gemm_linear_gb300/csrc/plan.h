@@ -25,6 +25,13 @@ int decode_plane_bytes(int rows_hi);               // one B box: rows_hi rounded
 int decode_stage_bytes(int rows_hi, int ksteps);   // ksteps x (16-row A box + B box)
 int decode_stages(int rows_hi, int ksteps);        // ring depth in 192 KB, at most 32
 int decode_ksteps(int rows_hi, int nk);            // 128-byte K steps per stage
+// Tiles with a linear-layer epilogue variant: 128 or 256 wide, and CTA pairs
+// (tile_m 256) when gated.
+bool tc_supported_epi_tile(int tile_m, int tile_n, bool gated);
+// The plan of a linear layer (dgl_linear): as choose_plan, restricted to the
+// tiles above; a gated layer is planned as a product with 2 n rows of B.
+void choose_linear_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, bool gated, int num_sms,
+                        dgl_plan_info* out);
 void choose_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int num_sms, dgl_plan_info* out);
 
 }  // namespace dgl

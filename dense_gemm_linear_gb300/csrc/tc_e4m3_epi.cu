@@ -1,0 +1,13 @@
+// E4M3 x E4M3 -> fp32 accumulate instantiations of the tcgen05 tile kernel with
+// the linear-layer epilogue (bias, activation, gated up projection on CTA pairs).
+#include "tc_launch.cuh"
+
+namespace dgl {
+
+cudaError_t launch_tc_e4m3_epi(int out, int tile_m, int tile_n, bool row_staging, const CUtensorMap& ta,
+                             const CUtensorMap& tb, const CUtensorMap& tc, const TcParams& p, int grid,
+                             cudaStream_t stream) {
+  return tc_launch<true, true>(out, tile_m, tile_n, row_staging, ta, tb, tc, p, grid, stream);
+}
+
+}  // namespace dgl

@@ -51,9 +51,12 @@ constexpr int tc_ring_stages(int stage_bytes, int staging_bytes) {
   return s < 8 ? s : 8;
 }
 
-template <int BN_, bool FP8_, bool OUT_F32_, bool ROWSTG_, int CG_ = 1>
+template <int BN_, bool FP8_, bool OUT_F32_, bool ROWSTG_, int CG_ = 1, bool EPI_ = false>
 struct TcConfig {
   static constexpr int CG = CG_;                        // CTAs per MMA: 1, or 2 for a CTA pair (M = 256)
+  // EPI: the linear-layer epilogue (bias, activation, and on CTA pairs the
+  // gated up projection) is compiled in; plain GEMM variants leave it out.
+  static constexpr bool EPI = EPI_;
   static constexpr int BM = 128;                        // rows of C per CTA
   static constexpr int TILE_M = BM * CG;                // rows of C per tile
   static constexpr int BN = BN_;                        // columns of C per tile
@@ -222,7 +225,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         int mb, nb;
         tile_coords(sg.tile, p.tiles_m, p.tiles_n, p.group_m, mb, nb);
         const int a_row = mb * Cfg::TILE_M + static_cast<int>(rank) * BM;
-        const int b_row = nb * BN + static_cast<int>(rank) * Cfg::B_ROWS;
+        // gated pairs: the leader loads gate rows, the peer the matching up rows
+        const int b_row = (Cfg::EPI && CG == 2 && p.gated) ? (rank == 0 ? 0 : p.n_up) + nb * Cfg::B_ROWS
+                                               : nb * BN + static_cast<int>(rank) * Cfg::B_ROWS;
         for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
           const bool ok = mbar_wait(&empty[stage], phase ^ 1);
           if (!ok) {
@@ -488,145 +493,209 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         }
       }
 
-      // The warp's share of the accumulator is read G chunks at a time, which
-      // bounds the registers it holds; the buffer goes back to the MMA once
-      // the last chunk has been read.
-      constexpr int G = CPW > 2 ? 2 : CPW;
+      // Output columns of this tile: BN, or BN / 2 when a gated pair's MMA
+      // computes the gate (leader's B rows) and up (peer's B rows) halves.
+      const bool gated = Cfg::EPI && CG == 2 && p.gated != 0;
+      const int out_w = gated ? BN / 2 : BN;
+      const int ocol0 = nb * out_w;
       float row_scale = 0.0f;
       if constexpr (Cfg::FP8) row_scale = (row0 + lane < p.m) ? p.sa[row0 + lane] : 0.0f;
       // row staging (bf16 C, rows not 16-byte aligned): this thread's row
       const int row = row0 + lane;
-      const int ncols = min(BN, p.n - nb * BN);
+      const int ncols = min(out_w, p.n - ocol0);
       const int L = (Cfg::ROWSTG && row < p.m) ? 2 * ncols : 0;  // valid bytes of the row's segment
       uint8_t* rowp = L > 0 ? reinterpret_cast<uint8_t*>(static_cast<__nv_bfloat16*>(p.C) +
-                                                         static_cast<int64_t>(row) * p.ldc + nb * BN)
+                                                         static_cast<int64_t>(row) * p.ldc + ocol0)
                             : nullptr;
       const int delta = static_cast<int>(reinterpret_cast<uintptr_t>(rowp) & 15);
       const uint32_t srow = stg_addr + lane * Cfg::ROW_PITCH + delta;  // staged byte 0 of the segment
       uint32_t buf = 0;
-#pragma unroll
-      for (int g0 = 0; g0 < CPW; g0 += G) {
-        uint32_t r[G][32];
-#pragma unroll
-        for (int uu = 0; uu < G; ++uu) tmem_ld_32x32b_x32(t_row + (half * CPW + g0 + uu) * 32, r[uu]);
-        tmem_ld_wait();
-#pragma unroll
-        for (int uu = 0; uu < G; ++uu) reg_fence(r[uu]);
-        if (g0 + G == CPW) {
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) {
-            if constexpr (CG == 2)
-              mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));  // the leader's MMA waits on it
-            else
-              mbar_arrive(&tempty[acc]);
-          }
-        }
 
-        if constexpr (Cfg::FP8) {
-#pragma unroll
-          for (int uu = 0; uu < G; ++uu) {
-            const int col0 = nb * BN + (half * CPW + g0 + uu) * 32;
-            const float col_scale = (col0 + lane < p.n) ? p.sb[col0 + lane] : 0.0f;
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              r[uu][j] = __float_as_uint((__uint_as_float(r[uu][j]) * row_scale) *
-                                         __shfl_sync(0xffffffffu, col_scale, j));
-          }
-        }
-
+      // Rounds output chunk `oc` (columns ocol0 + 32 oc ..; this thread's row
+      // in v) and stores it, or stages it for the row copy below.
+      auto emit = [&](uint32_t(&v)[32], int oc) {
         if constexpr (Cfg::ROWSTG) {
           // ---- stage whole rows, shifted by each row's misalignment
+          uint32_t w[16];
 #pragma unroll
-          for (int uu = 0; uu < G; ++uu) {
-            uint32_t w[16];
+          for (int t = 0; t < 16; ++t) {
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[2 * t]), __uint_as_float(v[2 * t + 1]));
+            w[t] = *reinterpret_cast<uint32_t*>(&h2);
+          }
+          const uint32_t base = srow + 64 * oc;
+          if ((delta & 2) == 0) {
 #pragma unroll
-            for (int t = 0; t < 16; ++t) {
-              __nv_bfloat162 h2 =
-                  __floats2bfloat162_rn(__uint_as_float(r[uu][2 * t]), __uint_as_float(r[uu][2 * t + 1]));
-              w[t] = *reinterpret_cast<uint32_t*>(&h2);
-            }
-            const uint32_t base = srow + 64 * (half * CPW + g0 + uu);
-            if ((delta & 2) == 0) {
+            for (int t = 0; t < 16; ++t) sts_u32(base + 4 * t, w[t]);
+          } else {
+            sts_u16(base, w[0] & 0xFFFFu);
 #pragma unroll
-              for (int t = 0; t < 16; ++t) sts_u32(base + 4 * t, w[t]);
-            } else {
-              sts_u16(base, w[0] & 0xFFFFu);
-#pragma unroll
-              for (int t = 0; t < 15; ++t) sts_u32(base + 2 + 4 * t, __byte_perm(w[t], w[t + 1], 0x5432));
-              sts_u16(base + 62, w[15] >> 16);
-            }
+            for (int t = 0; t < 15; ++t) sts_u32(base + 2 + 4 * t, __byte_perm(w[t], w[t + 1], 0x5432));
+            sts_u16(base + 62, w[15] >> 16);
           }
         } else {
           // bf16 chunks alternate between two 2 KB staging tiles, so a chunk's
           // TMA store may still be reading one while the next chunk fills the
           // other; fp32 chunks fill the whole 4 KB tile.
+          const int col0 = ocol0 + oc * 32;
+          uint8_t* stg_u = stg + buf * Cfg::STG_BYTES;
+          const uint32_t stg_addr_u = stg_addr + buf * Cfg::STG_BYTES;
+          // the store that last used this staging tile has finished reading it
+          if (p.c_tma && lane == 0) {
+            if constexpr (Cfg::OUT_F32)
+              bulk_wait_read0();
+            else
+              bulk_wait_read1();
+          }
+          __syncwarp();
+          // this thread's row (lane) of the 32 x 32 chunk -> staging, 16 bytes at a time
+          if constexpr (Cfg::OUT_F32) {
 #pragma unroll
-          for (int uu = 0; uu < G; ++uu) {
-            const int col0 = nb * BN + (half * CPW + g0 + uu) * 32;
-            uint8_t* stg_u = stg + buf * Cfg::STG_BYTES;
-            const uint32_t stg_addr_u = stg_addr + buf * Cfg::STG_BYTES;
-            // the store that last used this staging tile has finished reading it
-            if (p.c_tma && lane == 0) {
-              if constexpr (Cfg::OUT_F32)
-                bulk_wait_read0();
-              else
-                bulk_wait_read1();
+            for (int c16 = 0; c16 < 8; ++c16)
+              sts_v4(stg_addr_u + stg_offset<Cfg::STG_ROW>(lane, c16), v[4 * c16], v[4 * c16 + 1], v[4 * c16 + 2],
+                     v[4 * c16 + 3]);
+          } else {
+#pragma unroll
+            for (int c16 = 0; c16 < 4; ++c16) {
+              uint32_t w[4];
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                __nv_bfloat162 h2 =
+                    __floats2bfloat162_rn(__uint_as_float(v[8 * c16 + 2 * t]), __uint_as_float(v[8 * c16 + 2 * t + 1]));
+                w[t] = *reinterpret_cast<uint32_t*>(&h2);
+              }
+              sts_v4(stg_addr_u + stg_offset<Cfg::STG_ROW>(lane, c16), w[0], w[1], w[2], w[3]);
+            }
+          }
+          // A TMA store writes whole 16-byte units of a row, so a chunk that
+          // ends inside one (n * element size not a multiple of 16) takes the
+          // predicated path instead.
+          const bool tma_ok = p.c_tma && (col0 + 32 <= p.n || (p.n * Cfg::OUT_BYTES) % 16 == 0);
+          if (tma_ok) {
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0 && row0 < p.m && col0 < p.n) {
+              tma_store_2d(&tmC, stg_u, col0, row0);
+              bulk_commit();
+            }
+          } else {
+            __syncwarp();
+            // one row per step, a column per lane
+            const int col = col0 + lane;
+#pragma unroll 4
+            for (int rr = 0; rr < 32; ++rr) {
+              const int grow = row0 + rr;
+              if (grow < p.m && col < p.n) {
+                if constexpr (Cfg::OUT_F32) {
+                  const float y =
+                      *reinterpret_cast<const float*>(stg_u + stg_offset<128>(rr, lane >> 2) + (lane & 3) * 4);
+                  static_cast<float*>(p.C)[static_cast<int64_t>(grow) * p.ldc + col] = y;
+                } else {
+                  const uint16_t y =
+                      *reinterpret_cast<const uint16_t*>(stg_u + stg_offset<64>(rr, lane >> 3) + (lane & 7) * 2);
+                  reinterpret_cast<uint16_t*>(p.C)[static_cast<int64_t>(grow) * p.ldc + col] = y;
+                }
+              }
             }
             __syncwarp();
-            // this thread's row (lane) of the 32 x 32 chunk -> staging, 16 bytes at a time
-            if constexpr (Cfg::OUT_F32) {
-#pragma unroll
-              for (int c16 = 0; c16 < 8; ++c16)
-                sts_v4(stg_addr_u + stg_offset<Cfg::STG_ROW>(lane, c16), r[uu][4 * c16], r[uu][4 * c16 + 1],
-                       r[uu][4 * c16 + 2], r[uu][4 * c16 + 3]);
-            } else {
-#pragma unroll
-              for (int c16 = 0; c16 < 4; ++c16) {
-                uint32_t w[4];
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                  __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(r[uu][8 * c16 + 2 * t]),
-                                                            __uint_as_float(r[uu][8 * c16 + 2 * t + 1]));
-                  w[t] = *reinterpret_cast<uint32_t*>(&h2);
-                }
-                sts_v4(stg_addr_u + stg_offset<Cfg::STG_ROW>(lane, c16), w[0], w[1], w[2], w[3]);
-              }
-            }
-            // A TMA store writes whole 16-byte units of a row, so a chunk that
-            // ends inside one (n * element size not a multiple of 16) takes the
-            // predicated path instead.
-            const bool tma_ok = p.c_tma && (col0 + 32 <= p.n || (p.n * Cfg::OUT_BYTES) % 16 == 0);
-            if (tma_ok) {
-              fence_proxy_async_shared();
-              __syncwarp();
-              if (lane == 0 && row0 < p.m && col0 < p.n) {
-                tma_store_2d(&tmC, stg_u, col0, row0);
-                bulk_commit();
-              }
-            } else {
-              __syncwarp();
-              // one row per step, a column per lane
-              const int col = col0 + lane;
-#pragma unroll 4
-              for (int rr = 0; rr < 32; ++rr) {
-                const int grow = row0 + rr;
-                if (grow < p.m && col < p.n) {
-                  if constexpr (Cfg::OUT_F32) {
-                    const float v =
-                        *reinterpret_cast<const float*>(stg_u + stg_offset<128>(rr, lane >> 2) + (lane & 3) * 4);
-                    static_cast<float*>(p.C)[static_cast<int64_t>(grow) * p.ldc + col] = v;
-                  } else {
-                    const uint16_t v =
-                        *reinterpret_cast<const uint16_t*>(stg_u + stg_offset<64>(rr, lane >> 3) + (lane & 7) * 2);
-                    reinterpret_cast<uint16_t*>(p.C)[static_cast<int64_t>(grow) * p.ldc + col] = v;
-                  }
-                }
-              }
-              __syncwarp();
-            }
-            if constexpr (!Cfg::OUT_F32) buf ^= 1u;
           }
+          if constexpr (!Cfg::OUT_F32) buf ^= 1u;
+        }
+      };
+      auto hand_back = [&]() {
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (CG == 2)
+            mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));  // the leader's MMA waits on it
+          else
+            mbar_arrive(&tempty[acc]);
+        }
+      };
+
+      bool gated_done = false;
+      if constexpr (Cfg::EPI && CG == 2) {
+        if (gated) {
+          gated_done = true;
+          // ---- gated linear layer: output chunk oc combines gate chunk oc with
+          // up chunk oc + CHUNKS / 2; this warp takes CPW / 2 output chunks.
+          constexpr int OCPW = CPW / 2 > 0 ? CPW / 2 : 1;
+  #pragma unroll 1
+          for (int u = 0; u < OCPW; ++u) {
+            const int oc = half * OCPW + u;
+            uint32_t g[32], v[32];
+            tmem_ld_32x32b_x32(t_row + oc * 32, g);
+            tmem_ld_32x32b_x32(t_row + (oc + Cfg::CHUNKS / 2) * 32, v);
+            tmem_ld_wait();
+            reg_fence(g);
+            reg_fence(v);
+            if (u + 1 == OCPW) hand_back();
+            const int col = ocol0 + oc * 32 + lane;
+            const bool in = col < p.n;
+            float sg = 1.0f, su = 1.0f, bg = 0.0f, bu = 0.0f;
+            if constexpr (Cfg::FP8) {
+              sg = in ? p.sb[col] : 0.0f;
+              su = in ? p.sb[p.n_up + col] : 0.0f;
+            }
+            if (p.bias && in) {
+              bg = p.bias[col];
+              bu = p.bias[p.n_up + col];
+            }
+  #pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              float x = __uint_as_float(g[j]), y = __uint_as_float(v[j]);
+              if constexpr (Cfg::FP8) {
+                x = (x * row_scale) * __shfl_sync(0xffffffffu, sg, j);
+                y = (y * row_scale) * __shfl_sync(0xffffffffu, su, j);
+              }
+              x = apply_act(p.act, x + __shfl_sync(0xffffffffu, bg, j));
+              y += __shfl_sync(0xffffffffu, bu, j);
+              v[j] = __float_as_uint(x * y);
+            }
+            emit(v, oc);
+          }
+        }
+      }
+      if (!gated_done) {
+        // The warp's share of the accumulator is read G chunks at a time,
+        // which bounds the registers it holds; the buffer goes back to the MMA
+        // once the last chunk has been read.
+        constexpr int G = CPW > 2 ? 2 : CPW;
+        const bool epi = Cfg::EPI && (p.act != 0 || p.bias != nullptr);
+#pragma unroll
+        for (int g0 = 0; g0 < CPW; g0 += G) {
+          uint32_t r[G][32];
+#pragma unroll
+          for (int uu = 0; uu < G; ++uu) tmem_ld_32x32b_x32(t_row + (half * CPW + g0 + uu) * 32, r[uu]);
+          tmem_ld_wait();
+#pragma unroll
+          for (int uu = 0; uu < G; ++uu) reg_fence(r[uu]);
+          if (g0 + G == CPW) hand_back();
+
+          if constexpr (Cfg::FP8) {
+#pragma unroll
+            for (int uu = 0; uu < G; ++uu) {
+              const int col0 = ocol0 + (half * CPW + g0 + uu) * 32;
+              const float col_scale = (col0 + lane < p.n) ? p.sb[col0 + lane] : 0.0f;
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                r[uu][j] = __float_as_uint((__uint_as_float(r[uu][j]) * row_scale) *
+                                           __shfl_sync(0xffffffffu, col_scale, j));
+            }
+          }
+          if (Cfg::EPI && epi) {
+            // linear-layer epilogue: bias per column, then the activation
+#pragma unroll
+            for (int uu = 0; uu < G; ++uu) {
+              const int col = ocol0 + (half * CPW + g0 + uu) * 32 + lane;
+              const float b = (p.bias && col < p.n) ? p.bias[col] : 0.0f;
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                r[uu][j] = __float_as_uint(
+                    apply_act(p.act, __uint_as_float(r[uu][j]) + __shfl_sync(0xffffffffu, b, j)));
+            }
+          }
+#pragma unroll
+          for (int uu = 0; uu < G; ++uu) emit(r[uu], half * CPW + g0 + uu);
         }
       }
 

@@ -10,10 +10,10 @@
 
 namespace dgl {
 
-template <int BN, bool FP8, bool OUT_F32, bool ROWSTG, int CG>
+template <int BN, bool FP8, bool OUT_F32, bool ROWSTG, int CG, bool EPI>
 cudaError_t tc_launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const TcParams& p,
                           int grid, cudaStream_t stream) {
-  using Cfg = TcConfig<BN, FP8, OUT_F32, ROWSTG, CG>;
+  using Cfg = TcConfig<BN, FP8, OUT_F32, ROWSTG, CG, EPI>;
   auto kern = tc_gemm_kernel<Cfg>;
   static std::atomic<uint64_t> attr_done{0};  // one bit per device
   cudaError_t e = set_smem_attr_once(kern, Cfg::SMEM_BYTES, attr_done);
@@ -39,29 +39,33 @@ cudaError_t tc_launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CU
   }
 }
 
-template <int BN, bool FP8, int CG>
+template <int BN, bool FP8, int CG, bool EPI>
 cudaError_t tc_launch_bn(int out, bool row_staging, const CUtensorMap& ta, const CUtensorMap& tb,
                          const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t stream) {
-  if (out == 1) return tc_launch_one<BN, FP8, true, false, CG>(ta, tb, tc, p, grid, stream);
-  if (row_staging) return tc_launch_one<BN, FP8, false, true, CG>(ta, tb, tc, p, grid, stream);
-  return tc_launch_one<BN, FP8, false, false, CG>(ta, tb, tc, p, grid, stream);
+  if (out == 1) return tc_launch_one<BN, FP8, true, false, CG, EPI>(ta, tb, tc, p, grid, stream);
+  if (row_staging) return tc_launch_one<BN, FP8, false, true, CG, EPI>(ta, tb, tc, p, grid, stream);
+  return tc_launch_one<BN, FP8, false, false, CG, EPI>(ta, tb, tc, p, grid, stream);
 }
 
-template <bool FP8>
+// EPI: the linear-layer variants, compiled for the 128- and 256-wide tiles
+// only (tc_supported_epi_tile); the plain variants cover the whole ladder.
+template <bool FP8, bool EPI>
 cudaError_t tc_launch(int out, int tile_m, int tile_n, bool row_staging, const CUtensorMap& ta, const CUtensorMap& tb,
                       const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t stream) {
   if (tile_m == 128) {
     switch (tile_n) {
-      case 64: return tc_launch_bn<64, FP8, 1>(out, row_staging, ta, tb, tc, p, grid, stream);
-      case 128: return tc_launch_bn<128, FP8, 1>(out, row_staging, ta, tb, tc, p, grid, stream);
-      case 256: return tc_launch_bn<256, FP8, 1>(out, row_staging, ta, tb, tc, p, grid, stream);
+      case 64:
+        if constexpr (EPI) return cudaErrorInvalidValue;
+        else return tc_launch_bn<64, FP8, 1, EPI>(out, row_staging, ta, tb, tc, p, grid, stream);
+      case 128: return tc_launch_bn<128, FP8, 1, EPI>(out, row_staging, ta, tb, tc, p, grid, stream);
+      case 256: return tc_launch_bn<256, FP8, 1, EPI>(out, row_staging, ta, tb, tc, p, grid, stream);
       default: return cudaErrorInvalidValue;
     }
   }
   if (tile_m == 256) {
     switch (tile_n) {
-      case 128: return tc_launch_bn<128, FP8, 2>(out, row_staging, ta, tb, tc, p, grid, stream);
-      case 256: return tc_launch_bn<256, FP8, 2>(out, row_staging, ta, tb, tc, p, grid, stream);
+      case 128: return tc_launch_bn<128, FP8, 2, EPI>(out, row_staging, ta, tb, tc, p, grid, stream);
+      case 256: return tc_launch_bn<256, FP8, 2, EPI>(out, row_staging, ta, tb, tc, p, grid, stream);
       default: return cudaErrorInvalidValue;
     }
   }

@@ -69,6 +69,10 @@ typedef enum {
 typedef enum { DGL_OUT_BF16 = 0, DGL_OUT_F32 = 1 } dgl_out_t;
 typedef enum { DGL_DTYPE_BF16 = 0, DGL_DTYPE_E4M3 = 1 } dgl_dtype_t;
 typedef enum { DGL_PATH_TC = 0, DGL_PATH_DECODE = 1, DGL_PATH_EMPTY = 2 } dgl_path_t;
+/* Activations of dgl_linear: GELU(x) = x * Phi(x) (Phi the standard normal
+ * distribution function, the exact erf form); SiLU(x) = x * sigma(x) (sigma
+ * the logistic function). */
+typedef enum { DGL_ACT_NONE = 0, DGL_ACT_GELU = 1, DGL_ACT_SILU = 2 } dgl_act_t;
 
 /*
  * A launch plan: the path, the tile of the tile ladder, and the cost-model
@@ -169,6 +173,32 @@ dgl_status dgl_gemm_noalloc(int32_t dtype, const void* A, const void* B, const f
                             int32_t out_dtype, void* stream);
 
 /*
+ * A linear layer: the GEMM above with its epilogue fused into the kernel
+ * (Funlib GEMM issue, section "Investigate later optimizations": fused bias
+ * and activation to cut intermediate memory traffic).  The forward operation
+ * is Y = X W^T + b with b of length d_ff ("GEMM analysis in TraceLens",
+ * section "Backward pass GEMMs"; the trace's aten::addmm), followed in a
+ * feed-forward block by an activation (Funlib GEMM issue, "Description":
+ * XW1 -> GELU -> XW2).  The LLaMA MLP's up and gate projections of one input
+ * ("GEMM analysis in TraceLens", "Real-world example: LLaMA-2 7B") fuse into
+ * one call with gated = 1.
+ *   gated = 0:  C[i, j] = act(acc(i, j) + bias[j])
+ *   gated = 1:  C[i, j] = act(acc(i, j) + bias[j]) * (acc(i, n + j) + bias[n + j])
+ * where acc(i, r) is sum_k A[i, k] * B[r, k] (times sa[i] * sb[r] for E4M3)
+ * in fp32, and n = n_valid.  A gated layer's B holds 2 n rows: the gate
+ * projection's n rows, then the up projection's n rows; sb and bias then hold
+ * 2 n entries in the same order.  bias (fp32, 4-byte aligned) may be NULL.
+ * act: dgl_act_t.  plan: NULL for the library's choice, else as
+ * dgl_gemm_planned (a gated layer needs tile_m 256; tile_n 128 or 256).
+ * Layout, scales, validation and errors otherwise as dgl_gemm_bf16 /
+ * dgl_gemm_fp8.  Problems with m_valid <= 16 take the decode path unless
+ * gated; gated layers always run on CTA-pair tiles.
+ */
+dgl_status dgl_linear(int32_t dtype, const void* A, const void* B, const float* sa, const float* sb,
+                      const float* bias, void* C, int64_t M, int64_t N, int64_t K, int64_t m_valid, int64_t n_valid,
+                      int32_t out_dtype, int32_t act, int32_t gated, const dgl_plan_info* plan, void* stream);
+
+/*
  * The plan the library would use for a problem of m x n x K (valid extents)
  * on a device with num_sms SMs (num_sms <= 0: query the current device).
  * Pure host logic when num_sms > 0: needs no GPU.
@@ -179,6 +209,13 @@ dgl_status dgl_gemm_noalloc(int32_t dtype, const void* A, const void* B, const f
  */
 dgl_status dgl_plan(int32_t dtype, int64_t m, int64_t n, int64_t K, int32_t out_dtype, int32_t num_sms,
                     dgl_plan_info* out);
+
+/*
+ * The plan dgl_linear would use (gated: a layer whose B holds 2 n rows).
+ * Pure host logic when num_sms > 0.
+ */
+dgl_status dgl_plan_linear(int32_t dtype, int64_t m, int64_t n, int64_t K, int32_t out_dtype, int32_t gated,
+                           int32_t num_sms, dgl_plan_info* out);
 
 /*
  * Tile- and wave-quantisation metrics of an m x n output on tile_m x tile_n

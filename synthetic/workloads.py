@@ -27,6 +27,8 @@ RAGGED_SWEEP = [(1, 11008, 4096), (8, 4096, 4096), (16, 4096, 4096), (48, 4096, 
 LLAMA_SHAPES = [(597, 11008, 4096), (1, 11008, 4096), (4, 11008, 4096), (16, 11008, 4096)]
 SQUARE_SHAPES = [(2048, 2048, 2048), (4096, 4096, 4096), (8192, 8192, 8192)]
 FP8_SHAPES = [(4096, 4096, 4096), (597, 11008, 4096), (16, 11008, 4096)]
+STREAM_BIAS = 4
+ACT_IDS = {"none": 0, "gelu": 1, "silu": 2}
 
 
 @dataclass
@@ -43,14 +45,27 @@ class GemmCase:
     B: np.ndarray = field(repr=False)
     sa: np.ndarray | None = field(default=None, repr=False)
     sb: np.ndarray | None = field(default=None, repr=False)
+    # linear-layer epilogue (parameters only): activation 0 none / 1 GELU /
+    # 2 SiLU, a bias per row of B, and gated = B holds 2n rows (gate, then up)
+    act: int = 0
+    gated: bool = False
+    bias: np.ndarray | None = field(default=None, repr=False)
 
     @property
     def name(self) -> str:
         return f"{self.dtype}_{self.m}x{self.n}x{self.K}_{self.dist}_{self.out}"
 
     @property
+    def b_rows(self) -> int:
+        return 2 * self.n if self.gated else self.n
+
+    @property
+    def linear(self) -> bool:
+        return self.act != 0 or self.gated or self.bias is not None
+
+    @property
     def flops(self) -> int:
-        return 2 * self.m * self.n * self.K
+        return 2 * self.m * self.b_rows * self.K
 
 
 def make_case(dtype: str, m: int, n: int, K: int, *, out: str = "bf16",
@@ -106,6 +121,12 @@ WORKLOADS = {
     "llama7b_mlp": [("bf16", m, n, k, "bf16", "normal") for (m, n, k) in LLAMA_SHAPES],
     "square": [("bf16", m, n, k, "bf16", "square_normal") for (m, n, k) in SQUARE_SHAPES],
     "fp8": [("fp8", m, n, k, "bf16", "fp8") for (m, n, k) in FP8_SHAPES],
+    # linear layers with their epilogue: the GPT-3-XL forward addmm (TraceLens
+    # "Real-world example: GPT-3-XL": 10240 x 8192 x 2048, bias) followed by
+    # GELU, and the LLaMA-2 7B prefill up/gate pair as one gated call
+    "linear": [("bf16", 10240, 8192, 2048, "bf16", "normal", {"act": "gelu", "bias": True}),
+               ("bf16", 597, 11008, 4096, "bf16", "normal", {"act": "silu", "gated": True}),
+               ("fp8", 597, 11008, 4096, "bf16", "fp8", {"act": "silu", "gated": True})],
 }
 
 
@@ -114,7 +135,17 @@ def workload_shapes(name: str):
 
 
 def make_workload_case(entry, seed: int = 0) -> GemmCase:
-    dtype, m, n, k, out, dist = entry
+    dtype, m, n, k, out, dist = entry[:6]
+    epi = entry[6] if len(entry) > 6 else {}
+    rows_b = 2 * n if epi.get("gated") else n
     if dist == "square_normal":
-        return make_case(dtype, m, n, k, out=out, dist="normal", seed=seed, a_std=1.0, b_std=1.0)
-    return make_case(dtype, m, n, k, out=out, dist=dist, seed=seed)
+        case = make_case(dtype, m, rows_b, k, out=out, dist="normal", seed=seed, a_std=1.0, b_std=1.0)
+    else:
+        case = make_case(dtype, m, rows_b, k, out=out, dist=dist, seed=seed)
+    if epi:
+        case.n = n
+        case.gated = bool(epi.get("gated", False))
+        case.act = ACT_IDS[epi.get("act", "none")]
+        if epi.get("bias"):
+            case.bias = normal(seed, STREAM_BIAS, (rows_b,), 0.0, 0.5).astype(np.float32)
+    return case
