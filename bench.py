@@ -36,6 +36,9 @@ WORKLOAD_TEXT = {
     "square": "bf16 squares M=N=K in {2048,4096,8192}, A,B~N(0,1), bf16 C",
     "fp8": "E4M3 with per-row/per-column fp32 scales, bf16 C: (4096,4096,4096) (597,11008,4096) (16,11008,4096)",
     "square256": "bf16 256^3, fp32 C: uniform[-1,1] and integer [-4,4] variants",
+    "gpt3xl_train": "GPT-3-XL feed-forward projection, one training step, bf16 C: forward 10240x8192x2048 + bias "
+                    "+ GELU; dX = dY W 10240x2048x8192 (W read MN-major); dW = dY^T X 8192x2048x10240 "
+                    "(both operands MN-major)",
     "linear": "linear layers with fused epilogues, bf16 C: GPT-3-XL forward addmm 10240x8192x2048 + bias + GELU; "
               "LLaMA-2-7B prefill up/gate pair 597x(2x11008)x4096 as one gated SiLU call, bf16 and E4M3",
 }
@@ -273,8 +276,11 @@ def main():
     ops = []
     for c in cases:
         if c.dtype == "bf16":
-            A = torch.from_numpy(c.A.view(np.int16)).to(dev)
-            B = torch.from_numpy(c.B.view(np.int16)).to(dev)
+            # MN-major operands are stored transposed ([K][m], [K][n])
+            a_host = c.A if c.a_major == 0 else np.ascontiguousarray(c.A.T)
+            b_host = c.B if c.b_major == 0 else np.ascontiguousarray(c.B.T)
+            A = torch.from_numpy(a_host.view(np.int16)).to(dev)
+            B = torch.from_numpy(b_host.view(np.int16)).to(dev)
             sa = sb = None
         else:
             A = torch.from_numpy(c.A).to(dev)
@@ -292,7 +298,11 @@ def main():
         forced = dgl.PlanInfo(path=dgl.PATH_TC, tile_m=tm_, tile_n=tn_)
 
     def make_call(c, A, B, sa, sb, C, out_dtype, bias):
-        if c.linear:
+        if c.a_major or c.b_major:
+            args_ = (c.a_major, c.b_major, A.data_ptr(), A.shape[1], B.data_ptr(), B.shape[1], C.data_ptr(), c.n,
+                     c.m, c.n, c.K, out_dtype, ctypes.byref(forced) if forced is not None else None, s_handle)
+            fn = lib.dgl_gemm_bf16_ex
+        elif c.linear:
             dt = dgl.DTYPE_BF16 if c.dtype == "bf16" else dgl.DTYPE_E4M3
             args_ = (dt, A.data_ptr(), B.data_ptr(), sa.data_ptr() if sa is not None else None,
                      sb.data_ptr() if sb is not None else None, bias.data_ptr() if bias is not None else None,
@@ -338,6 +348,8 @@ def main():
         else:
             store = "predicated" if c.out == "f32" else "row-staging"
         epi = ", linear" if c.linear else ""
+        if c.a_major or c.b_major:
+            epi = f", {'mn' if c.a_major else 'k'}-{'mn' if c.b_major else 'k'} major"
         return f"tc_gemm_kernel<{c.dtype}, {p.tile_m}x{p.tile_n}, {store}{epi}>"
 
     knames = [kernel_name(c, p) for c, p in zip(cases, plans)]

@@ -35,10 +35,12 @@ PATH_EMPTY = 2
 ACT_NONE = 0
 ACT_GELU = 1
 ACT_SILU = 2
+K_MAJOR = 0
+MN_MAJOR = 1
 
 EXPORTED = ["dgl_gemm_bf16", "dgl_gemm_fp8", "dgl_gemm_planned", "dgl_plan", "dgl_tile_metrics",
             "dgl_device_status", "dgl_status_string", "dgl_version", "dgl_gemm_noalloc", "dgl_linear",
-            "dgl_plan_linear"]
+            "dgl_plan_linear", "dgl_gemm_bf16_ex"]
 
 
 class PlanInfo(ctypes.Structure):
@@ -85,6 +87,9 @@ def load_library(path: str | None = None):
     lib.dgl_linear.restype = i32
     lib.dgl_plan_linear.argtypes = [i32, i64, i64, i64, i32, i32, i32, ctypes.POINTER(PlanInfo)]
     lib.dgl_plan_linear.restype = i32
+    lib.dgl_gemm_bf16_ex.argtypes = [i32, i32, vp, i64, vp, i64, vp, i64, i64, i64, i64, i32,
+                                     ctypes.POINTER(PlanInfo), vp]
+    lib.dgl_gemm_bf16_ex.restype = i32
     lib.dgl_plan.argtypes = [i32, i64, i64, i64, i32, i32, ctypes.POINTER(PlanInfo)]
     lib.dgl_plan.restype = i32
     lib.dgl_tile_metrics.argtypes = [i64, i64, i32, i32, i32, ctypes.POINTER(PlanInfo)]
@@ -137,6 +142,13 @@ def dgl_linear(dtype, A, B, sa, sb, bias, C, M, N, K, m_valid=0, n_valid=0, out_
     """Linear layer act(A . B^T + bias), or the gated form (see include/dgl.h)."""
     return load_library().dgl_linear(dtype, A, B, sa, sb, bias, C, M, N, K, m_valid, n_valid, out_dtype, act, gated,
                                      ctypes.byref(plan) if plan is not None else None, stream)
+
+
+def dgl_gemm_bf16_ex(a_major, b_major, A, lda, B, ldb, C, ldc, m, n, K, out_dtype=OUT_BF16,
+                     plan: PlanInfo | None = None, stream=0) -> int:
+    """bf16 GEMM with K-major or MN-major operands and explicit pitches (see include/dgl.h)."""
+    return load_library().dgl_gemm_bf16_ex(a_major, b_major, A, lda, B, ldb, C, ldc, m, n, K, out_dtype,
+                                           ctypes.byref(plan) if plan is not None else None, stream)
 
 
 def dgl_plan(dtype, m, n, K, out_dtype=OUT_BF16, num_sms=0) -> PlanInfo:

@@ -148,15 +148,29 @@ dgl_status get_device(int* dev_out, DeviceState** st_out) {
 // box of box_rows rows and the 128-byte swizzle.  Reads outside
 // [0, inner) x [0, rows) return zeros.
 bool encode_operand_map(CUtensorMap* map, const void* base, bool e4m3, int64_t inner, int64_t rows,
-                        int box_rows) {
+                        int box_rows, int64_t pitch) {
   const CUtensorMapDataType dt = e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const int64_t esize = e4m3 ? 1 : 2;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner * esize)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch * esize)};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 2-D tensor map over an MN-major bf16 operand stored [K][mn] (row pitch
+// `pitch` elements): boxes of 64 MN elements (128 bytes) by 64 K rows with
+// the 128-byte swizzle, the layout the MN-major UMMA descriptor reads.
+bool encode_operand_map_mn(CUtensorMap* map, const void* base, int64_t mn, int64_t K, int64_t pitch) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(mn), static_cast<cuuint64_t>(K)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch * 2)};
+  cuuint32_t box[2] = {64, 64};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -183,7 +197,7 @@ bool encode_output_map(CUtensorMap* map, void* base, bool f32, int64_t cols, int
 struct MapKey {
   const void* base;
   int64_t d0, d1, pitch;
-  int box_rows, kind;  // kind: 0 bf16 operand, 1 E4M3 operand, 2 bf16 output, 3 fp32 output
+  int box_rows, kind;  // kind: 0 bf16 operand, 1 E4M3 operand, 2 bf16 output, 3 fp32 output, 4 MN-major bf16
   bool operator==(const MapKey& o) const {
     return base == o.base && d0 == o.d0 && d1 == o.d1 && pitch == o.pitch && box_rows == o.box_rows &&
            kind == o.kind;
@@ -224,9 +238,17 @@ bool cached_map(CUtensorMap* out, const MapKey& key, Encode encode) {
   return true;
 }
 
-bool cached_operand_map(CUtensorMap* map, const void* base, bool e4m3, int64_t inner, int64_t rows, int box_rows) {
-  const MapKey key{base, inner, rows, inner, box_rows, e4m3 ? 1 : 0};
-  return cached_map(map, key, [&](CUtensorMap* m) { return encode_operand_map(m, base, e4m3, inner, rows, box_rows); });
+bool cached_operand_map(CUtensorMap* map, const void* base, bool e4m3, int64_t inner, int64_t rows, int box_rows,
+                        int64_t pitch = 0) {
+  if (pitch <= 0) pitch = inner;
+  const MapKey key{base, inner, rows, pitch, box_rows, e4m3 ? 1 : 0};
+  return cached_map(map, key,
+                    [&](CUtensorMap* m) { return encode_operand_map(m, base, e4m3, inner, rows, box_rows, pitch); });
+}
+
+bool cached_operand_map_mn(CUtensorMap* map, const void* base, int64_t mn, int64_t K, int64_t pitch) {
+  const MapKey key{base, mn, K, pitch, 64, 4};
+  return cached_map(map, key, [&](CUtensorMap* m) { return encode_operand_map_mn(m, base, mn, K, pitch); });
 }
 
 bool cached_output_map(CUtensorMap* map, void* base, bool f32, int64_t cols, int64_t rows, int64_t ldc) {
@@ -246,6 +268,12 @@ struct Problem {
   const float* bias = nullptr;
   int act = 0;
   int gated = 0;
+  // operand layouts (dgl_gemm_bf16_ex): MN-major A is [K][m], B is [K][n];
+  // lda / ldb are row pitches in elements (0: the packed pitch)
+  int a_mn = 0;
+  int b_mn = 0;
+  int64_t lda = 0;
+  int64_t ldb = 0;
 };
 
 dgl_status validate(Problem& pr) {
@@ -268,6 +296,16 @@ dgl_status validate(Problem& pr) {
   if ((pr.K * esize) % 16 != 0) return DGL_ERR_ALIGN;
   if (!aligned(pr.A, 16) || !aligned(pr.B, 16)) return DGL_ERR_ALIGN;
   if (pr.K * esize > INT32_MAX) return DGL_ERR_SHAPE;
+  if (pr.a_mn || pr.b_mn) {
+    if (pr.dtype != DGL_DTYPE_BF16 || pr.gated || pr.act || pr.bias) return DGL_ERR_UNSUPPORTED;
+  }
+  // row pitches: at least the row's extent, and a multiple of 16 bytes (the TMA stride rule)
+  const int64_t a_row = pr.a_mn ? pr.m : pr.K, b_row = pr.b_mn ? pr.n : pr.K;
+  if (pr.lda == 0) pr.lda = a_row;
+  if (pr.ldb == 0) pr.ldb = b_row;
+  if (pr.lda < a_row || pr.ldb < b_row) return DGL_ERR_ARG;
+  if ((pr.lda * esize) % 16 != 0 || (pr.ldb * esize) % 16 != 0) return DGL_ERR_ALIGN;
+  if (pr.lda > INT32_MAX || pr.ldb > INT32_MAX) return DGL_ERR_SHAPE;
   if (pr.dtype == DGL_DTYPE_E4M3) {
     if (!pr.sa || !pr.sb) return DGL_ERR_ARG;
     if (!aligned(pr.sa, 4) || !aligned(pr.sb, 4)) return DGL_ERR_ALIGN;
@@ -296,7 +334,8 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream, Sta
   dgl_plan_info plan;
   if (forced) {
     if (forced->path == DGL_PATH_DECODE) {
-      if (pr.m > kDecodeMaxM || pr.gated) return DGL_ERR_UNSUPPORTED;
+      if (pr.m > kDecodeMaxM || pr.gated || pr.a_mn || pr.b_mn || pr.lda != pr.K || pr.ldb != pr.K)
+        return DGL_ERR_UNSUPPORTED;
       fill_decode_plan(pr.dtype, pr.out, pr.m, pr.n, pr.K, ds->num_sms, &plan);
     } else if (forced->path == DGL_PATH_TC) {
       if (!tc_supported_tile(forced->tile_m, forced->tile_n)) return DGL_ERR_UNSUPPORTED;
@@ -309,6 +348,10 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream, Sta
     if (forced->grid > 0) plan.grid = forced->grid;
   } else if (linear) {
     choose_linear_plan(pr.dtype, pr.out, pr.m, pr.n, pr.K, pr.gated != 0, ds->num_sms, &plan);
+  } else if (pr.a_mn || pr.b_mn || pr.lda != pr.K || pr.ldb != pr.K) {
+    // the decode path reads packed K-major operands only
+    choose_plan(pr.dtype, pr.out, pr.m, pr.n, pr.K, ds->num_sms, &plan);
+    if (plan.path != DGL_PATH_TC) fill_tc_plan(pr.dtype, pr.out, pr.m, pr.n, pr.K, 128, 128, ds->num_sms, &plan, 0);
   } else {
     PlanKey key{dev, pr.dtype, pr.out, pr.m, pr.n, pr.K};
     std::lock_guard<std::mutex> lock(g_mu);
@@ -369,9 +412,12 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream, Sta
   const int cg = plan.cta_group == 2 ? 2 : 1;
   // a gated layer's B holds the gate rows, then the up rows
   const int64_t b_rows = pr.gated ? 2 * pr.n : pr.n;
-  if (!cached_operand_map(&ta, pr.A, e4m3, pr.K, pr.m, 128) ||
-      !cached_operand_map(&tb, pr.B, e4m3, pr.K, b_rows, plan.tile_n / cg))
-    return DGL_ERR_CUDA;
+  const bool map_ok =
+      (pr.a_mn ? cached_operand_map_mn(&ta, pr.A, pr.m, pr.K, pr.lda)
+               : cached_operand_map(&ta, pr.A, e4m3, pr.K, pr.m, 128, pr.lda)) &&
+      (pr.b_mn ? cached_operand_map_mn(&tb, pr.B, b_rows, pr.K, pr.ldb)
+               : cached_operand_map(&tb, pr.B, e4m3, pr.K, b_rows, plan.tile_n / cg, pr.ldb));
+  if (!map_ok) return DGL_ERR_CUDA;
   const bool f32 = pr.out == DGL_OUT_F32;
   const bool c_tma = aligned(pr.C, 16) && (pr.N * (f32 ? 4 : 2)) % 16 == 0;
   std::memset(&tc, 0, sizeof(tc));
@@ -397,6 +443,8 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream, Sta
   p.act = pr.act;
   p.gated = pr.gated;
   p.n_up = static_cast<int>(pr.n);
+  p.a_mn = pr.a_mn;
+  p.b_mn = pr.b_mn;
   // grid counts CTAs; a pair per tile when cg == 2
   int grid = plan.grid > 0 ? plan.grid : p.num_tiles * cg;
   if (!plan.stream_k && grid > p.num_tiles * cg) grid = p.num_tiles * cg;
@@ -521,6 +569,21 @@ dgl_status dgl_plan(int32_t dtype, int64_t m, int64_t n, int64_t K, int32_t out_
   }
   choose_plan(dtype, out_dtype, m, n, K, num_sms, out);
   return DGL_OK;
+}
+
+dgl_status dgl_gemm_bf16_ex(int32_t a_major, int32_t b_major, const void* A, int64_t lda, const void* B, int64_t ldb,
+                           void* C, int64_t ldc, int64_t m, int64_t n, int64_t K, int32_t out_dtype,
+                           const dgl_plan_info* plan, void* stream) {
+  if ((a_major != DGL_K_MAJOR && a_major != DGL_MN_MAJOR) || (b_major != DGL_K_MAJOR && b_major != DGL_MN_MAJOR))
+    return DGL_ERR_ARG;
+  if (lda < 0 || ldb < 0 || ldc < 0 || m < 0 || n < 0) return DGL_ERR_ARG;
+  Problem pr{DGL_DTYPE_BF16, out_dtype, A, B, nullptr, nullptr, C, m, ldc == 0 ? n : ldc, K, m, n};
+  if (pr.N < n) return DGL_ERR_ARG;
+  pr.a_mn = a_major == DGL_MN_MAJOR;
+  pr.b_mn = b_major == DGL_MN_MAJOR;
+  pr.lda = lda;
+  pr.ldb = ldb;
+  return run(pr, plan, static_cast<cudaStream_t>(stream));
 }
 
 dgl_status dgl_plan_linear(int32_t dtype, int64_t m, int64_t n, int64_t K, int32_t out_dtype, int32_t gated,

@@ -46,6 +46,10 @@ struct TcParams {
   int act;              // 0 identity, 1 GELU (x * Phi(x)), 2 SiLU (x * sigma(x))
   int gated;
   int n_up;
+  // Operand majorness: 0 K-major (A [m][K], B [n][K]), 1 MN-major (A [K][m],
+  // B [K][n]: the backward-pass layouts; bf16 only).
+  int a_mn;
+  int b_mn;
 };
 
 // Decode (m <= 16) kernel parameters.  A and B are read through tensor maps.

@@ -213,10 +213,27 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   return d;
 }
 
+// The same for an MN-major operand tile (stored [K][MN], MN contiguous) as TMA
+// writes it from boxes of 64 MN elements (128 bytes) by 64 K rows with the
+// 128-byte swizzle: an atom is 8 K rows of 128 bytes (1024 bytes); atoms
+// follow one another along K at 1024 bytes (stride-dimension offset) and the
+// next 64 MN elements start one box, 8192 bytes, further (leading-dimension
+// offset).
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFF);
+  d |= static_cast<uint64_t>(8192 >> 4) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
 // Instruction descriptor (kind::f16 and kind::f8f6f4), dense, K-major A and B,
 // fp32 accumulator:
 //   bits 4-5 D format (1 = f32), bits 7-9 A format, bits 10-12 B format,
-//   bits 17-22 N >> 3, bits 24-28 M >> 4.
+//   bit 15 / 16: A / B is MN-major (set by the caller), bits 17-22 N >> 3,
+//   bits 24-28 M >> 4.
 // A/B format: kind::f16 -> 1 = bf16; kind::f8f6f4 -> 0 = E4M3.
 __host__ __device__ constexpr uint32_t idesc_f32acc(uint32_t ab_format, int M, int N) {
   return (1u << 4) | (ab_format << 7) | (ab_format << 10) | (static_cast<uint32_t>(N >> 3) << 17) |

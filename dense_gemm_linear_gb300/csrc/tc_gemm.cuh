@@ -138,6 +138,35 @@ __device__ __forceinline__ void store_row_pieces(uint8_t* g, uint32_t s, int lo,
   }
 }
 
+// Operand tiles in shared memory.  A K-major operand (rows of K contiguous)
+// arrives as one TMA box of BK elements by `rows` rows.  An MN-major operand
+// (stored [K][MN], MN contiguous: the backward-pass layouts) arrives as
+// rows / 64 boxes of 64 MN elements by BK = 64 K rows, 8 KB each, placed one
+// after another; each box is a column of 128-byte swizzle atoms (8 K rows by
+// 64 MN elements) at a 1024-byte stride.  (MN-major operands are bf16 only.)
+constexpr int MN_BOX_BYTES = 64 * 64 * 2;
+constexpr int MN_K_STEP_BYTES = 2 * 1024;  // one bf16 MMA's K = 16: two 8-row atoms
+
+// k0: the stage's first K element; row0: its first row (K-major) or MN index (MN-major).
+__device__ __forceinline__ void load_operand(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int k0, int row0,
+                                             int rows, int mn_major, uint64_t pol) {
+  if (!mn_major) {
+    tma_load_2d(dst, map, bar, k0, row0, pol);
+    return;
+  }
+  for (int i = 0; i < rows / 64; ++i) tma_load_2d(dst + i * MN_BOX_BYTES, map, bar, row0 + 64 * i, k0, pol);
+}
+
+__device__ __forceinline__ void load_operand_pair(uint8_t* dst, const CUtensorMap* map, uint32_t leader_bar, int k0,
+                                                  int row0, int rows, int mn_major, uint64_t pol) {
+  if (!mn_major) {
+    tma_load_2d_pair(dst, map, leader_bar, k0, row0, pol);
+    return;
+  }
+  for (int i = 0; i < rows / 64; ++i)
+    tma_load_2d_pair(dst + i * MN_BOX_BYTES, map, leader_bar, row0 + 64 * i, k0, pol);
+}
+
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -241,12 +270,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             // for a moment and the phase still waits for the leader's arrival.
             const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
             if (rank == 0) mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES * CG);
-            tma_load_2d_pair(sA + stage * Cfg::A_STAGE_BYTES, &tmA, fb, kb * Cfg::BK, a_row, pol);
-            tma_load_2d_pair(sB + stage * Cfg::B_STAGE_BYTES, &tmB, fb, kb * Cfg::BK, b_row, pol);
+            load_operand_pair(sA + stage * Cfg::A_STAGE_BYTES, &tmA, fb, kb * Cfg::BK, a_row, BM, p.a_mn, pol);
+            load_operand_pair(sB + stage * Cfg::B_STAGE_BYTES, &tmB, fb, kb * Cfg::BK, b_row, Cfg::B_ROWS, p.b_mn, pol);
           } else {
             mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
-            tma_load_2d(sA + stage * Cfg::A_STAGE_BYTES, &tmA, &full[stage], kb * Cfg::BK, a_row, pol);
-            tma_load_2d(sB + stage * Cfg::B_STAGE_BYTES, &tmB, &full[stage], kb * Cfg::BK, b_row, pol);
+            load_operand(sA + stage * Cfg::A_STAGE_BYTES, &tmA, &full[stage], kb * Cfg::BK, a_row, BM, p.a_mn, pol);
+            load_operand(sB + stage * Cfg::B_STAGE_BYTES, &tmB, &full[stage], kb * Cfg::BK, b_row, Cfg::B_ROWS, p.b_mn, pol);
           }
           ++issued;
           if (++stage == STAGES) {
@@ -270,7 +299,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && rank == 0) {
-      constexpr uint32_t idesc = idesc_f32acc(Cfg::FP8 ? 0u : 1u, Cfg::TILE_M, BN);
+      // MN-major operands set the instruction's transpose bits (15: A, 16: B)
+      const uint32_t idesc = idesc_f32acc(Cfg::FP8 ? 0u : 1u, Cfg::TILE_M, BN) |
+                             (p.a_mn ? 1u << 15 : 0u) | (p.b_mn ? 1u << 16 : 0u);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool issued_any = false;
       SegmentIter it(cluster_id, p.workers, p.num_kb, p.dp_tiles, p.sk_units);
@@ -294,8 +325,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           const uint32_t b_addr = smem_u32(sB + stage * Cfg::B_STAGE_BYTES);
 #pragma unroll
           for (int k = 0; k < Cfg::MMAS_PER_STAGE; ++k) {
-            const uint64_t ad = smem_desc_sw128(a_addr + k * Cfg::MMA_K_BYTES);
-            const uint64_t bd = smem_desc_sw128(b_addr + k * Cfg::MMA_K_BYTES);
+            const uint64_t ad = p.a_mn ? smem_desc_sw128_mn(a_addr + k * MN_K_STEP_BYTES)
+                                       : smem_desc_sw128(a_addr + k * Cfg::MMA_K_BYTES);
+            const uint64_t bd = p.b_mn ? smem_desc_sw128_mn(b_addr + k * MN_K_STEP_BYTES)
+                                       : smem_desc_sw128(b_addr + k * Cfg::MMA_K_BYTES);
             const uint32_t accumulate = (kb != sg.kb0 || k != 0) ? 1u : 0u;
             if constexpr (CG == 2) {
               if constexpr (Cfg::FP8)

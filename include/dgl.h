@@ -73,6 +73,10 @@ typedef enum { DGL_PATH_TC = 0, DGL_PATH_DECODE = 1, DGL_PATH_EMPTY = 2 } dgl_pa
  * distribution function, the exact erf form); SiLU(x) = x * sigma(x) (sigma
  * the logistic function). */
 typedef enum { DGL_ACT_NONE = 0, DGL_ACT_GELU = 1, DGL_ACT_SILU = 2 } dgl_act_t;
+/* Operand storage of dgl_gemm_bf16_ex: K-major rows hold K contiguous
+ * elements (A [m][K], B [n][K]); MN-major rows hold M (or N) contiguous
+ * elements (A [K][m], B [K][n]). */
+typedef enum { DGL_K_MAJOR = 0, DGL_MN_MAJOR = 1 } dgl_major_t;
 
 /*
  * A launch plan: the path, the tile of the tile ladder, and the cost-model
@@ -171,6 +175,25 @@ dgl_status dgl_gemm_planned(int32_t dtype, const void* A, const void* B, const f
 dgl_status dgl_gemm_noalloc(int32_t dtype, const void* A, const void* B, const float* sa, const float* sb,
                             void* C, int64_t M, int64_t N, int64_t K, int64_t m_valid, int64_t n_valid,
                             int32_t out_dtype, void* stream);
+
+/*
+ * bf16 GEMM with either operand stored K-major or MN-major and explicit row
+ * pitches: the three GEMMs of a linear layer's training step ("GEMM analysis
+ * in TraceLens", sections "Backward pass GEMMs" and "How PyTorch calls BLAS"):
+ *   forward  Y  = X W^T   A = X  [m][K]   K-major,  B = W [n][K]  K-major
+ *   backward dX = dY W    A = dY [m][K]   K-major,  B = W [K][n]  MN-major
+ *   backward dW = dY^T X  A = dY [K][m]   MN-major, B = X [K][n]  MN-major
+ * C[i, j] = sum_k A(i, k) B(j, k) for i < m, j < n, fp32 accumulation; C is
+ * [m][ldc] (ldc >= n, 0 = n).  lda / ldb: row pitches in elements (0 = the
+ * packed pitch: K for K-major, m or n for MN-major); each a multiple of 8
+ * (16 bytes) and at least the row's extent.  A, B 16-byte aligned.  Returns
+ * DGL_ERR_ALIGN for a pitch that breaks the 16-byte rule.  plan: NULL or as
+ * dgl_gemm_planned (tcgen05 path only; MN-major operands never take the
+ * decode path).  Otherwise as dgl_gemm_bf16.
+ */
+dgl_status dgl_gemm_bf16_ex(int32_t a_major, int32_t b_major, const void* A, int64_t lda, const void* B, int64_t ldb,
+                           void* C, int64_t ldc, int64_t m, int64_t n, int64_t K, int32_t out_dtype,
+                           const dgl_plan_info* plan, void* stream);
 
 /*
  * A linear layer: the GEMM above with its epilogue fused into the kernel

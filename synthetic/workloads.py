@@ -50,6 +50,10 @@ class GemmCase:
     act: int = 0
     gated: bool = False
     bias: np.ndarray | None = field(default=None, repr=False)
+    # operand storage on the device: 0 K-major (A [m][K], B [n][K]), 1 MN-major
+    # (A [K][m], B [K][n]); the codes above are always held K-major
+    a_major: int = 0
+    b_major: int = 0
 
     @property
     def name(self) -> str:
@@ -124,6 +128,13 @@ WORKLOADS = {
     # linear layers with their epilogue: the GPT-3-XL forward addmm (TraceLens
     # "Real-world example: GPT-3-XL": 10240 x 8192 x 2048, bias) followed by
     # GELU, and the LLaMA-2 7B prefill up/gate pair as one gated call
+    # one training step of a GPT-3-XL feed-forward projection (TraceLens
+    # "Real-world example: GPT-3-XL", d_model 2048, d_ff 8192, 5 x 2048
+    # tokens): the forward addmm with its bias and GELU, then dX = dY W
+    # (B MN-major) and dW = dY^T X (both MN-major)
+    "gpt3xl_train": [("bf16", 10240, 8192, 2048, "bf16", "normal", {"act": "gelu", "bias": True}),
+                     ("bf16", 10240, 2048, 8192, "bf16", "normal", {"layout": ("k", "mn")}),
+                     ("bf16", 8192, 2048, 10240, "bf16", "normal", {"layout": ("mn", "mn")})],
     "linear": [("bf16", 10240, 8192, 2048, "bf16", "normal", {"act": "gelu", "bias": True}),
                ("bf16", 597, 11008, 4096, "bf16", "normal", {"act": "silu", "gated": True}),
                ("fp8", 597, 11008, 4096, "bf16", "fp8", {"act": "silu", "gated": True})],
@@ -148,4 +159,6 @@ def make_workload_case(entry, seed: int = 0) -> GemmCase:
         case.act = ACT_IDS[epi.get("act", "none")]
         if epi.get("bias"):
             case.bias = normal(seed, STREAM_BIAS, (rows_b,), 0.0, 0.5).astype(np.float32)
+        a_l, b_l = epi.get("layout", ("k", "k"))
+        case.a_major, case.b_major = int(a_l == "mn"), int(b_l == "mn")
     return case
