@@ -13,8 +13,18 @@ cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb_lo, const CU
   static std::atomic<uint64_t> attr_done{0};  // one bit per device
   cudaError_t e = set_smem_attr_once(kern, DEC_SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;
-  kern<<<grid, DEC_THREADS, DEC_SMEM_BYTES, stream>>>(ta, tb_lo, tb_hi, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(DEC_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = DEC_SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  // the kernel waits for its predecessor (griddep_wait) before any global access
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb_lo, tb_hi, p);
 }
 
 template <typename T>

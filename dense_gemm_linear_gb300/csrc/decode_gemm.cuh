@@ -95,6 +95,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  griddep_launch_dependents();
+  griddep_wait();
 
   const int nk = (p.row_bytes + 127) >> 7;   // 128-byte steps of K
   const int ks = p.ksteps;                    // planes per stage

@@ -194,6 +194,19 @@ __device__ __forceinline__ void tc_fence_after_sync() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation may start while the previous kernel on its stream is still
+// finishing; griddep_wait() blocks until that kernel has completed and its
+// memory is visible, so it must come before the first global access to data
+// another kernel may produce or read.  griddep_launch_dependents() lets the
+// next kernel on the stream start launching once every CTA of this grid has
+// issued it (its CTAs still take SMs only as this grid's CTAs leave).  Both
+// are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Shared-memory matrix descriptor for a K-major operand tile stored as rows
 // of 128 bytes with the 128-byte swizzle (the layout TMA writes with
 // CU_TENSOR_MAP_SWIZZLE_128B).  Eight rows form one 1024-byte swizzle atom;

@@ -229,6 +229,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  // set-up touched no global data: let the next kernel launch, then wait for
+  // the previous one before reading operands or writing C
+  griddep_launch_dependents();
+  griddep_wait();
 
   int fail = 0;
   if constexpr (CG == 2) {
