@@ -117,9 +117,9 @@ def test_plan_decode_threshold(dgl):
                                    (597, 11008, 4096), (4096, 4096, 4096), (8192, 8192, 8192), (17, 5, 64)])
 def test_plan_padding_screen(dgl, m, n, k):
     """The chosen tile pads the output by at most 1.25x, unless no ladder tile
-    can or a measured pin overrides the screen (the 597-token prefill)."""
+    can or a measured pin overrides the screen (the 597-token prefill, 528^2)."""
     p = dgl.dgl_plan(0, m, n, k, num_sms=152)
-    pinned_past_screen = {(597, 11008, 4096)}
+    pinned_past_screen = {(597, 11008, 4096), (528, 528, 1024)}
     assert p.path == dgl.PATH_TC
     padded = -(-m // p.tile_m) * p.tile_m * -(-n // p.tile_n) * p.tile_n
     rungs = [(128, 64), (128, 128), (128, 256), (256, 128), (256, 256)]
