@@ -542,8 +542,11 @@ def main():
             "data": "synthetic (seeded SplitMix64 draws; no datasets or trained weights)",
             "config": {"workload": workload_text(args), "gemms_per_step": ncall,
                        "parallelism": "replicas" if world > 1 else "single GPU",
-                       "l2": f"inputs larger than L2: each step touches {ws:.0f} MiB of A/B/C against a "
-                             f"{l2_mb:.0f} MiB L2, so every GEMM's operands were last read a full step earlier"},
+                       "l2": (f"inputs larger than L2: each step touches {ws:.0f} MiB of A/B/C against a "
+                              f"{l2_mb:.0f} MiB L2, so every GEMM's operands were last read a full step earlier")
+                             if ws > l2_mb else
+                             (f"inputs fit in L2 ({ws:.0f} MiB of A/B/C against {l2_mb:.0f} MiB): a profiling run, "
+                              f"not a bench line")},
             "roofline": roofline, "roofline_decode": roofline_decode, "kernels": kernels, "per_shape": per_shape,
             "ms_per_step_with_call_events": ms_per_step_events,
             "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": K_steps * ncall, "clocks": clocks,
