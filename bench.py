@@ -59,6 +59,7 @@ def parse_args():
     ap.add_argument("--cpu-macs", type=float, default=4e9,
                     help="multiply-adds of the bounded CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-context", action="store_true", help="skip the torch.matmul (cuBLAS) context column")
     return ap.parse_args()
 
 
@@ -424,6 +425,30 @@ def main():
         ms_max = ms_per_step
     value = step_flops * world / (ms_max * 1e-3) / 1e12
 
+    # ---------------------------------------------------------- context: torch.matmul (cuBLAS), off the measured path
+    # Each plain bf16 GEMM of the step is timed once more through torch.matmul
+    # on the same device buffers (C = A B^T), back to back with events around
+    # 20 calls; E4M3, fused-epilogue and MN-major cases have no such column.
+    cublas_us = [None] * ncall
+    if not args.no_context:
+        for i, (c, A, B, sa, sb, C, _o, bias) in enumerate(ops):
+            if c.dtype != "bf16" or c.linear or c.a_major or c.b_major or c.out != "bf16":
+                continue
+            a_t = A.view(torch.bfloat16)
+            b_t = B.view(torch.bfloat16)
+            c_t = C
+            for _ in range(3):
+                torch.matmul(a_t, b_t.t(), out=c_t)
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(20):
+                torch.matmul(a_t, b_t.t(), out=c_t)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            cublas_us[i] = e0.elapsed_time(e1) / 20 * 1e3
+
     # ---------------------------------------------------------- roofline of the dominant kernel
     pk, pk_src = peaks()
     by_kernel = {}
@@ -472,7 +497,8 @@ def main():
                                         "gated": c.gated} if c.linear else None),
                           "us": per_call_ms[i] * 1e3, "tflops": flops[i] / t / 1e12,
                           "gbs": nbytes[i] / t / 1e9, "tile_eff": round(plans[i].tile_eff, 4),
-                          "wq_eff": round(plans[i].wq_eff, 4), "grid": plans[i].grid})
+                          "wq_eff": round(plans[i].wq_eff, 4), "grid": plans[i].grid,
+                          "torch_matmul_us": cublas_us[i]})
 
     # ---------------------------------------------------------- end to end through host buffers
     e2e = None
@@ -494,17 +520,37 @@ def main():
                 h2d += 4 * (hsa.numel() + hsb.numel())
             d2h += hC.numel() * hC.element_size()
 
+        # Pipelined as a caller would: inputs go up on a copy stream, the GEMMs
+        # run on the compute stream, results come down on a second copy
+        # stream, so one GEMM's copies overlap another's kernel.  Events keep
+        # each buffer's reuse in order across steps.
+        h2d_s = torch.cuda.Stream(device=dev)
+        d2h_s = torch.cuda.Stream(device=dev)
+        done = [torch.cuda.Event() for _ in ops]      # compute of op i finished (its inputs free)
+        drained = [torch.cuda.Event() for _ in ops]   # D2H of op i's C finished (C free)
+
         def e2e_step():
-            for (c, A, B, sa, sb, C, _o, bias), (hA, hB, hsa, hsb, hC, hbias), f in zip(ops, host, calls):
-                A.copy_(hA, non_blocking=True)
-                B.copy_(hB, non_blocking=True)
-                if bias is not None:
-                    bias.copy_(hbias, non_blocking=True)
-                if sa is not None:
-                    sa.copy_(hsa, non_blocking=True)
-                    sb.copy_(hsb, non_blocking=True)
+            for i, ((c, A, B, sa, sb, C, _o, bias), (hA, hB, hsa, hsb, hC, hbias), f) in enumerate(
+                    zip(ops, host, calls)):
+                with torch.cuda.stream(h2d_s):
+                    h2d_s.wait_event(done[i])
+                    A.copy_(hA, non_blocking=True)
+                    B.copy_(hB, non_blocking=True)
+                    if bias is not None:
+                        bias.copy_(hbias, non_blocking=True)
+                    if sa is not None:
+                        sa.copy_(hsa, non_blocking=True)
+                        sb.copy_(hsb, non_blocking=True)
+                    ready = torch.cuda.Event()
+                    ready.record(h2d_s)
+                stream.wait_event(ready)
+                stream.wait_event(drained[i])
                 f()
-                hC.copy_(C, non_blocking=True)
+                done[i].record(stream)
+                with torch.cuda.stream(d2h_s):
+                    d2h_s.wait_event(done[i])
+                    hC.copy_(C, non_blocking=True)
+                    drained[i].record(d2h_s)
 
         e2e_step()
         torch.cuda.synchronize()
@@ -512,8 +558,11 @@ def main():
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
+        h2d_s.wait_event(e0)
         for _ in range(args.e2e_steps):
             e2e_step()
+        for ev in drained:
+            stream.wait_event(ev)
         e1.record(stream)
         barrier()
         e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
