@@ -342,6 +342,7 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream, Sta
       if (linear && !tc_supported_epi_tile(forced->tile_m, forced->tile_n, pr.gated != 0)) return DGL_ERR_UNSUPPORTED;
       fill_tc_plan(pr.dtype, pr.out, pr.m, pr.gated ? 2 * pr.n : pr.n, pr.K, forced->tile_m, forced->tile_n,
                    ds->num_sms, &plan, forced->stream_k ? 1 : 0);
+      plan.split_tail = forced->split_tail && !plan.stream_k ? 1 : 0;
     } else {
       return DGL_ERR_UNSUPPORTED;
     }
@@ -418,6 +419,11 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream, Sta
       (pr.b_mn ? cached_operand_map_mn(&tb, pr.B, b_rows, pr.K, pr.ldb)
                : cached_operand_map(&tb, pr.B, e4m3, pr.K, b_rows, plan.tile_n / cg, pr.ldb));
   if (!map_ok) return DGL_ERR_CUDA;
+  // B with half-height boxes, for the half tiles of a split tail (else unused)
+  CUtensorMap tbh = tb;
+  if (plan.split_tail && !pr.b_mn && plan.tile_n == 256 &&
+      !cached_operand_map(&tbh, pr.B, e4m3, pr.K, b_rows, plan.tile_n / cg / 2, pr.ldb))
+    return DGL_ERR_CUDA;
   const bool f32 = pr.out == DGL_OUT_F32;
   const bool c_tma = aligned(pr.C, 16) && (pr.N * (f32 ? 4 : 2)) % 16 == 0;
   std::memset(&tc, 0, sizeof(tc));
@@ -454,9 +460,18 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream, Sta
   p.workers = grid / cg;
   p.dp_tiles = p.num_tiles;
   p.sk_units = 0;
+  p.half_tiles = 0;
   p.ws = nullptr;
   p.flags = nullptr;
   p.epoch = 0;
+  if (plan.split_tail && !plan.stream_k && !pr.gated && plan.tile_n == 256 && p.num_tiles > p.workers) {
+    // the last, partial wave as half tiles, one per worker
+    const int tail = p.num_tiles % p.workers;
+    if (tail > 0 && 2 * tail <= p.workers) {
+      p.dp_tiles = p.num_tiles - tail;
+      p.half_tiles = 2 * tail;
+    }
+  }
   if (plan.stream_k && p.num_tiles % p.workers != 0) {
     p.dp_tiles = p.num_tiles / p.workers * p.workers;
     p.sk_units = static_cast<int64_t>(p.num_tiles - p.dp_tiles) * p.num_kb;
@@ -483,11 +498,11 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream, Sta
   const bool row_staging = !c_tma && !f32;
   cudaError_t e;
   if (linear)
-    e = e4m3 ? launch_tc_e4m3_epi(pr.out, plan.tile_m, plan.tile_n, row_staging, ta, tb, tc, p, grid, stream)
-             : launch_tc_bf16_epi(pr.out, plan.tile_m, plan.tile_n, row_staging, ta, tb, tc, p, grid, stream);
+    e = e4m3 ? launch_tc_e4m3_epi(pr.out, plan.tile_m, plan.tile_n, row_staging, ta, tb, tbh, tc, p, grid, stream)
+             : launch_tc_bf16_epi(pr.out, plan.tile_m, plan.tile_n, row_staging, ta, tb, tbh, tc, p, grid, stream);
   else
-    e = e4m3 ? launch_tc_e4m3(pr.out, plan.tile_m, plan.tile_n, row_staging, ta, tb, tc, p, grid, stream)
-             : launch_tc_bf16(pr.out, plan.tile_m, plan.tile_n, row_staging, ta, tb, tc, p, grid, stream);
+    e = e4m3 ? launch_tc_e4m3(pr.out, plan.tile_m, plan.tile_n, row_staging, ta, tb, tbh, tc, p, grid, stream)
+             : launch_tc_bf16(pr.out, plan.tile_m, plan.tile_n, row_staging, ta, tb, tbh, tc, p, grid, stream);
   return e == cudaSuccess ? DGL_OK : DGL_ERR_CUDA;
 }
 

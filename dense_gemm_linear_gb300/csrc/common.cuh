@@ -50,6 +50,9 @@ struct TcParams {
   // B [K][n]: the backward-pass layouts; bf16 only).
   int a_mn;
   int b_mn;
+  // Split tail: the last, partial wave's tiles (from dp_tiles on) run as
+  // half_tiles halves of BN / 2 columns each, one per worker.
+  int half_tiles;
 };
 
 // Decode (m <= 16) kernel parameters.  A and B are read through tensor maps.
@@ -108,6 +111,7 @@ __device__ __forceinline__ float apply_act(int act, float x) {
 // One piece of a worker's schedule: k-stages [kb0, kb1) of one tile.
 struct Segment {
   int tile, kb0, kb1;
+  int half;  // 0: the whole tile; 1 / 2: its left / right half (BN / 2 columns)
 };
 
 __host__ __device__ inline int64_t sk_range_start(int64_t units, int workers, int w) {
@@ -122,24 +126,35 @@ __host__ __device__ inline int sk_worker_of(int64_t units, int workers, int64_t 
   return w;
 }
 
-// Walks worker w's segments in order: its data-parallel tiles, then its
-// stream-K range.  Every role of a CTA walks the same sequence.
+// Walks worker w's segments in order: its data-parallel tiles, then (split
+// tail) at most one half tile of the last wave, or (stream-K) its range of
+// the last wave's k-stages.  Every role of a CTA walks the same sequence.
 struct SegmentIter {
-  int w, workers, nk, dp_tiles, next_dp;
+  int w, workers, nk, dp_tiles, next_dp, half_tiles, next_half;
   int64_t u, u_end;
-  __host__ __device__ SegmentIter(int worker, int num_workers, int num_kb, int dp, int64_t units)
-      : w(worker), workers(num_workers), nk(num_kb), dp_tiles(dp), next_dp(worker), u(0), u_end(0) {
+  __host__ __device__ SegmentIter(int worker, int num_workers, int num_kb, int dp, int64_t units, int halves = 0)
+      : w(worker), workers(num_workers), nk(num_kb), dp_tiles(dp), next_dp(worker), half_tiles(halves),
+        next_half(worker), u(0), u_end(0) {
     if (units > 0) {
       u = sk_range_start(units, num_workers, worker);
       u_end = sk_range_start(units, num_workers, worker + 1);
     }
   }
   __host__ __device__ bool next(Segment& s) {
+    s.half = 0;
     if (next_dp < dp_tiles) {
       s.tile = next_dp;
       s.kb0 = 0;
       s.kb1 = nk;
       next_dp += workers;
+      return true;
+    }
+    if (next_half < half_tiles) {
+      s.tile = dp_tiles + next_half / 2;
+      s.half = 1 + next_half % 2;
+      s.kb0 = 0;
+      s.kb1 = nk;
+      next_half += workers;
       return true;
     }
     if (u < u_end) {

@@ -29,18 +29,21 @@ cudaError_t set_smem_attr_once(Kernel kern, int bytes, std::atomic<uint64_t>& do
 // row_staging (bf16 output only): C rows are not 16-byte aligned, so the
 // epilogue stages whole rows and writes each row's aligned body in bulk.
 // tc: tensor map of C for TMA stores (used when p.c_tma is set).
-cudaError_t launch_tc_bf16(int out, int tile_m, int tile_n, bool row_staging, const CUtensorMap& ta, const CUtensorMap& tb,
-                           const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_tc_e4m3(int out, int tile_m, int tile_n, bool row_staging, const CUtensorMap& ta, const CUtensorMap& tb,
-                           const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t stream);
+// tbh: B's map with half-height boxes, for the half tiles of a split tail.
+cudaError_t launch_tc_bf16(int out, int tile_m, int tile_n, bool row_staging, const CUtensorMap& ta,
+                           const CUtensorMap& tb, const CUtensorMap& tbh, const CUtensorMap& tc, const TcParams& p,
+                           int grid, cudaStream_t stream);
+cudaError_t launch_tc_e4m3(int out, int tile_m, int tile_n, bool row_staging, const CUtensorMap& ta,
+                           const CUtensorMap& tb, const CUtensorMap& tbh, const CUtensorMap& tc, const TcParams& p,
+                           int grid, cudaStream_t stream);
 // The same with the linear-layer epilogue compiled in (p.bias, p.act,
 // p.gated); tile_n 128 or 256 only.
 cudaError_t launch_tc_bf16_epi(int out, int tile_m, int tile_n, bool row_staging, const CUtensorMap& ta,
-                               const CUtensorMap& tb, const CUtensorMap& tc, const TcParams& p, int grid,
-                               cudaStream_t stream);
+                               const CUtensorMap& tb, const CUtensorMap& tbh, const CUtensorMap& tc,
+                               const TcParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_tc_e4m3_epi(int out, int tile_m, int tile_n, bool row_staging, const CUtensorMap& ta,
-                               const CUtensorMap& tb, const CUtensorMap& tc, const TcParams& p, int grid,
-                               cudaStream_t stream);
+                               const CUtensorMap& tb, const CUtensorMap& tbh, const CUtensorMap& tc,
+                               const TcParams& p, int grid, cudaStream_t stream);
 // Decode kernel: ta = A map (16-row box), tb_lo / tb_hi = B maps whose box
 // heights are the two part sizes floor(n/parts) and ceil(n/parts).
 cudaError_t launch_decode(int dtype, int out, const CUtensorMap& ta, const CUtensorMap& tb_lo,

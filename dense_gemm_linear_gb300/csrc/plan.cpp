@@ -126,6 +126,24 @@ bool stream_k_eligible(int64_t m, int64_t n, int64_t K, int dtype, int tile_m, i
   return tail != 0 && tail * nk >= 4 * units;
 }
 
+// Split tail: a 256-wide tile's last, partial wave runs as half tiles when
+// there is at least one full wave and the tail fills at most half the
+// workers, so the halves still run at once.  Only for short K (at most 16
+// k-blocks of 128 bytes): there a tile's fixed cost (fill, epilogue, store)
+// dominates and halving it pays; with long K a half tile loads 3/4 of a full
+// tile's bytes per k-block for half its MMA work and runs load-bound, and the
+// split measured no faster (4096^3) or slower (8192^3).
+bool split_tail_eligible(int64_t m, int64_t n, int64_t K, int dtype, int tile_m, int tile_n, int num_sms) {
+  if (tile_n != 256) return false;
+  const int64_t nk = (K * (dtype == DGL_DTYPE_E4M3 ? 1 : 2) + 127) / 128;
+  if (nk > 16) return false;
+  const int cg = tile_m == 256 ? 2 : 1;
+  const int64_t tiles = ((m + tile_m - 1) / tile_m) * ((n + tile_n - 1) / tile_n);
+  const int64_t units = std::max(1, num_sms / cg);
+  const int64_t tail = tiles % units;
+  return tiles > units && tail > 0 && 2 * tail <= units;
+}
+
 int tc_tile_k(int dtype) { return dtype == DGL_DTYPE_E4M3 ? 128 : 64; }
 
 int tc_stages(int tile_m, int tile_n) {
@@ -148,6 +166,7 @@ void fill_tc_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int
   out->cta_group = tile_m == 256 ? 2 : 1;
   tile_metrics(m, n, tile_m, tile_n, num_sms / out->cta_group, out);
   // stream_k: 1 force on (if eligible), 0 force off, -1 let the model decide
+  out->split_tail = split_tail_eligible(m, n, K, dtype, tile_m, tile_n, num_sms) ? 1 : 0;
   const bool sk_ok = stream_k_eligible(m, n, K, dtype, tile_m, tile_n, num_sms);
   int grid = 0;
   out->est_us = tc_estimate_us(dtype, out_dtype, m, n, K, tile_m, tile_n, num_sms, false, &grid);
@@ -160,6 +179,7 @@ void fill_tc_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int
       out->est_us = est_sk;
       out->grid = grid_sk;
       out->stream_k = 1;
+      out->split_tail = 0;
     }
   }
 }

@@ -17,6 +17,7 @@ bool tc_supported_tile(int tile_m, int tile_n);
 // stream_k: 1 on (when eligible), 0 off, -1 the cost model decides.
 void fill_tc_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int tile_m, int tile_n, int num_sms,
                   dgl_plan_info* out, int stream_k);
+bool split_tail_eligible(int64_t m, int64_t n, int64_t K, int dtype, int tile_m, int tile_n, int num_sms);
 bool stream_k_eligible(int64_t m, int64_t n, int64_t K, int dtype, int tile_m, int tile_n, int num_sms);
 void fill_decode_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int num_sms, dgl_plan_info* out);
 int decode_parts(int64_t n, int num_sms);

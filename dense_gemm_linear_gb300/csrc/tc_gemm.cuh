@@ -170,7 +170,8 @@ __device__ __forceinline__ void load_operand_pair(uint8_t* dst, const CUtensorMa
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, const TcParams p) {
+                   const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmC,
+                   const TcParams p) {
   constexpr int BM = Cfg::BM, BN = Cfg::BN, STAGES = Cfg::STAGES, CG = Cfg::CG;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -211,6 +212,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (p.half_tiles) tma_prefetch_desc(&tmBh);
     if (p.c_tma) tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
@@ -252,15 +254,21 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       const uint64_t pol = l2_policy_evict_last();
       uint32_t stage = 0, phase = 0;
       int64_t issued = 0;
-      SegmentIter it(cluster_id, p.workers, p.num_kb, p.dp_tiles, p.sk_units);
+      SegmentIter it(cluster_id, p.workers, p.num_kb, p.dp_tiles, p.sk_units, p.half_tiles);
       Segment sg;
       while (!fail && it.next(sg)) {
         int mb, nb;
         tile_coords(sg.tile, p.tiles_m, p.tiles_n, p.group_m, mb, nb);
         const int a_row = mb * Cfg::TILE_M + static_cast<int>(rank) * BM;
         // gated pairs: the leader loads gate rows, the peer the matching up rows
+        // half tiles: each CTA loads its BN / (2 CG) rows of the half through
+        // the half-height map (tmBh), and the stage carries fewer bytes
         const int b_row = (Cfg::EPI && CG == 2 && p.gated) ? (rank == 0 ? 0 : p.n_up) + nb * Cfg::B_ROWS
-                                               : nb * BN + static_cast<int>(rank) * Cfg::B_ROWS;
+                          : sg.half ? nb * BN + (sg.half - 1) * (BN / 2) + static_cast<int>(rank) * (Cfg::B_ROWS / 2)
+                                    : nb * BN + static_cast<int>(rank) * Cfg::B_ROWS;
+        const CUtensorMap* tmb = sg.half ? &tmBh : &tmB;
+        const int b_rows = sg.half ? Cfg::B_ROWS / 2 : Cfg::B_ROWS;
+        const uint32_t stage_bytes = sg.half ? Cfg::A_STAGE_BYTES + Cfg::B_STAGE_BYTES / 2 : Cfg::STAGE_BYTES;
         for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
           const bool ok = mbar_wait(&empty[stage], phase ^ 1);
           if (!ok) {
@@ -273,13 +281,15 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             // before that announcement: the transaction count goes negative
             // for a moment and the phase still waits for the leader's arrival.
             const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
-            if (rank == 0) mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES * CG);
+            if (rank == 0) mbar_arrive_expect_tx(&full[stage], stage_bytes * CG);
             load_operand_pair(sA + stage * Cfg::A_STAGE_BYTES, &tmA, fb, kb * Cfg::BK, a_row, BM, p.a_mn, pol);
-            load_operand_pair(sB + stage * Cfg::B_STAGE_BYTES, &tmB, fb, kb * Cfg::BK, b_row, Cfg::B_ROWS, p.b_mn, pol);
+            load_operand_pair(sB + stage * Cfg::B_STAGE_BYTES, p.b_mn ? &tmB : tmb, fb, kb * Cfg::BK, b_row, b_rows,
+                              p.b_mn, pol);
           } else {
-            mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
+            mbar_arrive_expect_tx(&full[stage], stage_bytes);
             load_operand(sA + stage * Cfg::A_STAGE_BYTES, &tmA, &full[stage], kb * Cfg::BK, a_row, BM, p.a_mn, pol);
-            load_operand(sB + stage * Cfg::B_STAGE_BYTES, &tmB, &full[stage], kb * Cfg::BK, b_row, Cfg::B_ROWS, p.b_mn, pol);
+            load_operand(sB + stage * Cfg::B_STAGE_BYTES, p.b_mn ? &tmB : tmb, &full[stage], kb * Cfg::BK, b_row, b_rows,
+                         p.b_mn, pol);
           }
           ++issued;
           if (++stage == STAGES) {
@@ -304,11 +314,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && rank == 0) {
       // MN-major operands set the instruction's transpose bits (15: A, 16: B)
-      const uint32_t idesc = idesc_f32acc(Cfg::FP8 ? 0u : 1u, Cfg::TILE_M, BN) |
-                             (p.a_mn ? 1u << 15 : 0u) | (p.b_mn ? 1u << 16 : 0u);
+      const uint32_t idesc_major = (p.a_mn ? 1u << 15 : 0u) | (p.b_mn ? 1u << 16 : 0u);
+      const uint32_t idesc_full = idesc_f32acc(Cfg::FP8 ? 0u : 1u, Cfg::TILE_M, BN) | idesc_major;
+      const uint32_t idesc_half = idesc_f32acc(Cfg::FP8 ? 0u : 1u, Cfg::TILE_M, BN / 2) | idesc_major;
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool issued_any = false;
-      SegmentIter it(cluster_id, p.workers, p.num_kb, p.dp_tiles, p.sk_units);
+      SegmentIter it(cluster_id, p.workers, p.num_kb, p.dp_tiles, p.sk_units, p.half_tiles);
       Segment sg;
       while (!fail && it.next(sg)) {
         const bool ok = mbar_wait(&tempty[acc], acc_phase ^ 1);
@@ -318,6 +329,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * BN;
+        const uint32_t idesc = sg.half ? idesc_half : idesc_full;  // a half tile: N = BN / 2
         for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
           const bool ok2 = mbar_wait(&full[stage], phase);
           if (!ok2) {
@@ -382,7 +394,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     uint8_t* stg = Cfg::ROWSTG ? sStg + q * 32 * Cfg::ROW_PITCH : sStg + e * 4096;
     const uint32_t stg_addr = smem_u32(stg);
     uint32_t acc = 0, acc_phase = 0, fx_phase = 0;
-    SegmentIter it(cluster_id, p.workers, p.num_kb, p.dp_tiles, p.sk_units);
+    SegmentIter it(cluster_id, p.workers, p.num_kb, p.dp_tiles, p.sk_units, p.half_tiles);
     Segment sg;
     while (it.next(sg)) {
       int mb, nb;
@@ -533,8 +545,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       // Output columns of this tile: BN, or BN / 2 when a gated pair's MMA
       // computes the gate (leader's B rows) and up (peer's B rows) halves.
       const bool gated = Cfg::EPI && CG == 2 && p.gated != 0;
-      const int out_w = gated ? BN / 2 : BN;
-      const int ocol0 = nb * out_w;
+      const int out_w = (gated || sg.half) ? BN / 2 : BN;
+      const int ocol0 = sg.half ? nb * BN + (sg.half - 1) * (BN / 2) : nb * out_w;
       float row_scale = 0.0f;
       if constexpr (Cfg::FP8) row_scale = (row0 + lane < p.m) ? p.sa[row0 + lane] : 0.0f;
       // row staging (bf16 C, rows not 16-byte aligned): this thread's row
@@ -650,8 +662,41 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       };
 
       bool gated_done = false;
+      if constexpr (BN == 256) {
+        if (sg.half) {
+          // ---- a half tile of the split tail: BN / 2 columns in TMEM
+          // columns [0, BN / 2); this warp takes CPW / 2 of their chunks
+          gated_done = true;
+          constexpr int HCPW = CPW / 2;
+#pragma unroll 1
+          for (int u = 0; u < HCPW; ++u) {
+            const int oc = half * HCPW + u;
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(t_row + oc * 32, v);
+            tmem_ld_wait();
+            reg_fence(v);
+            if (u + 1 == HCPW) hand_back();
+            const int col = ocol0 + oc * 32 + lane;
+            if constexpr (Cfg::FP8) {
+              const float col_scale = col < p.n ? p.sb[col] : 0.0f;
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                v[j] = __float_as_uint((__uint_as_float(v[j]) * row_scale) * __shfl_sync(0xffffffffu, col_scale, j));
+            }
+            if constexpr (Cfg::EPI) {
+              if (p.act != 0 || p.bias != nullptr) {
+                const float b = (p.bias && col < p.n) ? p.bias[col] : 0.0f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  v[j] = __float_as_uint(apply_act(p.act, __uint_as_float(v[j]) + __shfl_sync(0xffffffffu, b, j)));
+              }
+            }
+            emit(v, oc);
+          }
+        }
+      }
       if constexpr (Cfg::EPI && CG == 2) {
-        if (gated) {
+        if (gated && !gated_done) {
           gated_done = true;
           // ---- gated linear layer: output chunk oc combines gate chunk oc with
           // up chunk oc + CHUNKS / 2; this warp takes CPW / 2 output chunks.

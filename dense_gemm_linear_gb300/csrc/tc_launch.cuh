@@ -11,8 +11,8 @@
 namespace dgl {
 
 template <int BN, bool FP8, bool OUT_F32, bool ROWSTG, int CG, bool EPI>
-cudaError_t tc_launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const TcParams& p,
-                          int grid, cudaStream_t stream) {
+cudaError_t tc_launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tbh, const CUtensorMap& tc,
+                          const TcParams& p, int grid, cudaStream_t stream) {
   using Cfg = TcConfig<BN, FP8, OUT_F32, ROWSTG, CG, EPI>;
   auto kern = tc_gemm_kernel<Cfg>;
   static std::atomic<uint64_t> attr_done{0};  // one bit per device
@@ -38,36 +38,37 @@ cudaError_t tc_launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CU
     attr[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;
   }
-  return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, p);
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, tbh, tc, p);
 }
 
 template <int BN, bool FP8, int CG, bool EPI>
 cudaError_t tc_launch_bn(int out, bool row_staging, const CUtensorMap& ta, const CUtensorMap& tb,
-                         const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t stream) {
-  if (out == 1) return tc_launch_one<BN, FP8, true, false, CG, EPI>(ta, tb, tc, p, grid, stream);
-  if (row_staging) return tc_launch_one<BN, FP8, false, true, CG, EPI>(ta, tb, tc, p, grid, stream);
-  return tc_launch_one<BN, FP8, false, false, CG, EPI>(ta, tb, tc, p, grid, stream);
+                         const CUtensorMap& tbh, const CUtensorMap& tc, const TcParams& p, int grid,
+                         cudaStream_t stream) {
+  if (out == 1) return tc_launch_one<BN, FP8, true, false, CG, EPI>(ta, tb, tbh, tc, p, grid, stream);
+  if (row_staging) return tc_launch_one<BN, FP8, false, true, CG, EPI>(ta, tb, tbh, tc, p, grid, stream);
+  return tc_launch_one<BN, FP8, false, false, CG, EPI>(ta, tb, tbh, tc, p, grid, stream);
 }
 
 // EPI: the linear-layer variants, compiled for the 128- and 256-wide tiles
 // only (tc_supported_epi_tile); the plain variants cover the whole ladder.
 template <bool FP8, bool EPI>
 cudaError_t tc_launch(int out, int tile_m, int tile_n, bool row_staging, const CUtensorMap& ta, const CUtensorMap& tb,
-                      const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t stream) {
+                      const CUtensorMap& tbh, const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t stream) {
   if (tile_m == 128) {
     switch (tile_n) {
       case 64:
         if constexpr (EPI) return cudaErrorInvalidValue;
-        else return tc_launch_bn<64, FP8, 1, EPI>(out, row_staging, ta, tb, tc, p, grid, stream);
-      case 128: return tc_launch_bn<128, FP8, 1, EPI>(out, row_staging, ta, tb, tc, p, grid, stream);
-      case 256: return tc_launch_bn<256, FP8, 1, EPI>(out, row_staging, ta, tb, tc, p, grid, stream);
+        else return tc_launch_bn<64, FP8, 1, EPI>(out, row_staging, ta, tb, tbh, tc, p, grid, stream);
+      case 128: return tc_launch_bn<128, FP8, 1, EPI>(out, row_staging, ta, tb, tbh, tc, p, grid, stream);
+      case 256: return tc_launch_bn<256, FP8, 1, EPI>(out, row_staging, ta, tb, tbh, tc, p, grid, stream);
       default: return cudaErrorInvalidValue;
     }
   }
   if (tile_m == 256) {
     switch (tile_n) {
-      case 128: return tc_launch_bn<128, FP8, 2, EPI>(out, row_staging, ta, tb, tc, p, grid, stream);
-      case 256: return tc_launch_bn<256, FP8, 2, EPI>(out, row_staging, ta, tb, tc, p, grid, stream);
+      case 128: return tc_launch_bn<128, FP8, 2, EPI>(out, row_staging, ta, tb, tbh, tc, p, grid, stream);
+      case 256: return tc_launch_bn<256, FP8, 2, EPI>(out, row_staging, ta, tb, tbh, tc, p, grid, stream);
       default: return cudaErrorInvalidValue;
     }
   }

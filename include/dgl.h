@@ -99,7 +99,9 @@ typedef struct {
   double dim_eff;
   double est_us;      /* cost-model estimate of the kernel time, microseconds */
   int32_t stream_k;   /* 1: tiles of the last, partial wave are split along K across all workers */
-  int32_t reserved;   /* zero */
+  int32_t split_tail; /* 1: the last, partial wave's tiles (tile_n 256) run as two half tiles each, */
+                      /*    when that wave fills at most half the workers (not with stream_k or gated); */
+                      /*    the planner sets it only for K of at most 16 k-blocks of 128 bytes */
 } dgl_plan_info;
 
 /*
@@ -128,7 +130,7 @@ dgl_status dgl_gemm_fp8(const void* A, const void* B, const float* sa, const flo
  * forced-tile sweep of FlyDSL pull request 1303 ("a second test runs every
  * tile of both ladders against a shape that divides none of them").
  * dtype: dgl_dtype_t (sa/sb ignored for bf16).  plan->path, tile_m, tile_n,
- * stream_k and grid are honoured (grid <= 0 picks one), and for the decode
+ * stream_k, split_tail and grid are honoured (grid <= 0 picks one), and for the decode
  * path tile_k (K elements per ring stage, a multiple of 128 bytes, 0 = pick);
  * other fields are ignored.  A plan the library has no kernel for returns
  * DGL_ERR_UNSUPPORTED.

@@ -83,6 +83,14 @@ def test_layouts_small_m_take_the_tile_path(m):
     gu.assert_close_full(case, gu.host_valid(case, Cbuf))
 
 
+@pytest.mark.parametrize("layout", [(K_, MN_), (MN_, MN_)], ids=["dX", "dW"])
+def test_layouts_split_tail(layout):
+    case = make_case("bf16", 2304, 2304, 256, out="bf16")
+    plan = dgl.PlanInfo(path=dgl.PATH_TC, tile_m=256, tile_n=256, split_tail=1)
+    Cbuf = _run(case, *layout, plan=plan)
+    gu.assert_close_full(case, gu.host_valid(case, Cbuf))
+
+
 def test_layouts_stream_k():
     case = make_case("bf16", 600, 1100, 1024, out="f32")
     plan = dgl.PlanInfo(path=dgl.PATH_TC, tile_m=256, tile_n=256, stream_k=1)

@@ -132,6 +132,13 @@ def test_activation_accuracy_over_a_wide_range(act):
     assert (err <= 4e-6 * np.abs(x) + 1e-6).all(), f"max err {err.max():.3e}"
 
 
+def test_split_tail_with_linear_epilogue():
+    """The last wave's half tiles take the bias and activation too."""
+    case = _case("bf16", 2304, 2304, 256, "bf16", False)
+    plan = dgl.PlanInfo(path=dgl.PATH_TC, tile_m=256, tile_n=256, split_tail=1)
+    _full(case, _bias(2304), dgl.ACT_GELU, False, plan=plan, pad_cols=2)
+
+
 # ------------------------------------------------------------ gated up projection
 @pytest.mark.parametrize("act", ["gelu", "silu", "none"])
 @pytest.mark.parametrize("out", ["bf16", "f32"])

@@ -231,3 +231,31 @@ def test_torch_helpers_and_streams():
         C = dgl.gemm_bf16(A, B)
     s.synchronize()
     gu.assert_close_full(case, C.double().cpu().numpy())
+
+
+# -------------------------------------------------------------- split tail (half tiles in the last wave)
+SPLIT_TAIL_CASES = [
+    # (m, n, k, tile, dtype, out): at least one full wave, a tail of at most half the workers
+    (2304, 2304, 256, (256, 256), "bf16", "bf16"),    # 81 pair tiles: 76 + a tail of 5
+    (2300, 2290, 200, (256, 256), "bf16", "bf16"),    # ragged m, n, K; unaligned bf16 rows
+    (2304, 2304, 256, (256, 256), "fp8", "bf16"),
+    (1280, 4096, 128, (128, 256), "bf16", "f32"),      # 160 one-CTA tiles: 152 + a tail of 8
+    (1290, 4000, 136, (128, 256), "bf16", "bf16"),
+]
+
+
+@pytest.mark.parametrize("m,n,k,tile,dtype,out", SPLIT_TAIL_CASES)
+def test_split_tail(m, n, k, tile, dtype, out):
+    case = make_case(dtype, m, n, k, out=out, dist="fp8" if dtype == "fp8" else "normal")
+    plan = dgl.PlanInfo(path=dgl.PATH_TC, tile_m=tile[0], tile_n=tile[1], split_tail=1)
+    Cbuf, intact = gu.run(case, plan=plan, guard_rows=1, pad_cols=1)
+    assert intact
+    gu.assert_close_full(case, gu.host_valid(case, Cbuf))
+
+
+def test_split_tail_integer_exact():
+    case = make_case("bf16", 2304, 2304, 128, out="f32", dist="int")
+    plan = dgl.PlanInfo(path=dgl.PATH_TC, tile_m=256, tile_n=256, split_tail=1)
+    Cbuf, intact = gu.run(case, plan=plan)
+    assert intact
+    gu.assert_exact(case, gu.host_valid(case, Cbuf))

@@ -132,6 +132,25 @@ def test_plan_padding_screen(dgl, m, n, k):
     assert 0 < p.dim_eff <= 1.0 and p.est_us > 0
 
 
+def test_plan_split_tail_rule(dgl):
+    """The last partial wave of 256x256 pair tiles splits into half tiles only
+    with at least one full wave before it, a tail of at most half the 76 pair
+    workers, and K of at most 16 k-blocks of 128 bytes."""
+    def plan(dt, m, n, k):
+        p = dgl.dgl_plan(dt, m, n, k, num_sms=152)
+        return (p.tile_m, p.tile_n, p.num_tiles, p.split_tail)
+
+    # 256 tiles = 3 waves of 76 + 28: short K splits in both dtypes, long K does not
+    assert plan(0, 4095, 4095, 1024) == (256, 256, 256, 1)
+    assert plan(1, 4095, 4095, 2048) == (256, 256, 256, 1)
+    assert plan(0, 4095, 4095, 2048)[3] == 0
+    assert plan(0, 4096, 4096, 4096)[3] == 0
+    # 344 tiles = 4 waves + 40: more than half the workers, no split
+    assert plan(0, 2048, 11007, 1024) == (256, 256, 344, 0)
+    # no full wave before the tail
+    assert plan(0, 2048, 2048, 1024)[3] == 0
+
+
 def test_plan_argument_errors(dgl):
     info = dgl.PlanInfo()
     lib = dgl.load_library()
