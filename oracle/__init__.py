@@ -1,5 +1,6 @@
 """Reference oracle for C = A . B^T (bf16 and E4M3 inputs, fp64 arithmetic),
-and for the linear layer around it (bias, GELU / SiLU, gated up projection).
+for the linear layer around it (bias, GELU / SiLU, gated up projection), and
+for the block-scaled FP4 (MXFP4) product.
 
 TEST INFRASTRUCTURE ONLY.  The product library never imports this package;
 only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
@@ -69,6 +70,14 @@ def _bind(lib):
     lib.oracle_linear_points.argtypes = [ctypes.c_int, vp, vp, vp, vp, vp, c_i64, c_i64, c_i64, ctypes.c_int,
                                          ctypes.c_int, vp, vp, c_i64, vp, vp]
     lib.oracle_linear_points.restype = ctypes.c_int
+    lib.oracle_decode_e2m1.argtypes = [ctypes.c_uint8]
+    lib.oracle_decode_e2m1.restype = ctypes.c_double
+    lib.oracle_decode_e8m0.argtypes = [ctypes.c_uint8]
+    lib.oracle_decode_e8m0.restype = ctypes.c_double
+    lib.oracle_mxfp4_gemm.argtypes = [vp, vp, vp, vp, c_i64, c_i64, c_i64, vp, vp]
+    lib.oracle_mxfp4_gemm.restype = ctypes.c_int
+    lib.oracle_mxfp4_gemm_points.argtypes = [vp, vp, vp, vp, c_i64, c_i64, c_i64, vp, vp, c_i64, vp, vp]
+    lib.oracle_mxfp4_gemm_points.restype = ctypes.c_int
     lib.oracle_threads.argtypes = []
     lib.oracle_threads.restype = ctypes.c_int
     return lib
@@ -234,6 +243,65 @@ def round_bf16(x, lib=None):
     out = np.empty(x.shape, dtype=np.uint16)
     lib.oracle_round_bf16_n(_ptr(x), x.size, _ptr(out))
     return out
+
+
+def _mx_inputs(A, B, EA, EB):
+    arrs = [np.ascontiguousarray(x) for x in (A, B, EA, EB)]
+    for x in arrs:
+        if x.dtype != np.uint8 or x.ndim != 2:
+            raise TypeError("MXFP4 operands and scales are 2-D uint8 arrays")
+    A, B, EA, EB = arrs
+    m, half_k = A.shape
+    n = B.shape[0]
+    K = 2 * half_k
+    if B.shape[1] != half_k or K % 32 != 0:
+        raise ValueError("A and B hold K / 2 bytes per row, K a multiple of 32")
+    if EA.shape != (m, K // 32) or EB.shape != (n, K // 32):
+        raise ValueError("scales hold K / 32 bytes per row of A and of B")
+    return A, B, EA, EB, m, n, K
+
+
+def mxfp4_gemm(A, B, EA, EB, lib=None):
+    """Full reference MXFP4 product.
+
+    A [m, K/2], B [n, K/2]: packed E2M1 codes (element 2t in the low four bits
+    of byte t); EA [m, K/32], EB [n, K/32]: E8M0 scale codes, one per block of
+    32 elements along K.  Returns (C_ref, S_abs), float64 [m, n]."""
+    lib = lib or load()
+    A, B, EA, EB, m, n, K = _mx_inputs(A, B, EA, EB)
+    C = np.empty((m, n), dtype=np.float64)
+    S = np.empty((m, n), dtype=np.float64)
+    if lib.oracle_mxfp4_gemm(_ptr(A), _ptr(B), _ptr(EA), _ptr(EB), m, n, K, _ptr(C), _ptr(S)) != 0:
+        raise ValueError("oracle_mxfp4_gemm rejected its arguments")
+    return C, S
+
+
+def mxfp4_gemm_points(A, B, EA, EB, rows, cols, lib=None):
+    """Reference MXFP4 values at the points (rows[p], cols[p]); returns (C_ref, S_abs)."""
+    lib = lib or load()
+    A, B, EA, EB, m, n, K = _mx_inputs(A, B, EA, EB)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    cols = np.ascontiguousarray(cols, dtype=np.int64)
+    if rows.shape != cols.shape:
+        raise ValueError("rows and cols differ in length")
+    C = np.empty(rows.shape, dtype=np.float64)
+    S = np.empty(rows.shape, dtype=np.float64)
+    if lib.oracle_mxfp4_gemm_points(_ptr(A), _ptr(B), _ptr(EA), _ptr(EB), m, n, K, _ptr(rows), _ptr(cols),
+                                    rows.size, _ptr(C), _ptr(S)) != 0:
+        raise ValueError("oracle_mxfp4_gemm_points rejected its arguments")
+    return C, S
+
+
+def decode_e2m1(codes, lib=None):
+    lib = lib or load()
+    codes = np.asarray(codes, dtype=np.uint8)
+    return np.array([lib.oracle_decode_e2m1(int(c)) for c in codes.ravel()]).reshape(codes.shape)
+
+
+def decode_e8m0(codes, lib=None):
+    lib = lib or load()
+    codes = np.asarray(codes, dtype=np.uint8)
+    return np.array([lib.oracle_decode_e8m0(int(c)) for c in codes.ravel()]).reshape(codes.shape)
 
 
 def threads(lib=None) -> int:

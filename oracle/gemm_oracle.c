@@ -317,6 +317,106 @@ int oracle_linear_points(int dtype, const void* A, const void* B,
     return 0;
 }
 
+/*
+ * ---- Block-scaled FP4 (MXFP4) ------------------------------------------------
+ *
+ * The "Gemm Optimization" guide's bandwidth formulas (section 8.2, "FP4
+ * (MXFP4)") count half a byte per element of A and of B plus one byte per 32
+ * elements of K for every row of A and every row of B.  The page names the
+ * format and nothing more; the reading taken is the OCP Microscaling format
+ * it names: E2M1 elements, and one E8M0 scale for each block of 32
+ * consecutive elements of a row along K, so that
+ *   value(X, r, k) = 2^(E[r, k / 32] - 127) * e2m1(X[r, k])
+ *   C[i,j] = sum_k value(A, i, k) * value(B, j, k)
+ * Storage: X holds K / 2 bytes per row, element 2t in the low four bits of
+ * byte t and element 2t + 1 in the high four; E holds K / 32 bytes per row.
+ * K must be a multiple of 32 (whole blocks).
+ *
+ * Decoders from the format definitions:
+ *   E2M1: 1 sign bit, 2 exponent bits (bias 1), 1 fraction bit; exponent 0 is
+ *   subnormal (fraction * 2^-1); no infinities or NaN; largest magnitude 6.
+ *   E8M0: 8 exponent bits (bias 127), no sign or fraction; 0xFF is NaN.
+ */
+double oracle_decode_e2m1(uint8_t code)
+{
+    int sign = (code >> 3) & 1;
+    int expo = (code >> 1) & 3;
+    int frac = code & 1;
+    double v;
+    if (expo == 0)
+        v = ldexp((double)frac / 2.0, 1 - 1);          /* subnormal: 0.f * 2^(1-1) */
+    else
+        v = ldexp(1.0 + (double)frac / 2.0, expo - 1);
+    return sign ? -v : v;
+}
+
+double oracle_decode_e8m0(uint8_t code)
+{
+    if (code == 0xFF) return NAN;
+    return ldexp(1.0, (int)code - 127);
+}
+
+static double mx_value(const uint8_t* X, const uint8_t* E, int64_t K, int64_t r, int64_t k)
+{
+    uint8_t byte = X[r * (K / 2) + k / 2];
+    uint8_t code = (k % 2 == 0) ? (uint8_t)(byte & 0xF) : (uint8_t)(byte >> 4);
+    return oracle_decode_e8m0(E[r * (K / 32) + k / 32]) * oracle_decode_e2m1(code);
+}
+
+static void mx_element(const uint8_t* A, const uint8_t* B, const uint8_t* EA, const uint8_t* EB,
+                       int64_t K, int64_t i, int64_t j, double* c_out, double* s_out)
+{
+    double acc = 0.0, mag = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        double p = mx_value(A, EA, K, i, k) * mx_value(B, EB, K, j, k);
+        acc += p;
+        mag += fabs(p);
+    }
+    *c_out = acc;
+    *s_out = mag;
+}
+
+/*
+ * Full MXFP4 product over the valid region: A [m][K/2], B [n][K/2] packed
+ * E2M1 codes, EA [m][K/32], EB [n][K/32] E8M0 scales; C_ref and S_abs
+ * [m*n] row-major (S_abs may be NULL).  Returns 0, or -1 on a bad argument.
+ */
+int oracle_mxfp4_gemm(const uint8_t* A, const uint8_t* B, const uint8_t* EA, const uint8_t* EB,
+                      int64_t m, int64_t n, int64_t K, double* C_ref, double* S_abs)
+{
+    if (!A || !B || !EA || !EB || !C_ref || m < 0 || n < 0 || K < 0 || K % 32 != 0) return -1;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < m; ++i) {
+        for (int64_t j = 0; j < n; ++j) {
+            double c, s;
+            mx_element(A, B, EA, EB, K, i, j, &c, &s);
+            C_ref[i * n + j] = c;
+            if (S_abs) S_abs[i * n + j] = s;
+        }
+    }
+    return 0;
+}
+
+/* The MXFP4 product at a list of (row, col) points; as oracle_gemm_points. */
+int oracle_mxfp4_gemm_points(const uint8_t* A, const uint8_t* B, const uint8_t* EA, const uint8_t* EB,
+                             int64_t m, int64_t n, int64_t K, const int64_t* rows, const int64_t* cols,
+                             int64_t npts, double* C_ref, double* S_abs)
+{
+    if (!A || !B || !EA || !EB || !C_ref || !rows || !cols || npts < 0 || m < 0 || n < 0 || K < 0 ||
+        K % 32 != 0)
+        return -1;
+    for (int64_t p = 0; p < npts; ++p)
+        if (rows[p] < 0 || rows[p] >= m || cols[p] < 0 || cols[p] >= n) return -1;
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t p = 0; p < npts; ++p) {
+        double c, s;
+        mx_element(A, B, EA, EB, K, rows[p], cols[p], &c, &s);
+        C_ref[p] = c;
+        if (S_abs) S_abs[p] = s;
+    }
+    return 0;
+}
+
 /* Threads an OpenMP region of this library uses (1 without OpenMP). */
 int oracle_threads(void)
 {

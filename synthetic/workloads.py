@@ -16,7 +16,7 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-from .encode import to_bf16_codes, to_e4m3_codes
+from .encode import mx_quantize, pack_e2m1, to_bf16_codes, to_e4m3_codes
 from .rng import STREAM_A, STREAM_B, STREAM_SA, STREAM_SB, integers, normal, uniform
 
 # (m, n, K)
@@ -33,8 +33,11 @@ ACT_IDS = {"none": 0, "gelu": 1, "silu": 2}
 
 @dataclass
 class GemmCase:
-    """One GEMM problem: codes of A [m,K] and B [n,K], optional fp32 scales."""
-    dtype: str               # "bf16" or "fp8"
+    """One GEMM problem: codes of A [m,K] and B [n,K], optional scales.
+
+    dtype "mxfp4": A [m, K/2] and B [n, K/2] hold packed E2M1 codes and sa
+    [m, K/32], sb [n, K/32] their E8M0 block-scale codes (uint8)."""
+    dtype: str               # "bf16", "fp8" or "mxfp4"
     m: int
     n: int
     K: int
@@ -82,7 +85,14 @@ def make_case(dtype: str, m: int, n: int, K: int, *, out: str = "bf16",
       "uniform"  A, B ~ U[-1, 1)                                 (bf16)
       "int"      A, B integers in [-4, 4]; fp8 scales in {0.5, 1, 2}
       "fp8"      x ~ N(0,1); sa, sb ~ U[0.5, 2); codes = e4m3(x / scale)
+    dtype "mxfp4" (K a multiple of 32):
+      "mx"       A ~ N(0, a_std^2), B ~ N(0, b_std^2), block-quantised (OCP MX)
+      "int"      E2M1 codes of magnitude <= 3 with random signs, scale codes in
+                 {126, 127, 128}: every product is a multiple of 2^-4 and sums
+                 up to K = 4096 are exact in fp32
     """
+    if dtype == "mxfp4":
+        return _make_mx_case(m, n, K, out, dist, seed, a_std, b_std)
     if dtype not in ("bf16", "fp8"):
         raise ValueError(dtype)
     sa = sb = None
@@ -116,6 +126,23 @@ def make_case(dtype: str, m: int, n: int, K: int, *, out: str = "bf16",
             sa = np.ones(m, dtype=np.float32)
             sb = np.ones(n, dtype=np.float32)
     return GemmCase(dtype, m, n, K, out, dist, seed, A, B, sa, sb)
+
+
+def _make_mx_case(m, n, K, out, dist, seed, a_std, b_std) -> GemmCase:
+    if K % 32 != 0:
+        raise ValueError("MXFP4 blocks: K must be a multiple of 32")
+    if dist == "mx":
+        A, sa = mx_quantize(normal(seed, STREAM_A, (m, K), 0.0, a_std))
+        B, sb = mx_quantize(normal(seed, STREAM_B, (n, K), 0.0, b_std))
+    elif dist == "int":
+        codes = np.array([0, 1, 2, 3, 4, 5, 8, 9, 10, 11, 12, 13], dtype=np.uint8)  # |value| <= 3
+        A = pack_e2m1(codes[integers(seed, STREAM_A, (m, K), 0, 11).astype(np.int64)])
+        B = pack_e2m1(codes[integers(seed, STREAM_B, (n, K), 0, 11).astype(np.int64)])
+        sa = (126 + integers(seed, STREAM_SA, (m, K // 32), 0, 2)).astype(np.uint8)
+        sb = (126 + integers(seed, STREAM_SB, (n, K // 32), 0, 2)).astype(np.uint8)
+    else:
+        raise ValueError(dist)
+    return GemmCase("mxfp4", m, n, K, out, dist, seed, A, B, sa, sb)
 
 
 # name -> list of (dtype, m, n, K, out, dist)

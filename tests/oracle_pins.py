@@ -12,7 +12,13 @@ A check raises AssertionError when the oracle disagrees with:
   - for the linear layer: library routines for the normal distribution
     function and the logistic function, the symmetry act(x) - act(-x) = x,
     printed values (Phi(1), sigma(ln 3) = 3/4), and one-hot rows of A that
-    turn the product into a lookup of B, so bias, gate and up terms are exact.
+    turn the product into a lookup of B, so bias, gate and up terms are exact,
+  - for the block-scaled FP4 (MXFP4) product: the E2M1 value table the format
+    fixes, torch's E8M0 decoder over every code, hand-packed bytes whose
+    product is known (which byte holds which element, which block scale
+    covers which k), numpy's matmul when every scale is 1, and brute force in
+    exact rational arithmetic.  (Which nibble of a byte comes first cannot
+    change a product: A and B swap the same two elements of one block.)
 """
 from __future__ import annotations
 
@@ -291,10 +297,129 @@ def check_linear_points_match_full(lib):
     np.testing.assert_array_equal(Ep, E[rows, cols])
 
 
+# ------------------------------------------------------------ block-scaled FP4 (MXFP4)
+# E2M1 magnitudes of codes 0..7 as the format fixes them (OCP Microscaling
+# version 1.0, table of FP4 E2M1 values); bit 3 is the sign
+E2M1_TABLE = {0: 0.0, 1: 0.5, 2: 1.0, 3: 1.5, 4: 2.0, 5: 3.0, 6: 4.0, 7: 6.0}
+E2M1_ONE = 0x2
+
+
+def _e2m1_value(code):
+    v = E2M1_TABLE[code & 7]
+    return -v if code & 8 else v
+
+
+def _unpack(packed):
+    """[r, K/2] bytes -> [r, K] codes; element 2t is the low four bits of byte t."""
+    out = np.empty((packed.shape[0], packed.shape[1] * 2), dtype=np.uint8)
+    out[:, 0::2] = packed & 0xF
+    out[:, 1::2] = packed >> 4
+    return out
+
+
+def check_e2m1_decoder(lib):
+    got = oracle.decode_e2m1(np.arange(16, dtype=np.uint8), lib=lib)
+    for code in range(16):
+        want = _e2m1_value(code)
+        assert got[code] == want and np.signbit(got[code]) == (code >= 8), (code, got[code], want)
+
+
+def check_e8m0_decoder(lib):
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.decode_e8m0(codes, lib=lib)
+    want = torch.from_numpy(codes.copy()).view(torch.float8_e8m0fnu).float().numpy().astype(np.float64)
+    same = (got == want) | (np.isnan(got) & np.isnan(want))
+    assert same.all(), f"e8m0 decoder differs at codes {codes[~same][:8]}"
+    assert got[127] == 1.0 and got[128] == 2.0 and got[0] == 2.0 ** -127 and np.isnan(got[255])
+
+
+def check_mx_nibble_order(lib):
+    # B's row: element 0 is 0.5 (code 1), element 1 is 4.0 (code 6): byte 0 = 0x61
+    K = 32
+    B = np.zeros((1, K // 2), dtype=np.uint8)
+    B[0, 0] = 0x61
+    A = np.zeros((2, K // 2), dtype=np.uint8)
+    A[0, 0] = E2M1_ONE          # element 0 is 1.0
+    A[1, 0] = E2M1_ONE << 4     # element 1 is 1.0
+    ones = np.full((2, 1), 127, dtype=np.uint8)
+    C, S = oracle.mxfp4_gemm(A, B, ones, ones[:1], lib=lib)
+    assert C[0, 0] == 0.5 and C[1, 0] == 4.0, C
+    assert S[0, 0] == 0.5 and S[1, 0] == 4.0
+
+
+def check_mx_block_scales(lib):
+    # all elements 1.0 over K = 96 (three blocks); C = 32 * sum_b 2^(ea_b - 127) 2^(eb_b - 127)
+    K = 96
+    ones_byte = E2M1_ONE | (E2M1_ONE << 4)
+    A = np.full((2, K // 2), ones_byte, dtype=np.uint8)
+    B = np.full((2, K // 2), ones_byte, dtype=np.uint8)
+    EA = np.array([[127, 130, 127], [126, 127, 129]], dtype=np.uint8)
+    EB = np.array([[127, 127, 127], [129, 125, 127]], dtype=np.uint8)
+    C, _ = oracle.mxfp4_gemm(A, B, EA, EB, lib=lib)
+    for i in range(2):
+        for j in range(2):
+            want = 32 * sum(2.0 ** (int(EA[i, b]) - 127) * 2.0 ** (int(EB[j, b]) - 127) for b in range(3))
+            assert C[i, j] == want, (i, j, C[i, j], want)
+    # one element at k = 33 (block 1, the high nibble of byte 16) picks block 1's scales only
+    A1 = np.zeros((1, K // 2), dtype=np.uint8)
+    A1[0, 16] = E2M1_ONE << 4
+    C1, _ = oracle.mxfp4_gemm(A1, B[:1], EA[:1], EB[1:], lib=lib)
+    assert C1[0, 0] == 2.0 ** 3 * 2.0 ** -2
+
+
+def check_mx_unit_scales_match_matmul(lib):
+    rng = np.random.default_rng(7)
+    m, n, K = 9, 11, 160
+    A = rng.integers(0, 256, size=(m, K // 2), dtype=np.uint8)
+    B = rng.integers(0, 256, size=(n, K // 2), dtype=np.uint8)
+    C, S = oracle.mxfp4_gemm(A, B, np.full((m, K // 32), 127, np.uint8), np.full((n, K // 32), 127, np.uint8),
+                             lib=lib)
+    Av = np.vectorize(_e2m1_value)(_unpack(A))
+    Bv = np.vectorize(_e2m1_value)(_unpack(B))
+    np.testing.assert_array_equal(C, Av @ Bv.T)   # multiples of 1/4 below 2^12: exact in double
+    np.testing.assert_array_equal(S, np.abs(Av) @ np.abs(Bv).T)
+
+
+def check_mx_brute_force(lib):
+    rng = np.random.default_rng(31)
+    for trial in range(10):
+        m, n = (int(x) for x in rng.integers(1, 6, size=2))
+        K = 32 * int(rng.integers(1, 4))
+        A = rng.integers(0, 256, size=(m, K // 2), dtype=np.uint8)
+        B = rng.integers(0, 256, size=(n, K // 2), dtype=np.uint8)
+        EA = rng.integers(115, 140, size=(m, K // 32), dtype=np.uint8)
+        EB = rng.integers(115, 140, size=(n, K // 32), dtype=np.uint8)
+        C, _ = oracle.mxfp4_gemm(A, B, EA, EB, lib=lib)
+        Ac, Bc = _unpack(A), _unpack(B)
+        for i in range(m):
+            for j in range(n):
+                want = sum((Fraction(_e2m1_value(int(Ac[i, k]))) * Fraction(2) ** (int(EA[i, k // 32]) - 127) *
+                            Fraction(_e2m1_value(int(Bc[j, k]))) * Fraction(2) ** (int(EB[j, k // 32]) - 127)
+                            for k in range(K)), Fraction(0))
+                assert Fraction(C[i, j]) == want, (trial, i, j)
+
+
+def check_mx_points_match_full(lib):
+    rng = np.random.default_rng(5)
+    m, n, K = 13, 17, 64
+    A = rng.integers(0, 256, size=(m, K // 2), dtype=np.uint8)
+    B = rng.integers(0, 256, size=(n, K // 2), dtype=np.uint8)
+    EA = rng.integers(120, 135, size=(m, K // 32), dtype=np.uint8)
+    EB = rng.integers(120, 135, size=(n, K // 32), dtype=np.uint8)
+    C, S = oracle.mxfp4_gemm(A, B, EA, EB, lib=lib)
+    rows = np.array([0, m - 1, 4, 12])
+    cols = np.array([0, n - 1, 16, 9])
+    Cp, Sp = oracle.mxfp4_gemm_points(A, B, EA, EB, rows, cols, lib=lib)
+    np.testing.assert_array_equal(Cp, C[rows, cols])
+    np.testing.assert_array_equal(Sp, S[rows, cols])
+
+
 ALL_CHECKS = [check_bf16_decoder, check_e4m3_decoder, check_round_bf16, check_identity,
               check_permutation, check_rank1, check_all_ones, check_scaled_rank1_e4m3,
               check_brute_force, check_points_match_full, check_act_closed_forms, check_linear_bias_onehot,
-              check_linear_gated_onehot, check_linear_gated_scaled_e4m3, check_linear_points_match_full]
+              check_linear_gated_onehot, check_linear_gated_scaled_e4m3, check_linear_points_match_full,
+              check_e2m1_decoder, check_e8m0_decoder, check_mx_nibble_order, check_mx_block_scales,
+              check_mx_unit_scales_match_matmul, check_mx_brute_force, check_mx_points_match_full]
 
 
 def run_all(lib):

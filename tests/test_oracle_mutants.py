@@ -16,11 +16,13 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "gemm_oracle.c")
 
 MUTANTS = {
     # a dropped term: the first k is skipped
-    "drop_first_k": ("for (int64_t k = 0; k < K; ++k)", "for (int64_t k = 1; k < K; ++k)"),
+    "drop_first_k": ("for (int64_t k = 0; k < K; ++k) {\n        double p = load_code",
+                     "for (int64_t k = 1; k < K; ++k) {\n        double p = load_code"),
     # a dropped term: the last k is skipped
-    "drop_last_k": ("for (int64_t k = 0; k < K; ++k)", "for (int64_t k = 0; k + 1 < K; ++k)"),
+    "drop_last_k": ("for (int64_t k = 0; k < K; ++k) {\n        double p = load_code",
+                    "for (int64_t k = 0; k + 1 < K; ++k) {\n        double p = load_code"),
     # a wrong sign in the accumulation
-    "wrong_sign": ("acc += p;", "acc -= p;"),
+    "wrong_sign": ("load_code(dtype, B, j * K + k);\n        acc += p;", "load_code(dtype, B, j * K + k);\n        acc -= p;"),
     # a wrong index on B: k runs backwards along the row
     "reversed_k_on_B": ("load_code(dtype, B, j * K + k)", "load_code(dtype, B, j * K + (K - 1 - k))"),
     # a transposed operand read: B taken as [K, N] with the same buffer
@@ -38,7 +40,7 @@ MUTANTS = {
     "round_truncates": ("double r = nearbyint(a / q);", "double r = floor(a / q);"),
     "round_half_up": ("double r = nearbyint(a / q);", "double r = floor(a / q + 0.5);"),
     # magnitude sum wrong
-    "mag_signed": ("mag += fabs(p);", "mag += p;"),
+    "mag_signed": ("acc += p;\n        mag += fabs(p);\n    }\n    if (sa && sb)", "acc += p;\n        mag += p;\n    }\n    if (sa && sb)"),
     # linear layer: activation constants and signs
     "gelu_half_not_root2": ("x * 0.5 * erfc(-x / sqrt(2.0))", "x * 0.5 * erfc(-x / 2.0)"),
     "gelu_sign": ("x * 0.5 * erfc(-x / sqrt(2.0))", "x * 0.5 * erfc(x / sqrt(2.0))"),
@@ -49,6 +51,25 @@ MUTANTS = {
     "up_row_is_gate_row": ("one_element(dtype, A, B, sa, sb, K, i, n + j, &u, &su);", "one_element(dtype, A, B, sa, sb, K, i, j, &u, &su);"),
     "gate_and_up_swapped": ("*y_out = ax * v;", "*y_out = oracle_act(act, v) * x;"),
     "error_scale_drops_bias": ("*e_out = L * (sg + fabs(bg));", "*e_out = L * sg;"),
+    # block-scaled FP4: decoders, packing and block indexing
+    "e2m1_bias": ("v = ldexp(1.0 + (double)frac / 2.0, expo - 1);", "v = ldexp(1.0 + (double)frac / 2.0, expo);"),
+    "e2m1_subnormal_as_normal": ("v = ldexp((double)frac / 2.0, 1 - 1);", "v = ldexp(1.0 + (double)frac / 2.0, -1);"),
+    "e2m1_sign_bit": ("int sign = (code >> 3) & 1;\n    int expo = (code >> 1) & 3;",
+                      "int sign = (code >> 2) & 1;\n    int expo = (code >> 1) & 3;"),
+    "e8m0_bias": ("return ldexp(1.0, (int)code - 127);", "return ldexp(1.0, (int)code - 128);"),
+    # (reading the high nibble first is an equivalent mutant: A and B swap the
+    # same pair of elements of one block, so no product can tell; the packing
+    # pins hold the byte index instead)
+    "mx_bytes_reversed": ("uint8_t byte = X[r * (K / 2) + k / 2];", "uint8_t byte = X[r * (K / 2) + (K / 2 - 1 - k / 2)];"),
+    "mx_drop_first_k": ("for (int64_t k = 0; k < K; ++k) {\n        double p = mx_value",
+                        "for (int64_t k = 1; k < K; ++k) {\n        double p = mx_value"),
+    "mx_drop_last_k": ("for (int64_t k = 0; k < K; ++k) {\n        double p = mx_value",
+                       "for (int64_t k = 0; k + 1 < K; ++k) {\n        double p = mx_value"),
+    "mx_blocks_of_64": ("E[r * (K / 32) + k / 32]", "E[r * (K / 32) + k / 64]"),
+    "mx_scales_dropped": ("return oracle_decode_e8m0(E[r * (K / 32) + k / 32]) * oracle_decode_e2m1(code);",
+                          "return oracle_decode_e2m1(code);"),
+    "mx_mag_signed": ("double p = mx_value(A, EA, K, i, k) * mx_value(B, EB, K, j, k);\n        acc += p;\n        mag += fabs(p);",
+                      "double p = mx_value(A, EA, K, i, k) * mx_value(B, EB, K, j, k);\n        acc += p;\n        mag += p;"),
 }
 
 
