@@ -5,7 +5,8 @@ set -- decode batches of 1/8/16 tokens, 48x4096x48, 333/528/3402-token
 prefill shapes, the 1024x50257x512 lm_head, 2048x11007x1024, 4095^2x1024 --
 with N(0,1) activations, N(0,0.02) weights and bf16 C).  Prints one JSON line.
 
-  python bench.py [--gpus N --steps K --warmup W] [--workload ragged|llama7b_mlp|square|fp8|square256]
+  python bench.py [--gpus N --steps K --warmup W]
+                  [--workload ragged|llama7b_mlp|square|fp8|mxfp4|linear|gpt3xl_train|square256]
   python bench.py --impl reference      # the fp64 CPU oracle, timed on the host cores
 
 value = 2*m*n*K summed over the step's GEMMs (valid extents only) / step time,
@@ -35,6 +36,8 @@ WORKLOAD_TEXT = {
     "llama7b_mlp": "LLaMA-2-7B MLP up/gate shapes, bf16: (597,11008,4096) prefill, decode M in {1,4,16}",
     "square": "bf16 squares M=N=K in {2048,4096,8192}, A,B~N(0,1), bf16 C",
     "fp8": "E4M3 with per-row/per-column fp32 scales, bf16 C: (4096,4096,4096) (597,11008,4096) (16,11008,4096)",
+    "mxfp4": "MXFP4 (E2M1, one E8M0 scale per 32 of K), bf16 C: (4096,4096,4096) (597,11008,4096) "
+             "(16,11008,4096)",
     "square256": "bf16 256^3, fp32 C: uniform[-1,1] and integer [-4,4] variants",
     "gpt3xl_train": "GPT-3-XL feed-forward projection, one training step, bf16 C: forward 10240x8192x2048 + bias "
                     "+ GELU; dX = dY W 10240x2048x8192 (W read MN-major); dW = dY^T X 8192x2048x10240 "
@@ -157,6 +160,9 @@ class ClockSampler:
 # ------------------------------------------------------------------ CPU oracle timing
 def oracle_band(oracle, lib, c, rows):
     """The oracle on the first `rows` rows of case c (the GEMM, or the linear layer)."""
+    if c.dtype == "mxfp4":
+        oracle.mxfp4_gemm(c.A[:rows], c.B, c.sa[:rows], c.sb, lib=lib)
+        return
     dt = oracle.BF16 if c.dtype == "bf16" else oracle.E4M3
     sa = c.sa[:rows] if c.sa is not None else None
     if c.linear:
@@ -226,7 +232,7 @@ def shape_entry(text):
     m, n, k = (int(v) for v in parts[:3])
     dtype = parts[3] if len(parts) > 3 else "bf16"
     out = parts[4] if len(parts) > 4 else "bf16"
-    return (dtype, m, n, k, out, "fp8" if dtype == "fp8" else "normal")
+    return (dtype, m, n, k, out, {"fp8": "fp8", "mxfp4": "mx"}.get(dtype, "normal"))
 
 
 def workload_text(args):
@@ -316,6 +322,10 @@ def main():
                      sb.data_ptr() if sb is not None else None, C.data_ptr(), c.m, c.n, c.K, c.m, c.n, out_dtype,
                      ctypes.byref(forced), s_handle)
             fn = lib.dgl_gemm_planned
+        elif c.dtype == "mxfp4":
+            args_ = (A.data_ptr(), B.data_ptr(), sa.data_ptr(), sb.data_ptr(), C.data_ptr(), c.m, c.n, c.K, c.m,
+                     c.n, out_dtype, s_handle)
+            fn = lib.dgl_gemm_mxfp4
         elif c.dtype == "bf16":
             args_ = (A.data_ptr(), B.data_ptr(), C.data_ptr(), c.m, c.n, c.K, c.m, c.n, out_dtype, s_handle)
             fn = lib.dgl_gemm_bf16
@@ -331,9 +341,10 @@ def main():
         return call
 
     calls = [make_call(*o) for o in ops]
-    plans = [dgl.dgl_plan_linear(0 if c.dtype == "bf16" else 1, c.m, c.n, c.K,
+    dtype_ids = {"bf16": dgl.DTYPE_BF16, "fp8": dgl.DTYPE_E4M3, "mxfp4": dgl.DTYPE_MXFP4}
+    plans = [dgl.dgl_plan_linear(dtype_ids[c.dtype], c.m, c.n, c.K,
                                  dgl.OUT_F32 if c.out == "f32" else dgl.OUT_BF16, int(c.gated)) if c.linear else
-             dgl.dgl_plan(0 if c.dtype == "bf16" else 1, c.m, c.n, c.K,
+             dgl.dgl_plan(dtype_ids[c.dtype], c.m, c.n, c.K,
                           dgl.OUT_F32 if c.out == "f32" else dgl.OUT_BF16) for c in cases]
     if forced is not None:
         plans = [forced for _ in cases]
@@ -357,8 +368,12 @@ def main():
     flops = [float(c.flops) for c in cases]
     nbytes = []
     for c in cases:
-        e = 2 if c.dtype == "bf16" else 1
         o = 4 if c.out == "f32" else 2
+        if c.dtype == "mxfp4":
+            # the GEMM guide's MXFP4 formula (section 8.2), with C at its own element size
+            nbytes.append((c.m + c.n) * c.K // 2 + c.m * c.n * o + (c.m + c.n) * (c.K // 32))
+            continue
+        e = 2 if c.dtype == "bf16" else 1
         nbytes.append(c.m * c.K * e + c.b_rows * c.K * e + c.m * c.n * o +
                       (4 * (c.m + c.b_rows) if c.dtype == "fp8" else 0) + (4 * c.b_rows if c.bias is not None else 0))
 
@@ -461,13 +476,17 @@ def main():
     dominant = max(by_kernel, key=lambda k: by_kernel[k]["ms"])
     dk = by_kernel[dominant]
     if dominant.startswith("tc_gemm"):
-        peak_tf = pk["bf16_tflops"] * (2.0 if "fp8" in dominant else 1.0)
+        # a contraction's peak: the measured bf16 figure times the nominal dense
+        # ratio of its own type (E4M3 4.5 / 2.25 PFLOP/s, FP4 13.5 / 2.25)
+        ratio, ratio_txt = (6.0, " x6 (fp4 nominal ratio)") if "mxfp4" in dominant else \
+            ((2.0, " x2 (fp8 nominal ratio)") if "fp8" in dominant else (1.0, ""))
+        peak_tf = pk["bf16_tflops"] * ratio
         achieved = dk["flops"] / (dk["ms"] * 1e-3) / 1e12
         roofline = {"kernel": dominant, "bound": "tensor", "achieved": achieved, "peak": peak_tf,
                     "unit": "TFLOP/s", "frac": achieved / peak_tf,
                     "traffic": recorded_traffic(args.workload, dominant) if args.shape is None and forced is None
                     else None,
-                    "peak_source": f"{pk_src} bf16 burst" + (" x2 (fp8 nominal ratio)" if "fp8" in dominant else ""),
+                    "peak_source": f"{pk_src} bf16 burst" + ratio_txt,
                     "launches_per_step": dk["launches"], "avg_launch_us": dk["ms"] * 1e3 / dk["launches"],
                     "algorithmic_flops_per_launch": dk["flops"] / dk["launches"]}
     else:
@@ -517,7 +536,7 @@ def main():
             if hbias is not None:
                 h2d += 4 * hbias.numel()
             if hsa is not None:
-                h2d += 4 * (hsa.numel() + hsb.numel())
+                h2d += hsa.element_size() * (hsa.numel() + hsb.numel())
             d2h += hC.numel() * hC.element_size()
 
         # Pipelined as a caller would: inputs go up on a copy stream, the GEMMs
@@ -587,7 +606,8 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K_steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16" if all(c.dtype == "bf16" for c in cases) else "e4m3",
+            "vs_baseline": None,
+            "dtype": "+".join(sorted({{"bf16": "bf16", "fp8": "e4m3", "mxfp4": "e2m1"}[c.dtype] for c in cases})),
             "data": "synthetic (seeded SplitMix64 draws; no datasets or trained weights)",
             "config": {"workload": workload_text(args), "gemms_per_step": ncall,
                        "parallelism": "replicas" if world > 1 else "single GPU",

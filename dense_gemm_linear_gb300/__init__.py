@@ -1,4 +1,4 @@
-"""GB300 (sm_103a) dense linear-layer GEMM: C = A . B^T in bf16 and E4M3.
+"""GB300 (sm_103a) dense linear-layer GEMM: C = A . B^T in bf16, E4M3 and MXFP4.
 
 Python binding of the C ABI in ``include/dgl.h``.  Functions named ``dgl_*``
 marshal plain integers/pointers into the library one to one; the ``gemm_*``
@@ -29,6 +29,7 @@ OUT_BF16 = 0
 OUT_F32 = 1
 DTYPE_BF16 = 0
 DTYPE_E4M3 = 1
+DTYPE_MXFP4 = 2
 PATH_TC = 0
 PATH_DECODE = 1
 PATH_EMPTY = 2
@@ -40,7 +41,7 @@ MN_MAJOR = 1
 
 EXPORTED = ["dgl_gemm_bf16", "dgl_gemm_fp8", "dgl_gemm_planned", "dgl_plan", "dgl_tile_metrics",
             "dgl_device_status", "dgl_status_string", "dgl_version", "dgl_gemm_noalloc", "dgl_linear",
-            "dgl_plan_linear", "dgl_gemm_bf16_ex"]
+            "dgl_plan_linear", "dgl_gemm_bf16_ex", "dgl_gemm_mxfp4"]
 
 
 class PlanInfo(ctypes.Structure):
@@ -90,6 +91,8 @@ def load_library(path: str | None = None):
     lib.dgl_gemm_bf16_ex.argtypes = [i32, i32, vp, i64, vp, i64, vp, i64, i64, i64, i64, i32,
                                      ctypes.POINTER(PlanInfo), vp]
     lib.dgl_gemm_bf16_ex.restype = i32
+    lib.dgl_gemm_mxfp4.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i32, vp]
+    lib.dgl_gemm_mxfp4.restype = i32
     lib.dgl_plan.argtypes = [i32, i64, i64, i64, i32, i32, ctypes.POINTER(PlanInfo)]
     lib.dgl_plan.restype = i32
     lib.dgl_tile_metrics.argtypes = [i64, i64, i32, i32, i32, ctypes.POINTER(PlanInfo)]
@@ -124,6 +127,11 @@ def dgl_gemm_bf16(A, B, C, M, N, K, m_valid=0, n_valid=0, out_dtype=OUT_BF16, st
 
 def dgl_gemm_fp8(A, B, sa, sb, C, M, N, K, m_valid=0, n_valid=0, out_dtype=OUT_BF16, stream=0) -> int:
     return load_library().dgl_gemm_fp8(A, B, sa, sb, C, M, N, K, m_valid, n_valid, out_dtype, stream)
+
+
+def dgl_gemm_mxfp4(A, B, sfa, sfb, C, M, N, K, m_valid=0, n_valid=0, out_dtype=OUT_BF16, stream=0) -> int:
+    """Block-scaled FP4: A [m][K/2], B [n][K/2] packed E2M1 bytes; sfa [m][K/32], sfb [n][K/32] E8M0 bytes."""
+    return load_library().dgl_gemm_mxfp4(A, B, sfa, sfb, C, M, N, K, m_valid, n_valid, out_dtype, stream)
 
 
 def dgl_gemm_planned(dtype, A, B, sa, sb, C, M, N, K, m_valid, n_valid, out_dtype, plan: PlanInfo,
@@ -249,6 +257,27 @@ def gemm_fp8(A, B, sa, sb, out=None, *, out_dtype=OUT_BF16, stream=None, plan: P
         st = dgl_gemm_planned(DTYPE_E4M3, A.data_ptr(), B.data_ptr(), sa.data_ptr(), sb.data_ptr(),
                               C.data_ptr(), rows, ldc, K, m, n, out_dtype, plan, s)
     _check(st, "dgl_gemm_fp8")
+    return C
+
+
+def gemm_mxfp4(A, B, sfa, sfb, K, out=None, *, out_dtype=OUT_BF16, stream=None):
+    """C = sum_k 2^(sfa - 127) a * 2^(sfb - 127) b over E2M1 elements (MXFP4).
+
+    A [m, K/2] and B [n, K/2] are uint8 CUDA tensors of packed E2M1 codes
+    (element 2t in the low four bits of byte t); sfa [m, K/32] and sfb
+    [n, K/32] are uint8 E8M0 scales, one per 32 elements of K.  K is passed
+    explicitly (two elements per byte).  Returns C [m, n].
+    """
+    import torch
+    m, n = A.shape[0], B.shape[0]
+    for name, t, shape in (("A", A, (m, K // 2)), ("B", B, (n, K // 2)), ("sfa", sfa, (m, K // 32)),
+                           ("sfb", sfb, (n, K // 32))):
+        if t.dtype != torch.uint8 or not t.is_cuda or tuple(t.shape) != shape or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous uint8 CUDA tensor of shape {shape}")
+    C, ldc, rows = _out_tensor(out, m, n, out_dtype, A.device)
+    st = dgl_gemm_mxfp4(A.data_ptr(), B.data_ptr(), sfa.data_ptr(), sfb.data_ptr(), C.data_ptr(), rows, ldc, K, m,
+                        n, out_dtype, _stream_handle(stream))
+    _check(st, "dgl_gemm_mxfp4")
     return C
 
 

@@ -506,6 +506,70 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream, Sta
   return e == cudaSuccess ? DGL_OK : DGL_ERR_CUDA;
 }
 
+// Block-scaled FP4 (MXFP4): A and B as byte tensors of K / 2 bytes per row
+// (TMA moves the packed E2M1 codes untouched), E8M0 scales read by the
+// kernel's scale warps, 128 x 128 tiles.
+dgl_status run_mxfp4(Problem pr, const uint8_t* sfa, const uint8_t* sfb, cudaStream_t stream) {
+  if (pr.out != DGL_OUT_BF16 && pr.out != DGL_OUT_F32) return DGL_ERR_ARG;
+  if (pr.M < 0 || pr.N < 0 || pr.K < 0 || pr.m < 0 || pr.n < 0) return DGL_ERR_ARG;
+  if (pr.m == 0) pr.m = pr.M;
+  if (pr.n == 0) pr.n = pr.N;
+  if (pr.m > pr.M || pr.n > pr.N) return DGL_ERR_ARG;
+  if (pr.M > INT32_MAX || pr.N > INT32_MAX || pr.K > INT32_MAX) return DGL_ERR_SHAPE;
+  if (pr.m == 0 || pr.n == 0) return DGL_OK;
+  if (!pr.C) return DGL_ERR_ARG;
+  if (!aligned(pr.C, pr.out == DGL_OUT_F32 ? 4 : 2)) return DGL_ERR_ALIGN;
+  if (pr.K % 32 != 0) return DGL_ERR_ALIGN;
+  if (pr.K > 0) {
+    if (!pr.A || !pr.B || !sfa || !sfb) return DGL_ERR_ARG;
+    if (!aligned(pr.A, 16) || !aligned(pr.B, 16)) return DGL_ERR_ALIGN;
+  }
+  int dev = 0;
+  DeviceState* ds = nullptr;
+  dgl_status st = get_device(&dev, &ds);
+  if (st != DGL_OK) return st;
+  if (pr.K == 0)
+    return launch_zero_fill(pr.out, pr.C, pr.N, static_cast<int>(pr.m), static_cast<int>(pr.n), stream) ==
+                   cudaSuccess
+               ? DGL_OK
+               : DGL_ERR_CUDA;
+  if (ds->smem_optin < 232448) return DGL_ERR_UNSUPPORTED;
+  dgl_plan_info plan;
+  fill_mx_plan(pr.out, pr.m, pr.n, pr.K, ds->num_sms, &plan);
+  const int64_t row_bytes = pr.K / 2;
+  CUtensorMap ta, tb, tc;
+  if (!cached_operand_map(&ta, pr.A, true, row_bytes, pr.m, 128) ||
+      !cached_operand_map(&tb, pr.B, true, row_bytes, pr.n, 128))
+    return DGL_ERR_CUDA;
+  const bool f32 = pr.out == DGL_OUT_F32;
+  const bool c_tma = aligned(pr.C, 16) && (pr.N * (f32 ? 4 : 2)) % 16 == 0;
+  std::memset(&tc, 0, sizeof(tc));
+  if (c_tma && !cached_output_map(&tc, pr.C, f32, pr.n, pr.m, pr.N)) return DGL_ERR_CUDA;
+  TcParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.C = pr.C;
+  p.ldc = pr.N;
+  p.m = static_cast<int>(pr.m);
+  p.n = static_cast<int>(pr.n);
+  p.K = static_cast<int>(pr.K);
+  p.tiles_m = static_cast<int>((pr.m + 127) / 128);
+  p.tiles_n = static_cast<int>((pr.n + 127) / 128);
+  p.num_tiles = p.tiles_m * p.tiles_n;
+  p.num_kb = static_cast<int>((row_bytes + 127) / 128);
+  p.group_m = 16;
+  p.c_tma = c_tma ? 1 : 0;
+  p.status = ds->status;
+  p.n_up = p.n;
+  const int grid = plan.grid;
+  p.workers = grid;
+  p.dp_tiles = p.num_tiles;
+  p.sfa = sfa;
+  p.sfb = sfb;
+  p.sf_vec8 = (pr.K % 256 == 0 && aligned(sfa, 8) && aligned(sfb, 8)) ? 1 : 0;
+  const bool row_staging = !c_tma && !f32;
+  return launch_tc_mxfp4(pr.out, row_staging, ta, tb, tc, p, grid, stream) == cudaSuccess ? DGL_OK : DGL_ERR_CUDA;
+}
+
 // First use on a device: look up the array's device address and clear its
 // flags (synchronous; later calls enqueue work only).
 dgl_status noalloc_setup(int dev, StaticScratch** out) {
@@ -548,6 +612,12 @@ dgl_status dgl_gemm_fp8(const void* A, const void* B, const float* sa, const flo
   return run(pr, nullptr, static_cast<cudaStream_t>(stream));
 }
 
+dgl_status dgl_gemm_mxfp4(const void* A, const void* B, const uint8_t* sfa, const uint8_t* sfb, void* C, int64_t M,
+                          int64_t N, int64_t K, int64_t m_valid, int64_t n_valid, int32_t out_dtype, void* stream) {
+  Problem pr{DGL_DTYPE_MXFP4, out_dtype, A, B, nullptr, nullptr, C, M, N, K, m_valid, n_valid};
+  return run_mxfp4(pr, sfa, sfb, static_cast<cudaStream_t>(stream));
+}
+
 dgl_status dgl_gemm_planned(int32_t dtype, const void* A, const void* B, const float* sa, const float* sb, void* C,
                             int64_t M, int64_t N, int64_t K, int64_t m_valid, int64_t n_valid, int32_t out_dtype,
                             const dgl_plan_info* plan, void* stream) {
@@ -571,7 +641,7 @@ dgl_status dgl_linear(int32_t dtype, const void* A, const void* B, const float* 
 dgl_status dgl_plan(int32_t dtype, int64_t m, int64_t n, int64_t K, int32_t out_dtype, int32_t num_sms,
                     dgl_plan_info* out) {
   if (!out) return DGL_ERR_ARG;
-  if (dtype != DGL_DTYPE_BF16 && dtype != DGL_DTYPE_E4M3) return DGL_ERR_ARG;
+  if (dtype != DGL_DTYPE_BF16 && dtype != DGL_DTYPE_E4M3 && dtype != DGL_DTYPE_MXFP4) return DGL_ERR_ARG;
   if (out_dtype != DGL_OUT_BF16 && out_dtype != DGL_OUT_F32) return DGL_ERR_ARG;
   if (m < 0 || n < 0 || K < 0) return DGL_ERR_ARG;
   if (m > INT32_MAX || n > INT32_MAX || K > INT32_MAX) return DGL_ERR_SHAPE;

@@ -13,6 +13,7 @@ enum : int {
   STATUS_TIMEOUT_DRAIN = 8,
   STATUS_TMEM_MISMATCH = 16,  // a CTA pair's tensor-memory allocations differ
   STATUS_TIMEOUT_FIXUP = 32,  // a stream-K partial tile never arrived
+  STATUS_TIMEOUT_SCALES = 64, // block-scaled kernels: a scale slot was never released
 };
 
 // Persistent tcgen05 tile kernel: problem and schedule.
@@ -53,6 +54,12 @@ struct TcParams {
   // Split tail: the last, partial wave's tiles (from dp_tiles on) run as
   // half_tiles halves of BN / 2 columns each, one per worker.
   int half_tiles;
+  // Block-scaled FP4 (MXFP4): E8M0 scales, K / 32 bytes per row of A (sfa, m
+  // rows) and of B (sfb, n rows); K counts E2M1 elements.  sf_vec8: every
+  // stage's 8 scale bytes of a row may be read as one aligned 8-byte word.
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  int sf_vec8;
 };
 
 // Decode (m <= 16) kernel parameters.  A and B are read through tensor maps.

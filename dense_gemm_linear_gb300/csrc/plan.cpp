@@ -229,10 +229,37 @@ int decode_ksteps(int rows_hi, int nk) {
   return ks < nk ? ks : (nk > 0 ? nk : 1);
 }
 
+// Block-scaled FP4: one 128 x 128 tile, one CTA per tile, a 6-stage ring of
+// 128-byte (256-element) k-stages.  The estimate charges the MMA at four times
+// the bf16 rate, or HBM, whichever is slower.
+void fill_mx_plan(int out_dtype, int64_t m, int64_t n, int64_t K, int num_sms, dgl_plan_info* out) {
+  *out = dgl_plan_info{};
+  out->path = DGL_PATH_TC;
+  out->tile_m = 128;
+  out->tile_n = 128;
+  out->tile_k = 256;
+  out->stages = 6;
+  out->cta_group = 1;
+  tile_metrics(m, n, 128, 128, num_sms, out);
+  const int64_t tiles = out->num_tiles;
+  out->grid = static_cast<int>(std::min<int64_t>(tiles, num_sms));
+  const int64_t waves = (tiles + num_sms - 1) / num_sms;
+  const double k_stages = std::ceil(static_cast<double>(K) / 256.0);
+  const double o = out_dtype == DGL_OUT_F32 ? 4.0 : 2.0;
+  const double bytes = (static_cast<double>(m) + n) * K / 2.0 + (static_cast<double>(m) + n) * K / 32.0 +
+                       static_cast<double>(m) * n * o;
+  const double tc_us = kLaunchUs + static_cast<double>(waves) * (k_stages * 0.14 + 1.0);
+  out->est_us = std::max(tc_us, bytes / (kHbmGBs * 1e3) + kLaunchUs);
+}
+
 void choose_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int num_sms, dgl_plan_info* out) {
   if (m <= 0 || n <= 0) {
     *out = dgl_plan_info{};
     out->path = DGL_PATH_EMPTY;
+    return;
+  }
+  if (dtype == DGL_DTYPE_MXFP4) {
+    fill_mx_plan(out_dtype, m, n, K, num_sms, out);
     return;
   }
   if (m <= kDecodeMaxM) {

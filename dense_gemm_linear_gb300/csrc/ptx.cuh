@@ -293,6 +293,32 @@ __device__ __forceinline__ void umma_e4m3_pair(uint32_t d_tmem, uint64_t a_desc,
       : "memory");
 }
 
+// Instruction descriptor of the block-scaled kinds (kind::mxf4 here): dense,
+// K-major A and B, fp32 accumulator, E8M0 scale factors:
+//   bits 4-5 scale-factor id of B, bits 7-9 / 10-12 A / B format (kind::mxf4:
+//   1 = E2M1), bits 17-22 N >> 3, bit 23 scale type (1 = E8M0), bits 24-28
+//   M >> 4, bits 29-30 scale-factor id of A.  The id picks the byte of each
+//   32-bit scale word where the instruction's scales start: with two 32-element
+//   blocks per K = 64 instruction (scale_vec::2X) it is 0 or 2.
+__host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N, uint32_t a_sf_id, uint32_t b_sf_id) {
+  return (b_sf_id << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
+         (static_cast<uint32_t>(M >> 4) << 24) | (a_sf_id << 29);
+}
+
+// D (+)= (A x 2^sfa) . (B x 2^sfb)^T for E2M1 operands packed two per byte,
+// K = 64 per instruction, one E8M0 scale per 32 elements of K read from tensor
+// memory at sfa_tmem / sfb_tmem.
+__device__ __forceinline__ void umma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}\n" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on the mbarrier at the same offset in every CTA of `cta_mask`
 // when the pair's MMAs issued so far by this thread have completed.
 __device__ __forceinline__ void umma_commit_pair_multicast(uint64_t* bar, uint16_t cta_mask) {
@@ -355,6 +381,16 @@ __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_
         "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
         "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
         "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+// 32 lanes x 16 consecutive 32-bit columns from registers (as tmem_st_32x32b_x32).
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
+      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
 

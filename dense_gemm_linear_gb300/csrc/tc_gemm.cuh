@@ -12,11 +12,12 @@
 //              (four K=16 bf16 or K=32 E4M3 steps per 128-byte stage) into one
 //              of two TMEM accumulators and commits each stage back to the
 //              producer's "empty" barrier.
-//   warps 2-9  epilogue, two warps per TMEM lane quarter, each taking every
-//              other 32-column chunk of its 32 rows.  A warp reads all of its
-//              chunks out of TMEM at once and releases the accumulator, then
-//              per chunk: E4M3 row/column scales ("Gemm Optimization" guide,
-//              section 7.1: acc * scale_a * scale_b), round to bf16 (or keep
+//   warps 2-9  epilogue, two warps per TMEM lane quarter, each taking half
+//              of the 32-column chunks of its 32 rows.  A warp reads its
+//              chunks out of TMEM two at a time, releases the accumulator
+//              after the last, and per chunk applies the E4M3 row/column
+//              scales ("Gemm Optimization" guide, section 7.1:
+//              acc * scale_a * scale_b), rounds to bf16 (or keeps
 //              fp32), vector stores into a swizzled staging tile, and
 //                - a TMA tensor store of the 32 x 32 tile when C's row pitch
 //                  is 16-byte aligned (clipped at m and n by the tensor map:
@@ -51,7 +52,7 @@ constexpr int tc_ring_stages(int stage_bytes, int staging_bytes) {
   return s < 8 ? s : 8;
 }
 
-template <int BN_, bool FP8_, bool OUT_F32_, bool ROWSTG_, int CG_ = 1, bool EPI_ = false>
+template <int BN_, bool FP8_, bool OUT_F32_, bool ROWSTG_, int CG_ = 1, bool EPI_ = false, bool MX_ = false>
 struct TcConfig {
   static constexpr int CG = CG_;                        // CTAs per MMA: 1, or 2 for a CTA pair (M = 256)
   // EPI: the linear-layer epilogue (bias, activation, and on CTA pairs the
@@ -62,6 +63,11 @@ struct TcConfig {
   static constexpr int BN = BN_;                        // columns of C per tile
   static constexpr int B_ROWS = BN / CG;                // rows of B each CTA loads per stage
   static constexpr bool FP8 = FP8_;
+  // MX: block-scaled FP4 (MXFP4).  A and B hold E2M1 codes two to a byte; each
+  // 32 elements of K of a row share one E8M0 scale.  kind::mxf4 MMAs read the
+  // scales from tensor memory, where four more warps place each stage's scales
+  // (a ring of 16-column slots after the accumulators).  128 x 128 tiles, one CTA.
+  static constexpr bool MX = MX_;
   static constexpr bool OUT_F32 = OUT_F32_;
   // ROWSTG: bf16 C whose rows are not 16-byte aligned.  The epilogue stages
   // whole tile rows, shifted by each row's misalignment, so the aligned body
@@ -70,8 +76,8 @@ struct TcConfig {
   static_assert(!(ROWSTG && OUT_F32), "row staging is the bf16-output path");
   static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair");
   static constexpr int ROW_BYTES = 128;                 // one 128-byte swizzle span of K per stage
-  static constexpr int BK = FP8 ? 128 : 64;             // K elements per stage
-  static constexpr int MMA_K_BYTES = 32;                // K=16 bf16 or K=32 E4M3 per instruction
+  static constexpr int BK = FP8 || MX ? 128 : 64;       // tensor-map elements (K) per stage: 128 bytes
+  static constexpr int MMA_K_BYTES = 32;                // K=16 bf16, K=32 E4M3 or K=64 E2M1 per instruction
   static constexpr int MMAS_PER_STAGE = ROW_BYTES / MMA_K_BYTES;
   static constexpr int A_STAGE_BYTES = BM * ROW_BYTES;
   static constexpr int B_STAGE_BYTES = B_ROWS * ROW_BYTES;
@@ -87,9 +93,15 @@ struct TcConfig {
   static constexpr int ROW_PITCH = BN * 2 + 16;
   static constexpr int STG_TOTAL = ROWSTG ? 4 * 32 * ROW_PITCH : EPI_WARPS * 4096;
   static constexpr int STAGES = tc_ring_stages(STAGE_BYTES, STG_TOTAL);
-  static constexpr int THREADS = 64 + EPI_WARPS * 32;
-  static constexpr int TMEM_COLS = 2 * BN;              // two fp32 accumulators of BN columns
-  static constexpr int BAR_BYTES = 8 * (2 * STAGES + 6) + 8 + 32;
+  static constexpr int SCALE_WARPS = MX ? 4 : 0;
+  static constexpr int THREADS = 64 + EPI_WARPS * 32 + SCALE_WARPS * 32;
+  // two fp32 accumulators of BN columns (MX: and the scale ring after them)
+  static constexpr int TMEM_COLS = MX ? 512 : 2 * BN;
+  // MX scale ring: slot s holds stage s's scales in columns
+  // SCALE_COL0 + 16 s .. + 15 (A's k-blocks 0-3, 4-7, then B's)
+  static constexpr int SCALE_COL0 = 2 * BN;
+  static constexpr int SCALE_SLOT_COLS = 16;
+  static constexpr int BAR_BYTES = 8 * (3 * STAGES + 6) + 8 + 32;
   // stream-K: one CTA's fp32 partial tile, and how many fit in the ring
   static constexpr int SLOT_BYTES = BM * BN * 4;
   static constexpr int RING_SLOTS = STAGES * STAGE_BYTES / SLOT_BYTES;
@@ -102,6 +114,8 @@ struct TcConfig {
   static_assert((ROW_PITCH / 16) % 2 == 1, "row pitch: odd multiple of 16 bytes");
   static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation: power of two");
   static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
+  static_assert(!MX || (BN == 128 && CG == 1 && !FP8 && !EPI), "block-scaled FP4: 128 x 128 tiles, one CTA");
+  static_assert(!MX || SCALE_COL0 + STAGES * SCALE_SLOT_COLS <= TMEM_COLS, "scale ring fits in tensor memory");
   static_assert(B_STAGE_BYTES % 1024 == 0, "B stage tiles stay 1024-byte aligned");
   static_assert(RING_SLOTS >= 1, "a partial tile fits in the ring");
   static_assert(FX_WARP_BYTES >= 2048 && FX_WARP_BYTES % 16 == 0, "fix-up staging piece");
@@ -167,6 +181,53 @@ __device__ __forceinline__ void load_operand_pair(uint8_t* dst, const CUtensorMa
     tma_load_2d_pair(dst + i * MN_BOX_BYTES, map, leader_bar, row0 + 64 * i, k0, pol);
 }
 
+// The worker's k-stages in schedule order, one (tile row, tile column,
+// k-stage) at a time: the segments of SegmentIter, flattened.
+struct StageIter {
+  SegmentIter it;
+  Segment sg;
+  int kb = 0, kb1 = 0, mb = 0, nb = 0;
+  int tiles_m, tiles_n, group_m;
+  __device__ StageIter(int worker, const TcParams& prm)
+      : it(worker, prm.workers, prm.num_kb, prm.dp_tiles, prm.sk_units, prm.half_tiles), tiles_m(prm.tiles_m),
+        tiles_n(prm.tiles_n), group_m(prm.group_m) {}
+  __device__ bool next(int& mb_out, int& nb_out, int& kb_out) {
+    while (kb >= kb1) {
+      if (!it.next(sg)) return false;
+      tile_coords(sg.tile, tiles_m, tiles_n, group_m, mb, nb);
+      kb = sg.kb0;
+      kb1 = sg.kb1;
+    }
+    mb_out = mb;
+    nb_out = nb;
+    kb_out = kb++;
+    return true;
+  }
+};
+
+// The 8 E8M0 scale bytes of k-blocks 8 kb .. 8 kb + 7 of row r, as two
+// little-endian words (k-blocks 8 kb .. + 3, then + 4 .. + 7).  Rows past
+// `rows` and k-blocks past `nkblk` read as 127 (a scale of 1): their operand
+// elements are the tensor maps' zero fill.
+__device__ __forceinline__ void scale_words(const uint8_t* sf, int rows, int r, int kb, int nkblk, int vec8,
+                                            uint32_t& lo, uint32_t& hi) {
+  lo = hi = 0x7F7F7F7Fu;
+  if (r >= rows) return;
+  const uint8_t* row = sf + static_cast<int64_t>(r) * nkblk;
+  const int k0 = kb * 8;
+  if (vec8) {
+    const uint2 v = *reinterpret_cast<const uint2*>(row + k0);
+    lo = v.x;
+    hi = v.y;
+    return;
+  }
+  uint32_t b[8];
+#pragma unroll
+  for (int t = 0; t < 8; ++t) b[t] = k0 + t < nkblk ? row[k0 + t] : 0x7Fu;
+  lo = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
+  hi = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+}
+
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -184,7 +245,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint64_t* fixbar = drain + 1;                          // stream-K: partial tiles landed in the ring
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fixbar + 1);
+  uint64_t* sfull = fixbar + 1;                          // MX: a stage's scales are in tensor memory
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sfull + STAGES);
   volatile int* qflag = reinterpret_cast<volatile int*>(tmem_slot + 1);  // 8 epilogue-warp flags
 
   const int warp = threadIdx.x >> 5;
@@ -206,6 +268,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     }
     mbar_init(drain, 1);
     mbar_init(fixbar, 1);
+    if constexpr (Cfg::MX)
+      for (int s = 0; s < STAGES; ++s) mbar_init(&sfull[s], Cfg::SCALE_WARPS);
     fence_mbarrier_init();
     fence_proxy_async_shared();
   }
@@ -331,7 +395,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         const uint32_t d_tmem = tmem_base + acc * BN;
         const uint32_t idesc = sg.half ? idesc_half : idesc_full;  // a half tile: N = BN / 2
         for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
-          const bool ok2 = mbar_wait(&full[stage], phase);
+          // MX: the stage's scales must be in tensor memory too
+          const bool ok2 = mbar_wait(&full[stage], phase) && (!Cfg::MX || mbar_wait(&sfull[stage], phase));
           if (!ok2) {
             fail = STATUS_TIMEOUT_MMA;
             break;
@@ -352,10 +417,17 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
               else
                 umma_bf16_pair(d_tmem, ad, bd, idesc, accumulate);
             } else {
-              if constexpr (Cfg::FP8)
+              if constexpr (Cfg::MX) {
+                // instruction k covers k-blocks 2k, 2k + 1: word k / 2 of the
+                // slot's A and B columns, starting at byte 2 (k % 2)
+                const uint32_t id = static_cast<uint32_t>(k & 1) * 2u;
+                const uint32_t sf = tmem_base + Cfg::SCALE_COL0 + stage * Cfg::SCALE_SLOT_COLS + 4 * (k >> 1);
+                umma_mxf4(d_tmem, ad, bd, idesc_mxf4(Cfg::TILE_M, BN, id, id), sf, sf + 8, accumulate);
+              } else if constexpr (Cfg::FP8) {
                 umma_e4m3(d_tmem, ad, bd, idesc, accumulate);
-              else
+              } else {
                 umma_bf16(d_tmem, ad, bd, idesc, accumulate);
+              }
             }
           }
           issued_any = true;
@@ -385,7 +457,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         if (!mbar_wait(drain, 0)) fail |= STATUS_TIMEOUT_DRAIN;
       }
     }
-  } else {
+  } else if (warp < 2 + Cfg::EPI_WARPS) {
     // ------------------------------------------------------------ epilogue
     const int e = warp - 2;                 // 0..7
     const int q = warp & 3;                 // TMEM lanes 32q .. 32q+31 are reachable from this warp
@@ -802,6 +874,67 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       if (acc == 0) acc_phase ^= 1;
     }
     if ((Cfg::ROWSTG ? half == 0 : (p.c_tma && lane == 0))) bulk_wait0();
+  }
+
+  if constexpr (Cfg::MX) {
+    if (warp >= 2 + Cfg::EPI_WARPS) {
+      // ---------------------------------------------------------- scale warps (MX)
+      // Stage s's E8M0 scales go to tensor-memory slot s once the MMAs that
+      // read the slot's previous contents are done (the stage's "empty"
+      // barrier).  Slot layout, every lane quarter alike (the layout a
+      // 32-lane, 128-bit copy replicated to the four quarters produces):
+      // lane 32 q + l, column 4 w + j holds, for row 32 j + l of the tile, the
+      // four scale bytes of k-blocks 4 w' .. 4 w' + 3 of the stage, where w = 0,
+      // 1 are A's two words (w' = w) and w = 2, 3 are B's (w' = w - 2).
+      const int q = warp & 3;
+      const int nkblk = p.K / 32;
+      // Loads run SD stages ahead of the tensor-memory stores (a register
+      // queue, unrolled so every index is static), which hides their latency.
+      constexpr int SD = 4;
+      StageIter ahead(cluster_id, p), cur(cluster_id, p);
+      uint32_t w[SD][16];
+      auto gather = [&](uint32_t(&x)[16], int mb, int nb, int kb) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          scale_words(p.sfa, p.m, mb * BM + 32 * j + lane, kb, nkblk, p.sf_vec8, x[j], x[4 + j]);
+          scale_words(p.sfb, p.n, nb * BN + 32 * j + lane, kb, nkblk, p.sf_vec8, x[8 + j], x[12 + j]);
+        }
+      };
+      int mb, nb, kb;
+#pragma unroll
+      for (int d = 0; d < SD; ++d)
+        if (ahead.next(mb, nb, kb)) gather(w[d], mb, nb, kb);
+      uint32_t stage = 0, phase = 0;
+      bool more = true;
+      while (more && !fail) {
+#pragma unroll
+        for (int d = 0; d < SD; ++d) {
+          if (!more || fail) break;
+          if (!cur.next(mb, nb, kb)) {
+            more = false;
+            break;
+          }
+          const bool ok = __all_sync(0xffffffffu, mbar_wait(&empty[stage], phase ^ 1));
+          if (!ok) {
+            fail = STATUS_TIMEOUT_SCALES;
+            break;
+          }
+          tc_fence_after_sync();
+          tmem_st_32x32b_x16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + Cfg::SCALE_COL0 +
+                                 stage * Cfg::SCALE_SLOT_COLS,
+                             w[d]);
+          tmem_st_wait();
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sfull[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+          if (ahead.next(mb, nb, kb)) gather(w[d], mb, nb, kb);
+        }
+      }
+    }
   }
 
   if (fail) atomicOr(p.status, fail);

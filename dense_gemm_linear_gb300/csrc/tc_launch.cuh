@@ -10,10 +10,10 @@
 
 namespace dgl {
 
-template <int BN, bool FP8, bool OUT_F32, bool ROWSTG, int CG, bool EPI>
+template <int BN, bool FP8, bool OUT_F32, bool ROWSTG, int CG, bool EPI, bool MX = false>
 cudaError_t tc_launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tbh, const CUtensorMap& tc,
                           const TcParams& p, int grid, cudaStream_t stream) {
-  using Cfg = TcConfig<BN, FP8, OUT_F32, ROWSTG, CG, EPI>;
+  using Cfg = TcConfig<BN, FP8, OUT_F32, ROWSTG, CG, EPI, MX>;
   auto kern = tc_gemm_kernel<Cfg>;
   static std::atomic<uint64_t> attr_done{0};  // one bit per device
   cudaError_t e = set_smem_attr_once(kern, Cfg::SMEM_BYTES, attr_done);

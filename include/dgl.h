@@ -67,7 +67,7 @@ typedef enum {
 } dgl_status;
 
 typedef enum { DGL_OUT_BF16 = 0, DGL_OUT_F32 = 1 } dgl_out_t;
-typedef enum { DGL_DTYPE_BF16 = 0, DGL_DTYPE_E4M3 = 1 } dgl_dtype_t;
+typedef enum { DGL_DTYPE_BF16 = 0, DGL_DTYPE_E4M3 = 1, DGL_DTYPE_MXFP4 = 2 } dgl_dtype_t;
 typedef enum { DGL_PATH_TC = 0, DGL_PATH_DECODE = 1, DGL_PATH_EMPTY = 2 } dgl_path_t;
 /* Activations of dgl_linear: GELU(x) = x * Phi(x) (Phi the standard normal
  * distribution function, the exact erf form); SiLU(x) = x * sigma(x) (sigma
@@ -138,6 +138,32 @@ dgl_status dgl_gemm_fp8(const void* A, const void* B, const float* sa, const flo
 dgl_status dgl_gemm_planned(int32_t dtype, const void* A, const void* B, const float* sa, const float* sb,
                             void* C, int64_t M, int64_t N, int64_t K, int64_t m_valid, int64_t n_valid,
                             int32_t out_dtype, const dgl_plan_info* plan, void* stream);
+
+/*
+ * Block-scaled FP4 GEMM (MXFP4).  The "Gemm Optimization" guide's bandwidth
+ * formulas (section 8.2, "FP4 (MXFP4)") count half a byte per element of A
+ * and of B and one scale byte per 32 elements of K for every row of each;
+ * the format read into that name is OCP Microscaling MXFP4: E2M1 elements and
+ * one E8M0 scale (2^(e - 127); 0xFF is NaN) per block of 32 consecutive
+ * elements of a row along K.
+ *   C[i, j] = sum_k 2^(sfa[i][k/32] - 127) a(i, k) * 2^(sfb[j][k/32] - 127) b(j, k)
+ * accumulated in fp32 on the tensor cores (tcgen05 kind::mxf4), then
+ * rounded to bf16 (nearest even) or kept in fp32.
+ * A: m_valid rows of K / 2 bytes, B: n_valid rows of K / 2 bytes; element 2t
+ * of a row in the low four bits of byte t.  sfa: m_valid rows of K / 32
+ * bytes, sfb: n_valid rows of K / 32 bytes (unaligned is fine).
+ * C, M, N, m_valid, n_valid, out_dtype and the never-written region outside
+ * [0, m_valid) x [0, n_valid) as dgl_gemm_bf16.  K: a multiple of 32 (whole
+ * blocks; the K / 2-byte rows are then whole 16-byte units).  A, B 16-byte
+ * aligned.  Errors: DGL_ERR_ARG (null pointers, extents), DGL_ERR_ALIGN
+ * (K not a multiple of 32, A or B not 16-byte aligned, C not aligned to
+ * its element), DGL_ERR_SHAPE (extents past int32).  Every problem, small
+ * m included, runs on 128 x 128 tiles (the decode path is bf16 / E4M3 only).
+ * Results whose block-scale products leave fp32's range are not specified;
+ * the parity tests keep scales within 2^-20 .. 2^20.
+ */
+dgl_status dgl_gemm_mxfp4(const void* A, const void* B, const uint8_t* sfa, const uint8_t* sfb, void* C, int64_t M,
+                          int64_t N, int64_t K, int64_t m_valid, int64_t n_valid, int32_t out_dtype, void* stream);
 
 /*
  * Size in bytes of the fixed device array that dgl_gemm_noalloc uses for its
@@ -231,6 +257,7 @@ dgl_status dgl_linear(int32_t dtype, const void* A, const void* B, const float* 
  * screened by padded output area (rejecting a tile whose padded area exceeds
  * 1.25x the real one unless none passes, as in FlyDSL pull request 1303's
  * autotuner) and the survivor with the lowest cost-model time is chosen.
+ * dtype DGL_DTYPE_MXFP4 has one tile: 128 x 128 (tile_k 256 elements).
  */
 dgl_status dgl_plan(int32_t dtype, int64_t m, int64_t n, int64_t K, int32_t out_dtype, int32_t num_sms,
                     dgl_plan_info* out);

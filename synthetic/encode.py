@@ -40,12 +40,10 @@ def to_e2m1_codes(x) -> np.ndarray:
     """float array -> uint8 E2M1 codes (0..15), nearest, ties to even, saturating."""
     x = np.asarray(x, dtype=np.float64)
     a = np.minimum(np.abs(x), 6.0)
-    dist = np.abs(a[..., None] - E2M1_MAGNITUDES)
-    best = dist.min(axis=-1, keepdims=True)
-    # among the nearest magnitudes take the even code (fraction bit 0)
-    tie_ok = (dist == best) & ((np.arange(8) & 1) == 0)
-    near = dist == best
-    code = np.where(tie_ok.any(axis=-1), tie_ok.argmax(axis=-1), near.argmax(axis=-1)).astype(np.uint8)
+    mid = (E2M1_MAGNITUDES[1:] + E2M1_MAGNITUDES[:-1]) / 2      # 0.25, 0.75, ..., 5
+    code = np.searchsorted(mid, a, side="left")                    # midpoints strictly below a
+    tie = (code < mid.size) & (a == mid[np.minimum(code, mid.size - 1)])
+    code = np.where(tie & (code % 2 == 1), code + 1, code).astype(np.uint8)  # a tie goes to the even code
     sign = (np.signbit(x) & (code != 0)).astype(np.uint8) << 3
     return code | sign
 
@@ -56,15 +54,18 @@ def pack_e2m1(codes) -> np.ndarray:
     return (codes[..., 0::2] | (codes[..., 1::2] << 4)).astype(np.uint8)
 
 
-def mx_quantize(x, block: int = 32):
+def mx_quantize(x, block: int = 32, rows_per_chunk: int = 512):
     """[rows, K] floats -> (packed E2M1 codes [rows, K / 2], E8M0 scale codes [rows, K / block])."""
-    x = np.asarray(x, dtype=np.float64)
+    x = np.asarray(x)
     rows, K = x.shape
-    blocks = x.reshape(rows, K // block, block)
-    amax = np.abs(blocks).max(axis=-1)
-    with np.errstate(divide="ignore"):
+    packed = np.empty((rows, K // 2), dtype=np.uint8)
+    scales = np.empty((rows, K // block), dtype=np.uint8)
+    for r0 in range(0, rows, rows_per_chunk):
+        blocks = x[r0:r0 + rows_per_chunk].astype(np.float64).reshape(-1, K // block, block)
+        amax = np.abs(blocks).max(axis=-1)
         X = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 2, -127)
-    X = np.clip(X, -127, 127)
-    scaled = blocks / np.exp2(X)[..., None]
-    codes = to_e2m1_codes(scaled).reshape(rows, K)
-    return pack_e2m1(codes), (X + 127).astype(np.uint8)
+        X = np.clip(X, -127, 127)
+        codes = to_e2m1_codes(blocks / np.exp2(X)[..., None]).reshape(-1, K)
+        packed[r0:r0 + rows_per_chunk] = pack_e2m1(codes)
+        scales[r0:r0 + rows_per_chunk] = (X + 127).astype(np.uint8)
+    return packed, scales

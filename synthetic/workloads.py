@@ -162,6 +162,11 @@ WORKLOADS = {
     "gpt3xl_train": [("bf16", 10240, 8192, 2048, "bf16", "normal", {"act": "gelu", "bias": True}),
                      ("bf16", 10240, 2048, 8192, "bf16", "normal", {"layout": ("k", "mn")}),
                      ("bf16", 8192, 2048, 10240, "bf16", "normal", {"layout": ("mn", "mn")})],
+    # block-scaled FP4 (MXFP4; the GEMM guide's section 8.2 byte formula):
+    # the square and the LLaMA-2 7B up/gate prefill and decode shapes, OCP MX
+    # quantised N(0,1) activations and N(0, 0.02^2) weights
+    "mxfp4": [("mxfp4", 4096, 4096, 4096, "bf16", "mx"), ("mxfp4", 597, 11008, 4096, "bf16", "mx"),
+              ("mxfp4", 16, 11008, 4096, "bf16", "mx")],
     "linear": [("bf16", 10240, 8192, 2048, "bf16", "normal", {"act": "gelu", "bias": True}),
                ("bf16", 597, 11008, 4096, "bf16", "normal", {"act": "silu", "gated": True}),
                ("fp8", 597, 11008, 4096, "bf16", "fp8", {"act": "silu", "gated": True})],

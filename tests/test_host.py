@@ -140,11 +140,11 @@ def test_plan_split_tail_rule(dgl):
         p = dgl.dgl_plan(dt, m, n, k, num_sms=152)
         return (p.tile_m, p.tile_n, p.num_tiles, p.split_tail)
 
-    # 256 tiles = 3 waves of 76 + 28: short K splits in both dtypes, long K does not
-    assert plan(0, 4095, 4095, 1024) == (256, 256, 256, 1)
-    assert plan(1, 4095, 4095, 2048) == (256, 256, 256, 1)
-    assert plan(0, 4095, 4095, 2048)[3] == 0
-    assert plan(0, 4096, 4096, 4096)[3] == 0
+    # 336 tiles = 4 waves of 76 + 32: short K splits in both dtypes, long K does not
+    assert plan(0, 2048, 10752, 1024) == (256, 256, 336, 1)
+    assert plan(1, 2048, 10752, 2048) == (256, 256, 336, 1)
+    assert plan(0, 2048, 10752, 2048) == (256, 256, 336, 0)
+    assert plan(0, 2048, 10752, 4096) == (256, 256, 336, 0)
     # 344 tiles = 4 waves + 40: more than half the workers, no split
     assert plan(0, 2048, 11007, 1024) == (256, 256, 344, 0)
     # no full wave before the tail
