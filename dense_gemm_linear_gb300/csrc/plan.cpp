@@ -229,7 +229,7 @@ int decode_ksteps(int rows_hi, int nk) {
   return ks < nk ? ks : (nk > 0 ? nk : 1);
 }
 
-// Block-scaled FP4: one 128 x 128 tile, one CTA per tile, a 6-stage ring of
+// Block-scaled FP4: one 128 x 128 tile, one CTA per tile, a 5-stage ring of
 // 128-byte (256-element) k-stages.  The estimate charges the MMA at four times
 // the bf16 rate, or HBM, whichever is slower.
 void fill_mx_plan(int out_dtype, int64_t m, int64_t n, int64_t K, int num_sms, dgl_plan_info* out) {
@@ -238,7 +238,7 @@ void fill_mx_plan(int out_dtype, int64_t m, int64_t n, int64_t K, int num_sms, d
   out->tile_m = 128;
   out->tile_n = 128;
   out->tile_k = 256;
-  out->stages = 6;
+  out->stages = 5;
   out->cta_group = 1;
   tile_metrics(m, n, 128, 128, num_sms, out);
   const int64_t tiles = out->num_tiles;

@@ -305,6 +305,40 @@ __host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N, uint32_t a_sf_id
          (static_cast<uint32_t>(M >> 4) << 24) | (a_sf_id << 29);
 }
 
+// Shared-memory descriptor of a matrix without swizzle, as 8-row x 16-byte
+// core matrices stored contiguously (128 bytes each) one after another along
+// the rows: a 32-row x 16-byte matrix at saddr, row r at saddr + 16 r.  Both
+// core-matrix strides are 128 bytes (only the row direction has more than one).
+__device__ __forceinline__ uint64_t smem_desc_rows16(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFF);
+  d |= static_cast<uint64_t>(128 >> 4) << 16;
+  d |= static_cast<uint64_t>(128 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+
+// Copy a 32-row x 128-bit matrix from shared memory into tensor memory at
+// taddr (4 consecutive 32-bit columns), once into each of the four 32-lane
+// quarters: lane 32 w + r, column c + j receives bytes 4 j .. 4 j + 3 of row r.
+// Issued by one thread; executes in order with the MMAs the thread issues
+// after it.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Two 32-bit words from global memory at p (8-byte aligned) when pred is
+// set, else lo and hi keep their values; the load does not stall the thread
+// until lo or hi is read.
+__device__ __forceinline__ void ldg_pred_v2(const void* p, bool pred, uint32_t& lo, uint32_t& hi) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\t"
+      "setp.ne.b32 q, %3, 0;\n\t"
+      "@q ld.global.nc.v2.u32 {%0, %1}, [%2];\n\t}\n"
+      : "+r"(lo), "+r"(hi)
+      : "l"(p), "r"(static_cast<int>(pred)));
+}
+
 // D (+)= (A x 2^sfa) . (B x 2^sfb)^T for E2M1 operands packed two per byte,
 // K = 64 per instruction, one E8M0 scale per 32 elements of K read from tensor
 // memory at sfa_tmem / sfb_tmem.

@@ -65,8 +65,9 @@ struct TcConfig {
   static constexpr bool FP8 = FP8_;
   // MX: block-scaled FP4 (MXFP4).  A and B hold E2M1 codes two to a byte; each
   // 32 elements of K of a row share one E8M0 scale.  kind::mxf4 MMAs read the
-  // scales from tensor memory, where four more warps place each stage's scales
-  // (a ring of 16-column slots after the accumulators).  128 x 128 tiles, one CTA.
+  // scales from tensor memory.  Four more warps gather each stage's scales into
+  // shared memory, and the MMA thread copies them into a ring of 16-column
+  // tensor-memory slots after the accumulators.  128 x 128 tiles, one CTA.
   static constexpr bool MX = MX_;
   static constexpr bool OUT_F32 = OUT_F32_;
   // ROWSTG: bf16 C whose rows are not 16-byte aligned.  The epilogue stages
@@ -92,7 +93,9 @@ struct TcConfig {
   // multiple of 16 bytes so rows spread over the banks
   static constexpr int ROW_PITCH = BN * 2 + 16;
   static constexpr int STG_TOTAL = ROWSTG ? 4 * 32 * ROW_PITCH : EPI_WARPS * 4096;
-  static constexpr int STAGES = tc_ring_stages(STAGE_BYTES, STG_TOTAL);
+  // MX: per stage, 1 KB of A's scales and 1 KB of B's (two 512-byte atoms each)
+  static constexpr int SCALE_STAGE_BYTES = MX ? 2048 : 0;
+  static constexpr int STAGES = tc_ring_stages(STAGE_BYTES + SCALE_STAGE_BYTES, STG_TOTAL);
   static constexpr int SCALE_WARPS = MX ? 4 : 0;
   static constexpr int THREADS = 64 + EPI_WARPS * 32 + SCALE_WARPS * 32;
   // two fp32 accumulators of BN columns (MX: and the scale ring after them)
@@ -108,7 +111,8 @@ struct TcConfig {
   // fix-up staging per epilogue warp: 2 KB pieces, two of them when room allows
   static constexpr int FX_WARP_BYTES = ROWSTG ? 16 * ROW_PITCH : 4096;
   static constexpr int FX_BUFS = FX_WARP_BYTES >= 4096 ? 2 : 1;
-  static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + STAGES * STAGE_BYTES + STG_TOTAL + BAR_BYTES;
+  static constexpr int SMEM_BYTES =
+      1024 /* alignment slack */ + STAGES * (STAGE_BYTES + SCALE_STAGE_BYTES) + STG_TOTAL + BAR_BYTES;
   static_assert(BN == 64 || BN == 128 || BN == 256, "tile widths of the ladder");
   static_assert(STAGES >= 3, "ring too shallow");
   static_assert((ROW_PITCH / 16) % 2 == 1, "row pitch: odd multiple of 16 bytes");
@@ -212,15 +216,14 @@ struct StageIter {
 __device__ __forceinline__ void scale_words(const uint8_t* sf, int rows, int r, int kb, int nkblk, int vec8,
                                             uint32_t& lo, uint32_t& hi) {
   lo = hi = 0x7F7F7F7Fu;
-  if (r >= rows) return;
-  const uint8_t* row = sf + static_cast<int64_t>(r) * nkblk;
   const int k0 = kb * 8;
   if (vec8) {
-    const uint2 v = *reinterpret_cast<const uint2*>(row + k0);
-    lo = v.x;
-    hi = v.y;
+    // one predicated 8-byte load: the thread does not wait for it here
+    ldg_pred_v2(sf + static_cast<int64_t>(r < rows ? r : 0) * nkblk + k0, r < rows, lo, hi);
     return;
   }
+  if (r >= rows) return;
+  const uint8_t* row = sf + static_cast<int64_t>(r) * nkblk;
   uint32_t b[8];
 #pragma unroll
   for (int t = 0; t < 8; ++t) b[t] = k0 + t < nkblk ? row[k0 + t] : 0x7Fu;
@@ -238,14 +241,15 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = sA + STAGES * Cfg::A_STAGE_BYTES;
-  uint8_t* sStg = sB + STAGES * Cfg::B_STAGE_BYTES;      // 1024-aligned: stage sizes are multiples of 1 KB
+  uint8_t* sSc = sB + STAGES * Cfg::B_STAGE_BYTES;       // MX scale slots (none otherwise)
+  uint8_t* sStg = sSc + STAGES * Cfg::SCALE_STAGE_BYTES; // 1024-aligned: stage sizes are multiples of 1 KB
   uint64_t* full = reinterpret_cast<uint64_t*>(sStg + Cfg::STG_TOTAL);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint64_t* fixbar = drain + 1;                          // stream-K: partial tiles landed in the ring
-  uint64_t* sfull = fixbar + 1;                          // MX: a stage's scales are in tensor memory
+  uint64_t* sfull = fixbar + 1;                          // MX: a stage's scales are in shared memory
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sfull + STAGES);
   volatile int* qflag = reinterpret_cast<volatile int*>(tmem_slot + 1);  // 8 epilogue-warp flags
 
@@ -395,13 +399,21 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         const uint32_t d_tmem = tmem_base + acc * BN;
         const uint32_t idesc = sg.half ? idesc_half : idesc_full;  // a half tile: N = BN / 2
         for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
-          // MX: the stage's scales must be in tensor memory too
+          // MX: the stage's scales must be in shared memory too
           const bool ok2 = mbar_wait(&full[stage], phase) && (!Cfg::MX || mbar_wait(&sfull[stage], phase));
           if (!ok2) {
             fail = STATUS_TIMEOUT_MMA;
             break;
           }
           tc_fence_after_sync();
+          if constexpr (Cfg::MX) {
+            // the stage's four 512-byte scale atoms (A's k-blocks 0-3, 4-7,
+            // then B's) into its tensor-memory slot; the MMAs below run after
+            const uint32_t sc = smem_u32(sSc + stage * Cfg::SCALE_STAGE_BYTES);
+            const uint32_t tcol = tmem_base + Cfg::SCALE_COL0 + stage * Cfg::SCALE_SLOT_COLS;
+#pragma unroll
+            for (int a = 0; a < 4; ++a) tmem_cp_32x128b_warpx4(tcol + 4 * a, smem_desc_rows16(sc + 512 * a));
+          }
           const uint32_t a_addr = smem_u32(sA + stage * Cfg::A_STAGE_BYTES);
           const uint32_t b_addr = smem_u32(sB + stage * Cfg::B_STAGE_BYTES);
 #pragma unroll
@@ -879,26 +891,26 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   if constexpr (Cfg::MX) {
     if (warp >= 2 + Cfg::EPI_WARPS) {
       // ---------------------------------------------------------- scale warps (MX)
-      // Stage s's E8M0 scales go to tensor-memory slot s once the MMAs that
-      // read the slot's previous contents are done (the stage's "empty"
-      // barrier).  Slot layout, every lane quarter alike (the layout a
-      // 32-lane, 128-bit copy replicated to the four quarters produces):
-      // lane 32 q + l, column 4 w + j holds, for row 32 j + l of the tile, the
-      // four scale bytes of k-blocks 4 w' .. 4 w' + 3 of the stage, where w = 0,
-      // 1 are A's two words (w' = w) and w = 2, 3 are B's (w' = w - 2).
+      // Stage s's E8M0 scales go to shared-memory slot s once the MMAs (and
+      // the copy) that read the slot's previous contents are done: the
+      // stage's "empty" barrier.  A slot holds four 512-byte atoms (A's
+      // k-blocks 0-3 and 4-7 of the stage, then B's).  Row 32 j + l of the
+      // tile has its four scale bytes at atom offset 16 l + 4 j, which is the
+      // layout the MMA thread's 32-lane, 128-bit copy replicated to the four
+      // lane quarters turns into the one kind::mxf4 reads: lane 32 w + l,
+      // column 4 a + j holds row 32 j + l's word of atom a.  Warp q handles
+      // rows 32 q .. 32 q + 31 of A and of B.
       const int q = warp & 3;
       const int nkblk = p.K / 32;
-      // Loads run SD stages ahead of the tensor-memory stores (a register
-      // queue, unrolled so every index is static), which hides their latency.
+      // Loads run SD stages ahead of the shared-memory stores (a register
+      // queue, unrolled so every index is static); they are predicated rather
+      // than selected afterwards, so nothing waits for them before the store.
       constexpr int SD = 4;
       StageIter ahead(cluster_id, p), cur(cluster_id, p);
-      uint32_t w[SD][16];
-      auto gather = [&](uint32_t(&x)[16], int mb, int nb, int kb) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          scale_words(p.sfa, p.m, mb * BM + 32 * j + lane, kb, nkblk, p.sf_vec8, x[j], x[4 + j]);
-          scale_words(p.sfb, p.n, nb * BN + 32 * j + lane, kb, nkblk, p.sf_vec8, x[8 + j], x[12 + j]);
-        }
+      uint32_t w[SD][4];
+      auto gather = [&](uint32_t(&x)[4], int mb, int nb, int kb) {
+        scale_words(p.sfa, p.m, mb * BM + 32 * q + lane, kb, nkblk, p.sf_vec8, x[0], x[1]);
+        scale_words(p.sfb, p.n, nb * BN + 32 * q + lane, kb, nkblk, p.sf_vec8, x[2], x[3]);
       };
       int mb, nb, kb;
 #pragma unroll
@@ -919,12 +931,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             fail = STATUS_TIMEOUT_SCALES;
             break;
           }
-          tc_fence_after_sync();
-          tmem_st_32x32b_x16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + Cfg::SCALE_COL0 +
-                                 stage * Cfg::SCALE_SLOT_COLS,
-                             w[d]);
-          tmem_st_wait();
-          tc_fence_before_sync();
+          const uint32_t slot = smem_u32(sSc + stage * Cfg::SCALE_STAGE_BYTES) + 16 * lane + 4 * q;
+#pragma unroll
+          for (int a = 0; a < 4; ++a) sts_u32(slot + 512 * a, w[d][a]);
+          fence_proxy_async_shared();  // the tensor-memory copy reads the slot through the async proxy
           __syncwarp();
           if (lane == 0) mbar_arrive(&sfull[stage]);
           if (++stage == STAGES) {
