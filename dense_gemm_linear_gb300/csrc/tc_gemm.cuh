@@ -104,7 +104,7 @@ struct TcConfig {
   // SCALE_COL0 + 16 s .. + 15 (A's k-blocks 0-3, 4-7, then B's)
   static constexpr int SCALE_COL0 = 2 * BN;
   static constexpr int SCALE_SLOT_COLS = 16;
-  static constexpr int BAR_BYTES = 8 * (3 * STAGES + 6) + 8 + 32;
+  static constexpr int BAR_BYTES = 8 * (2 * STAGES + 6) + 8 + 32;
   // stream-K: one CTA's fp32 partial tile, and how many fit in the ring
   static constexpr int SLOT_BYTES = BM * BN * 4;
   static constexpr int RING_SLOTS = STAGES * STAGE_BYTES / SLOT_BYTES;
@@ -249,8 +249,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint64_t* fixbar = drain + 1;                          // stream-K: partial tiles landed in the ring
-  uint64_t* sfull = fixbar + 1;                          // MX: a stage's scales are in shared memory
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sfull + STAGES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fixbar + 1);
   volatile int* qflag = reinterpret_cast<volatile int*>(tmem_slot + 1);  // 8 epilogue-warp flags
 
   const int warp = threadIdx.x >> 5;
@@ -263,7 +262,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);                // the (leader's) producer's expect-tx arrival
+      // the (leader's) producer's expect-tx arrival, and with MX one arrival
+      // per scale warp once the stage's scales are in shared memory
+      mbar_init(&full[s], 1 + Cfg::SCALE_WARPS);
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -272,8 +273,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     }
     mbar_init(drain, 1);
     mbar_init(fixbar, 1);
-    if constexpr (Cfg::MX)
-      for (int s = 0; s < STAGES; ++s) mbar_init(&sfull[s], Cfg::SCALE_WARPS);
     fence_mbarrier_init();
     fence_proxy_async_shared();
   }
@@ -399,8 +398,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         const uint32_t d_tmem = tmem_base + acc * BN;
         const uint32_t idesc = sg.half ? idesc_half : idesc_full;  // a half tile: N = BN / 2
         for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
-          // MX: the stage's scales must be in shared memory too
-          const bool ok2 = mbar_wait(&full[stage], phase) && (!Cfg::MX || mbar_wait(&sfull[stage], phase));
+          // (MX: the stage's scales are in shared memory too)
+          const bool ok2 = mbar_wait(&full[stage], phase);
           if (!ok2) {
             fail = STATUS_TIMEOUT_MMA;
             break;
@@ -899,7 +898,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       // layout the MMA thread's 32-lane, 128-bit copy replicated to the four
       // lane quarters turns into the one kind::mxf4 reads: lane 32 w + l,
       // column 4 a + j holds row 32 j + l's word of atom a.  Warp q handles
-      // rows 32 q .. 32 q + 31 of A and of B.
+      // rows 32 q .. 32 q + 31 of A and of B, then arrives on the stage's
+      // full barrier beside the producer, so the MMA thread waits once.
       const int q = warp & 3;
       const int nkblk = p.K / 32;
       // Loads run SD stages ahead of the shared-memory stores (a register
@@ -936,7 +936,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           for (int a = 0; a < 4; ++a) sts_u32(slot + 512 * a, w[d][a]);
           fence_proxy_async_shared();  // the tensor-memory copy reads the slot through the async proxy
           __syncwarp();
-          if (lane == 0) mbar_arrive(&sfull[stage]);
+          if (lane == 0) mbar_arrive(&full[stage]);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
