@@ -508,7 +508,7 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream, Sta
 
 // Block-scaled FP4 (MXFP4): A and B as byte tensors of K / 2 bytes per row
 // (TMA moves the packed E2M1 codes untouched), E8M0 scales read by the
-// kernel's scale warps, 128 x 128 tiles.
+// kernel's scale warps, 128 x 256 tiles.
 dgl_status run_mxfp4(Problem pr, const uint8_t* sfa, const uint8_t* sfb, cudaStream_t stream) {
   if (pr.out != DGL_OUT_BF16 && pr.out != DGL_OUT_F32) return DGL_ERR_ARG;
   if (pr.M < 0 || pr.N < 0 || pr.K < 0 || pr.m < 0 || pr.n < 0) return DGL_ERR_ARG;
@@ -538,8 +538,8 @@ dgl_status run_mxfp4(Problem pr, const uint8_t* sfa, const uint8_t* sfb, cudaStr
   fill_mx_plan(pr.out, pr.m, pr.n, pr.K, ds->num_sms, &plan);
   const int64_t row_bytes = pr.K / 2;
   CUtensorMap ta, tb, tc;
-  if (!cached_operand_map(&ta, pr.A, true, row_bytes, pr.m, 128) ||
-      !cached_operand_map(&tb, pr.B, true, row_bytes, pr.n, 128))
+  if (!cached_operand_map(&ta, pr.A, true, row_bytes, pr.m, plan.tile_m) ||
+      !cached_operand_map(&tb, pr.B, true, row_bytes, pr.n, plan.tile_n))
     return DGL_ERR_CUDA;
   const bool f32 = pr.out == DGL_OUT_F32;
   const bool c_tma = aligned(pr.C, 16) && (pr.N * (f32 ? 4 : 2)) % 16 == 0;
@@ -552,8 +552,8 @@ dgl_status run_mxfp4(Problem pr, const uint8_t* sfa, const uint8_t* sfb, cudaStr
   p.m = static_cast<int>(pr.m);
   p.n = static_cast<int>(pr.n);
   p.K = static_cast<int>(pr.K);
-  p.tiles_m = static_cast<int>((pr.m + 127) / 128);
-  p.tiles_n = static_cast<int>((pr.n + 127) / 128);
+  p.tiles_m = static_cast<int>((pr.m + plan.tile_m - 1) / plan.tile_m);
+  p.tiles_n = static_cast<int>((pr.n + plan.tile_n - 1) / plan.tile_n);
   p.num_tiles = p.tiles_m * p.tiles_n;
   p.num_kb = static_cast<int>((row_bytes + 127) / 128);
   p.group_m = 16;

@@ -44,7 +44,7 @@ cudaError_t launch_tc_bf16_epi(int out, int tile_m, int tile_n, bool row_staging
 cudaError_t launch_tc_e4m3_epi(int out, int tile_m, int tile_n, bool row_staging, const CUtensorMap& ta,
                                const CUtensorMap& tb, const CUtensorMap& tbh, const CUtensorMap& tc,
                                const TcParams& p, int grid, cudaStream_t stream);
-// Block-scaled FP4 (MXFP4) tile kernel: 128 x 128 tiles, one CTA per tile;
+// Block-scaled FP4 (MXFP4) tile kernel: 128 x 256 tiles, one CTA per tile;
 // ta / tb: byte maps of the packed operands (K / 2 bytes per row); p.sfa,
 // p.sfb: the E8M0 scales.
 cudaError_t launch_tc_mxfp4(int out, bool row_staging, const CUtensorMap& ta, const CUtensorMap& tb,

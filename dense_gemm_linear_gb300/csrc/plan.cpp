@@ -229,18 +229,18 @@ int decode_ksteps(int rows_hi, int nk) {
   return ks < nk ? ks : (nk > 0 ? nk : 1);
 }
 
-// Block-scaled FP4: one 128 x 128 tile, one CTA per tile, a 5-stage ring of
-// 128-byte (256-element) k-stages.  The estimate charges the MMA at four times
-// the bf16 rate, or HBM, whichever is slower.
+// Block-scaled FP4: one 128 x 256 tile on one CTA, a 3-stage ring of
+// 128-byte (256-element) k-stages.  The estimate charges each stage's 48 KB of
+// operands at the tile path's load rate, or HBM, whichever is slower.
 void fill_mx_plan(int out_dtype, int64_t m, int64_t n, int64_t K, int num_sms, dgl_plan_info* out) {
   *out = dgl_plan_info{};
   out->path = DGL_PATH_TC;
   out->tile_m = 128;
-  out->tile_n = 128;
+  out->tile_n = 256;
   out->tile_k = 256;
-  out->stages = 5;
+  out->stages = 3;
   out->cta_group = 1;
-  tile_metrics(m, n, 128, 128, num_sms, out);
+  tile_metrics(m, n, 128, 256, num_sms, out);
   const int64_t tiles = out->num_tiles;
   out->grid = static_cast<int>(std::min<int64_t>(tiles, num_sms));
   const int64_t waves = (tiles + num_sms - 1) / num_sms;
@@ -248,7 +248,7 @@ void fill_mx_plan(int out_dtype, int64_t m, int64_t n, int64_t K, int num_sms, d
   const double o = out_dtype == DGL_OUT_F32 ? 4.0 : 2.0;
   const double bytes = (static_cast<double>(m) + n) * K / 2.0 + (static_cast<double>(m) + n) * K / 32.0 +
                        static_cast<double>(m) * n * o;
-  const double tc_us = kLaunchUs + static_cast<double>(waves) * (k_stages * 0.14 + 1.0);
+  const double tc_us = kLaunchUs + static_cast<double>(waves) * (k_stages * 0.40 + 1.5);
   out->est_us = std::max(tc_us, bytes / (kHbmGBs * 1e3) + kLaunchUs);
 }
 

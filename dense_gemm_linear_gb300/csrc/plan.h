@@ -34,7 +34,7 @@ bool tc_supported_epi_tile(int tile_m, int tile_n, bool gated);
 void choose_linear_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, bool gated, int num_sms,
                         dgl_plan_info* out);
 void choose_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int num_sms, dgl_plan_info* out);
-// The block-scaled FP4 plan: 128 x 128 tiles on one CTA each.
+// The block-scaled FP4 plan: 128 x 256 tiles on one CTA each.
 void fill_mx_plan(int out_dtype, int64_t m, int64_t n, int64_t K, int num_sms, dgl_plan_info* out);
 
 }  // namespace dgl

@@ -66,8 +66,10 @@ struct TcConfig {
   // MX: block-scaled FP4 (MXFP4).  A and B hold E2M1 codes two to a byte; each
   // 32 elements of K of a row share one E8M0 scale.  kind::mxf4 MMAs read the
   // scales from tensor memory.  Four more warps gather each stage's scales into
-  // shared memory, and the MMA thread copies them into a ring of 16-column
-  // tensor-memory slots after the accumulators.  128 x 128 tiles, one CTA.
+  // shared memory, and the MMA thread copies them into a ring of tensor-memory
+  // slots after the accumulator.  128 x 256 tiles on one CTA, with a single
+  // 256-column accumulator (the other 256 columns hold the scale ring); the
+  // epilogue hands it back as soon as it has been read out.
   static constexpr bool MX = MX_;
   static constexpr bool OUT_F32 = OUT_F32_;
   // ROWSTG: bf16 C whose rows are not 16-byte aligned.  The epilogue stages
@@ -93,17 +95,20 @@ struct TcConfig {
   // multiple of 16 bytes so rows spread over the banks
   static constexpr int ROW_PITCH = BN * 2 + 16;
   static constexpr int STG_TOTAL = ROWSTG ? 4 * 32 * ROW_PITCH : EPI_WARPS * 4096;
-  // MX: per stage, 1 KB of A's scales and 1 KB of B's (two 512-byte atoms each)
-  static constexpr int SCALE_STAGE_BYTES = MX ? 2048 : 0;
+  // MX: per stage, 512-byte scale atoms for each 128 rows and each 4 k-blocks:
+  // 2 of A's, 2 per 128 rows of B
+  static constexpr int SCALE_ATOMS = MX ? 2 + 2 * (BN / 128) : 0;
+  static constexpr int SCALE_STAGE_BYTES = 512 * SCALE_ATOMS;
   static constexpr int STAGES = tc_ring_stages(STAGE_BYTES + SCALE_STAGE_BYTES, STG_TOTAL);
   static constexpr int SCALE_WARPS = MX ? 4 : 0;
   static constexpr int THREADS = 64 + EPI_WARPS * 32 + SCALE_WARPS * 32;
-  // two fp32 accumulators of BN columns (MX: and the scale ring after them)
+  // fp32 accumulators of BN columns: two, so the epilogue of one tile
+  // overlaps the main loop of the next, or one with MX 128 x 256 tiles
+  static constexpr int ACC_BUFS = MX && BN == 256 ? 1 : 2;
   static constexpr int TMEM_COLS = MX ? 512 : 2 * BN;
-  // MX scale ring: slot s holds stage s's scales in columns
-  // SCALE_COL0 + 16 s .. + 15 (A's k-blocks 0-3, 4-7, then B's)
-  static constexpr int SCALE_COL0 = 2 * BN;
-  static constexpr int SCALE_SLOT_COLS = 16;
+  // MX scale ring: slot s holds stage s's scale atoms, 4 columns each
+  static constexpr int SCALE_COL0 = ACC_BUFS * BN;
+  static constexpr int SCALE_SLOT_COLS = 4 * SCALE_ATOMS;
   static constexpr int BAR_BYTES = 8 * (2 * STAGES + 6) + 8 + 32;
   // stream-K: one CTA's fp32 partial tile, and how many fit in the ring
   static constexpr int SLOT_BYTES = BM * BN * 4;
@@ -118,7 +123,7 @@ struct TcConfig {
   static_assert((ROW_PITCH / 16) % 2 == 1, "row pitch: odd multiple of 16 bytes");
   static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation: power of two");
   static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
-  static_assert(!MX || (BN == 128 && CG == 1 && !FP8 && !EPI), "block-scaled FP4: 128 x 128 tiles, one CTA");
+  static_assert(!MX || ((BN == 128 || BN == 256) && CG == 1 && !FP8 && !EPI), "block-scaled FP4: 128-row tiles, one CTA");
   static_assert(!MX || SCALE_COL0 + STAGES * SCALE_SLOT_COLS <= TMEM_COLS, "scale ring fits in tensor memory");
   static_assert(B_STAGE_BYTES % 1024 == 0, "B stage tiles stay 1024-byte aligned");
   static_assert(RING_SLOTS >= 1, "a partial tile fits in the ring");
@@ -229,6 +234,18 @@ __device__ __forceinline__ void scale_words(const uint8_t* sf, int rows, int r, 
   for (int t = 0; t < 8; ++t) b[t] = k0 + t < nkblk ? row[k0 + t] : 0x7Fu;
   lo = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
   hi = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+}
+
+// Next accumulator buffer and its barrier phase: alternate between two, or
+// reuse the only one.
+template <int BUFS>
+__device__ __forceinline__ void next_acc(uint32_t& acc, uint32_t& acc_phase) {
+  if constexpr (BUFS == 2) {
+    acc ^= 1;
+    if (acc == 0) acc_phase ^= 1;
+  } else {
+    acc_phase ^= 1;
+  }
 }
 
 template <class Cfg>
@@ -406,12 +423,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           }
           tc_fence_after_sync();
           if constexpr (Cfg::MX) {
-            // the stage's four 512-byte scale atoms (A's k-blocks 0-3, 4-7,
-            // then B's) into its tensor-memory slot; the MMAs below run after
+            // the stage's 512-byte scale atoms into its tensor-memory slot,
+            // atom a to columns 4 a .. 4 a + 3; the MMAs below run after
             const uint32_t sc = smem_u32(sSc + stage * Cfg::SCALE_STAGE_BYTES);
             const uint32_t tcol = tmem_base + Cfg::SCALE_COL0 + stage * Cfg::SCALE_SLOT_COLS;
 #pragma unroll
-            for (int a = 0; a < 4; ++a) tmem_cp_32x128b_warpx4(tcol + 4 * a, smem_desc_rows16(sc + 512 * a));
+            for (int a = 0; a < Cfg::SCALE_ATOMS; ++a)
+              tmem_cp_32x128b_warpx4(tcol + 4 * a, smem_desc_rows16(sc + 512 * a));
           }
           const uint32_t a_addr = smem_u32(sA + stage * Cfg::A_STAGE_BYTES);
           const uint32_t b_addr = smem_u32(sB + stage * Cfg::B_STAGE_BYTES);
@@ -430,10 +448,19 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             } else {
               if constexpr (Cfg::MX) {
                 // instruction k covers k-blocks 2k, 2k + 1: word k / 2 of the
-                // slot's A and B columns, starting at byte 2 (k % 2)
+                // slot's atoms, starting at byte 2 (k % 2).  Atoms: A's k-blocks
+                // 0-3 and 4-7, then for each of those B's rows 0-127 (and
+                // 128-255).  Each 128-column half of the tile is one N = 128
+                // instruction with its own rows of B and their scales.
                 const uint32_t id = static_cast<uint32_t>(k & 1) * 2u;
-                const uint32_t sf = tmem_base + Cfg::SCALE_COL0 + stage * Cfg::SCALE_SLOT_COLS + 4 * (k >> 1);
-                umma_mxf4(d_tmem, ad, bd, idesc_mxf4(Cfg::TILE_M, BN, id, id), sf, sf + 8, accumulate);
+                const uint32_t slot = tmem_base + Cfg::SCALE_COL0 + stage * Cfg::SCALE_SLOT_COLS;
+                constexpr int NH = BN / 128;
+#pragma unroll
+                for (int h = 0; h < NH; ++h) {
+                  const uint64_t bdh = smem_desc_sw128(b_addr + h * 128 * Cfg::ROW_BYTES + k * Cfg::MMA_K_BYTES);
+                  umma_mxf4(d_tmem + 128 * h, ad, bdh, idesc_mxf4(Cfg::TILE_M, 128, id, id), slot + 4 * (k >> 1),
+                            slot + 8 + 4 * (NH * (k >> 1) + h), accumulate);
+                }
               } else if constexpr (Cfg::FP8) {
                 umma_e4m3(d_tmem, ad, bd, idesc, accumulate);
               } else {
@@ -456,8 +483,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           umma_commit_pair_multicast(&tfull[acc], 0x3);  // both CTAs' epilogues
         else
           umma_commit(&tfull[acc]);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1;
+        next_acc<Cfg::ACC_BUFS>(acc, acc_phase);
       }
       // Every MMA this thread issued has finished before TMEM is released.
       if (issued_any) {
@@ -557,8 +583,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         }
         named_bar_sync(5, Cfg::EPI_WARPS * 32);  // every epilogue warp's pieces are written
         if (warp == 2 && lane == 0) st_release_gpu(p.flags + cluster_id * CG + rank, p.epoch);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1;
+        next_acc<Cfg::ACC_BUFS>(acc, acc_phase);
         continue;
       }
       if (sg.kb1 < p.num_kb) {
@@ -881,8 +906,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           }
         }
       }
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1;
+      next_acc<Cfg::ACC_BUFS>(acc, acc_phase);
     }
     if ((Cfg::ROWSTG ? half == 0 : (p.c_tma && lane == 0))) bulk_wait0();
   }
@@ -892,8 +916,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       // ---------------------------------------------------------- scale warps (MX)
       // Stage s's E8M0 scales go to shared-memory slot s once the MMAs (and
       // the copy) that read the slot's previous contents are done: the
-      // stage's "empty" barrier.  A slot holds four 512-byte atoms (A's
-      // k-blocks 0-3 and 4-7 of the stage, then B's).  Row 32 j + l of the
+      // stage's "empty" barrier.  A slot holds 512-byte atoms (A's k-blocks
+      // 0-3 and 4-7 of the stage, then B's per 128-row half).  Row 32 j + l of the
       // tile has its four scale bytes at atom offset 16 l + 4 j, which is the
       // layout the MMA thread's 32-lane, 128-bit copy replicated to the four
       // lane quarters turns into the one kind::mxf4 reads: lane 32 w + l,
@@ -906,11 +930,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       // queue, unrolled so every index is static); they are predicated rather
       // than selected afterwards, so nothing waits for them before the store.
       constexpr int SD = 4;
+      constexpr int NH = BN / 128;
       StageIter ahead(cluster_id, p), cur(cluster_id, p);
-      uint32_t w[SD][4];
-      auto gather = [&](uint32_t(&x)[4], int mb, int nb, int kb) {
+      uint32_t w[SD][Cfg::SCALE_ATOMS];
+      // atom order: A's k-blocks 0-3, 4-7, then B's: for k-blocks 0-3 each
+      // 128-row half, then for 4-7 each half
+      auto gather = [&](uint32_t(&x)[Cfg::SCALE_ATOMS], int mb, int nb, int kb) {
         scale_words(p.sfa, p.m, mb * BM + 32 * q + lane, kb, nkblk, p.sf_vec8, x[0], x[1]);
-        scale_words(p.sfb, p.n, nb * BN + 32 * q + lane, kb, nkblk, p.sf_vec8, x[2], x[3]);
+#pragma unroll
+        for (int h = 0; h < NH; ++h)
+          scale_words(p.sfb, p.n, nb * BN + 128 * h + 32 * q + lane, kb, nkblk, p.sf_vec8, x[2 + h], x[2 + NH + h]);
       };
       int mb, nb, kb;
 #pragma unroll
@@ -933,7 +962,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           }
           const uint32_t slot = smem_u32(sSc + stage * Cfg::SCALE_STAGE_BYTES) + 16 * lane + 4 * q;
 #pragma unroll
-          for (int a = 0; a < 4; ++a) sts_u32(slot + 512 * a, w[d][a]);
+          for (int a = 0; a < Cfg::SCALE_ATOMS; ++a) sts_u32(slot + 512 * a, w[d][a]);
           fence_proxy_async_shared();  // the tensor-memory copy reads the slot through the async proxy
           __syncwarp();
           if (lane == 0) mbar_arrive(&full[stage]);

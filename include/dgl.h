@@ -158,7 +158,7 @@ dgl_status dgl_gemm_planned(int32_t dtype, const void* A, const void* B, const f
  * aligned.  Errors: DGL_ERR_ARG (null pointers, extents), DGL_ERR_ALIGN
  * (K not a multiple of 32, A or B not 16-byte aligned, C not aligned to
  * its element), DGL_ERR_SHAPE (extents past int32).  Every problem, small
- * m included, runs on 128 x 128 tiles (the decode path is bf16 / E4M3 only).
+ * m included, runs on 128 x 256 tiles (the decode path is bf16 / E4M3 only).
  * Results whose block-scale products leave fp32's range are not specified;
  * the parity tests keep scales within 2^-20 .. 2^20.
  */
@@ -257,7 +257,7 @@ dgl_status dgl_linear(int32_t dtype, const void* A, const void* B, const float* 
  * screened by padded output area (rejecting a tile whose padded area exceeds
  * 1.25x the real one unless none passes, as in FlyDSL pull request 1303's
  * autotuner) and the survivor with the lowest cost-model time is chosen.
- * dtype DGL_DTYPE_MXFP4 has one tile: 128 x 128 (tile_k 256 elements).
+ * dtype DGL_DTYPE_MXFP4 has one tile: 128 x 256 (tile_k 256 elements).
  */
 dgl_status dgl_plan(int32_t dtype, int64_t m, int64_t n, int64_t K, int32_t out_dtype, int32_t num_sms,
                     dgl_plan_info* out);

@@ -2,6 +2,7 @@
 every symbol include/dgl.h declares; the planner's metric helpers match the
 worked examples printed on the pages; planner rules; the input generator."""
 import ctypes
+import json
 import os
 import re
 import subprocess
@@ -52,28 +53,26 @@ def test_version_and_status_strings(dgl):
 
 
 # ------------------------------------------------------------ TraceLens worked examples
-def test_tile_metrics_tracelens_example_1(dgl):
-    """M=10240, N=2048, tile 256x64, 304 CUs: 1280 tiles, tile_eff 1.0, 5 rounds, wq_eff 0.842."""
-    m = dgl.dgl_tile_metrics(10240, 2048, 256, 64, 304)
-    assert m.num_tiles == 1280
-    assert m.tile_eff == 1.0
-    assert round(m.wq_eff, 3) == 0.842 and round(m.dim_eff, 3) == 0.842
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
 
-def test_tile_metrics_tracelens_example_2(dgl):
-    """M=2048, N=10240, tile 256x144, 304 CUs: 576 tiles, tile_eff ~0.9877, wq_eff ~0.947, dim_eff ~0.935."""
-    m = dgl.dgl_tile_metrics(2048, 10240, 256, 144, 304)
-    assert m.num_tiles == 576
-    # the page prints these to three or four digits with "approximately"
-    assert abs(m.tile_eff - 0.9877) < 1e-4
-    assert abs(m.wq_eff - 0.947) < 1e-3
-    assert abs(m.dim_eff - 0.935) < 1e-3
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
 
 
-def test_tile_metrics_tracelens_output_example(dgl):
-    """The enhanced-output row: 2048x2048 on a 256x64 macro tile, 304 CUs -> 256 tiles, wq_eff 0.84."""
-    m = dgl.dgl_tile_metrics(2048, 2048, 256, 64, 304)
-    assert m.num_tiles == 256 and m.tile_eff == 1.0 and round(m.wq_eff, 2) == 0.84
+@pytest.mark.parametrize("idx", range(3))
+def test_tile_metrics_tracelens_examples(dgl, idx):
+    """The page's calculation examples and output row (tests/golden/tracelens_dim_eff.json):
+    tile count, tile_eff, wq_eff and dim_eff to the digits the page prints."""
+    g = _golden("tracelens_dim_eff.json")
+    c = g["cases"][idx]
+    m = dgl.dgl_tile_metrics(c["m"], c["n"], c["mt_m"], c["mt_n"], g["num_units"])
+    assert m.num_tiles == c["num_tiles"]
+    tol = 10.0 ** -c["digits"]  # the page rounds or truncates ("approximately") to these digits
+    assert abs(m.wq_eff - c["wq_eff"]) <= tol and abs(m.dim_eff - c["dim_eff"]) <= tol
+    assert abs(m.tile_eff - c["tile_eff"]) < 1e-4
+    assert -(-m.num_tiles // g["num_units"]) == c["rounds"]
 
 
 def test_tile_metrics_errors(dgl):
@@ -83,18 +82,20 @@ def test_tile_metrics_errors(dgl):
         dgl.dgl_tile_metrics(10, 10, 64, 64, 0)
 
 
-# ------------------------------------------------------------ the guide's worked example (section 14)
+# ------------------------------------------------------------ the guide's worked example
 def test_guide_worked_example_flops_and_bytes():
-    """5120x5120x8320 FP8 with bf16 C and per-token scales: 436 GFLOP and 137.6 MB;
-    at ~500 TFLOP/s that is ~0.87 ms and ~158 GB/s."""
+    """tests/golden/gemm_guide_worked_example.json: 436 GFLOP and 137.6 MB; at
+    ~500 TFLOP/s that is ~0.87 ms and ~158 GB/s."""
     from dense_gemm_linear_gb300 import metrics
-    f = metrics.gemm_flops(5120, 5120, 8320)
-    b = metrics.gemm_bytes(5120, 5120, 8320, in_bytes=1, out_bytes=2, scaled=True)
-    assert round(f / 1e9) == 436
-    assert abs(b / 1e6 - 137.6) < 0.1          # 137.67 MB; the page truncates to 137.6
-    t = f / 500e12
-    assert round(t * 1e3, 2) == 0.87
-    assert round(b / t / 1e9) == 158
+    g = _golden("gemm_guide_worked_example.json")
+    f = metrics.gemm_flops(g["m"], g["n"], g["k"])
+    b = metrics.gemm_bytes(g["m"], g["n"], g["k"], in_bytes=g["in_bytes"], out_bytes=g["out_bytes"],
+                           scaled=g["scaled"])
+    assert round(f / 1e9) == g["gflop"]
+    assert abs(b / 1e6 - g["mbytes"]) < 0.1          # 137.67 MB; the page truncates to 137.6
+    t = f / (g["target_tflops"] * 1e12)
+    assert round(t * 1e3, 2) == g["ms"]
+    assert round(b / t / 1e9) == g["gbs"]
 
 
 def test_arithmetic_intensity_classification():
