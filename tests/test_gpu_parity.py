@@ -171,6 +171,23 @@ def test_decode_many_rows_per_cta():
     gu.assert_close_full(case, gu.host_valid(case, Cbuf))
 
 
+@pytest.mark.parametrize("m", list(range(1, 17)))
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_decode_every_m(m, out):
+    """The decode path for every m in both output types; n = 1001 leaves
+    ragged parts and K = 264 a partial 128-byte step."""
+    _full(make_case("bf16", m, 1001, 264, out=out), guard_rows=1, pad_cols=3)
+
+
+@pytest.mark.parametrize("m,n,k", [(1, 11008, 4096), (8, 4096, 4096), (16, 4096, 4096), (3, 16, 8)])
+def test_decode_full_shapes(m, n, k):
+    """The decode shapes of the benchmarks at full size (sampled), and K = 8."""
+    case = make_case("bf16", m, n, k, out="f32")
+    Cbuf, intact = gu.run(case, guard_rows=1, pad_cols=1)
+    assert intact
+    gu.assert_close_sampled(case, Cbuf, tile_m=16, tile_n=128)
+
+
 def test_forced_decode_vs_tile_same_result():
     """m <= 16 through both paths: both within tolerance of the oracle."""
     case = make_case("bf16", 12, 640, 512, out="f32")
