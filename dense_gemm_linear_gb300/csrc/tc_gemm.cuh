@@ -450,17 +450,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 // instruction k covers k-blocks 2k, 2k + 1: word k / 2 of the
                 // slot's atoms, starting at byte 2 (k % 2).  Atoms: A's k-blocks
                 // 0-3 and 4-7, then for each of those B's rows 0-127 (and
-                // 128-255).  Each 128-column half of the tile is one N = 128
-                // instruction with its own rows of B and their scales.
+                // 128-255).  One N = BN instruction reads B's scales for rows
+                // 128 r .. 128 r + 127 from the r-th 4-column group after the
+                // address it is given (measured: the parity tests pass with it).
                 const uint32_t id = static_cast<uint32_t>(k & 1) * 2u;
                 const uint32_t slot = tmem_base + Cfg::SCALE_COL0 + stage * Cfg::SCALE_SLOT_COLS;
                 constexpr int NH = BN / 128;
-#pragma unroll
-                for (int h = 0; h < NH; ++h) {
-                  const uint64_t bdh = smem_desc_sw128(b_addr + h * 128 * Cfg::ROW_BYTES + k * Cfg::MMA_K_BYTES);
-                  umma_mxf4(d_tmem + 128 * h, ad, bdh, idesc_mxf4(Cfg::TILE_M, 128, id, id), slot + 4 * (k >> 1),
-                            slot + 8 + 4 * (NH * (k >> 1) + h), accumulate);
-                }
+                umma_mxf4(d_tmem, ad, bd, idesc_mxf4(Cfg::TILE_M, BN, id, id), slot + 4 * (k >> 1),
+                          slot + 8 + 4 * NH * (k >> 1), accumulate);
               } else if constexpr (Cfg::FP8) {
                 umma_e4m3(d_tmem, ad, bd, idesc, accumulate);
               } else {
