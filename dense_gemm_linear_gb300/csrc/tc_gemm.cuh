@@ -1,7 +1,9 @@
 // Persistent, warp-specialised tcgen05 GEMM:  C[i,j] = sum_k A[i,k] B[j,k]
-// (times sa[i] sb[j] for E4M3), fp32 accumulation in tensor memory.
+// (times sa[i] sb[j] for E4M3; with per-32-element block scales for MXFP4),
+// fp32 accumulation in tensor memory.
 //
-// One CTA per SM walks a raster of 128 x BN output tiles.  Roles:
+// One CTA per SM (or one CTA pair per two SMs, 256-row tiles) walks a raster
+// of 128 x BN output tiles.  Roles:
 //   warp 0     TMA producer: fills an S-stage shared-memory ring with the
 //              128 x 128-byte slice of A and the BN x 128-byte slice of B for
 //              each k-stage.  The tensor maps are bounded at the valid rows
@@ -9,9 +11,9 @@
 //              zeros and the k-loop carries no predicate (the descriptor-bound
 //              M edge of FlyDSL pull request 1303, applied to every extent).
 //   warp 1     allocates tensor memory, then one thread issues tcgen05.mma
-//              (four K=16 bf16 or K=32 E4M3 steps per 128-byte stage) into one
-//              of two TMEM accumulators and commits each stage back to the
-//              producer's "empty" barrier.
+//              (four K=16 bf16, K=32 E4M3 or K=64 E2M1 steps per 128-byte
+//              stage) into one of two TMEM accumulators and commits each stage
+//              back to the producer's "empty" barrier.
 //   warps 2-9  epilogue, two warps per TMEM lane quarter, each taking half
 //              of the 32-column chunks of its 32 rows.  A warp reads its
 //              chunks out of TMEM two at a time, releases the accumulator
@@ -33,8 +35,10 @@
 //              head and tail bytes take narrow stores.
 //              The staging transpose is section 7.2's "CShuffle" idea: re-map
 //              threads so each store covers contiguous columns of a row.
+//   warps 10-13 (MXFP4 only) gather each stage's E8M0 scales into shared
+//              memory for the MMA thread to copy into tensor memory.
 // The two accumulators let the epilogue of tile t overlap the main loop of
-// tile t+1.
+// tile t+1 (the MXFP4 variant has one: see TcConfig).
 #pragma once
 
 #include <cuda_bf16.h>
