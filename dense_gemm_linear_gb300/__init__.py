@@ -49,7 +49,7 @@ class PlanInfo(ctypes.Structure):
                 ("tile_k", ctypes.c_int32), ("stages", ctypes.c_int32), ("cta_group", ctypes.c_int32),
                 ("grid", ctypes.c_int32), ("num_tiles", ctypes.c_int32), ("tile_eff", ctypes.c_double),
                 ("wq_eff", ctypes.c_double), ("dim_eff", ctypes.c_double), ("est_us", ctypes.c_double),
-                ("stream_k", ctypes.c_int32), ("split_tail", ctypes.c_int32)]
+                ("stream_k", ctypes.c_int32), ("split_tail", ctypes.c_int32), ("k_group", ctypes.c_int32)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

@@ -387,18 +387,22 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream, Sta
     p.parts = parts;
     p.rows_hi = rows_hi;
     const int nk = static_cast<int>((pr.K * esize + 127) / 128);
-    int ks = decode_ksteps(rows_hi, nk);
+    const int g = decode_group(rows_hi, nk);
+    int ks = decode_ksteps(rows_hi, nk, g);
     if (forced && forced->tile_k > 0) {
-      // a forced plan may choose the stage width (K elements, a multiple of 128 bytes)
+      // a forced plan may choose the stage width (K elements, a multiple of
+      // 128 bytes and of the group's steps)
       const int want = static_cast<int>(forced->tile_k * esize / 128);
-      if (want < 1 || want > 8 || forced->tile_k * esize % 128 != 0 || decode_stages(rows_hi, want) < 2)
+      if (want < 1 || want > 16 || want % g != 0 || forced->tile_k * esize % 128 != 0 ||
+          decode_stages(rows_hi, want, g) < 2)
         return DGL_ERR_UNSUPPORTED;
       ks = want;
     }
+    p.group = g;
     p.ksteps = ks;
-    p.b_plane_bytes = decode_plane_bytes(rows_hi);
-    p.stage_bytes = decode_stage_bytes(rows_hi, ks);
-    p.stages = decode_stages(rows_hi, ks);
+    p.b_plane_bytes = decode_plane_bytes(rows_hi, g);
+    p.stage_bytes = decode_stage_bytes(rows_hi, ks, g);
+    p.stages = decode_stages(rows_hi, ks, g);
     p.status = ds->status;
     p.bias = pr.bias;
     p.act = pr.act;

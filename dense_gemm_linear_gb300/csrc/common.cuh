@@ -73,8 +73,9 @@ struct DecodeParams {
   int parts;            // B rows are cut into this many balanced parts
   int rows_hi;          // ceil(n / parts): parts of this size use the second B map
   int stages;           // ring depth
-  int ksteps;           // 128-byte K steps per stage
-  int b_plane_bytes;    // one B box: rows_hi rounded up to 8, x 128 bytes
+  int ksteps;           // 128-byte K steps per stage (a multiple of group)
+  int group;            // K steps stacked into one 128-row MMA operand (1, 2, 4, 8, 16)
+  int b_plane_bytes;    // one B slot: 128 / group rows (group 1: rows_hi rounded up to 8), x 128 bytes
   int stage_bytes;      // ksteps x (A box (2 KB) + B box)
   int* status;          // device status word
   const float* bias;    // linear-layer epilogue: bias per column of C, or null

@@ -6,17 +6,18 @@ namespace dgl {
 
 namespace {
 
-template <bool FP8, bool OUT_F32>
+template <bool FP8, bool OUT_F32, bool STACK>
 cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb_lo, const CUtensorMap& tb_hi,
                        const DecodeParams& p, int grid, cudaStream_t stream) {
-  auto kern = decode_gemm_kernel<FP8, OUT_F32>;
+  auto kern = decode_gemm_kernel<FP8, OUT_F32, STACK>;
+  constexpr int smem = dec_smem_bytes(STACK);
   static std::atomic<uint64_t> attr_done{0};  // one bit per device
-  cudaError_t e = set_smem_attr_once(kern, DEC_SMEM_BYTES, attr_done);
+  cudaError_t e = set_smem_attr_once(kern, smem, attr_done);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(DEC_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = DEC_SMEM_BYTES;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   // the kernel waits for its predecessor (griddep_wait) before any global access
@@ -42,11 +43,18 @@ __global__ void zero_fill_kernel(T* C, int64_t ldc, int m, int n) {
 cudaError_t launch_decode(int dtype, int out, const CUtensorMap& ta, const CUtensorMap& tb_lo,
                           const CUtensorMap& tb_hi, const DecodeParams& p, int grid, cudaStream_t stream) {
   const bool f32 = out == 1;
+  if (p.group > 1) {
+    if (dtype == 1)
+      return f32 ? launch_one<true, true, true>(ta, tb_lo, tb_hi, p, grid, stream)
+                 : launch_one<true, false, true>(ta, tb_lo, tb_hi, p, grid, stream);
+    return f32 ? launch_one<false, true, true>(ta, tb_lo, tb_hi, p, grid, stream)
+               : launch_one<false, false, true>(ta, tb_lo, tb_hi, p, grid, stream);
+  }
   if (dtype == 1)
-    return f32 ? launch_one<true, true>(ta, tb_lo, tb_hi, p, grid, stream)
-               : launch_one<true, false>(ta, tb_lo, tb_hi, p, grid, stream);
-  return f32 ? launch_one<false, true>(ta, tb_lo, tb_hi, p, grid, stream)
-             : launch_one<false, false>(ta, tb_lo, tb_hi, p, grid, stream);
+    return f32 ? launch_one<true, true, false>(ta, tb_lo, tb_hi, p, grid, stream)
+               : launch_one<true, false, false>(ta, tb_lo, tb_hi, p, grid, stream);
+  return f32 ? launch_one<false, true, false>(ta, tb_lo, tb_hi, p, grid, stream)
+             : launch_one<false, false, false>(ta, tb_lo, tb_hi, p, grid, stream);
 }
 
 cudaError_t launch_zero_fill(int out, void* C, int64_t ldc, int m, int n, cudaStream_t stream) {

@@ -22,9 +22,19 @@
 //     box (B rows past the part, A rows past m) read whatever the ring holds
 //     there; each feeds only its own row or column of D, which is never
 //     stored.
+//   * A part of at most 128 / G rows (G = 2, 4, 8 or 16) fills the 128-row
+//     operand with G consecutive K steps instead: slot s (rows s R .. s R +
+//     R - 1, R = 128 / G) holds the part's rows at K step k0 + s, and the
+//     N = 16 G operand holds A's rows at the same G steps, slot s at columns
+//     16 s .. 16 s + 15.  The diagonal blocks D[slot s][A slot s] accumulate
+//     the part's products over the K steps congruent to s; the off-diagonal
+//     blocks mix K steps and are never read.  One MMA then does the work of
+//     G, which matters because a small-N MMA costs about the same whatever
+//     its valid rows.
 //   * warps 2-5 read D (lane = row of B, 16 columns = rows of A), scale
 //     (E4M3), round and store C[i][j]: for each i the warp's 32 lanes write 32
-//     consecutive columns.
+//     consecutive columns.  With G > 1 they first add the G diagonal blocks
+//     through shared memory, in slot order.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -42,14 +52,21 @@ constexpr int DEC_RING_BYTES = 196608;             // 192 KB of stages
 // The 128-row MMA operand of the ring's last plane reaches up to 16 KB past
 // that plane's start; the slack keeps every such read inside the allocation.
 constexpr int DEC_SLACK_BYTES = 16384;
-constexpr int DEC_SMEM_BYTES = 1024 + DEC_RING_BYTES + DEC_SLACK_BYTES + 8 * (2 * DEC_MAX_STAGES + 5) + 8;
+// G > 1: the 128 stacked rows' 16 partial sums, padded to 17 floats a row so
+// that a warp's 32 rows fall in 32 different banks
+constexpr int DEC_RED_STRIDE = 17;
+constexpr int DEC_RED_BYTES = 128 * DEC_RED_STRIDE * 4;
+// dynamic shared memory: the ring, the barriers and (stacked K steps only)
+// the partial sums
+__host__ __device__ constexpr int dec_smem_bytes(bool stack) {
+  return 1024 + DEC_RING_BYTES + DEC_SLACK_BYTES + 8 * (2 * DEC_MAX_STAGES + 7) + 8 + (stack ? DEC_RED_BYTES : 0);
+}
 constexpr int DEC_A_BOX_BYTES = 16 * 128;
 // Independent accumulators per part: the four MMAs of a 128-byte K step go to
-// four separate 16-column TMEM accumulators, so consecutive MMAs do not wait
-// on one another's result; the epilogue adds the four.
-constexpr int DEC_NACC = 4;
-constexpr int DEC_ACC_COLS = 16 * DEC_NACC;         // one accumulator buffer (of two)
-constexpr int DEC_TMEM_COLS = 2 * DEC_ACC_COLS;
+// separate 16 G-column TMEM accumulators (four, or 16 / G when G >= 8, so
+// that two buffers fit in 512 columns), so consecutive MMAs do not wait on
+// one another's result; the epilogue adds them.
+__host__ __device__ constexpr int dec_nacc(int group) { return group >= 8 ? 16 / group : 4; }
 
 // Row range of part `part` of n rows cut into `parts` balanced pieces.
 __device__ __forceinline__ void part_rows(int part, int parts, int n, int& r0, int& r1) {
@@ -57,7 +74,8 @@ __device__ __forceinline__ void part_rows(int part, int parts, int n, int& r0, i
   r1 = static_cast<int>(static_cast<int64_t>(part + 1) * n / parts);
 }
 
-template <bool FP8, bool OUT_F32>
+// STACK: G = p.group > 1 K steps per MMA; otherwise G = 1 at compile time.
+template <bool FP8, bool OUT_F32, bool STACK>
 __global__ void __launch_bounds__(DEC_THREADS, 1)
     decode_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB_lo,
                        const __grid_constant__ CUtensorMap tmB_hi, const DecodeParams p) {
@@ -68,7 +86,9 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
   uint64_t* tfull = empty + DEC_MAX_STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* redbar = drain + 1;  // G > 1: partial sums written [0], read [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(redbar + 2);
+  float* red = reinterpret_cast<float*>(redbar + 3);
   const int stages = p.stages;
   const int stage_bytes = p.stage_bytes;
   const int warp = threadIdx.x >> 5;
@@ -84,11 +104,17 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
       mbar_init(&tempty[b], 4);
     }
     mbar_init(drain, 1);
+    mbar_init(&redbar[0], 4);
+    mbar_init(&redbar[1], 4);
     fence_mbarrier_init();
     fence_proxy_async_shared();
   }
+  const int G = STACK ? p.group : 1;
+  const int nacc = dec_nacc(G);
+  const int acc_cols = nacc * 16 * G;            // one accumulator buffer (of two)
+  const uint32_t tmem_cols = 2 * acc_cols;       // 128, 256 or 512: a power of two
   if (warp == 1) {
-    tmem_alloc(tmem_slot, DEC_TMEM_COLS);
+    tmem_alloc(tmem_slot, tmem_cols);
     tmem_relinquish();
   }
   tc_fence_before_sync();
@@ -145,7 +171,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f32acc(FP8 ? 0u : 1u, 128, 16);
+      const uint32_t idesc = idesc_f32acc(FP8 ? 0u : 1u, 128, 16 * G);
+      const uint32_t ring_lo = smem_desc_sw128_lo(smem_u32(ring));
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool issued_any = false;
       for (int part = blockIdx.x; part < p.parts && !fail; part += gridDim.x) {
@@ -154,7 +181,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
           break;
         }
         tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + acc * DEC_ACC_COLS;
+        const uint32_t d_tmem = tmem_base + acc * acc_cols;
         for (int kb0 = 0; kb0 < nk; kb0 += ks) {
           if (!mbar_wait(&full[stage], phase)) {
             fail = STATUS_TIMEOUT_MMA;
@@ -162,20 +189,29 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
           }
           tc_fence_after_sync();
           const int planes = min(ks, nk - kb0);
-          const uint32_t sbase = smem_u32(ring + stage * stage_bytes);
-          for (int j = 0; j < planes; ++j) {
-            const uint32_t w_addr = sbase + a_bytes + j * b_plane;   // B rows: the 128-row operand
-            const uint32_t x_addr = sbase + j * DEC_A_BOX_BYTES;     // A rows: the 16-row operand
+          // Descriptors differ only in their low word (the address field), so
+          // each MMA's pair is two 32-bit adds: a small-N MMA is short enough
+          // that the issuing thread's instruction count shows.
+          uint32_t w_lo = ring_lo + static_cast<uint32_t>((stage * stage_bytes + a_bytes) >> 4);  // B rows
+          uint32_t x_lo = ring_lo + static_cast<uint32_t>((stage * stage_bytes) >> 4);            // A rows
+          uint32_t accumulate = kb0 != 0;  // accumulator k mod nacc starts at the part's first group
+          // planes is a multiple of G: each group of G planes is one
+          // 128-row B operand (G slots) and one 16 G-row A operand
+          for (int j = 0; j < planes; j += G) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const uint64_t wd = smem_desc_sw128(w_addr + 32 * k);
-              const uint64_t xd = smem_desc_sw128(x_addr + 32 * k);
-              const uint32_t accumulate_k = (kb0 | j) != 0;  // accumulator k starts at the part's first plane
+              const uint64_t wd = desc_sw128_from_lo(w_lo + 2 * k);
+              const uint64_t xd = desc_sw128_from_lo(x_lo + 2 * k);
+              const uint32_t a = static_cast<uint32_t>(k & (nacc - 1));
+              const uint32_t accumulate_k = accumulate | (k >= nacc ? 1u : 0u);
               if constexpr (FP8)
-                umma_e4m3(d_tmem + 16 * k, wd, xd, idesc, accumulate_k);
+                umma_e4m3(d_tmem + a * 16 * G, wd, xd, idesc, accumulate_k);
               else
-                umma_bf16(d_tmem + 16 * k, wd, xd, idesc, accumulate_k);
+                umma_bf16(d_tmem + a * 16 * G, wd, xd, idesc, accumulate_k);
             }
+            accumulate = 1;
+            w_lo += static_cast<uint32_t>((G * b_plane) >> 4);
+            x_lo += static_cast<uint32_t>((G * DEC_A_BOX_BYTES) >> 4);
           }
           issued_any = true;
           umma_commit(&empty[stage]);
@@ -196,8 +232,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lanes 32q .. 32q+31: rows 32q .. 32q+31 of the part
-    uint32_t acc = 0, acc_phase = 0;
+    const int q = warp & 3;  // TMEM lanes 32q .. 32q+31: rows 32q .. 32q+31 of the stacked operand
+    uint32_t acc = 0, acc_phase = 0, red_phase = 0;
     for (int part = blockIdx.x; part < p.parts; part += gridDim.x) {
       int r0, r1;
       part_rows(part, p.parts, p.n, r0, r1);
@@ -207,42 +243,107 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         break;
       }
       tc_fence_after_sync();
-      uint32_t r[16];
-      {
-        uint32_t r2[32];
-        const uint32_t t = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * DEC_ACC_COLS;
-        tmem_ld_32x32b_x32(t, r2);           // accumulators 0 and 1
-        tmem_ld_wait();
-        reg_fence(r2);
+      const uint32_t t = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * acc_cols;
+      if constexpr (!STACK) {
+        uint32_t r[16];
+        {
+          uint32_t r2[32];
+          tmem_ld_32x32b_x32(t, r2);           // accumulators 0 and 1
+          tmem_ld_wait();
+          reg_fence(r2);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r2[i]) + __uint_as_float(r2[16 + i]));
-        tmem_ld_32x32b_x32(t + 32, r2);      // accumulators 2 and 3
-        tmem_ld_wait();
-        reg_fence(r2);
+          for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r2[i]) + __uint_as_float(r2[16 + i]));
+          tmem_ld_32x32b_x32(t + 32, r2);      // accumulators 2 and 3
+          tmem_ld_wait();
+          reg_fence(r2);
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          r[i] = __float_as_uint(__uint_as_float(r[i]) + (__uint_as_float(r2[i]) + __uint_as_float(r2[16 + i])));
-      }
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
-      const int col = r0 + q * 32 + lane;   // column of C = row of B
-      if (col < r1) {
-        float sbv = 1.0f;
-        if constexpr (FP8) sbv = p.sb[col];
-        const float bv = p.bias ? p.bias[col] : 0.0f;
+          for (int i = 0; i < 16; ++i)
+            r[i] = __float_as_uint(__uint_as_float(r[i]) + (__uint_as_float(r2[i]) + __uint_as_float(r2[16 + i])));
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+        const int col = r0 + q * 32 + lane;   // column of C = row of B
+        if (col < r1) {
+          float sbv = 1.0f;
+          if constexpr (FP8) sbv = p.sb[col];
+          const float bv = p.bias ? p.bias[col] : 0.0f;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            if (i < p.m) {
+              float v = __uint_as_float(r[i]);
+              if constexpr (FP8) v = (v * p.sa[i]) * sbv;
+              v = apply_act(p.act, v + bv);
+              if constexpr (OUT_F32)
+                static_cast<float*>(p.C)[static_cast<int64_t>(i) * p.ldc + col] = v;
+              else
+                static_cast<__nv_bfloat16*>(p.C)[static_cast<int64_t>(i) * p.ldc + col] = __float2bfloat16_rn(v);
+            }
+          }
+        }
+      } else {
+        // ---- G slots of R rows: this lane's stacked row r is the part's row
+        // r mod R at the K steps of slot r / R, whose 16 sums sit in columns
+        // 16 (r / R) .. + 15 of each accumulator.  A warp's 32 rows span
+        // S = 32 / R slots when R < 32; nacc * S is 4 for every G.
+        const int R = 128 / G;
+        const int lgR = __ffs(R) - 1;
+        const int r = 32 * q + lane;
+        const int slot = r >> lgR;
+        const int S = R >= 32 ? 1 : 32 / R;
+        const int slot0 = (32 * q) >> lgR;
+        uint32_t x[4][16];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) tmem_ld_32x32b_x16(t + (u / S) * 16 * G + 16 * (slot0 + u % S), x[u]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int u = 0; u < 4; ++u) reg_fence16(x[u]);
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+        float* mine = red + r * DEC_RED_STRIDE;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          if (i < p.m) {
-            float v = __uint_as_float(r[i]);
-            if constexpr (FP8) v = (v * p.sa[i]) * sbv;
-            v = apply_act(p.act, v + bv);
+          float v = 0.0f;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) v += (slot == slot0 + u % S) ? __uint_as_float(x[u][i]) : 0.0f;
+          mine[i] = v;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&redbar[0]);
+        if (!__all_sync(0xffffffffu, mbar_wait(&redbar[0], red_phase))) {
+          fail = STATUS_TIMEOUT_EPILOGUE;
+          break;
+        }
+        // output (i, row): the sum of the G slots' partials, in slot order;
+        // consecutive threads take consecutive rows (columns of C)
+        const int rows = r1 - r0;
+        for (int idx = r; idx < (p.m << lgR); idx += 128) {
+          const int i = idx >> lgR;
+          const int pr = idx & (R - 1);
+          if (pr < rows) {
+            const float* src = red + pr * DEC_RED_STRIDE + i;
+            float v = src[0];
+            for (int sl = 1; sl < G; ++sl) v += src[sl * R * DEC_RED_STRIDE];
+            const int col = r0 + pr;
+            if constexpr (FP8) v = (v * p.sa[i]) * p.sb[col];
+            v = apply_act(p.act, v + (p.bias ? p.bias[col] : 0.0f));
             if constexpr (OUT_F32)
               static_cast<float*>(p.C)[static_cast<int64_t>(i) * p.ldc + col] = v;
             else
               static_cast<__nv_bfloat16*>(p.C)[static_cast<int64_t>(i) * p.ldc + col] = __float2bfloat16_rn(v);
           }
         }
+        if (part + static_cast<int>(gridDim.x) < p.parts) {
+          // every warp has read the partials before the next part's land
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&redbar[1]);
+          if (!__all_sync(0xffffffffu, mbar_wait(&redbar[1], red_phase))) {
+            fail = STATUS_TIMEOUT_EPILOGUE;
+            break;
+          }
+        }
+        red_phase ^= 1;
       }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
@@ -254,7 +355,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, DEC_TMEM_COLS);
+    tmem_dealloc(tmem_base, tmem_cols);
   }
 }
 

@@ -159,6 +159,7 @@ void fill_tc_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int
                   dgl_plan_info* out, int stream_k) {
   *out = dgl_plan_info{};
   out->path = DGL_PATH_TC;
+  out->k_group = 1;
   out->tile_m = tile_m;
   out->tile_n = tile_n;
   out->tile_k = tc_tile_k(dtype);
@@ -203,9 +204,11 @@ void fill_decode_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K,
   out->grid = decode_grid(n, num_sms);
   out->num_tiles = decode_parts(n, num_sms);
   const int nk = static_cast<int>((K * (dtype == DGL_DTYPE_E4M3 ? 1 : 2) + 127) / 128);
-  const int ks = decode_ksteps(out->tile_n, nk);
+  const int g = decode_group(out->tile_n, nk);
+  out->k_group = g;
+  const int ks = decode_ksteps(out->tile_n, nk, g);
   out->tile_k = ks * (dtype == DGL_DTYPE_E4M3 ? 128 : 64);
-  out->stages = decode_stages(out->tile_n, ks);
+  out->stages = decode_stages(out->tile_n, ks, g);
   out->tile_eff = static_cast<double>(m) / 16.0;
   out->wq_eff = static_cast<double>(out->num_tiles) /
                 (static_cast<double>((out->num_tiles + out->grid - 1) / out->grid) * out->grid);
@@ -213,19 +216,33 @@ void fill_decode_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K,
   out->est_us = operand_bytes(dtype, out_dtype, m, n, K) / (kHbmGBs * 1e3) + kLaunchUs;
 }
 
-int decode_plane_bytes(int rows_hi) { return (rows_hi + 7) / 8 * 8 * 128; }
+int decode_group(int rows_hi, int nk) {
+  // The largest G <= 16 (a power of two) with rows_hi <= 128 / G that divides
+  // the number of 128-byte K steps: G steps of a part fill one 128-row operand.
+  if (nk <= 0) return 1;
+  int g = 16;
+  while (g > 1 && (rows_hi > 128 / g || nk % g != 0)) g >>= 1;
+  return g;
+}
 
-int decode_stage_bytes(int rows_hi, int ksteps) { return ksteps * (2048 + decode_plane_bytes(rows_hi)); }
+int decode_plane_bytes(int rows_hi, int group) {
+  return (group > 1 ? 128 / group : (rows_hi + 7) / 8 * 8) * 128;
+}
 
-int decode_stages(int rows_hi, int ksteps) {
-  const int s = 196608 / decode_stage_bytes(rows_hi, ksteps);
+int decode_stage_bytes(int rows_hi, int ksteps, int group) {
+  return ksteps * (2048 + decode_plane_bytes(rows_hi, group));
+}
+
+int decode_stages(int rows_hi, int ksteps, int group) {
+  const int s = 196608 / decode_stage_bytes(rows_hi, ksteps, group);
   return s < 32 ? s : 32;
 }
 
-int decode_ksteps(int rows_hi, int nk) {
-  // the widest stage that still leaves at least four in the ring
-  int ks = 8;
-  while (ks > 1 && decode_stages(rows_hi, ks) < 4) ks >>= 1;
+int decode_ksteps(int rows_hi, int nk, int group) {
+  // the widest stage (a multiple of the group) that still leaves at least
+  // four in the ring
+  int ks = group > 8 ? group : 8;
+  while (ks > group && decode_stages(rows_hi, ks, group) < 4) ks >>= 1;
   return ks < nk ? ks : (nk > 0 ? nk : 1);
 }
 
@@ -235,6 +252,7 @@ int decode_ksteps(int rows_hi, int nk) {
 void fill_mx_plan(int out_dtype, int64_t m, int64_t n, int64_t K, int num_sms, dgl_plan_info* out) {
   *out = dgl_plan_info{};
   out->path = DGL_PATH_TC;
+  out->k_group = 1;
   out->tile_m = 128;
   out->tile_n = 256;
   out->tile_k = 256;

@@ -22,10 +22,12 @@ bool stream_k_eligible(int64_t m, int64_t n, int64_t K, int dtype, int tile_m, i
 void fill_decode_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int num_sms, dgl_plan_info* out);
 int decode_parts(int64_t n, int num_sms);
 int decode_grid(int64_t n, int num_sms);
-int decode_plane_bytes(int rows_hi);               // one B box: rows_hi rounded up to 8, x 128 bytes
-int decode_stage_bytes(int rows_hi, int ksteps);   // ksteps x (16-row A box + B box)
-int decode_stages(int rows_hi, int ksteps);        // ring depth in 192 KB, at most 32
-int decode_ksteps(int rows_hi, int nk);            // 128-byte K steps per stage
+int decode_group(int rows_hi, int nk);                         // K steps stacked into one 128-row MMA operand
+int decode_plane_bytes(int rows_hi, int group);               // one B slot: 128 / group rows (group 1: rows_hi
+                                                              // rounded up to 8), x 128 bytes
+int decode_stage_bytes(int rows_hi, int ksteps, int group);   // ksteps x (16-row A box + B slot)
+int decode_stages(int rows_hi, int ksteps, int group);        // ring depth in 192 KB, at most 32
+int decode_ksteps(int rows_hi, int nk, int group);            // 128-byte K steps per stage, a multiple of group
 // Tiles with a linear-layer epilogue variant: 128 or 256 wide, and CTA pairs
 // (tile_m 256) when gated.
 bool tc_supported_epi_tile(int tile_m, int tile_n, bool gated);

@@ -195,6 +195,16 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   return d;
 }
 
+// The descriptor's low 32-bit word alone (address field and the unused
+// leading offset); the high word is the same for every K-major 128-byte
+// swizzle tile.  Shared addresses stay below 256 KB, so adding a multiple of
+// 16 bytes >> 4 to the low word never carries out of the 14-bit field.
+__device__ __forceinline__ uint32_t smem_desc_sw128_lo(uint32_t saddr) { return ((saddr >> 4) & 0x3FFF) | (1u << 16); }
+__device__ __forceinline__ uint64_t desc_sw128_from_lo(uint32_t lo) {
+  constexpr uint32_t hi = (1024 >> 4) | (1u << 14) | (2u << 29);  // bits 32-45, 46, 61-63
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
 // The same for an MN-major operand tile (stored [K][MN], MN contiguous) as TMA
 // writes it from boxes of 64 MN elements (128 bytes) by 64 K rows with the
 // 128-byte swizzle: an atom is 8 K rows of 128 bytes (1024 bytes); atoms
@@ -356,6 +366,17 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
       : "memory");
 }
 
+// 32 lanes x 16 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
 // 32 lanes x 32 consecutive 32-bit columns, registers -> tensor memory.
 __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
@@ -382,6 +403,12 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
                  "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
                  "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
                  "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
+}
+__device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]));
 }
 
 // 2-D tiled store of one box from shared memory (bulk-group completion).

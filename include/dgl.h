@@ -102,6 +102,8 @@ typedef struct {
   int32_t split_tail; /* 1: the last, partial wave's tiles (tile_n 256) run as two half tiles each, */
                       /*    when that wave fills at most half the workers (not with stream_k or gated); */
                       /*    the planner sets it only for K of at most 16 k-blocks of 128 bytes */
+  int32_t k_group;    /* decode path: 128-byte K steps stacked into one 128-row MMA operand (1, 2, 4, */
+                      /*    8 or 16: parts of at most 128 / k_group rows); 1 on the tcgen05 tile path */
 } dgl_plan_info;
 
 /*

@@ -106,6 +106,14 @@ def test_decode_bias_activation(m):
     _full(case, _bias(777), dgl.ACT_SILU, False, guard_rows=1, pad_cols=1)
 
 
+@pytest.mark.parametrize("dtype,k", [("bf16", 512), ("fp8", 1024)])
+def test_decode_stacked_bias_activation(dtype, k):
+    """The decode epilogue after the G-slot sum (777 columns in parts of 6 rows: G = 8)."""
+    case = _case(dtype, 5, 777, k, "bf16", False)
+    assert dgl.dgl_plan(0 if dtype == "bf16" else 1, 5, 777, k).k_group == 8
+    _full(case, _bias(777), dgl.ACT_GELU, False, guard_rows=1, pad_cols=1)
+
+
 @pytest.mark.parametrize("act", ["gelu", "silu"])
 def test_e4m3_scaled_bias_activation(act):
     case = _case("fp8", 260, 384, 256, "bf16", False)

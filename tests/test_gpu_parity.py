@@ -179,6 +179,27 @@ def test_decode_every_m(m, out):
     _full(make_case("bf16", m, 1001, 264, out=out), guard_rows=1, pad_cols=3)
 
 
+@pytest.mark.parametrize("dtype,n,k,g", [("bf16", 1100, 1024, 16), ("bf16", 2000, 512, 8), ("bf16", 4000, 1024, 4),
+                                         ("bf16", 9000, 512, 2), ("fp8", 1100, 2048, 16), ("fp8", 4000, 2048, 4)])
+@pytest.mark.parametrize("m,out", [(1, "bf16"), (7, "f32"), (16, "bf16")])
+def test_decode_stacked_k_steps(dtype, n, k, g, m, out):
+    """Parts of at most 128 / G rows: G K steps share one MMA and the epilogue
+    adds the G diagonal blocks (every G, ragged parts since 152 divides no n)."""
+    assert dgl.dgl_plan(0 if dtype == "bf16" else 1, m, n, k).k_group == g
+    case = make_case(dtype, m, n, k, out=out, dist="fp8" if dtype == "fp8" else "normal")
+    _full(case, guard_rows=1, pad_cols=3)
+
+
+@pytest.mark.parametrize("n,k,grid", [(2000, 512, 7), (1100, 1024, 3), (9000, 512, 64)])
+def test_decode_stacked_many_parts_per_cta(n, k, grid):
+    """A forced small grid: each CTA walks many parts, so the shared-memory
+    partial sums and both TMEM buffers are reused; integer inputs, exact."""
+    case = make_case("bf16", 9, n, k, out="f32", dist="int")
+    Cbuf, intact = gu.run(case, plan=dgl.PlanInfo(path=dgl.PATH_DECODE, grid=grid), guard_rows=1, pad_cols=1)
+    assert intact
+    gu.assert_exact(case, gu.host_valid(case, Cbuf))
+
+
 @pytest.mark.parametrize("m,n,k", [(1, 11008, 4096), (8, 4096, 4096), (16, 4096, 4096), (3, 16, 8)])
 def test_decode_full_shapes(m, n, k):
     """The decode shapes of the benchmarks at full size (sampled), and K = 8."""

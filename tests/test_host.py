@@ -113,6 +113,26 @@ def test_plan_decode_threshold(dgl):
     assert dgl.dgl_plan(0, 0, 10, 10, num_sms=152).path == dgl.PATH_EMPTY
 
 
+@pytest.mark.parametrize("dtype,n,k,want", [(0, 11008, 4096, 1), (0, 4096, 4096, 4), (0, 1100, 1024, 16),
+                                             (0, 2000, 512, 8), (0, 9000, 512, 2), (0, 1001, 264, 1),
+                                             (0, 300, 8192, 16), (0, 300, 4104, 1), (1, 4000, 2048, 4),
+                                             (1, 11008, 4096, 1), (0, 50257, 64, 1)])
+def test_plan_decode_k_group(dgl, dtype, n, k, want):
+    """Decode parts of at most 128 / G rows stack G 128-byte K steps into one
+    128-row MMA operand: G is the largest power of two <= 16 whose slots hold
+    the part and that divides the step count; each ring stage is whole groups."""
+    p = dgl.dgl_plan(dtype, 8, n, k, num_sms=152)
+    assert p.path == dgl.PATH_DECODE
+    assert p.k_group == want
+    nk = -(-k * (1 if dtype == 1 else 2) // 128)
+    g = p.k_group
+    assert p.tile_n <= 128 // g and nk % g == 0
+    assert g == 16 or p.tile_n > 128 // (2 * g) or nk % (2 * g) != 0
+    ks = p.tile_k // (128 if dtype == 1 else 64)
+    assert ks % g == 0 and p.stages >= 2
+    assert dgl.dgl_plan(0, 600, 600, 600, num_sms=152).k_group == 1
+
+
 @pytest.mark.parametrize("m,n,k", [(48, 4096, 48), (333, 4096, 1024), (528, 528, 1024), (3402, 4096, 1024),
                                    (1024, 50257, 512), (2048, 11007, 1024), (4095, 4095, 1024),
                                    (597, 11008, 4096), (4096, 4096, 4096), (8192, 8192, 8192), (17, 5, 64)])
