@@ -405,6 +405,15 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       const uint32_t idesc_major = (p.a_mn ? 1u << 15 : 0u) | (p.b_mn ? 1u << 16 : 0u);
       const uint32_t idesc_full = idesc_f32acc(Cfg::FP8 ? 0u : 1u, Cfg::TILE_M, BN) | idesc_major;
       const uint32_t idesc_half = idesc_f32acc(Cfg::FP8 ? 0u : 1u, Cfg::TILE_M, BN / 2) | idesc_major;
+      // Shared-memory descriptors differ only in their low word: the address
+      // field (bits 0-13) and the leading offset (bits 16-29: unused for a
+      // K-major tile, 8192 bytes between an MN-major tile's 64-element
+      // boxes).  Each MMA's pair is then two 32-bit adds, which keeps the
+      // single issuing thread ahead of the tensor pipe.
+      const uint32_t a_lo0 = smem_desc_sw128_lo(smem_u32(sA)) + (p.a_mn ? ((8192u >> 4) - 1u) << 16 : 0u);
+      const uint32_t b_lo0 = smem_desc_sw128_lo(smem_u32(sB)) + (p.b_mn ? ((8192u >> 4) - 1u) << 16 : 0u);
+      const uint32_t a_kstep = (p.a_mn ? MN_K_STEP_BYTES : Cfg::MMA_K_BYTES) >> 4;
+      const uint32_t b_kstep = (p.b_mn ? MN_K_STEP_BYTES : Cfg::MMA_K_BYTES) >> 4;
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool issued_any = false;
       SegmentIter it(cluster_id, p.workers, p.num_kb, p.dp_tiles, p.sk_units, p.half_tiles);
@@ -435,15 +444,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             for (int a = 0; a < Cfg::SCALE_ATOMS; ++a)
               tmem_cp_32x128b_warpx4(tcol + 4 * a, smem_desc_rows16(sc + 512 * a));
           }
-          const uint32_t a_addr = smem_u32(sA + stage * Cfg::A_STAGE_BYTES);
-          const uint32_t b_addr = smem_u32(sB + stage * Cfg::B_STAGE_BYTES);
+          const uint32_t a_lo = a_lo0 + static_cast<uint32_t>((stage * Cfg::A_STAGE_BYTES) >> 4);
+          const uint32_t b_lo = b_lo0 + static_cast<uint32_t>((stage * Cfg::B_STAGE_BYTES) >> 4);
+          const uint32_t acc_first = kb != sg.kb0 ? 1u : 0u;
 #pragma unroll
           for (int k = 0; k < Cfg::MMAS_PER_STAGE; ++k) {
-            const uint64_t ad = p.a_mn ? smem_desc_sw128_mn(a_addr + k * MN_K_STEP_BYTES)
-                                       : smem_desc_sw128(a_addr + k * Cfg::MMA_K_BYTES);
-            const uint64_t bd = p.b_mn ? smem_desc_sw128_mn(b_addr + k * MN_K_STEP_BYTES)
-                                       : smem_desc_sw128(b_addr + k * Cfg::MMA_K_BYTES);
-            const uint32_t accumulate = (kb != sg.kb0 || k != 0) ? 1u : 0u;
+            const uint64_t ad = desc_sw128_from_lo(a_lo + k * a_kstep);
+            const uint64_t bd = desc_sw128_from_lo(b_lo + k * b_kstep);
+            const uint32_t accumulate = k != 0 ? 1u : acc_first;
             if constexpr (CG == 2) {
               if constexpr (Cfg::FP8)
                 umma_e4m3_pair(d_tmem, ad, bd, idesc, accumulate);
