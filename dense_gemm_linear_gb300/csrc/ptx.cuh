@@ -297,6 +297,16 @@ __device__ __forceinline__ uint64_t smem_desc_rows16(uint32_t saddr) {
   return d;
 }
 
+// The same descriptor from its low word (address field and leading offset);
+// the high word is the same for every such matrix.
+__device__ __forceinline__ uint32_t smem_desc_rows16_lo(uint32_t saddr) {
+  return ((saddr >> 4) & 0x3FFF) | ((128u >> 4) << 16);
+}
+__device__ __forceinline__ uint64_t desc_rows16_from_lo(uint32_t lo) {
+  constexpr uint32_t hi = (128 >> 4) | (1u << 14);  // bits 32-45, 46
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
 // Copy a 32-row x 128-bit matrix from shared memory into tensor memory at
 // taddr (4 consecutive 32-bit columns), once into each of the four 32-lane
 // quarters: lane 32 w + r, column c + j receives bytes 4 j .. 4 j + 3 of row r.

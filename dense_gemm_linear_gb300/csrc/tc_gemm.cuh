@@ -412,6 +412,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       // single issuing thread ahead of the tensor pipe.
       const uint32_t a_lo0 = smem_desc_sw128_lo(smem_u32(sA)) + (p.a_mn ? ((8192u >> 4) - 1u) << 16 : 0u);
       const uint32_t b_lo0 = smem_desc_sw128_lo(smem_u32(sB)) + (p.b_mn ? ((8192u >> 4) - 1u) << 16 : 0u);
+      const uint32_t sc_lo0 = Cfg::MX ? smem_desc_rows16_lo(smem_u32(sSc)) : 0u;  // MX scale atoms
       const uint32_t a_kstep = (p.a_mn ? MN_K_STEP_BYTES : Cfg::MMA_K_BYTES) >> 4;
       const uint32_t b_kstep = (p.b_mn ? MN_K_STEP_BYTES : Cfg::MMA_K_BYTES) >> 4;
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
@@ -438,11 +439,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           if constexpr (Cfg::MX) {
             // the stage's 512-byte scale atoms into its tensor-memory slot,
             // atom a to columns 4 a .. 4 a + 3; the MMAs below run after
-            const uint32_t sc = smem_u32(sSc + stage * Cfg::SCALE_STAGE_BYTES);
+            const uint32_t sc_lo = sc_lo0 + static_cast<uint32_t>((stage * Cfg::SCALE_STAGE_BYTES) >> 4);
             const uint32_t tcol = tmem_base + Cfg::SCALE_COL0 + stage * Cfg::SCALE_SLOT_COLS;
 #pragma unroll
             for (int a = 0; a < Cfg::SCALE_ATOMS; ++a)
-              tmem_cp_32x128b_warpx4(tcol + 4 * a, smem_desc_rows16(sc + 512 * a));
+              tmem_cp_32x128b_warpx4(tcol + 4 * a, desc_rows16_from_lo(sc_lo + 32 * a));
           }
           const uint32_t a_lo = a_lo0 + static_cast<uint32_t>((stage * Cfg::A_STAGE_BYTES) >> 4);
           const uint32_t b_lo = b_lo0 + static_cast<uint32_t>((stage * Cfg::B_STAGE_BYTES) >> 4);
