@@ -58,7 +58,7 @@ constexpr Pin kPins[] = {
     {DGL_DTYPE_BF16, 2048, 2048, 2048, 128, 256},  // one wave either way; 17.9 us vs 19.7 us
     {DGL_DTYPE_BF16, 48, 4096, 48, 128, 128},      // 4.2-4.4 us vs 4.5-4.9 us (128x256)
     {DGL_DTYPE_BF16, 528, 528, 1024, 128, 64},     // 8.2 us vs 8.6-8.7 us (128x128), 9.5 us (256x128)
-    {DGL_DTYPE_BF16, 3402, 4096, 1024, 128, 256},  // 21.4 us vs 22.2 us (256x256)
+    {DGL_DTYPE_BF16, 3402, 4096, 1024, 256, 256},  // 21.7 us vs 22.9 us (128x256)
     {DGL_DTYPE_BF16, 597, 11008, 4096, 256, 256},  // 47.0 us vs 54.9 us (128x256, the screen's pick)
     {DGL_DTYPE_E4M3, 597, 11008, 4096, 256, 256},  // 30.4 us vs 33.4 us
 };
