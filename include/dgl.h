@@ -15,9 +15,10 @@
  * B[N,K]^T, and the epilogue value = acc * scale_a * scale_b, follow the
  * "Gemm Optimization" guide (sections 1.1 "Three-Level Tiling" and 7.1
  * "Direct Store").  m_valid / n_valid are the real extents behind a tiled
- * problem, as in FlyDSL pull request 1303 (RDNA3 WMMA GEMM: "m_valid/n_valid
- * parameters: build over whole tiles and tell the kernel how much of the last
- * one is real"); passing 0 selects the full extent, the old behaviour.
+ * problem, as in FlyDSL pull request 1303 (RDNA3 WMMA GEMM): the caller sizes
+ * the problem in whole tiles and these two arguments say how many rows and
+ * columns of the last tile hold data; passing 0 selects the full extent, the
+ * old behaviour.
  *
  * Layout (all row-major, last dimension contiguous -- flattening is free only
  * when it is, "GEMM analysis in TraceLens", section "Edge cases"):
@@ -93,7 +94,7 @@ typedef struct {
   int32_t stages;     /* shared-memory ring depth */
   int32_t cta_group;  /* CTAs sharing one MMA: 1, or 2 (a CTA pair, tile_m 256) */
   int32_t grid;       /* CTAs launched (persistent: at most one per SM) */
-  int32_t num_tiles;  /* output tiles (tcgen05 path) or 8-row groups (decode path) */
+  int32_t num_tiles;  /* output tiles (tcgen05 path) or parts of B's rows (decode path) */
   double tile_eff;
   double wq_eff;
   double dim_eff;
@@ -129,11 +130,12 @@ dgl_status dgl_gemm_fp8(const void* A, const void* B, const float* sa, const flo
 
 /*
  * Either GEMM with a caller-chosen plan instead of the planner's choice: the
- * forced-tile sweep of FlyDSL pull request 1303 ("a second test runs every
- * tile of both ladders against a shape that divides none of them").
+ * forced-tile sweep of FlyDSL pull request 1303, whose tests run each tile of
+ * both ladders on a shape that no tile divides.
  * dtype: dgl_dtype_t (sa/sb ignored for bf16).  plan->path, tile_m, tile_n,
  * stream_k, split_tail and grid are honoured (grid <= 0 picks one), and for the decode
- * path tile_k (K elements per ring stage, a multiple of 128 bytes, 0 = pick);
+ * path tile_k (K elements per ring stage: a multiple of 128 bytes and of
+ * k_group such steps, 0 = pick);
  * other fields are ignored.  A plan the library has no kernel for returns
  * DGL_ERR_UNSUPPORTED.
  */
