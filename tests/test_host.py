@@ -24,7 +24,8 @@ def dgl():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    with open(HEADER) as f:
+        text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(dgl_[a-z0-9_]+)\s*\(", text)))
 

@@ -76,7 +76,8 @@ MUTANTS = {
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_pins_reject_mutant(tmp_path, name):
     old, new = MUTANTS[name]
-    src = open(SRC).read()
+    with open(SRC) as f:
+        src = f.read()
     assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
     mutant_src = tmp_path / f"{name}.c"
     mutant_src.write_text(src.replace(old, new))
