@@ -227,6 +227,24 @@ def run_reference(args):
     return 0
 
 
+def over_ranks(ms_per_step, step_flops, dist=None, device=None):
+    """The job's step time and throughput from each rank's own step time.
+
+    Every rank runs the whole step on its own GPU (replicas, no data-path
+    collective), so the job does `world` steps' work in the slowest rank's
+    time: returns (max over ranks of ms_per_step, TFLOP/s of the whole job).
+    dist: torch.distributed when initialised, else None (one process)."""
+    world = 1
+    ms_max = ms_per_step
+    if dist is not None:
+        import torch
+        world = dist.get_world_size()
+        t = torch.tensor([ms_per_step], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    return ms_max, step_flops * world / (ms_max * 1e-3) / 1e12
+
+
 def shape_entry(text):
     parts = text.split(",")
     m, n, k = (int(v) for v in parts[:3])
@@ -432,13 +450,7 @@ def main():
     per_call_ms = [v / K_steps for v in per_call_ms]
 
     step_flops = sum(flops)
-    if dist is not None:
-        t = torch.tensor([ms_per_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
-    else:
-        ms_max = ms_per_step
-    value = step_flops * world / (ms_max * 1e-3) / 1e12
+    ms_max, value = over_ranks(ms_per_step, step_flops, dist, dev)
 
     # ---------------------------------------------------------- context: torch.matmul (cuBLAS), off the measured path
     # Each plain bf16 GEMM of the step is timed once more through torch.matmul
@@ -584,12 +596,8 @@ def main():
             stream.wait_event(ev)
         e1.record(stream)
         barrier()
-        e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-        if dist is not None:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": step_flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e_ms, e2e_value = over_ranks(e0.elapsed_time(e1) / args.e2e_steps, step_flops, dist, dev)
+        e2e = {"value": e2e_value, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                "steps": args.e2e_steps}
 
