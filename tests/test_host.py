@@ -134,6 +134,31 @@ def test_plan_decode_k_group(dgl, dtype, n, k, want):
     assert dgl.dgl_plan(0, 600, 600, 600, num_sms=152).k_group == 1
 
 
+def test_plan_decode_invariants_sweep(dgl):
+    """Over a seeded sweep of n and K: parts of at most 128 / G rows, G a power
+    of two dividing the 128-byte K steps, whole groups per ring stage, and the
+    ring within its 192 KB with at least two stages."""
+    import numpy as np
+    rng = np.random.default_rng(11)
+    for _ in range(400):
+        dtype = int(rng.integers(0, 2))
+        n = int(rng.integers(1, 60000))
+        K = int(rng.integers(1, 1200)) * 16
+        p = dgl.dgl_plan(dtype, int(rng.integers(1, 17)), n, K, num_sms=152)
+        assert p.path == dgl.PATH_DECODE
+        g = p.k_group
+        assert g in (1, 2, 4, 8, 16)
+        nk = -(-K * (1 if dtype == 1 else 2) // 128)
+        assert nk % g == 0
+        assert p.tile_n <= 128 // g
+        parts = p.num_tiles
+        assert 1 <= parts <= n and p.tile_n == -(-n // parts)  # balanced parts of at most ceil(n / parts) rows
+        ks = p.tile_k // (128 if dtype == 1 else 64)
+        assert ks >= 1 and ks % g == 0 and ks <= max(nk, 1)
+        slot_rows = 128 // g if g > 1 else -(-p.tile_n // 8) * 8
+        assert p.stages >= 2 and p.stages * ks * (2048 + slot_rows * 128) <= 196608
+
+
 @pytest.mark.parametrize("m,n,k", [(48, 4096, 48), (333, 4096, 1024), (528, 528, 1024), (3402, 4096, 1024),
                                    (1024, 50257, 512), (2048, 11007, 1024), (4095, 4095, 1024),
                                    (597, 11008, 4096), (4096, 4096, 4096), (8192, 8192, 8192), (17, 5, 64)])
