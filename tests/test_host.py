@@ -134,6 +134,17 @@ def test_plan_decode_k_group(dgl, dtype, n, k, want):
     assert dgl.dgl_plan(0, 600, 600, 600, num_sms=152).k_group == 1
 
 
+@pytest.mark.parametrize("dtype,m,n,k,tile", [(0, 1024, 50257, 512, (128, 256)), (0, 2048, 2048, 2048, (128, 256)),
+                                              (0, 48, 4096, 48, (128, 128)), (0, 528, 528, 1024, (128, 64)),
+                                              (0, 3402, 4096, 1024, (256, 256)), (0, 597, 11008, 4096, (256, 256)),
+                                              (1, 597, 11008, 4096, (256, 256))])
+def test_plan_measured_pins(dgl, dtype, m, n, k, tile):
+    """Shapes whose best tile was measured on GB300 take that tile."""
+    p = dgl.dgl_plan(dtype, m, n, k, num_sms=152)
+    assert p.path == dgl.PATH_TC and (p.tile_m, p.tile_n) == tile
+    assert p.cta_group == (2 if tile[0] == 256 else 1)
+
+
 def test_plan_decode_invariants_sweep(dgl):
     """Over a seeded sweep of n and K: parts of at most 128 / G rows, G a power
     of two dividing the 128-byte K steps, whole groups per ring stage, and the
