@@ -1,6 +1,7 @@
 """Reference oracle for C = A . B^T (bf16 and E4M3 inputs, fp64 arithmetic),
-for the linear layer around it (bias, GELU / SiLU, gated up projection), and
-for the block-scaled FP4 (MXFP4) product.
+for the linear layer around it (bias, GELU / SiLU, gated up projection), for
+the block-scaled FP4 (MXFP4) product, and for E4M3 activations times E2M1
+weights (W4A8).
 
 TEST INFRASTRUCTURE ONLY.  The product library never imports this package;
 only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
@@ -78,6 +79,10 @@ def _bind(lib):
     lib.oracle_mxfp4_gemm.restype = ctypes.c_int
     lib.oracle_mxfp4_gemm_points.argtypes = [vp, vp, vp, vp, c_i64, c_i64, c_i64, vp, vp, c_i64, vp, vp]
     lib.oracle_mxfp4_gemm_points.restype = ctypes.c_int
+    lib.oracle_w4a8_gemm.argtypes = [vp, vp, vp, vp, c_i64, c_i64, c_i64, vp, vp]
+    lib.oracle_w4a8_gemm.restype = ctypes.c_int
+    lib.oracle_w4a8_gemm_points.argtypes = [vp, vp, vp, vp, c_i64, c_i64, c_i64, vp, vp, c_i64, vp, vp]
+    lib.oracle_w4a8_gemm_points.restype = ctypes.c_int
     lib.oracle_threads.argtypes = []
     lib.oracle_threads.restype = ctypes.c_int
     return lib
@@ -289,6 +294,51 @@ def mxfp4_gemm_points(A, B, EA, EB, rows, cols, lib=None):
     if lib.oracle_mxfp4_gemm_points(_ptr(A), _ptr(B), _ptr(EA), _ptr(EB), m, n, K, _ptr(rows), _ptr(cols),
                                     rows.size, _ptr(C), _ptr(S)) != 0:
         raise ValueError("oracle_mxfp4_gemm_points rejected its arguments")
+    return C, S
+
+
+def _w4a8_inputs(A, B, sa, sb):
+    A = np.ascontiguousarray(A)
+    B = np.ascontiguousarray(B)
+    if A.dtype != np.uint8 or B.dtype != np.uint8 or A.ndim != 2 or B.ndim != 2:
+        raise TypeError("W4A8 operands are 2-D uint8 arrays")
+    m, K = A.shape
+    n = B.shape[0]
+    if B.shape[1] * 2 != K:
+        raise ValueError("B holds K / 2 bytes per row (two E2M1 codes a byte)")
+    sa = np.ascontiguousarray(sa, dtype=np.float32)
+    sb = np.ascontiguousarray(sb, dtype=np.float32)
+    if sa.shape != (m,) or sb.shape != (n,):
+        raise ValueError("scale lengths must be m and n")
+    return A, B, sa, sb, m, n, K
+
+
+def w4a8_gemm(A, B, sa, sb, lib=None):
+    """Full reference W4A8 product: A [m, K] E4M3 codes, B [n, K/2] packed E2M1
+    codes (element 2t in the low four bits of byte t), sa [m], sb [n] fp32.
+    Returns (C_ref, S_abs), float64 [m, n]."""
+    lib = lib or load()
+    A, B, sa, sb, m, n, K = _w4a8_inputs(A, B, sa, sb)
+    C = np.empty((m, n), dtype=np.float64)
+    S = np.empty((m, n), dtype=np.float64)
+    if lib.oracle_w4a8_gemm(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), m, n, K, _ptr(C), _ptr(S)) != 0:
+        raise ValueError("oracle_w4a8_gemm rejected its arguments")
+    return C, S
+
+
+def w4a8_gemm_points(A, B, sa, sb, rows, cols, lib=None):
+    """Reference W4A8 values at the points (rows[p], cols[p]); returns (C_ref, S_abs)."""
+    lib = lib or load()
+    A, B, sa, sb, m, n, K = _w4a8_inputs(A, B, sa, sb)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    cols = np.ascontiguousarray(cols, dtype=np.int64)
+    if rows.shape != cols.shape:
+        raise ValueError("rows and cols differ in length")
+    C = np.empty(rows.shape, dtype=np.float64)
+    S = np.empty(rows.shape, dtype=np.float64)
+    if lib.oracle_w4a8_gemm_points(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), m, n, K, _ptr(rows), _ptr(cols),
+                                   rows.size, _ptr(C), _ptr(S)) != 0:
+        raise ValueError("oracle_w4a8_gemm_points rejected its arguments")
     return C, S
 
 

@@ -417,6 +417,80 @@ int oracle_mxfp4_gemm_points(const uint8_t* A, const uint8_t* B, const uint8_t* 
     return 0;
 }
 
+/*
+ * ---- 8-bit activations, 4-bit weights (W4A8) ----------------------------------
+ *
+ * The "Gemm Optimization" guide's bandwidth formulas (section 8.2) give, for
+ * its "INT4" case, one byte per element of A, half a byte per element of B,
+ * a bf16 C and (M + N) fp32 scales: 8-bit activations with a per-token scale
+ * and 4-bit weights with a per-output-channel scale.  Reading taken: A holds
+ * E4M3 codes (the 8-bit type the FP8/INT8 formula above it counts) with a
+ * per-row scale sa; B holds 4-bit E2M1 codes, two per byte (element 2t in the
+ * low four bits of byte t), with a per-row scale sb (one per column of C):
+ *   C[i,j] = sa[i] * sb[j] * sum_k e4m3(A[i,k]) * e2m1(B[j,k])
+ * in the order of the E4M3 product above (the sum first, then sa * sb).
+ * A: m rows of K bytes; B: n rows of K / 2 bytes; K even.
+ */
+static double w4_value(const uint8_t* B, int64_t K, int64_t j, int64_t k)
+{
+    uint8_t byte = B[j * (K / 2) + k / 2];
+    return oracle_decode_e2m1((k % 2 == 0) ? (uint8_t)(byte & 0xF) : (uint8_t)(byte >> 4));
+}
+
+static void w4a8_element(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb, int64_t K,
+                         int64_t i, int64_t j, double* c_out, double* s_out)
+{
+    double acc = 0.0, mag = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        double p = oracle_decode_e4m3(A[i * K + k]) * w4_value(B, K, j, k);
+        acc += p;
+        mag += fabs(p);
+    }
+    const double scale = (double)sa[i] * (double)sb[j];
+    *c_out = acc * scale;
+    *s_out = mag * fabs(scale);
+}
+
+/*
+ * Full W4A8 product over the valid region: A [m][K] E4M3 codes, B [n][K/2]
+ * packed E2M1 codes, sa [m], sb [n] fp32 scales; C_ref and S_abs [m*n]
+ * row-major (S_abs may be NULL).  Returns 0, or -1 on a bad argument.
+ */
+int oracle_w4a8_gemm(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb,
+                     int64_t m, int64_t n, int64_t K, double* C_ref, double* S_abs)
+{
+    if (!A || !B || !sa || !sb || !C_ref || m < 0 || n < 0 || K < 0 || K % 2 != 0) return -1;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < m; ++i) {
+        for (int64_t j = 0; j < n; ++j) {
+            double c, s;
+            w4a8_element(A, B, sa, sb, K, i, j, &c, &s);
+            C_ref[i * n + j] = c;
+            if (S_abs) S_abs[i * n + j] = s;
+        }
+    }
+    return 0;
+}
+
+/* The W4A8 product at a list of (row, col) points; as oracle_gemm_points. */
+int oracle_w4a8_gemm_points(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb,
+                            int64_t m, int64_t n, int64_t K, const int64_t* rows, const int64_t* cols,
+                            int64_t npts, double* C_ref, double* S_abs)
+{
+    if (!A || !B || !sa || !sb || !C_ref || !rows || !cols || npts < 0 || m < 0 || n < 0 || K < 0 || K % 2 != 0)
+        return -1;
+    for (int64_t p = 0; p < npts; ++p)
+        if (rows[p] < 0 || rows[p] >= m || cols[p] < 0 || cols[p] >= n) return -1;
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t p = 0; p < npts; ++p) {
+        double c, s;
+        w4a8_element(A, B, sa, sb, K, rows[p], cols[p], &c, &s);
+        C_ref[p] = c;
+        if (S_abs) S_abs[p] = s;
+    }
+    return 0;
+}
+
 /* Threads an OpenMP region of this library uses (1 without OpenMP). */
 int oracle_threads(void)
 {

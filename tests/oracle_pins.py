@@ -416,12 +416,98 @@ def check_mx_points_match_full(lib):
     np.testing.assert_array_equal(Sp, S[rows, cols])
 
 
+# ------------------------------------------------------------ W4A8: E4M3 activations x E2M1 weights
+def _e4m3_values(codes):
+    """E4M3 codes -> float64 through torch's float8_e4m3fn (a library decoder)."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    return torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+
+
+def check_w4a8_nibble_order_and_scales(lib):
+    # A one-hot: row i holds 1.0 at k = i, so C[i, j] = sa[i] sb[j] e2m1(B[j, i]);
+    # element 2t of a B row is the low four bits of byte t
+    K = 32
+    A = np.zeros((4, K), dtype=np.uint8)
+    for i in range(4):
+        A[i, i] = E4M3_ONE
+    B = np.zeros((2, K // 2), dtype=np.uint8)
+    B[0, 0] = 0x61            # k = 0: 0.5 (code 1), k = 1: 4.0 (code 6)
+    B[0, 1] = 0xA7            # k = 2: 6.0 (code 7), k = 3: -1.0 (code 0xA)
+    B[1, 0] = 0x5D            # k = 0: -3.0 (code 0xD), k = 1: 3.0 (code 5)
+    B[1, 1] = 0x0F            # k = 2: -6.0 (code 0xF), k = 3: 0
+    sa = np.array([1.0, 2.0, 0.5, 4.0], dtype=np.float32)
+    sb = np.array([1.0, 0.25], dtype=np.float32)
+    C, S = oracle.w4a8_gemm(A, B, sa, sb, lib=lib)
+    vals = [[0.5, 4.0, 6.0, -1.0], [-3.0, 3.0, -6.0, 0.0]]
+    for i in range(4):
+        for j in range(2):
+            assert C[i, j] == sa[i] * sb[j] * vals[j][i], (i, j, C[i, j])
+            assert S[i, j] == abs(sa[i] * sb[j] * vals[j][i])
+
+
+def check_w4a8_brute_force(lib):
+    rng = np.random.default_rng(41)
+    for trial in range(10):
+        m, n = (int(x) for x in rng.integers(1, 6, size=2))
+        K = 2 * int(rng.integers(1, 40))
+        A = rng.integers(0, 256, size=(m, K), dtype=np.uint8)
+        A[(A & 0x7F) == 0x7F] = 0x3C          # no NaN codes
+        B = rng.integers(0, 256, size=(n, K // 2), dtype=np.uint8)
+        sa = (2.0 ** rng.integers(-3, 4, size=m)).astype(np.float32)
+        sb = (2.0 ** rng.integers(-3, 4, size=n)).astype(np.float32)
+        C, _ = oracle.w4a8_gemm(A, B, sa, sb, lib=lib)
+        Av = _e4m3_values(A)
+        Bc = _unpack(B)
+        for i in range(m):
+            for j in range(n):
+                want = sum((Fraction(float(Av[i, k])) * Fraction(_e2m1_value(int(Bc[j, k]))) for k in range(K)),
+                           Fraction(0)) * Fraction(float(sa[i])) * Fraction(float(sb[j]))
+                assert Fraction(C[i, j]) == want, (trial, i, j)
+
+
+def check_w4a8_matches_e4m3_product(lib):
+    # every E2M1 value is an E4M3 value: re-encoding B as E4M3 codes gives the
+    # same products in the same order, so the E4M3 product (pinned above)
+    # must agree bit for bit
+    rng = np.random.default_rng(43)
+    m, n, K = 7, 9, 96
+    A = rng.integers(0, 256, size=(m, K), dtype=np.uint8)
+    A[(A & 0x7F) == 0x7F] = 0xB8
+    B = rng.integers(0, 256, size=(n, K // 2), dtype=np.uint8)
+    sa = rng.uniform(0.5, 2.0, size=m).astype(np.float32)
+    sb = rng.uniform(0.5, 2.0, size=n).astype(np.float32)
+    Bv = np.vectorize(_e2m1_value)(_unpack(B))
+    B8 = torch.from_numpy(Bv.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert (_e4m3_values(B8) == Bv).all()
+    C, S = oracle.w4a8_gemm(A, B, sa, sb, lib=lib)
+    C8, S8 = oracle.gemm(oracle.E4M3, A, B8, sa, sb, lib=lib)
+    np.testing.assert_array_equal(C, C8)
+    np.testing.assert_array_equal(S, S8)
+
+
+def check_w4a8_points_match_full(lib):
+    rng = np.random.default_rng(47)
+    m, n, K = 11, 13, 64
+    A = rng.integers(0, 0x70, size=(m, K), dtype=np.uint8)
+    B = rng.integers(0, 256, size=(n, K // 2), dtype=np.uint8)
+    sa = rng.uniform(0.5, 2.0, size=m).astype(np.float32)
+    sb = rng.uniform(0.5, 2.0, size=n).astype(np.float32)
+    C, S = oracle.w4a8_gemm(A, B, sa, sb, lib=lib)
+    rows = np.array([0, m - 1, 3, 10])
+    cols = np.array([0, n - 1, 12, 5])
+    Cp, Sp = oracle.w4a8_gemm_points(A, B, sa, sb, rows, cols, lib=lib)
+    np.testing.assert_array_equal(Cp, C[rows, cols])
+    np.testing.assert_array_equal(Sp, S[rows, cols])
+
+
 ALL_CHECKS = [check_bf16_decoder, check_e4m3_decoder, check_round_bf16, check_identity,
               check_permutation, check_rank1, check_all_ones, check_scaled_rank1_e4m3,
               check_brute_force, check_points_match_full, check_act_closed_forms, check_linear_bias_onehot,
               check_linear_gated_onehot, check_linear_gated_scaled_e4m3, check_linear_points_match_full,
               check_e2m1_decoder, check_e8m0_decoder, check_mx_nibble_order, check_mx_block_scales,
-              check_mx_unit_scales_match_matmul, check_mx_brute_force, check_mx_points_match_full]
+              check_mx_unit_scales_match_matmul, check_mx_brute_force, check_mx_points_match_full,
+              check_w4a8_nibble_order_and_scales, check_w4a8_brute_force, check_w4a8_matches_e4m3_product,
+              check_w4a8_points_match_full]
 
 
 def run_all(lib):

@@ -70,6 +70,18 @@ MUTANTS = {
                           "return oracle_decode_e2m1(code);"),
     "mx_mag_signed": ("double p = mx_value(A, EA, K, i, k) * mx_value(B, EB, K, j, k);\n        acc += p;\n        mag += fabs(p);",
                       "double p = mx_value(A, EA, K, i, k) * mx_value(B, EB, K, j, k);\n        acc += p;\n        mag += p;"),
+    # W4A8: the weight nibble order (observable here: A is not packed), B's
+    # row pitch, dropped terms and scales, the magnitude sum
+    "w4_nibbles_swapped": ("return oracle_decode_e2m1((k % 2 == 0) ? (uint8_t)(byte & 0xF) : (uint8_t)(byte >> 4));",
+                           "return oracle_decode_e2m1((k % 2 == 1) ? (uint8_t)(byte & 0xF) : (uint8_t)(byte >> 4));"),
+    "w4_row_pitch_K": ("uint8_t byte = B[j * (K / 2) + k / 2];", "uint8_t byte = B[j * K + k / 2];"),
+    "w4_drop_first_k": ("for (int64_t k = 0; k < K; ++k) {\n        double p = oracle_decode_e4m3",
+                        "for (int64_t k = 1; k < K; ++k) {\n        double p = oracle_decode_e4m3"),
+    "w4_drop_last_k": ("for (int64_t k = 0; k < K; ++k) {\n        double p = oracle_decode_e4m3",
+                       "for (int64_t k = 0; k + 1 < K; ++k) {\n        double p = oracle_decode_e4m3"),
+    "w4_drop_sa": ("const double scale = (double)sa[i] * (double)sb[j];", "const double scale = (double)sb[j];"),
+    "w4_a_index_transposed": ("oracle_decode_e4m3(A[i * K + k])", "oracle_decode_e4m3(A[(k * K + i) % (K * (i + 1))])"),
+    "w4_mag_signed": ("*s_out = mag * fabs(scale);", "*s_out = acc * fabs(scale);"),
 }
 
 
