@@ -63,6 +63,8 @@ def parse_args():
                     help="multiply-adds of the bounded CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-context", action="store_true", help="skip the torch.matmul (cuBLAS) context column")
+    ap.add_argument("--no-headline", action="store_true",
+                    help="skip the headline shapes (4096^3 bf16 / E4M3, decode) timed one by one")
     return ap.parse_args()
 
 
@@ -352,8 +354,8 @@ def main():
                      c.n, out_dtype, s_handle)
             fn = lib.dgl_gemm_fp8
 
-        def call():
-            st = fn(*args_)
+        def call(s=s_handle):
+            st = fn(*args_[:-1], s)
             if st != 0:
                 raise RuntimeError(f"GEMM {c.name} failed: {dgl.status_string(st)}")
         return call
@@ -404,12 +406,18 @@ def main():
     if st != 0:
         raise RuntimeError(f"device status after warm-up: {dgl.status_string(st)}")
 
+    # One step captured as a CUDA graph: the ten calls' host work (argument
+    # checks, plan and tensor-map cache look-ups, launch) then leaves the timed
+    # loop, which replays the same launches back to back.
+    step_graph = capture_graph(torch, lambda s: [f(s) for f in calls])
+    launch_mode = "cuda graph of one step" if step_graph is not None else "stream launches"
+
     # ---------------------------------------------------------- device-timed region
     # Pass 1 times whole steps (the reported value): the calls go back to back,
     # so each kernel's launch and set-up can overlap the previous kernel's end
     # (programmatic dependent launch).  Pass 2 repeats the steps with an event
     # between calls, which serialises them, for each kernel's own duration
-    # (per_shape and roofline).
+    # (per-shape times and the roofline).
     K_steps = args.steps
     ncall = len(calls)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(ncall + 1)] for _ in range(K_steps)]
@@ -421,8 +429,11 @@ def main():
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for s in range(K_steps):
-        for f in calls:
-            f()
+        if step_graph is not None:
+            step_graph.replay()
+        else:
+            for f in calls:
+                f()
     t_end.record(stream)
     barrier()
     t2_start = torch.cuda.Event(enable_timing=True)
@@ -436,7 +447,6 @@ def main():
             ev[i + 1].record(stream)
     t2_end.record(stream)
     barrier()
-    clocks = sampler.stop()
     st = lib.dgl_device_status(s_handle)
     if st != 0:
         raise RuntimeError(f"device status after timed region: {dgl.status_string(st)}")
@@ -451,6 +461,13 @@ def main():
 
     step_flops = sum(flops)
     ms_max, value = over_ranks(ms_per_step, step_flops, dist, dev)
+
+    # ---------------------------------------------------------- headline shapes, each on its own
+    pk, pk_src = peaks()
+    headline = None
+    if not args.no_headline and args.shape is None:
+        headline = headline_run(torch, dgl, lib, dev, pk)
+    clocks = sampler.stop()
 
     # ---------------------------------------------------------- context: torch.matmul (cuBLAS), off the measured path
     # Each plain bf16 GEMM of the step is timed once more through torch.matmul
@@ -477,7 +494,6 @@ def main():
             cublas_us[i] = e0.elapsed_time(e1) / 20 * 1e3
 
     # ---------------------------------------------------------- roofline of the dominant kernel
-    pk, pk_src = peaks()
     by_kernel = {}
     for i, kn in enumerate(knames):
         d = by_kernel.setdefault(kn, {"ms": 0.0, "flops": 0.0, "bytes": 0.0, "launches": 0})
@@ -491,7 +507,7 @@ def main():
         # a contraction's peak: the measured bf16 figure times the nominal dense
         # ratio of its own type (E4M3 4.5 / 2.25 PFLOP/s, FP4 13.5 / 2.25)
         ratio, ratio_txt = (6.0, " x6 (fp4 nominal ratio)") if "mxfp4" in dominant else \
-            ((2.0, " x2 (fp8 nominal ratio)") if "fp8" in dominant else (1.0, ""))
+            ((2.0, " x2 (fp8 nominal ratio)") if ("fp8" in dominant or "w4a8" in dominant) else (1.0, ""))
         peak_tf = pk["bf16_tflops"] * ratio
         achieved = dk["flops"] / (dk["ms"] * 1e-3) / 1e12
         roofline = {"kernel": dominant, "bound": "tensor", "achieved": achieved, "peak": peak_tf,
@@ -615,23 +631,146 @@ def main():
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K_steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "+".join(sorted({{"bf16": "bf16", "fp8": "e4m3", "mxfp4": "e2m1"}[c.dtype] for c in cases})),
-            "data": "synthetic (seeded SplitMix64 draws; no datasets or trained weights)",
-            "config": {"workload": workload_text(args), "gemms_per_step": ncall,
+            "dtype": "+".join(sorted({{"bf16": "bf16", "fp8": "e4m3", "mxfp4": "e2m1", "w4a8": "e4m3xe2m1"}[c.dtype]
+                                      for c in cases})),
+            "data": "synthetic (seeded SplitMix64 draws)",
+            "config": {"workload": workload_text(args), "gemms_per_step": ncall, "launch": launch_mode,
                        "parallelism": "replicas" if world > 1 else "single GPU",
-                       "l2": (f"inputs larger than L2: each step touches {ws:.0f} MiB of A/B/C against a "
-                              f"{l2_mb:.0f} MiB L2, so every GEMM's operands were last read a full step earlier")
+                       "l2": (f"inputs larger than L2: {ws:.0f} MiB per step vs {l2_mb:.0f} MiB")
                              if ws > l2_mb else
-                             (f"inputs fit in L2 ({ws:.0f} MiB of A/B/C against {l2_mb:.0f} MiB): a profiling run, "
+                             (f"inputs fit in L2 ({ws:.0f} MiB vs {l2_mb:.0f} MiB): a profiling run, "
                               f"not a bench line")},
-            "roofline": roofline, "roofline_decode": roofline_decode, "kernels": kernels, "per_shape": per_shape,
-            "ms_per_step_with_call_events": ms_per_step_events,
             "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": K_steps * ncall, "clocks": clocks,
+            "roofline": roofline,
         }
-        print(json.dumps(line), flush=True)
+        detail = dict(line)
+        detail.update({"roofline_decode": roofline_decode, "kernels": kernels, "per_shape": per_shape,
+                       "ms_per_step_with_call_events": ms_per_step_events, "headline": headline})
+        # the full record on stderr; stdout carries one compact line whose
+        # tail holds the per-shape times and the headline shapes
+        print(json.dumps(detail), file=sys.stderr, flush=True)
+        line["cpu_baseline"] = cpu and {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        if cpu:
+            line["cpu_baseline"]["sample"] = "first rows of each GEMM of the step"
+        line["roofline"] = {k: roofline[k] for k in ("kernel", "bound", "achieved", "peak", "unit", "frac",
+                                                      "traffic", "peak_source", "avg_launch_us")}
+        if roofline_decode:
+            line["roofline_decode"] = {"achieved": round(roofline_decode["achieved"], 1),
+                                       "frac": round(roofline_decode["frac"], 4)}
+        line["per_shape_us"] = {f"{c.m}x{c.n}x{c.K}": round(per_call_ms[i] * 1e3, 2) for i, c in enumerate(cases)}
+        line["headline"] = headline
+        print(json.dumps(line, separators=(",", ":")), flush=True)
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def capture_graph(torch, body):
+    """Capture body(stream_handle) into a CUDA graph; None if capture fails."""
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            body(torch.cuda.current_stream().cuda_stream)
+        g.replay()
+        torch.cuda.synchronize()
+        return g
+    except Exception as exc:  # noqa: BLE001 -- any capture failure falls back to stream launches
+        print(f"graph capture failed, timing stream launches: {exc}", file=sys.stderr)
+        torch.cuda.synchronize()
+        return None
+
+
+# The shapes the targets are stated on, each timed on its own: 4096^3 in bf16
+# and E4M3 against the dense tensor peak, and the decode shapes (the LLaMA-2 7B
+# up/gate projection at 1 and 16 tokens, 16 x 4096 x 4096) against HBM.
+HEADLINE = [("bf16", 4096, 4096, 4096, "bf16", "square_normal"),
+            ("fp8", 4096, 4096, 4096, "bf16", "fp8"),
+            ("bf16", 1, 11008, 4096, "bf16", "normal"),
+            ("bf16", 16, 11008, 4096, "bf16", "normal"),
+            ("bf16", 16, 4096, 4096, "bf16", "normal")]
+NOMINAL_TFLOPS = {"bf16": 2250.0, "fp8": 4500.0}
+NOMINAL_HBM_GBS = 8000.0
+
+
+def headline_run(torch, dgl, lib, dev, pk, launches=48, reps=7):
+    """Time each HEADLINE shape alone: its operands rotate through
+    ceil(3 L2 / (|A| + |B|)) copies, so every launch reads them from HBM, and
+    `launches` back-to-back calls are replayed as one CUDA graph.  Returns
+    {shape: {us, rate, fractions of the nominal and measured peaks}}."""
+    import math
+
+    from synthetic import make_workload_case
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    out = {}
+    for entry in HEADLINE:
+        c = make_workload_case(entry)
+        if c.dtype == "bf16":
+            A = torch.from_numpy(c.A.view("int16")).to(dev)
+            B = torch.from_numpy(c.B.view("int16")).to(dev)
+            sa = sb = None
+            e = 2
+        else:
+            A = torch.from_numpy(c.A).to(dev)
+            B = torch.from_numpy(c.B).to(dev)
+            sa = torch.from_numpy(c.sa).to(dev)
+            sb = torch.from_numpy(c.sb).to(dev)
+            e = 1
+        ab = (c.m + c.n) * c.K * e
+        copies = max(2, math.ceil(3 * l2 / ab))
+        As = [A] + [A.clone() for _ in range(copies - 1)]
+        Bs = [B] + [B.clone() for _ in range(copies - 1)]
+        Cs = [torch.empty((c.m, c.n), dtype=torch.bfloat16, device=dev) for _ in range(copies)]
+
+        def launch(r, s):
+            if c.dtype == "bf16":
+                st = lib.dgl_gemm_bf16(As[r].data_ptr(), Bs[r].data_ptr(), Cs[r].data_ptr(), c.m, c.n, c.K, c.m, c.n,
+                                       dgl.OUT_BF16, s)
+            else:
+                st = lib.dgl_gemm_fp8(As[r].data_ptr(), Bs[r].data_ptr(), sa.data_ptr(), sb.data_ptr(),
+                                      Cs[r].data_ptr(), c.m, c.n, c.K, c.m, c.n, dgl.OUT_BF16, s)
+            if st != 0:
+                raise RuntimeError(f"headline {c.name}: {dgl.status_string(st)}")
+
+        cur = torch.cuda.current_stream(dev).cuda_stream
+        for r in range(copies):
+            launch(r, cur)
+        torch.cuda.synchronize()
+        L = copies * max(1, math.ceil(launches / copies))
+        g = capture_graph(torch, lambda s: [launch(t % copies, s) for t in range(L)])
+        times = []
+        for i in range(reps + 2):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            if g is not None:
+                g.replay()
+            else:
+                for t in range(L):
+                    launch(t % copies, cur)
+            e1.record()
+            e1.synchronize()
+            if i >= 2:
+                times.append(e0.elapsed_time(e1) * 1e3 / L)
+        us = statistics.median(times)
+        key = f"{c.m}x{c.n}x{c.K} {'e4m3' if c.dtype == 'fp8' else 'bf16'}"
+        plan = dgl.dgl_plan(dgl.DTYPE_BF16 if c.dtype == "bf16" else dgl.DTYPE_E4M3, c.m, c.n, c.K)
+        rec = {"us": round(us, 2), "copies": copies,
+               "tile": "decode" if plan.path == dgl.PATH_DECODE else f"{plan.tile_m}x{plan.tile_n}"}
+        if c.m > 16:
+            tf = 2.0 * c.m * c.n * c.K / (us * 1e-6) / 1e12
+            meas = pk["bf16_tflops"] * (2.0 if c.dtype == "fp8" else 1.0)
+            rec.update({"TFLOP/s": round(tf, 1), "of_nominal": round(tf / NOMINAL_TFLOPS[c.dtype], 4),
+                        "of_measured": round(tf / meas, 4), "target_of_nominal": 0.70})
+        else:
+            nb = (c.m * c.K + c.n * c.K) * e + c.m * c.n * 2 + (4 * (c.m + c.n) if c.dtype == "fp8" else 0)
+            gbs = nb / (us * 1e-6) / 1e9
+            rec.update({"GB/s": round(gbs, 1), "of_nominal": round(gbs / NOMINAL_HBM_GBS, 4),
+                        "of_measured": round(gbs / pk["hbm_gbs"], 4), "target_of_nominal": 0.60})
+        out[key] = rec
+        del g, As, Bs, Cs, A, B
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
 
 
 if __name__ == "__main__":
