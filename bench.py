@@ -409,7 +409,7 @@ def main():
     # One step captured as a CUDA graph: the ten calls' host work (argument
     # checks, plan and tensor-map cache look-ups, launch) then leaves the timed
     # loop, which replays the same launches back to back.
-    step_graph = capture_graph(torch, lambda s: [f(s) for f in calls])
+    step_graph = capture_graph(torch, lambda s: [f(s) for f in calls], stream)
     launch_mode = "cuda graph of one step" if step_graph is not None else "stream launches"
 
     # ---------------------------------------------------------- device-timed region
@@ -665,12 +665,14 @@ def main():
     return 0
 
 
-def capture_graph(torch, body):
-    """Capture body(stream_handle) into a CUDA graph; None if capture fails."""
+def capture_graph(torch, body, stream=None):
+    """Capture body(stream_handle) into a CUDA graph on `stream` (default: the
+    current stream); None if capture fails."""
+    stream = stream or torch.cuda.current_stream()
     try:
         g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            body(torch.cuda.current_stream().cuda_stream)
+        with torch.cuda.graph(g, stream=stream):
+            body(stream.cuda_stream)
         g.replay()
         torch.cuda.synchronize()
         return g
@@ -731,23 +733,27 @@ def headline_run(torch, dgl, lib, dev, pk, launches=48, reps=7):
             if st != 0:
                 raise RuntimeError(f"headline {c.name}: {dgl.status_string(st)}")
 
-        cur = torch.cuda.current_stream(dev).cuda_stream
+        # one stream for the warm-up, the capture and the timing events, so a
+        # split schedule's workspace exists before the capture
+        stream = torch.cuda.Stream(device=dev)
+        cur = stream.cuda_stream
         for r in range(copies):
             launch(r, cur)
         torch.cuda.synchronize()
         L = copies * max(1, math.ceil(launches / copies))
-        g = capture_graph(torch, lambda s: [launch(t % copies, s) for t in range(L)])
+        g = capture_graph(torch, lambda s: [launch(t % copies, s) for t in range(L)], stream)
         times = []
         for i in range(reps + 2):
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
-            e0.record()
+            e0.record(stream)
             if g is not None:
-                g.replay()
+                with torch.cuda.stream(stream):
+                    g.replay()
             else:
                 for t in range(L):
                     launch(t % copies, cur)
-            e1.record()
+            e1.record(stream)
             e1.synchronize()
             if i >= 2:
                 times.append(e0.elapsed_time(e1) * 1e3 / L)

@@ -30,6 +30,7 @@ OUT_F32 = 1
 DTYPE_BF16 = 0
 DTYPE_E4M3 = 1
 DTYPE_MXFP4 = 2
+DTYPE_W4A8 = 3
 PATH_TC = 0
 PATH_DECODE = 1
 PATH_EMPTY = 2
@@ -41,7 +42,7 @@ MN_MAJOR = 1
 
 EXPORTED = ["dgl_gemm_bf16", "dgl_gemm_fp8", "dgl_gemm_planned", "dgl_plan", "dgl_tile_metrics",
             "dgl_device_status", "dgl_status_string", "dgl_version", "dgl_gemm_noalloc", "dgl_linear",
-            "dgl_plan_linear", "dgl_gemm_bf16_ex", "dgl_gemm_mxfp4"]
+            "dgl_plan_linear", "dgl_gemm_bf16_ex", "dgl_gemm_mxfp4", "dgl_shutdown", "dgl_gemm_w4a8"]
 
 
 class PlanInfo(ctypes.Structure):
@@ -91,12 +92,16 @@ def load_library(path: str | None = None):
     lib.dgl_gemm_bf16_ex.argtypes = [i32, i32, vp, i64, vp, i64, vp, i64, i64, i64, i64, i32,
                                      ctypes.POINTER(PlanInfo), vp]
     lib.dgl_gemm_bf16_ex.restype = i32
+    lib.dgl_gemm_w4a8.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i32, vp]
+    lib.dgl_gemm_w4a8.restype = i32
     lib.dgl_gemm_mxfp4.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i32, vp]
     lib.dgl_gemm_mxfp4.restype = i32
     lib.dgl_plan.argtypes = [i32, i64, i64, i64, i32, i32, ctypes.POINTER(PlanInfo)]
     lib.dgl_plan.restype = i32
     lib.dgl_tile_metrics.argtypes = [i64, i64, i32, i32, i32, ctypes.POINTER(PlanInfo)]
     lib.dgl_tile_metrics.restype = i32
+    lib.dgl_shutdown.argtypes = []
+    lib.dgl_shutdown.restype = i32
     lib.dgl_device_status.argtypes = [vp]
     lib.dgl_device_status.restype = i32
     lib.dgl_status_string.argtypes = [i32]
@@ -132,6 +137,11 @@ def dgl_gemm_fp8(A, B, sa, sb, C, M, N, K, m_valid=0, n_valid=0, out_dtype=OUT_B
 def dgl_gemm_mxfp4(A, B, sfa, sfb, C, M, N, K, m_valid=0, n_valid=0, out_dtype=OUT_BF16, stream=0) -> int:
     """Block-scaled FP4: A [m][K/2], B [n][K/2] packed E2M1 bytes; sfa [m][K/32], sfb [n][K/32] E8M0 bytes."""
     return load_library().dgl_gemm_mxfp4(A, B, sfa, sfb, C, M, N, K, m_valid, n_valid, out_dtype, stream)
+
+
+def dgl_gemm_w4a8(A, B, sa, sb, C, M, N, K, m_valid=0, n_valid=0, out_dtype=OUT_BF16, stream=0) -> int:
+    """E4M3 A [m][K] x packed E2M1 B [n][K/2] (two codes a byte), fp32 scales sa [m], sb [n]."""
+    return load_library().dgl_gemm_w4a8(A, B, sa, sb, C, M, N, K, m_valid, n_valid, out_dtype, stream)
 
 
 def dgl_gemm_planned(dtype, A, B, sa, sb, C, M, N, K, m_valid, n_valid, out_dtype, plan: PlanInfo,
@@ -181,6 +191,11 @@ def dgl_tile_metrics(m, n, tile_m, tile_n, num_units) -> PlanInfo:
 
 def dgl_device_status(stream=0) -> int:
     return load_library().dgl_device_status(stream)
+
+
+def dgl_shutdown() -> int:
+    """Free the library's workspaces and caches on the current device (see include/dgl.h)."""
+    return load_library().dgl_shutdown()
 
 
 def dgl_version() -> int:
@@ -278,6 +293,30 @@ def gemm_mxfp4(A, B, sfa, sfb, K, out=None, *, out_dtype=OUT_BF16, stream=None):
     st = dgl_gemm_mxfp4(A.data_ptr(), B.data_ptr(), sfa.data_ptr(), sfb.data_ptr(), C.data_ptr(), rows, ldc, K, m,
                         n, out_dtype, _stream_handle(stream))
     _check(st, "dgl_gemm_mxfp4")
+    return C
+
+
+def gemm_w4a8(A, B, sa, sb, K, out=None, *, out_dtype=OUT_BF16, stream=None):
+    """C = (A . B^T) * sa[:, None] * sb[None, :] for E4M3 A [m, K] and E2M1 B.
+
+    A is a float8_e4m3fn (or uint8) CUDA tensor [m, K]; B a uint8 CUDA tensor
+    [n, K/2] of packed E2M1 codes (element 2t in the low four bits of byte t);
+    sa [m], sb [n] fp32.  K is passed explicitly.  Returns C [m, n].
+    """
+    import torch
+    m, n = A.shape[0], B.shape[0]
+    if A.dtype not in (torch.float8_e4m3fn, torch.uint8) or not A.is_cuda or tuple(A.shape) != (m, K) \
+            or not A.is_contiguous():
+        raise ValueError(f"A must be a contiguous E4M3 CUDA tensor of shape {(m, K)}")
+    if B.dtype != torch.uint8 or not B.is_cuda or tuple(B.shape) != (n, K // 2) or not B.is_contiguous():
+        raise ValueError(f"B must be a contiguous uint8 CUDA tensor of shape {(n, K // 2)}")
+    for name, s_, length in (("sa", sa, m), ("sb", sb, n)):
+        if s_.dtype != torch.float32 or not s_.is_cuda or s_.numel() != length or not s_.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous fp32 CUDA tensor of length {length}")
+    C, ldc, rows = _out_tensor(out, m, n, out_dtype, A.device)
+    st = dgl_gemm_w4a8(A.data_ptr(), B.data_ptr(), sa.data_ptr(), sb.data_ptr(), C.data_ptr(), rows, ldc, K, m, n,
+                       out_dtype, _stream_handle(stream))
+    _check(st, "dgl_gemm_w4a8")
     return C
 
 

@@ -23,8 +23,8 @@ LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
                 "-I", INCLUDE, "-I", CSRC]
-SOURCES = ["api.cu", "plan.cpp", "tc_bf16.cu", "tc_e4m3.cu", "tc_bf16_epi.cu", "tc_e4m3_epi.cu", "tc_mxfp4.cu",
-           "decode.cu"]
+SOURCES = ["api.cu", "plan.cpp", "tc_bf16.cu", "tc_e4m3.cu", "tc_bf16_m64.cu", "tc_e4m3_m64.cu", "tc_bf16_epi.cu",
+           "tc_e4m3_epi.cu", "tc_mxfp4.cu", "decode.cu"]
 
 
 def nvcc() -> str:

@@ -10,6 +10,7 @@
 #include <mutex>
 #include <tuple>
 #include <unordered_map>
+#include <vector>
 
 #include "common.cuh"
 #include "dgl.h"
@@ -55,48 +56,104 @@ struct PlanKeyHash {
 };
 std::unordered_map<PlanKey, dgl_plan_info, PlanKeyHash> g_plans;
 
-// Stream-K workspace, one per (device, stream): fp32 partial tiles and one
-// epoch flag per partial slot.  Launches on one stream run in order, so they
-// can share it; each launch gets a fresh epoch so stale flags never match.
+// Stream-K workspaces: fp32 partial tiles and one flag per partial slot, one
+// workspace per (device, stream).  Launches on one stream run in order, so
+// they can share it.  A contributor sets its flag to 1 once its partial is
+// written; the worker that adds the partial clears it again after reading
+// it, so every launch leaves the flags at zero (a CUDA graph replays the same
+// launch parameters, which rules out a per-launch tag).  At most
+// kWorkspacesPerDevice are kept per device: a new
+// stream's workspace replaces the least recently used one (after the device
+// has drained, since that stream's kernels may still read it), so a caller
+// that makes a stream per request does not grow device memory without bound.
+// dgl_shutdown() frees them all.
+constexpr int kWorkspacesPerDevice = 4;
 struct Workspace {
+  int dev = -1;
+  cudaStream_t stream = nullptr;
   float* ws = nullptr;
   size_t ws_bytes = 0;
   int* flags = nullptr;
   int nflags = 0;
-  int epoch = 0;
+  uint64_t last_use = 0;
 };
-std::map<std::pair<int, cudaStream_t>, Workspace> g_workspaces;
+std::vector<Workspace> g_workspaces;  // guarded by g_mu
+uint64_t g_ws_clock = 0;
 
-dgl_status acquire_workspace(int dev, cudaStream_t stream, size_t bytes, int nflags, float** ws, int** flags,
-                             int* epoch) {
+void free_workspace(Workspace& w) {
+  if (w.ws) cudaFree(w.ws);
+  if (w.flags) cudaFree(w.flags);
+  w.ws = nullptr;
+  w.flags = nullptr;
+  w.ws_bytes = 0;
+  w.nflags = 0;
+}
+
+// Whether (dev, stream) already has a workspace of at least bytes / nflags.
+bool workspace_ready(int dev, cudaStream_t stream, size_t bytes, int nflags) {
   std::lock_guard<std::mutex> lock(g_mu);
-  Workspace& w = g_workspaces[std::make_pair(dev, stream)];
-  if (w.ws_bytes < bytes || w.nflags < nflags || w.epoch == INT32_MAX) {
+  for (const Workspace& x : g_workspaces)
+    if (x.dev == dev && x.stream == stream) return x.ws && x.ws_bytes >= bytes && x.nflags >= nflags;
+  return false;
+}
+
+dgl_status acquire_workspace(int dev, cudaStream_t stream, size_t bytes, int nflags, float** ws, int** flags) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  Workspace* w = nullptr;
+  int on_dev = 0;
+  for (Workspace& x : g_workspaces) {
+    if (x.dev != dev) continue;
+    ++on_dev;
+    if (x.stream == stream) w = &x;
+  }
+  if (!w) {
+    if (on_dev >= kWorkspacesPerDevice) {
+      // evict the device's least recently used workspace once its work is done
+      size_t lru = g_workspaces.size();
+      for (size_t i = 0; i < g_workspaces.size(); ++i)
+        if (g_workspaces[i].dev == dev && (lru == g_workspaces.size() || g_workspaces[i].last_use < g_workspaces[lru].last_use))
+          lru = i;
+      if (cudaDeviceSynchronize() != cudaSuccess) return DGL_ERR_CUDA;
+      free_workspace(g_workspaces[lru]);
+      g_workspaces.erase(g_workspaces.begin() + static_cast<std::ptrdiff_t>(lru));
+    }
+    Workspace fresh;
+    fresh.dev = dev;
+    fresh.stream = stream;
+    g_workspaces.push_back(fresh);
+    w = &g_workspaces.back();
+  }
+  if (w->ws_bytes < bytes || w->nflags < nflags) {
     // growing frees the old buffers, which waits for work still using them
-    if (w.ws) cudaFree(w.ws);
-    if (w.flags) cudaFree(w.flags);
-    w = Workspace{};
+    free_workspace(*w);
     const size_t want = bytes > (size_t(24) << 20) ? bytes : (size_t(24) << 20);
     const int want_flags = nflags > 512 ? nflags : 512;
-    if (cudaMalloc(reinterpret_cast<void**>(&w.ws), want) != cudaSuccess) return DGL_ERR_CUDA;
-    if (cudaMalloc(reinterpret_cast<void**>(&w.flags), sizeof(int) * want_flags) != cudaSuccess) {
-      cudaFree(w.ws);
-      w = Workspace{};
+    if (cudaMalloc(reinterpret_cast<void**>(&w->ws), want) != cudaSuccess) {
+      w->ws = nullptr;
       return DGL_ERR_CUDA;
     }
-    if (cudaMemset(w.flags, 0, sizeof(int) * want_flags) != cudaSuccess) return DGL_ERR_CUDA;
-    w.ws_bytes = want;
-    w.nflags = want_flags;
+    if (cudaMalloc(reinterpret_cast<void**>(&w->flags), sizeof(int) * want_flags) != cudaSuccess) {
+      w->flags = nullptr;
+      free_workspace(*w);
+      return DGL_ERR_CUDA;
+    }
+    w->ws_bytes = want;
+    w->nflags = want_flags;
+    if (cudaMemset(w->flags, 0, sizeof(int) * want_flags) != cudaSuccess) {
+      free_workspace(*w);
+      return DGL_ERR_CUDA;
+    }
   }
-  *ws = w.ws;
-  *flags = w.flags;
-  *epoch = ++w.epoch;
+  w->last_use = ++g_ws_clock;
+  *ws = w->ws;
+  *flags = w->flags;
   return DGL_OK;
 }
 
 // ---- scratch of dgl_gemm_noalloc: a fixed device array instead of cudaMalloc.
-// Layout: DGL_NOALLOC_SCRATCH_BYTES of fp32 partial tiles, then one epoch flag
-// per partial slot.  Every device that loads the library holds it until exit.
+// Layout: DGL_NOALLOC_SCRATCH_BYTES of fp32 partial tiles, then one flag per
+// partial slot (zero between launches).  Every device that loads the library
+// holds it until exit.
 constexpr int kNoallocFlags = 160;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[DGL_NOALLOC_SCRATCH_BYTES + kNoallocFlags * sizeof(int)];
 
@@ -109,9 +166,10 @@ struct StaticScratch {
   size_t ws_bytes = 0;
   int* flags = nullptr;
   int nflags = 0;
-  int epoch = 0;  // last epoch handed out; flags hold earlier epochs or zero
 };
 StaticScratch g_noalloc[kMaxDevices];
+std::mutex g_noalloc_mu;  // set-up of g_noalloc
+
 
 dgl_status get_device(int* dev_out, DeviceState** st_out) {
   int dev = 0;
@@ -161,6 +219,24 @@ bool encode_operand_map(CUtensorMap* map, const void* base, bool e4m3, int64_t i
   return r == CUDA_SUCCESS;
 }
 
+// 2-D tensor map over packed 4-bit codes, [rows][K / 2] bytes (element 2t in
+// the low four bits of byte t), with a box of 128 elements by box_rows rows
+// and the 128-byte swizzle.  The 16U4_ALIGN16B type lands each 16 elements
+// (8 bytes) in a 16-byte unit of shared memory, the layout the kind::f8f6f4
+// MMA reads a 4-bit operand from: a box row spans 128 bytes there, as an
+// E4M3 row does.  Needs K a multiple of 128, a 32-byte-aligned base and a
+// row pitch that is a multiple of 32 bytes.
+bool encode_w4_map(CUtensorMap* map, const void* base, int64_t K, int64_t rows, int box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
+  cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 2-D tensor map over an MN-major bf16 operand stored [K][mn] (row pitch
 // `pitch` elements): boxes of 64 MN elements (128 bytes) by 64 K rows with
 // the 128-byte swizzle, the layout the MN-major UMMA descriptor reads.
@@ -175,15 +251,17 @@ bool encode_operand_map_mn(CUtensorMap* map, const void* base, int64_t mn, int64
   return r == CUDA_SUCCESS;
 }
 
-// 2-D tensor map over C [rows, cols] (row pitch ldc elements) for 32 x 32
-// TMA stores from the epilogue's swizzled staging tile.  Writes outside
-// [0, cols) x [0, rows) are dropped.
-bool encode_output_map(CUtensorMap* map, void* base, bool f32, int64_t cols, int64_t rows, int64_t ldc) {
+// 2-D tensor map over C [rows, cols] (row pitch ldc elements) for 32-column
+// TMA stores of box_rows rows (32, or 16 for 64-row tiles) from the
+// epilogue's swizzled staging tile.  Writes outside [0, cols) x [0, rows) are
+// dropped.
+bool encode_output_map(CUtensorMap* map, void* base, bool f32, int64_t cols, int64_t rows, int64_t ldc,
+                       int box_rows) {
   const CUtensorMapDataType dt = f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const int64_t esize = f32 ? 4 : 2;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldc * esize)};
-  cuuint32_t box[2] = {32, 32};
+  cuuint32_t box[2] = {32, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(map, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
@@ -197,7 +275,8 @@ bool encode_output_map(CUtensorMap* map, void* base, bool f32, int64_t cols, int
 struct MapKey {
   const void* base;
   int64_t d0, d1, pitch;
-  int box_rows, kind;  // kind: 0 bf16 operand, 1 E4M3 operand, 2 bf16 output, 3 fp32 output, 4 MN-major bf16
+  int box_rows, kind;  // kind: 0 bf16 operand, 1 E4M3 operand, 2 bf16 output, 3 fp32 output, 4 MN-major bf16,
+                       // 5 packed 4-bit operand
   bool operator==(const MapKey& o) const {
     return base == o.base && d0 == o.d0 && d1 == o.d1 && pitch == o.pitch && box_rows == o.box_rows &&
            kind == o.kind;
@@ -246,15 +325,45 @@ bool cached_operand_map(CUtensorMap* map, const void* base, bool e4m3, int64_t i
                     [&](CUtensorMap* m) { return encode_operand_map(m, base, e4m3, inner, rows, box_rows, pitch); });
 }
 
+bool cached_w4_map(CUtensorMap* map, const void* base, int64_t K, int64_t rows, int box_rows) {
+  const MapKey key{base, K, rows, K / 2, box_rows, 5};
+  return cached_map(map, key, [&](CUtensorMap* m) { return encode_w4_map(m, base, K, rows, box_rows); });
+}
+
+// B's map: E4M3 / bf16 codes, or packed 4-bit codes (w4).
+bool cached_b_map(CUtensorMap* map, const void* base, bool e4m3, bool w4, int64_t K, int64_t rows, int box_rows,
+                  int64_t pitch = 0) {
+  return w4 ? cached_w4_map(map, base, K, rows, box_rows)
+            : cached_operand_map(map, base, e4m3, K, rows, box_rows, pitch);
+}
+
 bool cached_operand_map_mn(CUtensorMap* map, const void* base, int64_t mn, int64_t K, int64_t pitch) {
   const MapKey key{base, mn, K, pitch, 64, 4};
   return cached_map(map, key, [&](CUtensorMap* m) { return encode_operand_map_mn(m, base, mn, K, pitch); });
 }
 
-bool cached_output_map(CUtensorMap* map, void* base, bool f32, int64_t cols, int64_t rows, int64_t ldc) {
-  const MapKey key{base, cols, rows, ldc, 32, f32 ? 3 : 2};
-  return cached_map(map, key, [&](CUtensorMap* m) { return encode_output_map(m, base, f32, cols, rows, ldc); });
+bool cached_output_map(CUtensorMap* map, void* base, bool f32, int64_t cols, int64_t rows, int64_t ldc,
+                       int box_rows = 32) {
+  const MapKey key{base, cols, rows, ldc, box_rows, f32 ? 3 : 2};
+  return cached_map(map, key,
+                    [&](CUtensorMap* m) { return encode_output_map(m, base, f32, cols, rows, ldc, box_rows); });
 }
+
+// L2 prefetch before the wait for the previous kernel on the stream
+// (measured on GB300, back to back, operands rotated through 3x L2):
+//  * decode: a CTA prefetches its first ring's worth of B when its part is
+//    at least twice the ring (1 and 16 x 11008 x 4096: 16.6 -> 14.6 and
+//    17.1 -> 15.0 us); with parts about one ring long (16 x 4096 x 4096) any
+//    prefetch measured slower (9.9 -> 10.2-11.8 us), since the ring's own
+//    loads follow at once;
+//  * tile kernel: the first ring of its first tile when K spans at least
+//    four rings (4096^3 bf16 79.1 -> 77.9 us); never for short K, where the
+//    ring's loads follow at once.
+constexpr int kDecodeRingBytes = 196608;
+
+// The E2M1 code of the kind::f8f6f4 instruction descriptor's A / B format
+// fields (bits 7-9 / 10-12; E4M3 is 0).
+constexpr uint32_t kIdescE2M1 = 5;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -274,6 +383,9 @@ struct Problem {
   int b_mn = 0;
   int64_t lda = 0;
   int64_t ldb = 0;
+  // W4A8 (dgl_gemm_w4a8): dtype E4M3 for A, B holds packed E2M1 codes (K / 2
+  // bytes a row)
+  int w4 = 0;
 };
 
 dgl_status validate(Problem& pr) {
@@ -295,6 +407,9 @@ dgl_status validate(Problem& pr) {
   const int64_t esize = pr.dtype == DGL_DTYPE_E4M3 ? 1 : 2;
   if ((pr.K * esize) % 16 != 0) return DGL_ERR_ALIGN;
   if (!aligned(pr.A, 16) || !aligned(pr.B, 16)) return DGL_ERR_ALIGN;
+  // packed 4-bit B: whole 128-element boxes along K, a 32-byte-aligned base
+  // (the tensor-map rules of the 16U4_ALIGN16B type)
+  if (pr.w4 && (pr.K % 128 != 0 || !aligned(pr.B, 32))) return DGL_ERR_ALIGN;
   if (pr.K * esize > INT32_MAX) return DGL_ERR_SHAPE;
   if (pr.a_mn || pr.b_mn) {
     if (pr.dtype != DGL_DTYPE_BF16 || pr.gated || pr.act || pr.bias) return DGL_ERR_UNSUPPORTED;
@@ -304,7 +419,7 @@ dgl_status validate(Problem& pr) {
   if (pr.lda == 0) pr.lda = a_row;
   if (pr.ldb == 0) pr.ldb = b_row;
   if (pr.lda < a_row || pr.ldb < b_row) return DGL_ERR_ARG;
-  if ((pr.lda * esize) % 16 != 0 || (pr.ldb * esize) % 16 != 0) return DGL_ERR_ALIGN;
+  if ((pr.lda * esize) % 16 != 0 || (!pr.w4 && (pr.ldb * esize) % 16 != 0)) return DGL_ERR_ALIGN;
   if (pr.lda > INT32_MAX || pr.ldb > INT32_MAX) return DGL_ERR_SHAPE;
   if (pr.dtype == DGL_DTYPE_E4M3) {
     if (!pr.sa || !pr.sb) return DGL_ERR_ARG;
@@ -339,10 +454,12 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream, Sta
       fill_decode_plan(pr.dtype, pr.out, pr.m, pr.n, pr.K, ds->num_sms, &plan);
     } else if (forced->path == DGL_PATH_TC) {
       if (!tc_supported_tile(forced->tile_m, forced->tile_n)) return DGL_ERR_UNSUPPORTED;
+      // 64-row tiles read K-major operands only
+      if (forced->tile_m == 64 && (pr.a_mn || pr.b_mn)) return DGL_ERR_UNSUPPORTED;
       if (linear && !tc_supported_epi_tile(forced->tile_m, forced->tile_n, pr.gated != 0)) return DGL_ERR_UNSUPPORTED;
       fill_tc_plan(pr.dtype, pr.out, pr.m, pr.gated ? 2 * pr.n : pr.n, pr.K, forced->tile_m, forced->tile_n,
-                   ds->num_sms, &plan, forced->stream_k ? 1 : 0);
-      plan.split_tail = forced->split_tail && !plan.stream_k ? 1 : 0;
+                   ds->num_sms, &plan, forced->stream_k > 0 ? forced->stream_k : 0);
+      plan.split_tail = forced->split_tail && !plan.stream_k && forced->tile_m != 64 ? 1 : 0;
     } else {
       return DGL_ERR_UNSUPPORTED;
     }
@@ -353,6 +470,8 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream, Sta
     // the decode path reads packed K-major operands only
     choose_plan(pr.dtype, pr.out, pr.m, pr.n, pr.K, ds->num_sms, &plan);
     if (plan.path != DGL_PATH_TC) fill_tc_plan(pr.dtype, pr.out, pr.m, pr.n, pr.K, 128, 128, ds->num_sms, &plan, 0);
+    if (plan.tile_m == 64 && (pr.a_mn || pr.b_mn))
+      fill_tc_plan(pr.dtype, pr.out, pr.m, pr.n, pr.K, 128, plan.tile_n, ds->num_sms, &plan, 0);
   } else {
     PlanKey key{dev, pr.dtype, pr.out, pr.m, pr.n, pr.K};
     std::lock_guard<std::mutex> lock(g_mu);
@@ -373,10 +492,16 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream, Sta
     const int rows_hi = static_cast<int>((pr.n + parts - 1) / parts);
     CUtensorMap ta, tb_lo, tb_hi;
     if (!cached_operand_map(&ta, pr.A, e4m3, pr.K, pr.m, static_cast<int>(pr.m)) ||
-        !cached_operand_map(&tb_lo, pr.B, e4m3, pr.K, pr.n, rows_lo) ||
-        !cached_operand_map(&tb_hi, pr.B, e4m3, pr.K, pr.n, rows_hi))
+        !cached_b_map(&tb_lo, pr.B, e4m3, pr.w4, pr.K, pr.n, rows_lo) ||
+        !cached_b_map(&tb_hi, pr.B, e4m3, pr.w4, pr.K, pr.n, rows_hi))
       return DGL_ERR_CUDA;
     DecodeParams p;
+    // B's rows are the MMA's A operand here: E2M1 goes in the A format field
+    p.idesc_or = pr.w4 ? kIdescE2M1 << 7 : 0u;
+    p.b_tx_shift = pr.w4 ? 1 : 0;
+    p.prefetch_planes = static_cast<int64_t>(rows_hi) * pr.K * esize >= 2 * kDecodeRingBytes
+                            ? kDecodeRingBytes / (rows_hi * 128)
+                            : 0;
     p.sa = pr.sa;
     p.sb = pr.sb;
     p.C = pr.C;
@@ -419,19 +544,19 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream, Sta
   const int64_t b_rows = pr.gated ? 2 * pr.n : pr.n;
   const bool map_ok =
       (pr.a_mn ? cached_operand_map_mn(&ta, pr.A, pr.m, pr.K, pr.lda)
-               : cached_operand_map(&ta, pr.A, e4m3, pr.K, pr.m, 128, pr.lda)) &&
+               : cached_operand_map(&ta, pr.A, e4m3, pr.K, pr.m, plan.tile_m == 64 ? 64 : 128, pr.lda)) &&
       (pr.b_mn ? cached_operand_map_mn(&tb, pr.B, b_rows, pr.K, pr.ldb)
-               : cached_operand_map(&tb, pr.B, e4m3, pr.K, b_rows, plan.tile_n / cg, pr.ldb));
+               : cached_b_map(&tb, pr.B, e4m3, pr.w4, pr.K, b_rows, plan.tile_n / cg, pr.ldb));
   if (!map_ok) return DGL_ERR_CUDA;
   // B with half-height boxes, for the half tiles of a split tail (else unused)
   CUtensorMap tbh = tb;
   if (plan.split_tail && !pr.b_mn && plan.tile_n == 256 &&
-      !cached_operand_map(&tbh, pr.B, e4m3, pr.K, b_rows, plan.tile_n / cg / 2, pr.ldb))
+      !cached_b_map(&tbh, pr.B, e4m3, pr.w4, pr.K, b_rows, plan.tile_n / cg / 2, pr.ldb))
     return DGL_ERR_CUDA;
   const bool f32 = pr.out == DGL_OUT_F32;
   const bool c_tma = aligned(pr.C, 16) && (pr.N * (f32 ? 4 : 2)) % 16 == 0;
   std::memset(&tc, 0, sizeof(tc));
-  if (c_tma && !cached_output_map(&tc, pr.C, f32, pr.n, pr.m, pr.N)) return DGL_ERR_CUDA;
+  if (c_tma && !cached_output_map(&tc, pr.C, f32, pr.n, pr.m, pr.N, plan.tile_m == 64 ? 16 : 32)) return DGL_ERR_CUDA;
   TcParams p;
   p.C = pr.C;
   p.ldc = pr.N;
@@ -455,20 +580,35 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream, Sta
   p.n_up = static_cast<int>(pr.n);
   p.a_mn = pr.a_mn;
   p.b_mn = pr.b_mn;
+  p.idesc_or = pr.w4 ? kIdescE2M1 << 10 : 0u;  // E2M1 in the B format field
+  p.b_tx_shift = pr.w4 ? 1 : 0;
+  p.prefetch_stages = p.num_kb >= 4 * plan.stages ? plan.stages : 0;
+  // A split schedule needs the stream's workspace.  A stream being captured
+  // into a CUDA graph cannot have one allocated, so a captured call on a
+  // stream without one runs the data-parallel schedule instead.
+  bool split = plan.stream_k != 0;
+  if (split && !fixed) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return DGL_ERR_CUDA;
+    if (cs != cudaStreamCaptureStatusNone &&
+        !workspace_ready(dev, stream, sizeof(float) * 128 * static_cast<size_t>(plan.tile_n) * ds->num_sms,
+                         ds->num_sms))
+      split = false;
+  }
   // grid counts CTAs; a pair per tile when cg == 2
   int grid = plan.grid > 0 ? plan.grid : p.num_tiles * cg;
-  if (!plan.stream_k && grid > p.num_tiles * cg) grid = p.num_tiles * cg;
+  if (!split && grid > p.num_tiles * cg) grid = p.num_tiles * cg;
   if (grid > ds->num_sms) grid = ds->num_sms;
   grid = grid / cg * cg;
   if (grid < cg) grid = cg;
   p.workers = grid / cg;
   p.dp_tiles = p.num_tiles;
   p.sk_units = 0;
+  p.sk_workers = p.workers;
   p.half_tiles = 0;
   p.ws = nullptr;
   p.flags = nullptr;
-  p.epoch = 0;
-  if (plan.split_tail && !plan.stream_k && !pr.gated && plan.tile_n == 256 && p.num_tiles > p.workers) {
+  if (plan.split_tail && !split && !pr.gated && plan.tile_n == 256 && p.num_tiles > p.workers) {
     // the last, partial wave as half tiles, one per worker
     const int tail = p.num_tiles % p.workers;
     if (tail > 0 && 2 * tail <= p.workers) {
@@ -476,25 +616,23 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream, Sta
       p.half_tiles = 2 * tail;
     }
   }
-  if (plan.stream_k && p.num_tiles % p.workers != 0) {
+  if (split && p.num_tiles % p.workers != 0) {
     p.dp_tiles = p.num_tiles / p.workers * p.workers;
     p.sk_units = static_cast<int64_t>(p.num_tiles - p.dp_tiles) * p.num_kb;
+    // stream_k = S >= 2: each tail tile's k-stages in S equal ranges, one per
+    // worker (tail x S workers), instead of all workers sharing them
+    const int tail = p.num_tiles - p.dp_tiles;
+    if (plan.stream_k >= 2 && static_cast<int64_t>(tail) * plan.stream_k <= p.workers)
+      p.sk_workers = tail * plan.stream_k;
     const size_t slot_floats = static_cast<size_t>(128) * plan.tile_n;
     const size_t bytes = sizeof(float) * slot_floats * static_cast<size_t>(grid);
     if (fixed) {
       // the caller's problem needs more partial tiles than the array holds
       if (bytes > fixed->ws_bytes || grid > fixed->nflags) return DGL_ERR_SHAPE;
-      std::lock_guard<std::mutex> lock(g_mu);
-      if (fixed->epoch == INT32_MAX) {
-        // epochs ran out: clear the flags so that counting can restart
-        if (cudaMemsetAsync(fixed->flags, 0, sizeof(int) * fixed->nflags, stream) != cudaSuccess) return DGL_ERR_CUDA;
-        fixed->epoch = 0;
-      }
       p.ws = fixed->ws;
       p.flags = fixed->flags;
-      p.epoch = ++fixed->epoch;
     } else {
-      const dgl_status wst = acquire_workspace(dev, stream, bytes, grid, &p.ws, &p.flags, &p.epoch);
+      const dgl_status wst = acquire_workspace(dev, stream, bytes, grid, &p.ws, &p.flags);
       if (wst != DGL_OK) return wst;
     }
   }
@@ -576,8 +714,23 @@ dgl_status run_mxfp4(Problem pr, const uint8_t* sfa, const uint8_t* sfb, cudaStr
 
 // First use on a device: look up the array's device address and clear its
 // flags (synchronous; later calls enqueue work only).
+// Whether the stream-K split of a plan fits the array on a device of num_sms
+// SMs: one 128 x tile_n fp32 slot and one flag per CTA of the grid.  On 152
+// SMs every plan fits (at most 152 slots of 128 KB).
+bool noalloc_fits(const Problem& pr, const dgl_plan_info& plan, int num_sms) {
+  if (plan.path != DGL_PATH_TC ||
+      !stream_k_eligible(pr.m, pr.n, pr.K, pr.dtype, plan.tile_m, plan.tile_n, num_sms))
+    return true;
+  const int cg = plan.cta_group == 2 ? 2 : 1;
+  const int64_t grid = static_cast<int64_t>(num_sms / cg) * cg;
+  const int64_t bytes = static_cast<int64_t>(sizeof(float)) * 128 * plan.tile_n * grid;
+  return bytes <= static_cast<int64_t>(DGL_NOALLOC_SCRATCH_BYTES) && grid <= kNoallocFlags;
+}
+
+// Its own lock: the synchronous set-up must not hold up other threads' calls,
+// which take g_mu.
 dgl_status noalloc_setup(int dev, StaticScratch** out) {
-  std::lock_guard<std::mutex> lock(g_mu);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
   StaticScratch& sc = g_noalloc[dev];
   if (!sc.ready) {
     void* ptr = nullptr;
@@ -590,7 +743,6 @@ dgl_status noalloc_setup(int dev, StaticScratch** out) {
     sc.ws_bytes = DGL_NOALLOC_SCRATCH_BYTES;
     sc.flags = flags;
     sc.nflags = kNoallocFlags;
-    sc.epoch = 0;
     sc.ready = true;
   }
   *out = &sc;
@@ -616,6 +768,13 @@ dgl_status dgl_gemm_fp8(const void* A, const void* B, const float* sa, const flo
   return run(pr, nullptr, static_cast<cudaStream_t>(stream));
 }
 
+dgl_status dgl_gemm_w4a8(const void* A, const void* B, const float* sa, const float* sb, void* C, int64_t M,
+                         int64_t N, int64_t K, int64_t m_valid, int64_t n_valid, int32_t out_dtype, void* stream) {
+  Problem pr{DGL_DTYPE_E4M3, out_dtype, A, B, sa, sb, C, M, N, K, m_valid, n_valid};
+  pr.w4 = 1;
+  return run(pr, nullptr, static_cast<cudaStream_t>(stream));
+}
+
 dgl_status dgl_gemm_mxfp4(const void* A, const void* B, const uint8_t* sfa, const uint8_t* sfb, void* C, int64_t M,
                           int64_t N, int64_t K, int64_t m_valid, int64_t n_valid, int32_t out_dtype, void* stream) {
   Problem pr{DGL_DTYPE_MXFP4, out_dtype, A, B, nullptr, nullptr, C, M, N, K, m_valid, n_valid};
@@ -626,8 +785,11 @@ dgl_status dgl_gemm_planned(int32_t dtype, const void* A, const void* B, const f
                             int64_t M, int64_t N, int64_t K, int64_t m_valid, int64_t n_valid, int32_t out_dtype,
                             const dgl_plan_info* plan, void* stream) {
   if (!plan) return DGL_ERR_ARG;
+  const bool w4 = dtype == DGL_DTYPE_W4A8;
+  if (w4) dtype = DGL_DTYPE_E4M3;
   Problem pr{dtype, out_dtype, A, B, dtype == DGL_DTYPE_E4M3 ? sa : nullptr,
              dtype == DGL_DTYPE_E4M3 ? sb : nullptr, C, M, N, K, m_valid, n_valid};
+  pr.w4 = w4 ? 1 : 0;
   return run(pr, plan, static_cast<cudaStream_t>(stream));
 }
 
@@ -645,7 +807,9 @@ dgl_status dgl_linear(int32_t dtype, const void* A, const void* B, const float* 
 dgl_status dgl_plan(int32_t dtype, int64_t m, int64_t n, int64_t K, int32_t out_dtype, int32_t num_sms,
                     dgl_plan_info* out) {
   if (!out) return DGL_ERR_ARG;
-  if (dtype != DGL_DTYPE_BF16 && dtype != DGL_DTYPE_E4M3 && dtype != DGL_DTYPE_MXFP4) return DGL_ERR_ARG;
+  if (dtype != DGL_DTYPE_BF16 && dtype != DGL_DTYPE_E4M3 && dtype != DGL_DTYPE_MXFP4 && dtype != DGL_DTYPE_W4A8)
+    return DGL_ERR_ARG;
+  if (dtype == DGL_DTYPE_W4A8) dtype = DGL_DTYPE_E4M3;  // the E4M3 tiles and decode path
   if (out_dtype != DGL_OUT_BF16 && out_dtype != DGL_OUT_F32) return DGL_ERR_ARG;
   if (m < 0 || n < 0 || K < 0) return DGL_ERR_ARG;
   if (m > INT32_MAX || n > INT32_MAX || K > INT32_MAX) return DGL_ERR_SHAPE;
@@ -714,6 +878,22 @@ dgl_status dgl_device_status(void* stream) {
   if (word != 0) {
     const int zero = 0;
     if (cudaMemcpy(ds->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return DGL_ERR_CUDA;
+    // A kernel that gave up may have left partial-tile flags set: clear every
+    // flag of this device once its work has drained, so no later launch takes
+    // a stale partial for a fresh one.
+    if (cudaDeviceSynchronize() != cudaSuccess) return DGL_ERR_CUDA;
+    {
+      std::lock_guard<std::mutex> lock(g_mu);
+      for (const Workspace& w : g_workspaces)
+        if (w.dev == dev && w.flags && cudaMemset(w.flags, 0, sizeof(int) * w.nflags) != cudaSuccess)
+          return DGL_ERR_CUDA;
+    }
+    {
+      std::lock_guard<std::mutex> lock(g_noalloc_mu);
+      if (g_noalloc[dev].ready && cudaMemset(g_noalloc[dev].flags, 0, sizeof(int) * g_noalloc[dev].nflags) != cudaSuccess)
+        return DGL_ERR_CUDA;
+    }
+    if (cudaDeviceSynchronize() != cudaSuccess) return DGL_ERR_CUDA;
     return DGL_ERR_TIMEOUT;
   }
   return DGL_OK;
@@ -732,17 +912,51 @@ dgl_status dgl_gemm_noalloc(int32_t dtype, const void* A, const void* B, const f
   DeviceState* ds = nullptr;
   st = get_device(&dev, &ds);
   if (st != DGL_OK) return st;
+  // the planner's path and tile; on the tcgen05 path a partial last wave is
+  // split along K when stream-K applies to it
+  dgl_plan_info plan;
+  choose_plan(pr.dtype, pr.out, pr.m, pr.n, pr.K, ds->num_sms, &plan);
+  // checked before the set-up, so a refused call enqueues nothing
+  if (!noalloc_fits(pr, plan, ds->num_sms)) return DGL_ERR_SHAPE;
   StaticScratch* sc = nullptr;
   st = noalloc_setup(dev, &sc);
   if (st != DGL_OK) return st;
-  // the planner's path and tile; on the tcgen05 path the last, partial wave
-  // is always split along K (when it has one)
-  dgl_plan_info plan;
-  choose_plan(pr.dtype, pr.out, pr.m, pr.n, pr.K, ds->num_sms, &plan);
   plan.stream_k = plan.path == DGL_PATH_TC ? 1 : 0;
   plan.grid = 0;
   plan.tile_k = 0;
   return run(pr, &plan, static_cast<cudaStream_t>(stream), sc);
+}
+
+dgl_status dgl_shutdown(void) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DGL_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return DGL_ERR_UNSUPPORTED;
+  dgl_status st = DGL_OK;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    bool any = false;
+    for (const Workspace& w : g_workspaces) any = any || w.dev == dev;
+    // the device's queued kernels may still read a workspace
+    if (any && cudaDeviceSynchronize() != cudaSuccess) st = DGL_ERR_CUDA;
+    for (size_t i = g_workspaces.size(); i-- > 0;) {
+      if (g_workspaces[i].dev != dev) continue;
+      free_workspace(g_workspaces[i]);
+      g_workspaces.erase(g_workspaces.begin() + static_cast<std::ptrdiff_t>(i));
+    }
+    for (auto it = g_plans.begin(); it != g_plans.end();) {
+      if (it->first.dev == dev)
+        it = g_plans.erase(it);
+      else
+        ++it;
+    }
+  }
+  {
+    // encoded tensor maps hold only addresses and extents; dropping them all
+    // means none outlives the buffers it was made for
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    for (MapSlot& s : g_map_cache) s.valid = false;
+  }
+  return st;
 }
 
 const char* dgl_status_string(int32_t status) {

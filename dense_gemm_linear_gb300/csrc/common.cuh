@@ -36,9 +36,12 @@ struct TcParams {
   int workers;
   int dp_tiles;
   int64_t sk_units;
+  // Workers the stream-K units are split over: all of them, or (a split-K
+  // tail) tail tiles x S, so that each tail tile's k-stages fall into S equal
+  // ranges, one per worker, aligned to the tile.
+  int sk_workers;
   float* ws;            // workers x CTAs-per-worker slots of 128 x BN fp32 partials
-  int* flags;           // one per slot: the epoch of the partial it holds
-  int epoch;            // differs from every earlier launch on this workspace
+  int* flags;           // one per slot: 1 once its partial is written, 0 again once it was read
   // Linear-layer epilogue: y = act(acc (* scales) + bias[col]); gated (CTA
   // pairs only): B holds the gate rows, then the up rows from row n_up, and
   // y = act(gate + bias[col]) * (up + bias[n_up + col]).  sb and bias follow
@@ -60,6 +63,17 @@ struct TcParams {
   const uint8_t* sfa;
   const uint8_t* sfb;
   int sf_vec8;
+  // Bits OR-ed into the MMA instruction descriptor: an operand format other
+  // than the kernel's own (W4A8: E2M1 in B's format field of a kind::f8f6f4
+  // kernel, whose B tiles then hold packed 4-bit codes unpacked by TMA).
+  uint32_t idesc_or;
+  // B's transaction bytes per stage are its shared-memory bytes >> b_tx_shift:
+  // 1 for packed 4-bit B, whose TMA copies count the bytes read from global
+  // memory, half of what they write to shared memory
+  int b_tx_shift;
+  // k-stages of the worker's first tile whose A and B boxes are prefetched
+  // into L2 before the wait for the previous kernel (0: none)
+  int prefetch_stages;
 };
 
 // Decode (m <= 16) kernel parameters.  A and B are read through tensor maps.
@@ -80,6 +94,9 @@ struct DecodeParams {
   int* status;          // device status word
   const float* bias;    // linear-layer epilogue: bias per column of C, or null
   int act;              // 0 identity, 1 GELU, 2 SiLU
+  uint32_t idesc_or;    // bits OR-ed into the MMA instruction descriptor (W4A8: E2M1 B rows)
+  int b_tx_shift;       // B boxes' transaction bytes = shared-memory bytes >> b_tx_shift (1: packed 4-bit B)
+  int prefetch_planes;  // K steps of the CTA's first part of B prefetched into L2 before the wait (0: none)
 };
 
 // The activations of the linear-layer epilogue.
@@ -136,16 +153,20 @@ __host__ __device__ inline int sk_worker_of(int64_t units, int workers, int64_t 
 
 // Walks worker w's segments in order: its data-parallel tiles, then (split
 // tail) at most one half tile of the last wave, or (stream-K) its range of
-// the last wave's k-stages.  Every role of a CTA walks the same sequence.
+// the last wave's k-stages: the units are cut into sk_workers equal ranges
+// (0: one per worker), and workers from sk_workers on get none.  Every role
+// of a CTA walks the same sequence.
 struct SegmentIter {
   int w, workers, nk, dp_tiles, next_dp, half_tiles, next_half;
   int64_t u, u_end;
-  __host__ __device__ SegmentIter(int worker, int num_workers, int num_kb, int dp, int64_t units, int halves = 0)
+  __host__ __device__ SegmentIter(int worker, int num_workers, int num_kb, int dp, int64_t units, int halves = 0,
+                                  int sk_workers = 0)
       : w(worker), workers(num_workers), nk(num_kb), dp_tiles(dp), next_dp(worker), half_tiles(halves),
         next_half(worker), u(0), u_end(0) {
-    if (units > 0) {
-      u = sk_range_start(units, num_workers, worker);
-      u_end = sk_range_start(units, num_workers, worker + 1);
+    const int skw = sk_workers > 0 ? sk_workers : num_workers;
+    if (units > 0 && worker < skw) {
+      u = sk_range_start(units, skw, worker);
+      u_end = sk_range_start(units, skw, worker + 1);
     }
   }
   __host__ __device__ bool next(Segment& s) {

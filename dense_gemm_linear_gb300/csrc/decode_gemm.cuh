@@ -121,10 +121,25 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  const int nk = (p.row_bytes + 127) >> 7;   // 128-byte steps of K
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB_lo);
+    tma_prefetch_desc(&tmB_hi);
+    // While the previous kernel on the stream finishes, warm L2 with the first
+    // K steps of this CTA's first part of B.  The prefetch only moves
+    // lines into L2, the point where every SM's global writes land, so what
+    // the loads read after the wait below is current whatever the previous
+    // kernel wrote.
+    int r0, r1;
+    part_rows(blockIdx.x, p.parts, p.n, r0, r1);
+    const CUtensorMap* mb = (r1 - r0) == p.rows_hi ? &tmB_hi : &tmB_lo;
+    const int planes = min(nk, p.prefetch_planes);
+    for (int j = 0; j < planes; ++j) tma_prefetch_l2_2d(mb, j * (FP8 ? 128 : 64), r0);
+  }
   griddep_launch_dependents();
   griddep_wait();
 
-  const int nk = (p.row_bytes + 127) >> 7;   // 128-byte steps of K
   const int ks = p.ksteps;                    // planes per stage
   const int b_plane = p.b_plane_bytes;        // one B box, rows rounded up to 8, x 128 bytes
   const int a_bytes = ks * DEC_A_BOX_BYTES;   // A planes first, then B planes
@@ -132,9 +147,6 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      tma_prefetch_desc(&tmA);
-      tma_prefetch_desc(&tmB_lo);
-      tma_prefetch_desc(&tmB_hi);
       const uint64_t pol_a = l2_policy_evict_last();
       const uint64_t pol_b = l2_policy_evict_first();
       const int kstep = FP8 ? 128 : 64;  // elements per 128 bytes
@@ -144,7 +156,9 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         int r0, r1;
         part_rows(part, p.parts, p.n, r0, r1);
         const CUtensorMap* mb = (r1 - r0) == p.rows_hi ? &tmB_hi : &tmB_lo;
-        const uint32_t tx = (p.m + (r1 - r0)) * 128;  // A box of m rows + B box of the part's rows
+        // A box of m rows + B box of the part's rows, counted as the bytes the
+        // copies read (packed 4-bit B: 64 a row for 128 bytes of shared memory)
+        const uint32_t tx = p.m * 128 + ((r1 - r0) * 128 >> p.b_tx_shift);
         for (int kb0 = 0; kb0 < nk; kb0 += ks) {
           if (!mbar_wait(&empty[stage], phase ^ 1)) {
             fail = STATUS_TIMEOUT_PRODUCER;
@@ -171,7 +185,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_f32acc(FP8 ? 0u : 1u, 128, 16 * G);
+      const uint32_t idesc = idesc_f32acc(FP8 ? 0u : 1u, 128, 16 * G) | p.idesc_or;
       const uint32_t ring_lo = smem_desc_sw128_lo(smem_u32(ring));
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool issued_any = false;

@@ -24,8 +24,8 @@ cudaError_t set_smem_attr_once(Kernel kern, int bytes, std::atomic<uint64_t>& do
 }
 
 // tcgen05 tile kernel.  out: 0 bf16, 1 fp32.  tile_m: 128 (one CTA per tile)
-// or 256 (a CTA pair per tile, launched as clusters of two).  tile_n: 64, 128
-// or 256.
+// or 256 (a CTA pair per tile, launched as clusters of two), or 64 (passed on
+// to the 64-row variants below; tbh unused).  tile_n: 64, 128 or 256.
 // row_staging (bf16 output only): C rows are not 16-byte aligned, so the
 // epilogue stages whole rows and writes each row's aligned body in bulk.
 // tc: tensor map of C for TMA stores (used when p.c_tma is set).
@@ -44,6 +44,13 @@ cudaError_t launch_tc_bf16_epi(int out, int tile_m, int tile_n, bool row_staging
 cudaError_t launch_tc_e4m3_epi(int out, int tile_m, int tile_n, bool row_staging, const CUtensorMap& ta,
                                const CUtensorMap& tb, const CUtensorMap& tbh, const CUtensorMap& tc,
                                const TcParams& p, int grid, cudaStream_t stream);
+// 64-row tiles (tile_m 64: one CTA per tile, M = 64 MMAs; tile_n 64, 128 or
+// 256), plain GEMM only.  The C map tc has 16-row boxes: each epilogue warp
+// holds 16 rows of such a tile.
+cudaError_t launch_tc_bf16_m64(int out, int tile_n, bool row_staging, const CUtensorMap& ta, const CUtensorMap& tb,
+                               const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_tc_e4m3_m64(int out, int tile_n, bool row_staging, const CUtensorMap& ta, const CUtensorMap& tb,
+                               const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t stream);
 // Block-scaled FP4 (MXFP4) tile kernel: 128 x 256 tiles, one CTA per tile;
 // ta / tb: byte maps of the packed operands (K / 2 bytes per row); p.sfa,
 // p.sfb: the E8M0 scales.

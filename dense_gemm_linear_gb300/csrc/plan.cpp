@@ -34,12 +34,13 @@ constexpr double kLaunchUs = 5.0;
 constexpr double kHbmGBs = 6500.0;              // achievable HBM bandwidth
 
 struct Rung {
-  int tile_m, tile_n;  // tile_m 256 = a CTA pair (cta_group::2), 128 rows per CTA
+  int tile_m, tile_n;  // tile_m 256 = a CTA pair (cta_group::2), 128 rows per CTA; 64 = one CTA, M = 64 MMAs
   double stage_us;     // per 128-byte k-stage
   double tile_us;      // per tile: accumulator drain, epilogue not hidden
 };
 constexpr Rung kLadder[] = {
-    {128, 64, 0.260, 1.0}, {128, 128, 0.265, 1.0}, {128, 256, 0.322, 2.6},
+    {64, 64, 0.200, 1.0},   {64, 128, 0.230, 1.0},   {64, 256, 0.300, 2.0},
+    {128, 64, 0.260, 1.0},  {128, 128, 0.265, 1.0},  {128, 256, 0.322, 2.6},
     {256, 128, 0.270, 1.0}, {256, 256, 0.278, 2.2},
 };
 
@@ -56,8 +57,8 @@ struct Pin {
 constexpr Pin kPins[] = {
     {DGL_DTYPE_BF16, 1024, 50257, 512, 128, 256},  // lm_head: short K, epilogue-bound; 58.9 us vs 67.0 us
     {DGL_DTYPE_BF16, 2048, 2048, 2048, 128, 256},  // one wave either way; 17.9 us vs 19.7 us
-    {DGL_DTYPE_BF16, 48, 4096, 48, 128, 128},      // 4.2-4.4 us vs 4.5-4.9 us (128x256)
-    {DGL_DTYPE_BF16, 528, 528, 1024, 128, 64},     // 8.2 us vs 8.6-8.7 us (128x128), 9.5 us (256x128)
+    {DGL_DTYPE_BF16, 48, 4096, 48, 64, 64},        // 3.57 us vs 3.73 us (128x128), 3.67 us (128x64)
+    {DGL_DTYPE_BF16, 528, 528, 1024, 64, 64},      // 7.12 us vs 7.25 us (128x64), 7.52 us (128x128)
     {DGL_DTYPE_BF16, 3402, 4096, 1024, 256, 256},  // 21.7 us vs 22.9 us (128x256)
     {DGL_DTYPE_BF16, 597, 11008, 4096, 256, 256},  // 47.0 us vs 54.9 us (128x256, the screen's pick)
     {DGL_DTYPE_E4M3, 597, 11008, 4096, 256, 256},  // 30.4 us vs 33.4 us
@@ -91,10 +92,12 @@ static const Rung* find_rung(int tile_m, int tile_n) {
   return nullptr;
 }
 
-constexpr double kFixupUs = 2.0;  // write + read of one fp32 partial tile per split tile
+constexpr double kFixupUs = 8.0;  // hand-over of fp32 partial tiles: write, wait, read, add (measured)
 
+// stream_k: 0 data-parallel, 1 the tail's k-stages over all workers, S >= 2
+// each tail tile over S workers.
 static double tc_estimate_us(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int tile_m, int tile_n,
-                             int num_sms, bool stream_k, int* grid_out) {
+                             int num_sms, int stream_k, int* grid_out) {
   const Rung* r = find_rung(tile_m, tile_n);
   const int cg = tile_m == 256 ? 2 : 1;
   const double esize = dtype == DGL_DTYPE_E4M3 ? 1.0 : 2.0;
@@ -107,7 +110,8 @@ static double tc_estimate_us(int dtype, int out_dtype, int64_t m, int64_t n, int
   double us = kLaunchUs + static_cast<double>(waves) * tile_us;
   if (stream_k) {
     const int64_t full = tiles / units;                       // whole waves, data-parallel
-    const double tail_stages = static_cast<double>(tiles - full * units) * k_stages / units;
+    const double tail_stages = stream_k >= 2 ? std::ceil(k_stages / stream_k)
+                                             : static_cast<double>(tiles - full * units) * k_stages / units;
     us = kLaunchUs + static_cast<double>(full) * tile_us + tail_stages * r->stage_us + kFixupUs + r->tile_us;
   }
   const double hbm_us = operand_bytes(dtype, out_dtype, m, n, K) / (kHbmGBs * 1e3) + kLaunchUs;
@@ -118,12 +122,35 @@ static double tc_estimate_us(int dtype, int out_dtype, int64_t m, int64_t n, int
 // Stream-K pays when the last wave is partial and each worker gets at least
 // a few k-stages of the tail.
 bool stream_k_eligible(int64_t m, int64_t n, int64_t K, int dtype, int tile_m, int tile_n, int num_sms) {
+  if (tile_m == 64) return false;  // 64-row tiles: small problems, no partial-tile hand-over
   const int cg = tile_m == 256 ? 2 : 1;
   const int64_t tiles = ((m + tile_m - 1) / tile_m) * ((n + tile_n - 1) / tile_n);
   const int64_t units = std::max(1, num_sms / cg);
   const int64_t nk = (K * (dtype == DGL_DTYPE_E4M3 ? 1 : 2) + 127) / 128;
   const int64_t tail = tiles % units;
   return tail != 0 && tail * nk >= 4 * units;
+}
+
+// Split-K tail: with long K, each tile of a partial last wave that fills at
+// most half the workers runs on S = floor(workers / tail) workers (at most 4),
+// each taking an equal, tile-aligned range of its k-stages; the worker holding
+// the first range adds the others' fp32 partials before the epilogue.  The
+// wave of whole tiles before it is unchanged.  Needs at least one whole wave
+// before the tail and 64 or more k-blocks of 128 bytes (16 or more per
+// range): the hand-over of a partial tile costs about 8 us (measured at
+// 4096^3: bf16, 64 k-blocks, 77.9 -> 76.4 us; E4M3, 32 k-blocks, 44.5 ->
+// 47.1 us, a loss).  Short K takes the half tiles below.  Returns S, or 0.
+int tail_split_ways(int64_t m, int64_t n, int64_t K, int dtype, int tile_m, int tile_n, int num_sms) {
+  if (tile_m == 64) return 0;
+  const int cg = tile_m == 256 ? 2 : 1;
+  const int64_t tiles = ((m + tile_m - 1) / tile_m) * ((n + tile_n - 1) / tile_n);
+  const int64_t units = std::max(1, num_sms / cg);
+  const int64_t nk = (K * (dtype == DGL_DTYPE_E4M3 ? 1 : 2) + 127) / 128;
+  const int64_t tail = tiles % units;
+  if (tiles <= units || tail == 0 || nk < 64) return 0;
+  int ways = static_cast<int>(std::min<int64_t>(4, units / tail));
+  while (ways > 1 && nk / ways < 16) --ways;
+  return ways >= 2 ? ways : 0;
 }
 
 // Split tail: a 256-wide tile's last, partial wave runs as half tiles when
@@ -134,7 +161,7 @@ bool stream_k_eligible(int64_t m, int64_t n, int64_t K, int dtype, int tile_m, i
 // tile's bytes per k-block for half its MMA work and runs load-bound, and the
 // split measured no faster (4096^3) or slower (8192^3).
 bool split_tail_eligible(int64_t m, int64_t n, int64_t K, int dtype, int tile_m, int tile_n, int num_sms) {
-  if (tile_n != 256) return false;
+  if (tile_n != 256 || tile_m == 64) return false;
   const int64_t nk = (K * (dtype == DGL_DTYPE_E4M3 ? 1 : 2) + 127) / 128;
   if (nk > 16) return false;
   const int cg = tile_m == 256 ? 2 : 1;
@@ -148,7 +175,7 @@ int tc_tile_k(int dtype) { return dtype == DGL_DTYPE_E4M3 ? 128 : 64; }
 
 int tc_stages(int tile_m, int tile_n) {
   const int cg = tile_m == 256 ? 2 : 1;
-  const int stage = 128 * 128 + tile_n / cg * 128;
+  const int stage = (tile_m == 64 ? 64 : 128) * 128 + tile_n / cg * 128;
   const int s = (232448 - 1024 - 32768 - 512) / stage;
   return s < 8 ? s : 8;
 }
@@ -166,16 +193,35 @@ void fill_tc_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int
   out->stages = tc_stages(tile_m, tile_n);
   out->cta_group = tile_m == 256 ? 2 : 1;
   tile_metrics(m, n, tile_m, tile_n, num_sms / out->cta_group, out);
-  // stream_k: 1 force on (if eligible), 0 force off, -1 let the model decide
+  // stream_k: -2 the planner's default (a split-K tail where
+  // tail_split_ways allows one), -1 the model decides between stream-K and
+  // none, 0 none, 1 stream-K over all workers (if eligible), S >= 2 a split-K
+  // tail over S workers per tile (if the tail allows it)
   out->split_tail = split_tail_eligible(m, n, K, dtype, tile_m, tile_n, num_sms) ? 1 : 0;
   const bool sk_ok = stream_k_eligible(m, n, K, dtype, tile_m, tile_n, num_sms);
   int grid = 0;
-  out->est_us = tc_estimate_us(dtype, out_dtype, m, n, K, tile_m, tile_n, num_sms, false, &grid);
+  out->est_us = tc_estimate_us(dtype, out_dtype, m, n, K, tile_m, tile_n, num_sms, 0, &grid);
   out->grid = grid;
   out->stream_k = 0;
-  if (sk_ok && stream_k != 0) {
+  int ways = 0;
+  if (stream_k == -2) {
+    ways = tail_split_ways(m, n, K, dtype, tile_m, tile_n, num_sms);
+  } else if (stream_k >= 2 && tile_m != 64) {
+    const int cg = tile_m == 256 ? 2 : 1;
+    const int64_t tiles = ((m + tile_m - 1) / tile_m) * ((n + tile_n - 1) / tile_n);
+    const int64_t units = std::max(1, num_sms / cg);
+    const int64_t tail = tiles % units;
+    if (tail > 0 && tail * stream_k <= units) ways = stream_k;
+  }
+  if (ways >= 2) {
     int grid_sk = 0;
-    const double est_sk = tc_estimate_us(dtype, out_dtype, m, n, K, tile_m, tile_n, num_sms, true, &grid_sk);
+    out->est_us = tc_estimate_us(dtype, out_dtype, m, n, K, tile_m, tile_n, num_sms, ways, &grid_sk);
+    out->grid = grid_sk;
+    out->stream_k = ways;
+    out->split_tail = 0;
+  } else if (sk_ok && (stream_k == 1 || stream_k == -1)) {
+    int grid_sk = 0;
+    const double est_sk = tc_estimate_us(dtype, out_dtype, m, n, K, tile_m, tile_n, num_sms, 1, &grid_sk);
     if (stream_k == 1 || est_sk < 0.97 * out->est_us) {
       out->est_us = est_sk;
       out->grid = grid_sk;
@@ -286,7 +332,7 @@ void choose_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int 
   }
   for (const Pin& pin : kPins) {
     if (pin.dtype == dtype && pin.m == m && pin.n == n && pin.K == K) {
-      fill_tc_plan(dtype, out_dtype, m, n, K, pin.tile_m, pin.tile_n, num_sms, out, 0);
+      fill_tc_plan(dtype, out_dtype, m, n, K, pin.tile_m, pin.tile_n, num_sms, out, -2);
       return;
     }
   }
@@ -304,7 +350,7 @@ void choose_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int 
                           std::ceil(static_cast<double>(n) / r.tile_n) * r.tile_n;
     if (any_pass && padded > 1.25 * area) continue;
     dgl_plan_info cand;
-    fill_tc_plan(dtype, out_dtype, m, n, K, r.tile_m, r.tile_n, num_sms, &cand, 0);
+    fill_tc_plan(dtype, out_dtype, m, n, K, r.tile_m, r.tile_n, num_sms, &cand, -2);
     // ties go to the larger tile (later rungs are larger)
     if (!have || cand.est_us <= best.est_us * (1.0 + 1e-9)) {
       best = cand;
@@ -319,7 +365,7 @@ void choose_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int 
 namespace dgl {
 
 bool tc_supported_epi_tile(int tile_m, int tile_n, bool gated) {
-  if (!tc_supported_tile(tile_m, tile_n) || (tile_n != 128 && tile_n != 256)) return false;
+  if (!tc_supported_tile(tile_m, tile_n) || tile_m == 64 || (tile_n != 128 && tile_n != 256)) return false;
   return !gated || tile_m == 256;
 }
 
@@ -328,7 +374,8 @@ void choose_linear_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t 
   if (!gated) {
     choose_plan(dtype, out_dtype, m, n, K, num_sms, out);
     if (out->path == DGL_PATH_TC && !tc_supported_epi_tile(out->tile_m, out->tile_n, false))
-      fill_tc_plan(dtype, out_dtype, m, n, K, out->tile_m, 128, num_sms, out, 0);
+      fill_tc_plan(dtype, out_dtype, m, n, K, out->tile_m == 64 ? 128 : out->tile_m, out->tile_n == 64 ? 128 : out->tile_n,
+                   num_sms, out, 0);
     return;
   }
   // gate and up rows side by side: a product with 2 n rows of B on CTA pairs

@@ -14,11 +14,14 @@ double operand_bytes(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K);
 int tc_tile_k(int dtype);
 int tc_stages(int tile_m, int tile_n);
 bool tc_supported_tile(int tile_m, int tile_n);
-// stream_k: 1 on (when eligible), 0 off, -1 the cost model decides.
+// stream_k: -2 the planner's default (split-K tail where it applies), -1 the
+// cost model decides on stream-K, 0 off, 1 stream-K over all workers (when
+// eligible), S >= 2 a split-K tail over S workers per tile (when it fits).
 void fill_tc_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int tile_m, int tile_n, int num_sms,
                   dgl_plan_info* out, int stream_k);
 bool split_tail_eligible(int64_t m, int64_t n, int64_t K, int dtype, int tile_m, int tile_n, int num_sms);
 bool stream_k_eligible(int64_t m, int64_t n, int64_t K, int dtype, int tile_m, int tile_n, int num_sms);
+int tail_split_ways(int64_t m, int64_t n, int64_t K, int dtype, int tile_m, int tile_n, int num_sms);
 void fill_decode_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int num_sms, dgl_plan_info* out);
 int decode_parts(int64_t n, int num_sms);
 int decode_grid(int64_t n, int num_sms);

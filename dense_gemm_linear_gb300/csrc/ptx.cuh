@@ -119,6 +119,16 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
+// Bring one box of a tiled tensor into L2 (no shared memory, no barrier): a
+// hint that lets a later load of the same box hit L2.  c0 is the innermost
+// coordinate.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t c0, int32_t c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1)
+               : "memory");
+}
+
 // L2 eviction-priority policies for cache hints.
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   uint64_t p;

@@ -56,13 +56,19 @@ constexpr int tc_ring_stages(int stage_bytes, int staging_bytes) {
   return s < 8 ? s : 8;
 }
 
-template <int BN_, bool FP8_, bool OUT_F32_, bool ROWSTG_, int CG_ = 1, bool EPI_ = false, bool MX_ = false>
+template <int BN_, bool FP8_, bool OUT_F32_, bool ROWSTG_, int CG_ = 1, bool EPI_ = false, bool MX_ = false,
+          int BM_ = 128>
 struct TcConfig {
   static constexpr int CG = CG_;                        // CTAs per MMA: 1, or 2 for a CTA pair (M = 256)
   // EPI: the linear-layer epilogue (bias, activation, and on CTA pairs the
   // gated up projection) is compiled in; plain GEMM variants leave it out.
   static constexpr bool EPI = EPI_;
-  static constexpr int BM = 128;                        // rows of C per CTA
+  // Rows of C per CTA: 128, or 64 for the small rungs of the ladder (one CTA,
+  // an M = 64 MMA).  An M = 64 accumulator puts row 16 q + r (r < 16) in
+  // tensor-memory lane 32 q + r, so each epilogue warp of lane quarter q holds
+  // 16 rows, in its threads 0-15.
+  static constexpr int BM = BM_;
+  static constexpr int WARP_ROWS = BM / 4;              // tile rows per lane quarter: 32, or 16
   static constexpr int TILE_M = BM * CG;                // rows of C per tile
   static constexpr int BN = BN_;                        // columns of C per tile
   static constexpr int B_ROWS = BN / CG;                // rows of B each CTA loads per stage
@@ -115,7 +121,7 @@ struct TcConfig {
   static constexpr int SCALE_SLOT_COLS = 4 * SCALE_ATOMS;
   static constexpr int BAR_BYTES = 8 * (2 * STAGES + 6) + 8 + 32;
   // stream-K: one CTA's fp32 partial tile, and how many fit in the ring
-  static constexpr int SLOT_BYTES = BM * BN * 4;
+  static constexpr int SLOT_BYTES = 128 * BN * 4;
   static constexpr int RING_SLOTS = STAGES * STAGE_BYTES / SLOT_BYTES;
   // fix-up staging per epilogue warp: 2 KB pieces, two of them when room allows
   static constexpr int FX_WARP_BYTES = ROWSTG ? 16 * ROW_PITCH : 4096;
@@ -123,6 +129,7 @@ struct TcConfig {
   static constexpr int SMEM_BYTES =
       1024 /* alignment slack */ + STAGES * (STAGE_BYTES + SCALE_STAGE_BYTES) + STG_TOTAL + BAR_BYTES;
   static_assert(BN == 64 || BN == 128 || BN == 256, "tile widths of the ladder");
+  static_assert(BM == 128 || (BM == 64 && CG == 1 && !EPI && !MX), "64-row tiles: one CTA, plain GEMM");
   static_assert(STAGES >= 3, "ring too shallow");
   static_assert((ROW_PITCH / 16) % 2 == 1, "row pitch: odd multiple of 16 bytes");
   static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation: power of two");
@@ -130,7 +137,10 @@ struct TcConfig {
   static_assert(!MX || ((BN == 128 || BN == 256) && CG == 1 && !FP8 && !EPI), "block-scaled FP4: 128-row tiles, one CTA");
   static_assert(!MX || SCALE_COL0 + STAGES * SCALE_SLOT_COLS <= TMEM_COLS, "scale ring fits in tensor memory");
   static_assert(B_STAGE_BYTES % 1024 == 0, "B stage tiles stay 1024-byte aligned");
-  static_assert(RING_SLOTS >= 1, "a partial tile fits in the ring");
+  // stream-K (partial tiles handed over through a workspace) runs on the
+  // 128-row tiles only; the host never splits a 64-row tile's k-stages
+  static constexpr bool STREAM_K = BM == 128;
+  static_assert(RING_SLOTS >= 1 || !STREAM_K, "a partial tile fits in the ring");
   static_assert(FX_WARP_BYTES >= 2048 && FX_WARP_BYTES % 16 == 0, "fix-up staging piece");
 };
 
@@ -202,7 +212,8 @@ struct StageIter {
   int kb = 0, kb1 = 0, mb = 0, nb = 0;
   int tiles_m, tiles_n, group_m;
   __device__ StageIter(int worker, const TcParams& prm)
-      : it(worker, prm.workers, prm.num_kb, prm.dp_tiles, prm.sk_units, prm.half_tiles), tiles_m(prm.tiles_m),
+      : it(worker, prm.workers, prm.num_kb, prm.dp_tiles, prm.sk_units, prm.half_tiles, prm.sk_workers),
+        tiles_m(prm.tiles_m),
         tiles_n(prm.tiles_n), group_m(prm.group_m) {}
   __device__ bool next(int& mb_out, int& nb_out, int& kb_out) {
     while (kb >= kb1) {
@@ -319,6 +330,27 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  if (warp == 0 && lane == 0 && p.prefetch_stages > 0 && !p.a_mn && !p.b_mn) {
+    // While the previous kernel on the stream finishes, warm L2 with the first
+    // k-stages of this CTA's first tile.  The prefetch only moves lines
+    // into L2, the point where every SM's global writes land, so what the
+    // loads read after the wait below is current whatever the previous kernel
+    // wrote.
+    SegmentIter it0(cluster_id, p.workers, p.num_kb, p.dp_tiles, p.sk_units, p.half_tiles, p.sk_workers);
+    Segment s0;
+    if (it0.next(s0) && !s0.half) {
+      int mb, nb;
+      tile_coords(s0.tile, p.tiles_m, p.tiles_n, p.group_m, mb, nb);
+      const int a_row = mb * Cfg::TILE_M + static_cast<int>(rank) * BM;
+      const int b_row = (Cfg::EPI && CG == 2 && p.gated) ? (rank == 0 ? 0 : p.n_up) + nb * Cfg::B_ROWS
+                                                         : nb * BN + static_cast<int>(rank) * Cfg::B_ROWS;
+      const int kb1 = min(s0.kb1, s0.kb0 + min(STAGES, p.prefetch_stages));
+      for (int kb = s0.kb0; kb < kb1; ++kb) {
+        tma_prefetch_l2_2d(&tmA, kb * Cfg::BK, a_row);
+        tma_prefetch_l2_2d(&tmB, kb * Cfg::BK, b_row);
+      }
+    }
+  }
   // set-up touched no global data: let the next kernel launch, then wait for
   // the previous one before reading operands or writing C
   griddep_launch_dependents();
@@ -342,7 +374,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       const uint64_t pol = l2_policy_evict_last();
       uint32_t stage = 0, phase = 0;
       int64_t issued = 0;
-      SegmentIter it(cluster_id, p.workers, p.num_kb, p.dp_tiles, p.sk_units, p.half_tiles);
+      SegmentIter it(cluster_id, p.workers, p.num_kb, p.dp_tiles, p.sk_units, p.half_tiles, p.sk_workers);
       Segment sg;
       while (!fail && it.next(sg)) {
         int mb, nb;
@@ -356,7 +388,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                                     : nb * BN + static_cast<int>(rank) * Cfg::B_ROWS;
         const CUtensorMap* tmb = sg.half ? &tmBh : &tmB;
         const int b_rows = sg.half ? Cfg::B_ROWS / 2 : Cfg::B_ROWS;
-        const uint32_t stage_bytes = sg.half ? Cfg::A_STAGE_BYTES + Cfg::B_STAGE_BYTES / 2 : Cfg::STAGE_BYTES;
+        // a stage's transaction bytes: what the copies read from global
+        // memory (packed 4-bit B lands in twice its size of shared memory)
+        const uint32_t stage_bytes =
+            Cfg::A_STAGE_BYTES + ((sg.half ? Cfg::B_STAGE_BYTES / 2 : Cfg::B_STAGE_BYTES) >> p.b_tx_shift);
         for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
           const bool ok = mbar_wait(&empty[stage], phase ^ 1);
           if (!ok) {
@@ -402,7 +437,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && rank == 0) {
       // MN-major operands set the instruction's transpose bits (15: A, 16: B)
-      const uint32_t idesc_major = (p.a_mn ? 1u << 15 : 0u) | (p.b_mn ? 1u << 16 : 0u);
+      const uint32_t idesc_major = (p.a_mn ? 1u << 15 : 0u) | (p.b_mn ? 1u << 16 : 0u) | p.idesc_or;
       const uint32_t idesc_full = idesc_f32acc(Cfg::FP8 ? 0u : 1u, Cfg::TILE_M, BN) | idesc_major;
       const uint32_t idesc_half = idesc_f32acc(Cfg::FP8 ? 0u : 1u, Cfg::TILE_M, BN / 2) | idesc_major;
       // Shared-memory descriptors differ only in their low word: the address
@@ -417,7 +452,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       const uint32_t b_kstep = (p.b_mn ? MN_K_STEP_BYTES : Cfg::MMA_K_BYTES) >> 4;
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool issued_any = false;
-      SegmentIter it(cluster_id, p.workers, p.num_kb, p.dp_tiles, p.sk_units, p.half_tiles);
+      SegmentIter it(cluster_id, p.workers, p.num_kb, p.dp_tiles, p.sk_units, p.half_tiles, p.sk_workers);
       Segment sg;
       while (!fail && it.next(sg)) {
         const bool ok = mbar_wait(&tempty[acc], acc_phase ^ 1);
@@ -513,7 +548,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     uint8_t* stg = Cfg::ROWSTG ? sStg + q * 32 * Cfg::ROW_PITCH : sStg + e * 4096;
     const uint32_t stg_addr = smem_u32(stg);
     uint32_t acc = 0, acc_phase = 0, fx_phase = 0;
-    SegmentIter it(cluster_id, p.workers, p.num_kb, p.dp_tiles, p.sk_units, p.half_tiles);
+    SegmentIter it(cluster_id, p.workers, p.num_kb, p.dp_tiles, p.sk_units, p.half_tiles, p.sk_workers);
     Segment sg;
     while (it.next(sg)) {
       int mb, nb;
@@ -535,7 +570,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         break;
       }
       tc_fence_after_sync();
-      const int row0 = mb * Cfg::TILE_M + static_cast<int>(rank) * BM + q * 32;
+      const int row0 = mb * Cfg::TILE_M + static_cast<int>(rank) * BM + q * Cfg::WARP_ROWS;
+      const bool row_lane = lane < Cfg::WARP_ROWS;  // this thread holds a row of the tile
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
 
       // ---- stream-K: a segment that does not hold the tile's first k-stage
@@ -545,7 +581,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       // ((c * 4 + q) * 8 + t) * 32 + lane holds columns 32c + 4t .. 32c + 4t + 3
       // of slab row 32q + lane, so each warp's 32 x 32 chunk is 4 KB of
       // contiguous memory, written and read with bulk copies.
-      if (sg.kb0 > 0) {
+      if (Cfg::STREAM_K && sg.kb0 > 0) {
         uint8_t* slot = reinterpret_cast<uint8_t*>(p.ws) + (static_cast<int64_t>(cluster_id) * CG + rank) * Cfg::SLOT_BYTES;
         const uint32_t fx = Cfg::ROWSTG ? stg_addr + half * Cfg::FX_WARP_BYTES : stg_addr;
         int piece = 0;
@@ -592,19 +628,19 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           __threadfence();
         }
         named_bar_sync(5, Cfg::EPI_WARPS * 32);  // every epilogue warp's pieces are written
-        if (warp == 2 && lane == 0) st_release_gpu(p.flags + cluster_id * CG + rank, p.epoch);
+        if (warp == 2 && lane == 0) st_release_gpu(p.flags + cluster_id * CG + rank, 1);
         next_acc<Cfg::ACC_BUFS>(acc, acc_phase);
         continue;
       }
-      if (sg.kb1 < p.num_kb) {
+      if (Cfg::STREAM_K && sg.kb1 < p.num_kb) {
         // Finisher: the tile's other k-stages belong to workers cluster_id + 1
         // .. w_last (an empty range holds none).  This is the worker's last
         // segment, so every MMA has finished and the operand ring is free:
         // partial tiles are bulk-copied into it, RING_SLOTS at a time.
         const int64_t t_rel = sg.tile - p.dp_tiles;
-        const int w_last = sk_worker_of(p.sk_units, p.workers, (t_rel + 1) * p.num_kb - 1);
+        const int w_last = sk_worker_of(p.sk_units, p.sk_workers, (t_rel + 1) * p.num_kb - 1);
         auto nonempty = [&](int w) {
-          return sk_range_start(p.sk_units, p.workers, w) != sk_range_start(p.sk_units, p.workers, w + 1);
+          return sk_range_start(p.sk_units, p.sk_workers, w) != sk_range_start(p.sk_units, p.sk_workers, w + 1);
         };
         const uint32_t ring = smem_u32(sA);
         int wc = cluster_id + 1;
@@ -619,7 +655,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             int i = 0;
             for (int w = w_first; w < wc; ++w) {
               if (!nonempty(w)) continue;
-              if (!wait_flag_gpu(p.flags + w * CG + rank, p.epoch)) fail |= STATUS_TIMEOUT_FIXUP;
+              if (!wait_flag_gpu(p.flags + w * CG + rank, 1)) fail |= STATUS_TIMEOUT_FIXUP;
               if (i == 0) {
                 fence_proxy_async_global();
                 fence_proxy_async_shared();
@@ -634,6 +670,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           }
           if (!mbar_wait(fixbar, fx_phase)) fail |= STATUS_TIMEOUT_FIXUP;
           fx_phase ^= 1;
+          if (warp == 2 && lane == 0) {
+            // the partials are in shared memory: clear their flags for the
+            // next launch on this workspace
+            for (int w = w_first; w < wc; ++w)
+              if (nonempty(w)) p.flags[w * CG + rank] = 0;
+          }
 #pragma unroll 1
           for (int u = 0; u < CPW; ++u) {
             const int c = half * CPW + u;
@@ -666,11 +708,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       const int out_w = (gated || sg.half) ? BN / 2 : BN;
       const int ocol0 = sg.half ? nb * BN + (sg.half - 1) * (BN / 2) : nb * out_w;
       float row_scale = 0.0f;
-      if constexpr (Cfg::FP8) row_scale = (row0 + lane < p.m) ? p.sa[row0 + lane] : 0.0f;
+      if constexpr (Cfg::FP8) row_scale = (row_lane && row0 + lane < p.m) ? p.sa[row0 + lane] : 0.0f;
       // row staging (bf16 C, rows not 16-byte aligned): this thread's row
       const int row = row0 + lane;
       const int ncols = min(out_w, p.n - ocol0);
-      const int L = (Cfg::ROWSTG && row < p.m) ? 2 * ncols : 0;  // valid bytes of the row's segment
+      const int L = (Cfg::ROWSTG && row_lane && row < p.m) ? 2 * ncols : 0;  // valid bytes of the row's segment
       uint8_t* rowp = L > 0 ? reinterpret_cast<uint8_t*>(static_cast<__nv_bfloat16*>(p.C) +
                                                          static_cast<int64_t>(row) * p.ldc + ocol0)
                             : nullptr;
@@ -749,7 +791,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             // one row per step, a column per lane
             const int col = col0 + lane;
 #pragma unroll 4
-            for (int rr = 0; rr < 32; ++rr) {
+            for (int rr = 0; rr < Cfg::WARP_ROWS; ++rr) {
               const int grow = row0 + rr;
               if (grow < p.m && col < p.n) {
                 if constexpr (Cfg::OUT_F32) {

@@ -10,10 +10,10 @@
 
 namespace dgl {
 
-template <int BN, bool FP8, bool OUT_F32, bool ROWSTG, int CG, bool EPI, bool MX = false>
+template <int BN, bool FP8, bool OUT_F32, bool ROWSTG, int CG, bool EPI, bool MX = false, int BM = 128>
 cudaError_t tc_launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tbh, const CUtensorMap& tc,
                           const TcParams& p, int grid, cudaStream_t stream) {
-  using Cfg = TcConfig<BN, FP8, OUT_F32, ROWSTG, CG, EPI, MX>;
+  using Cfg = TcConfig<BN, FP8, OUT_F32, ROWSTG, CG, EPI, MX, BM>;
   auto kern = tc_gemm_kernel<Cfg>;
   static std::atomic<uint64_t> attr_done{0};  // one bit per device
   cudaError_t e = set_smem_attr_once(kern, Cfg::SMEM_BYTES, attr_done);
@@ -41,17 +41,32 @@ cudaError_t tc_launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CU
   return cudaLaunchKernelEx(&cfg, kern, ta, tb, tbh, tc, p);
 }
 
-template <int BN, bool FP8, int CG, bool EPI>
+template <int BN, bool FP8, int CG, bool EPI, int BM = 128>
 cudaError_t tc_launch_bn(int out, bool row_staging, const CUtensorMap& ta, const CUtensorMap& tb,
                          const CUtensorMap& tbh, const CUtensorMap& tc, const TcParams& p, int grid,
                          cudaStream_t stream) {
-  if (out == 1) return tc_launch_one<BN, FP8, true, false, CG, EPI>(ta, tb, tbh, tc, p, grid, stream);
-  if (row_staging) return tc_launch_one<BN, FP8, false, true, CG, EPI>(ta, tb, tbh, tc, p, grid, stream);
-  return tc_launch_one<BN, FP8, false, false, CG, EPI>(ta, tb, tbh, tc, p, grid, stream);
+  if (out == 1) return tc_launch_one<BN, FP8, true, false, CG, EPI, false, BM>(ta, tb, tbh, tc, p, grid, stream);
+  if (row_staging)
+    return tc_launch_one<BN, FP8, false, true, CG, EPI, false, BM>(ta, tb, tbh, tc, p, grid, stream);
+  return tc_launch_one<BN, FP8, false, false, CG, EPI, false, BM>(ta, tb, tbh, tc, p, grid, stream);
+}
+
+// 64-row tiles (one CTA, M = 64 MMAs): plain GEMM variants only, compiled
+// in their own translation units.
+template <bool FP8>
+cudaError_t tc_launch_m64(int out, int tile_n, bool row_staging, const CUtensorMap& ta, const CUtensorMap& tb,
+                          const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t stream) {
+  switch (tile_n) {
+    case 64: return tc_launch_bn<64, FP8, 1, false, 64>(out, row_staging, ta, tb, tb, tc, p, grid, stream);
+    case 128: return tc_launch_bn<128, FP8, 1, false, 64>(out, row_staging, ta, tb, tb, tc, p, grid, stream);
+    case 256: return tc_launch_bn<256, FP8, 1, false, 64>(out, row_staging, ta, tb, tb, tc, p, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 // EPI: the linear-layer variants, compiled for the 128- and 256-wide tiles
-// only (tc_supported_epi_tile); the plain variants cover the whole ladder.
+// only (tc_supported_epi_tile); the plain variants cover the ladder's 128- and
+// 256-row tiles (the 64-row ones: tc_launch_m64).
 template <bool FP8, bool EPI>
 cudaError_t tc_launch(int out, int tile_m, int tile_n, bool row_staging, const CUtensorMap& ta, const CUtensorMap& tb,
                       const CUtensorMap& tbh, const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t stream) {

@@ -33,14 +33,22 @@
  *
  * Memory and ownership: A, B, C, sa, sb are DEVICE pointers owned by the
  * caller, on the current CUDA device.  The library never copies to or from the
- * host.  It keeps a small per-device plan cache and, for plans with
- * stream_k = 1, a per-(device, stream) workspace of fp32 partial tiles
- * (about 20 MB), allocated with cudaMalloc on the first such call on that
- * stream and kept until the process exits; that first call therefore must not
- * be made while the stream is being captured into a CUDA graph.  Calls are
- * asynchronous with respect to the host: work is enqueued on `stream` (a
- * cudaStream_t; NULL = the legacy default stream) and buffers must stay
- * valid until it completes.
+ * host.  It keeps a small per-device plan cache, a cache of encoded tensor
+ * maps and, for plans with stream_k = 1, a per-(device, stream) workspace of
+ * fp32 partial tiles (at least 24 MB), allocated with cudaMalloc on the first
+ * such call on that stream.  At most four such workspaces are kept per
+ * device: a call on a fifth stream first waits for the device to drain, then
+ * frees the least recently used one.  dgl_shutdown() frees them all.  A call
+ * made while its stream is being captured into a CUDA graph never allocates:
+ * if the stream has no workspace yet it runs the data-parallel schedule
+ * instead (make one call on that stream before capturing to keep the split
+ * schedule).  Every launch leaves the workspace's flags cleared, so a
+ * captured graph may be replayed.  Other calls that allocate or free a
+ * workspace must not be made while another stream of the device is being
+ * captured.  Calls are asynchronous
+ * with respect to the host: work is enqueued on `stream` (a cudaStream_t;
+ * NULL = the legacy default stream) and buffers must stay valid until it
+ * completes.
  *
  * Errors: arguments are validated on the host before any launch; a failed
  * check returns an error code and enqueues nothing.  Nothing is printed and
@@ -68,7 +76,7 @@ typedef enum {
 } dgl_status;
 
 typedef enum { DGL_OUT_BF16 = 0, DGL_OUT_F32 = 1 } dgl_out_t;
-typedef enum { DGL_DTYPE_BF16 = 0, DGL_DTYPE_E4M3 = 1, DGL_DTYPE_MXFP4 = 2 } dgl_dtype_t;
+typedef enum { DGL_DTYPE_BF16 = 0, DGL_DTYPE_E4M3 = 1, DGL_DTYPE_MXFP4 = 2, DGL_DTYPE_W4A8 = 3 } dgl_dtype_t;
 typedef enum { DGL_PATH_TC = 0, DGL_PATH_DECODE = 1, DGL_PATH_EMPTY = 2 } dgl_path_t;
 /* Activations of dgl_linear: GELU(x) = x * Phi(x) (Phi the standard normal
  * distribution function, the exact erf form); SiLU(x) = x * sigma(x) (sigma
@@ -99,7 +107,9 @@ typedef struct {
   double wq_eff;
   double dim_eff;
   double est_us;      /* cost-model estimate of the kernel time, microseconds */
-  int32_t stream_k;   /* 1: tiles of the last, partial wave are split along K across all workers */
+  int32_t stream_k;   /* 1: tiles of the last, partial wave are split along K across all workers; */
+                      /* S >= 2: each such tile's k-stages in S equal ranges on S workers (a split-K tail, */
+                      /*    the planner's choice for long K when that wave fills at most half the workers) */
   int32_t split_tail; /* 1: the last, partial wave's tiles (tile_n 256) run as two half tiles each, */
                       /*    when that wave fills at most half the workers (not with stream_k or gated); */
                       /*    the planner sets it only for K of at most 16 k-blocks of 128 bytes */
@@ -132,7 +142,8 @@ dgl_status dgl_gemm_fp8(const void* A, const void* B, const float* sa, const flo
  * Either GEMM with a caller-chosen plan instead of the planner's choice: the
  * forced-tile sweep of FlyDSL pull request 1303, whose tests run each tile of
  * both ladders on a shape that no tile divides.
- * dtype: dgl_dtype_t (sa/sb ignored for bf16).  plan->path, tile_m, tile_n,
+ * dtype: dgl_dtype_t: bf16 (sa/sb ignored), E4M3 or W4A8 (the operands of
+ * dgl_gemm_w4a8).  plan->path, tile_m, tile_n,
  * stream_k, split_tail and grid are honoured (grid <= 0 picks one), and for the decode
  * path tile_k (K elements per ring stage: a multiple of 128 bytes and of
  * k_group such steps, 0 = pick);
@@ -170,6 +181,25 @@ dgl_status dgl_gemm_mxfp4(const void* A, const void* B, const uint8_t* sfa, cons
                           int64_t N, int64_t K, int64_t m_valid, int64_t n_valid, int32_t out_dtype, void* stream);
 
 /*
+ * 8-bit activations times 4-bit weights (W4A8).  The "Gemm Optimization"
+ * guide's bandwidth formulas (section 8.2) count, for 4-bit weights, one byte
+ * per element of A, half a byte per element of B, a bf16 C and (M + N) fp32
+ * scales.  Read on GB300, whose tensor cores take E4M3 and E2M1 operands in
+ * one kind::f8f6f4 instruction: A holds E4M3 codes with a per-row scale sa,
+ * B holds E2M1 codes (values 0, +-0.5, +-1, +-1.5, +-2, +-3, +-4, +-6) two
+ * to a byte, element 2t in the low four bits of byte t, with a per-row scale
+ * sb (one per column of C):
+ *   C[i, j] = (acc * sa[i]) * sb[j],  acc = fp32 sum of e4m3(A[i, k]) e2m1(B[j, k])
+ * A: m_valid rows of K bytes (16-byte aligned).  B: n_valid rows of K / 2
+ * bytes (32-byte aligned).  K: a multiple of 128.  sa, sb, C, M, N, m_valid,
+ * n_valid, out_dtype and the never-written region as dgl_gemm_fp8, whose
+ * tiles and decode path (m_valid <= 16) it shares.  Errors: DGL_ERR_ALIGN for
+ * K not a multiple of 128 or B not 32-byte aligned; otherwise as dgl_gemm_fp8.
+ */
+dgl_status dgl_gemm_w4a8(const void* A, const void* B, const float* sa, const float* sb, void* C, int64_t M,
+                         int64_t N, int64_t K, int64_t m_valid, int64_t n_valid, int32_t out_dtype, void* stream);
+
+/*
  * Size in bytes of the fixed device array that dgl_gemm_noalloc uses for its
  * fp32 partial tiles: 20 MiB, one 128 x 256 fp32 tile for each of 160 CTAs.
  */
@@ -185,22 +215,32 @@ dgl_status dgl_gemm_mxfp4(const void* A, const void* B, const uint8_t* sfa, cons
  *
  * It computes what dgl_gemm_bf16 (dtype = DGL_DTYPE_BF16; sa and sb ignored)
  * or dgl_gemm_fp8 (dtype = DGL_DTYPE_E4M3) compute, with the same arguments,
- * layouts, validation and error codes.  On the tcgen05 path it always splits
- * the tiles of the last, partial wave along K across all CTAs (stream-K); the
- * partial tiles go through a static device array of DGL_NOALLOC_SCRATCH_BYTES
- * plus 160 flags that the library holds on every device that loads it, until
- * the process exits.  A problem whose split would need more partial tiles
- * than the array holds (more than DGL_NOALLOC_SCRATCH_BYTES, or more than 160
- * CTAs) returns DGL_ERR_SHAPE and enqueues nothing.  Problems without a
- * partial last wave, and those on the decode path (m_valid <= 16), run as
- * dgl_gemm_bf16 / dgl_gemm_fp8 would and do not touch the array.
+ * layouts, validation and error codes.  On the tcgen05 path, when the last
+ * wave of tiles is partial and each worker (CTA or CTA pair) gets at least
+ * four 128-byte k-stages of it, those tiles are split along K across all
+ * workers (stream-K); the partial tiles go through a static device array of
+ * DGL_NOALLOC_SCRATCH_BYTES plus 160 flags that the library holds on every
+ * device that loads it, until the process exits.  A problem whose split would
+ * need more partial tiles than the array holds (more than
+ * DGL_NOALLOC_SCRATCH_BYTES, or more than 160 CTAs: possible only on a device
+ * with more than 160 SMs) returns DGL_ERR_SHAPE and enqueues nothing.  Other
+ * partial-wave shapes (a short tail), problems without a partial last wave,
+ * and those on the decode path (m_valid <= 16) run as dgl_gemm_bf16 /
+ * dgl_gemm_fp8 would and do not touch the array.
+ *
+ * Device memory: the array belongs to the library's CUDA module, whose memory
+ * the driver commits when the module is loaded: by the first dgl_* call that
+ * touches a device (modules load lazily by default), or when the library is
+ * loaded if CUDA_MODULE_LOADING=EAGER.  A caller whose own pool reserves the
+ * device's memory must make one dgl_* call on each device before the pool
+ * takes it.
  *
  * Set-up: the first call on a device (the current device) looks the array's
  * address up and clears its flags, synchronously; make that first call
  * before any stream capture.  Later calls only enqueue work.
  * The array is shared by every call on a device and keeps what the last call
- * left in it (each call tags its flags with a new epoch, so stale contents
- * are never taken for fresh ones).  Calls whose kernels overlap on the GPU,
+ * left in it: partial tiles (never read before they are rewritten) and its
+ * flags, which every call leaves cleared.  Calls whose kernels overlap on the GPU,
  * for example on two streams, race on it: order them, or use dgl_gemm_bf16 /
  * dgl_gemm_fp8.
  */
@@ -262,6 +302,7 @@ dgl_status dgl_linear(int32_t dtype, const void* A, const void* B, const float* 
  * 1.25x the real one unless none passes, as in FlyDSL pull request 1303's
  * autotuner) and the survivor with the lowest cost-model time is chosen.
  * dtype DGL_DTYPE_MXFP4 has one tile: 128 x 256 (tile_k 256 elements).
+ * dtype DGL_DTYPE_W4A8 is planned as DGL_DTYPE_E4M3 (the same tiles).
  */
 dgl_status dgl_plan(int32_t dtype, int64_t m, int64_t n, int64_t K, int32_t out_dtype, int32_t num_sms,
                     dgl_plan_info* out);
@@ -283,9 +324,25 @@ dgl_status dgl_tile_metrics(int64_t m, int64_t n, int32_t tile_m, int32_t tile_n
                             dgl_plan_info* out);
 
 /*
+ * Release what the library holds on the current device: wait for the device's
+ * queued work, free every stream-K workspace, and drop the cached plans and
+ * tensor maps.  The caller owns every other buffer (the Funlib GEMM issue,
+ * "Support device-resident tensors": each allocation has an owner that frees
+ * it); this gives the library's own allocation an explicit end.  Later calls
+ * rebuild what they need.  The static array of dgl_gemm_noalloc is not
+ * freed (it lives as long as the library is loaded).  Must not race with
+ * other threads' calls on this device, nor run while a stream of the device
+ * is being captured.  Returns DGL_ERR_CUDA if the synchronisation reported an
+ * error (the state is released anyway), else DGL_OK.
+ */
+dgl_status dgl_shutdown(void);
+
+/*
  * Synchronise `stream`, then report and clear the current device's status
  * word: DGL_ERR_TIMEOUT if any kernel's bounded wait gave up since the last
- * call, DGL_ERR_CUDA if synchronisation failed, else DGL_OK.
+ * call (the device is then drained and every partial-tile flag of the
+ * library on it cleared), DGL_ERR_CUDA if synchronisation failed, else
+ * DGL_OK.
  */
 dgl_status dgl_device_status(void* stream);
 

@@ -16,7 +16,7 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-from .encode import mx_quantize, pack_e2m1, to_bf16_codes, to_e4m3_codes
+from .encode import mx_quantize, pack_e2m1, to_bf16_codes, to_e2m1_codes, to_e4m3_codes
 from .rng import STREAM_A, STREAM_B, STREAM_SA, STREAM_SB, integers, normal, uniform
 
 # (m, n, K)
@@ -36,8 +36,10 @@ class GemmCase:
     """One GEMM problem: codes of A [m,K] and B [n,K], optional scales.
 
     dtype "mxfp4": A [m, K/2] and B [n, K/2] hold packed E2M1 codes and sa
-    [m, K/32], sb [n, K/32] their E8M0 block-scale codes (uint8)."""
-    dtype: str               # "bf16", "fp8" or "mxfp4"
+    [m, K/32], sb [n, K/32] their E8M0 block-scale codes (uint8).
+    dtype "w4a8": A [m, K] E4M3 codes, B [n, K/2] packed E2M1 codes, sa [m] and
+    sb [n] fp32 scales."""
+    dtype: str               # "bf16", "fp8", "mxfp4" or "w4a8"
     m: int
     n: int
     K: int
@@ -93,6 +95,8 @@ def make_case(dtype: str, m: int, n: int, K: int, *, out: str = "bf16",
     """
     if dtype == "mxfp4":
         return _make_mx_case(m, n, K, out, dist, seed, a_std, b_std)
+    if dtype == "w4a8":
+        return _make_w4a8_case(m, n, K, out, dist, seed, b_std)
     if dtype not in ("bf16", "fp8"):
         raise ValueError(dtype)
     sa = sb = None
@@ -145,6 +149,37 @@ def _make_mx_case(m, n, K, out, dist, seed, a_std, b_std) -> GemmCase:
     return GemmCase("mxfp4", m, n, K, out, dist, seed, A, B, sa, sb)
 
 
+def _make_w4a8_case(m, n, K, out, dist, seed, b_std) -> GemmCase:
+    """E4M3 activations and packed E2M1 weights (K even).
+
+    "w4a8": activations x ~ N(0,1), sa ~ U[0.5, 2), codes e4m3(x / sa) (the
+            fp8 recipe); weights w ~ N(0, b_std^2) with one scale per row,
+            sb = max |w_row| / 6 (the row's largest magnitude on E2M1's
+            largest value, 6), codes e2m1(w / sb), nearest, ties to even
+    "int":  A integers in [-4, 4], B any E2M1 code (multiples of 1/2 up to 6),
+            scales in {0.5, 1, 2}: every partial sum is a multiple of 1/4
+            below 2^24, exact in fp32
+    """
+    if K % 2:
+        raise ValueError("packed E2M1 rows: K must be even")
+    if dist == "w4a8":
+        sa = uniform(seed, STREAM_SA, (m,), 0.5, 2.0).astype(np.float32)
+        A = to_e4m3_codes(normal(seed, STREAM_A, (m, K)) / sa[:, None].astype(np.float64))
+        w = normal(seed, STREAM_B, (n, K), 0.0, b_std)
+        amax = np.abs(w).max(axis=1)
+        sb = np.where(amax > 0, amax / 6.0, 1.0).astype(np.float32)
+        B = pack_e2m1(to_e2m1_codes(w / sb[:, None].astype(np.float64)))
+    elif dist == "int":
+        A = to_e4m3_codes(integers(seed, STREAM_A, (m, K), -4, 4))
+        B = pack_e2m1(integers(seed, STREAM_B, (n, K), 0, 15).astype(np.uint8))
+        pick = np.array([0.5, 1.0, 2.0], dtype=np.float32)
+        sa = pick[integers(seed, STREAM_SA, (m,), 0, 2).astype(np.int64)]
+        sb = pick[integers(seed, STREAM_SB, (n,), 0, 2).astype(np.int64)]
+    else:
+        raise ValueError(dist)
+    return GemmCase("w4a8", m, n, K, out, dist, seed, A, B, sa, sb)
+
+
 # name -> list of (dtype, m, n, K, out, dist)
 WORKLOADS = {
     "square256": [("bf16", 256, 256, 256, "f32", "uniform"), ("bf16", 256, 256, 256, "f32", "int")],
@@ -167,6 +202,11 @@ WORKLOADS = {
     # quantised N(0,1) activations and N(0, 0.02^2) weights
     "mxfp4": [("mxfp4", 4096, 4096, 4096, "bf16", "mx"), ("mxfp4", 597, 11008, 4096, "bf16", "mx"),
               ("mxfp4", 16, 11008, 4096, "bf16", "mx")],
+    # 8-bit activations, 4-bit weights (the GEMM guide's section 8.2 formula
+    # for 4-bit weights): the LLaMA-2 7B up/gate prefill and decode shapes and
+    # the square, E4M3 activations and per-row-scaled E2M1 weights
+    "w4a8": [("w4a8", 4096, 4096, 4096, "bf16", "w4a8"), ("w4a8", 597, 11008, 4096, "bf16", "w4a8"),
+             ("w4a8", 16, 11008, 4096, "bf16", "w4a8"), ("w4a8", 1, 11008, 4096, "bf16", "w4a8")],
     "linear": [("bf16", 10240, 8192, 2048, "bf16", "normal", {"act": "gelu", "bias": True}),
                ("bf16", 597, 11008, 4096, "bf16", "normal", {"act": "silu", "gated": True}),
                ("fp8", 597, 11008, 4096, "bf16", "fp8", {"act": "silu", "gated": True})],

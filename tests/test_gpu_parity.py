@@ -78,7 +78,8 @@ def test_integer_bit_exact_all_paths(dtype, m):
 
 
 # -------------------------------------------------------------- every ladder rung, forced
-LADDER = [(dgl.PATH_TC, 128, 64), (dgl.PATH_TC, 128, 128), (dgl.PATH_TC, 128, 256), (dgl.PATH_TC, 256, 128),
+LADDER = [(dgl.PATH_TC, 64, 64), (dgl.PATH_TC, 64, 128), (dgl.PATH_TC, 64, 256),
+          (dgl.PATH_TC, 128, 64), (dgl.PATH_TC, 128, 128), (dgl.PATH_TC, 128, 256), (dgl.PATH_TC, 256, 128),
           (dgl.PATH_TC, 256, 256)]
 
 
@@ -94,7 +95,7 @@ def test_forced_tile_on_shape_no_tile_divides(path, tm, tn, dtype, out):
 
 @pytest.mark.parametrize("pad,base", [(0, 0), (8, 0), (3, 0), (1, 1), (0, 1), (5, 3)])
 @pytest.mark.parametrize("out", ["bf16", "f32"])
-@pytest.mark.parametrize("tm,tn", [(128, 64), (128, 128), (128, 256), (256, 128), (256, 256)])
+@pytest.mark.parametrize("tm,tn", [(64, 64), (64, 256), (128, 64), (128, 128), (128, 256), (256, 128), (256, 256)])
 def test_output_store_paths(pad, base, out, tm, tn):
     """C pitch and base alignment select the TMA-store or the predicated-store
     epilogue; odd pitches alternate row alignment, an odd base shifts every row."""
@@ -105,7 +106,7 @@ def test_output_store_paths(pad, base, out, tm, tn):
     gu.assert_close_full(case, gu.host_valid(case, Cbuf))
 
 
-@pytest.mark.parametrize("tm,grid", [(128, 1), (128, 3), (128, 7), (256, 2), (256, 6)])
+@pytest.mark.parametrize("tm,grid", [(64, 1), (64, 5), (128, 1), (128, 3), (128, 7), (256, 2), (256, 6)])
 def test_persistent_tile_loop_small_grid(tm, grid):
     """Fewer CTAs (or CTA pairs) than tiles: each walks many tiles through both accumulators."""
     case = make_case("bf16", 700, 900, 264, out="f32")
@@ -297,3 +298,78 @@ def test_split_tail_integer_exact():
     Cbuf, intact = gu.run(case, plan=plan)
     assert intact
     gu.assert_exact(case, gu.host_valid(case, Cbuf))
+
+
+# -------------------------------------------------------------- 64-row rungs (M = 64 MMAs)
+@pytest.mark.parametrize("tn", [64, 128, 256])
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("m", [1, 15, 16, 17, 63, 64, 65, 130])
+def test_m64_rungs_integer_exact(tn, dtype, m):
+    """64-row tiles hold 16 rows per epilogue warp (tensor-memory lanes
+    32 q .. 32 q + 15): every row count around the 16-row warp slices and the
+    64-row tile must come out exact, guard bands intact."""
+    case = make_case(dtype, m, 300, 512, out="f32", dist="int")
+    plan = dgl.PlanInfo(path=dgl.PATH_TC, tile_m=64, tile_n=tn)
+    Cbuf, intact = gu.run(case, plan=plan, guard_rows=3, pad_cols=2)
+    assert intact
+    gu.assert_exact(case, gu.host_valid(case, Cbuf))
+
+
+@pytest.mark.parametrize("tn", [64, 128, 256])
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_m64_rungs_long_k_many_tiles(tn, out):
+    """Several waves of 64-row tiles through both accumulators, K of 4096."""
+    case = make_case("bf16", 333, 1100, 4096, out=out)
+    plan = dgl.PlanInfo(path=dgl.PATH_TC, tile_m=64, tile_n=tn)
+    _full(case, plan=plan, guard_rows=2, pad_cols=5)
+
+
+def test_m64_rejected_for_mn_major_and_linear():
+    """64-row tiles are plain K-major GEMMs: other forced uses are refused."""
+    import torch
+    case = make_case("bf16", 128, 128, 64, out="f32")
+    A, B, _, _ = gu.to_device(case)
+    C = torch.empty((128, 128), dtype=torch.float32, device="cuda")
+    plan = dgl.PlanInfo(path=dgl.PATH_TC, tile_m=64, tile_n=128)
+    st = dgl.dgl_gemm_bf16_ex(dgl.MN_MAJOR, dgl.K_MAJOR, A.data_ptr(), 0, B.data_ptr(), 0, C.data_ptr(), 0, 128,
+                              128, 64, dgl.OUT_F32, plan, torch.cuda.current_stream().cuda_stream)
+    assert st == dgl.DGL_ERR_UNSUPPORTED
+    st = dgl.dgl_linear(dgl.DTYPE_BF16, A.data_ptr(), B.data_ptr(), None, None, None, C.data_ptr(), 128, 128, 64,
+                        128, 128, dgl.OUT_F32, dgl.ACT_GELU, 0, plan, torch.cuda.current_stream().cuda_stream)
+    assert st == dgl.DGL_ERR_UNSUPPORTED
+
+
+# -------------------------------------------------------------- split-K tail (stream_k = S >= 2)
+# One whole wave plus a tail of 19 tiles: 76 CTA pairs (or 152 CTAs) leave room
+# for up to four workers per tail tile.
+SPLIT_K_SHAPES = {(256, 256): (1200, 4800), (256, 128): (1200, 2400), (128, 256): (1250, 4800)}
+
+
+@pytest.mark.parametrize("tm,tn", list(SPLIT_K_SHAPES))
+@pytest.mark.parametrize("ways", [2, 4])
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_split_k_tail_integer_exact(tm, tn, ways, dtype):
+    """Each tail tile's k-stages in `ways` tile-aligned ranges, partials added by
+    the worker holding the first range: exact on integer inputs, twice in a
+    row on the shared workspace."""
+    m, n = SPLIT_K_SHAPES[(tm, tn)]
+    case = make_case(dtype, m, n, 512, out="f32", dist="int")
+    plan = dgl.PlanInfo(path=dgl.PATH_TC, tile_m=tm, tile_n=tn, stream_k=ways)
+    ops = gu.to_device(case)
+    for _ in range(2):
+        Cbuf, intact = gu.run(case, plan=plan, dev_ops=ops, guard_rows=2, pad_cols=3)
+        assert intact
+        gu.assert_exact(case, gu.host_valid(case, Cbuf))
+
+
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_split_k_tail_general_values(out):
+    """The planner's own choice for a long-K shape with a short tail (K = 4096,
+    four workers per tail tile): a seeded sample and whole corner tiles."""
+    case = make_case("bf16", 1200, 4800, 4096, out=out)
+    p = dgl.dgl_plan(dgl.DTYPE_BF16, case.m, case.n, case.K, dgl.OUT_F32 if out == "f32" else dgl.OUT_BF16,
+                     num_sms=152)
+    assert p.stream_k >= 2, "test setup: the planner should split this tail"
+    Cbuf, intact = gu.run(case, guard_rows=2, pad_cols=5)
+    assert intact
+    gu.assert_close_sampled(case, Cbuf, p.tile_m, p.tile_n)

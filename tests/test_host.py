@@ -135,7 +135,7 @@ def test_plan_decode_k_group(dgl, dtype, n, k, want):
 
 
 @pytest.mark.parametrize("dtype,m,n,k,tile", [(0, 1024, 50257, 512, (128, 256)), (0, 2048, 2048, 2048, (128, 256)),
-                                              (0, 48, 4096, 48, (128, 128)), (0, 528, 528, 1024, (128, 64)),
+                                              (0, 48, 4096, 48, (64, 64)), (0, 528, 528, 1024, (64, 64)),
                                               (0, 3402, 4096, 1024, (256, 256)), (0, 597, 11008, 4096, (256, 256)),
                                               (1, 597, 11008, 4096, (256, 256))])
 def test_plan_measured_pins(dgl, dtype, m, n, k, tile):
@@ -180,7 +180,7 @@ def test_plan_padding_screen(dgl, m, n, k):
     pinned_past_screen = {(597, 11008, 4096), (528, 528, 1024)}
     assert p.path == dgl.PATH_TC
     padded = -(-m // p.tile_m) * p.tile_m * -(-n // p.tile_n) * p.tile_n
-    rungs = [(128, 64), (128, 128), (128, 256), (256, 128), (256, 256)]
+    rungs = [(64, 64), (64, 128), (64, 256), (128, 64), (128, 128), (128, 256), (256, 128), (256, 256)]
     any_ok = any(-(-m // tm) * tm * -(-n // tn) * tn <= 1.25 * m * n for tm, tn in rungs)
     if any_ok and (m, n, k) not in pinned_past_screen:
         assert padded <= 1.25 * m * n

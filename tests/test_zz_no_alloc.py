@@ -6,10 +6,12 @@ allocation after start-up.  dgl_gemm_noalloc serves them by keeping its
 stream-K partial tiles in a fixed device array instead of a workspace it
 allocates.  These tests call it through the C ABI on problems whose last wave
 is split (so the array is really used) and compare each of two calls in a row
-with the existing entry point (dgl_gemm_bf16 / dgl_gemm_fp8): within the
-parity tolerance |C - C_ref| <= 1e-4 * sum_k |a_ik b_jk| + 1e-6 (plus
-1e-2 |C_ref| for bf16 output), and bit for bit on integer-valued inputs.
-The file is named to run last.
+with the existing entry point (dgl_gemm_bf16 / dgl_gemm_fp8) and with the
+oracle (a seeded sample plus whole corner tiles): within the parity tolerance
+|C - C_ref| <= 1e-4 * sum_k |a_ik b_jk| + 1e-6 (plus 1e-2 |C_ref| for bf16
+output), and bit for bit on integer-valued inputs.  One test checks that a
+call leaves the device's free memory unchanged while the allocating stream-K
+path does not.  The file is named to run last.
 """
 import math
 
@@ -89,9 +91,12 @@ def test_noalloc_matches_existing_entry_point(dtype, m, n, k, out, dist):
     assert intact
     ref = ref.double()
     bound = (1e-2 if out == "bf16" else 0.0) * ref.abs() + 1e-4 * _abs_sum(case, A, B, sa, sb) + 1e-6
+    plan = dgl.dgl_plan(dgl.DTYPE_BF16 if dtype == "bf16" else dgl.DTYPE_E4M3, m, n, k, out_dtype)
     for call in range(2):  # the second call finds the array as the first one left it
         got, intact = _call(case, A, B, sa, sb, noalloc=True)
         assert intact, f"call {call}: wrote outside the valid region"
+        # against the oracle: a seeded sample and whole tiles at every corner
+        gu.assert_close_sampled(case, got, plan.tile_m, plan.tile_n, seed=call)
         got = got.double()
         assert torch.isfinite(got).all(), f"call {call}: non-finite output"
         err = (got - ref).abs()
@@ -121,3 +126,36 @@ def test_noalloc_decode_shape_runs_without_the_array():
     got, intact = _call(case, A, B, sa, sb, noalloc=True)
     assert intact
     assert torch.equal(got.view(torch.int32), ref.view(torch.int32))
+
+
+def test_noalloc_allocates_no_device_memory():
+    """The defining property: a call on a fresh stream leaves the device's free
+    memory unchanged, where the stream-K path of dgl_gemm_planned allocates a
+    workspace of at least 24 MiB for the same problem on a fresh stream."""
+    case = make_case("bf16", 1800, 7000, 2048, out="f32", dist="normal")
+    assert _split_last_wave(case, dgl.OUT_F32), "test setup: this shape should split its last wave"
+    A, B, _sa, _sb = gu.to_device(case)
+    C = torch.empty((case.m, case.n), dtype=torch.float32, device="cuda")
+    s_warm, s_new, s_ctl = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+
+    def noalloc(stream):
+        return dgl.dgl_gemm_noalloc(dgl.DTYPE_BF16, A.data_ptr(), B.data_ptr(), None, None, C.data_ptr(),
+                                    case.m, case.n, case.K, case.m, case.n, dgl.OUT_F32, stream.cuda_stream)
+
+    assert noalloc(s_warm) == dgl.DGL_OK  # first call: set-up, kernel modules loaded
+    assert dgl.dgl_shutdown() == dgl.DGL_OK  # no workspace left from earlier tests
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    assert noalloc(s_new) == dgl.DGL_OK
+    torch.cuda.synchronize()
+    free1 = torch.cuda.mem_get_info()[0]
+    assert dgl.dgl_device_status(s_new.cuda_stream) == dgl.DGL_OK
+    assert free1 == free0, f"dgl_gemm_noalloc changed free device memory by {free0 - free1} bytes"
+    plan = dgl.PlanInfo(path=dgl.PATH_TC, tile_m=256, tile_n=256, stream_k=1)
+    st = dgl.dgl_gemm_planned(dgl.DTYPE_BF16, A.data_ptr(), B.data_ptr(), None, None, C.data_ptr(), case.m,
+                              case.n, case.K, case.m, case.n, dgl.OUT_F32, plan, s_ctl.cuda_stream)
+    assert st == dgl.DGL_OK
+    torch.cuda.synchronize()
+    free2 = torch.cuda.mem_get_info()[0]
+    assert free1 - free2 >= 24 << 20, "control: the allocating path should have taken a workspace"
+    assert dgl.dgl_shutdown() == dgl.DGL_OK
