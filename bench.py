@@ -6,7 +6,7 @@ prefill shapes, the 1024x50257x512 lm_head, 2048x11007x1024, 4095^2x1024 --
 with N(0,1) activations, N(0,0.02) weights and bf16 C).  Prints one JSON line.
 
   python bench.py [--gpus N --steps K --warmup W]
-                  [--workload ragged|llama7b_mlp|square|fp8|mxfp4|linear|gpt3xl_train|square256]
+                  [--workload ragged|llama7b_mlp|square|fp8|mxfp4|w4a8|linear|gpt3xl_train|square256]
   python bench.py --impl reference      # the fp64 CPU oracle, timed on the host cores
 
 value = 2*m*n*K summed over the step's GEMMs (valid extents only) / step time,
@@ -38,6 +38,8 @@ WORKLOAD_TEXT = {
     "fp8": "E4M3 with per-row/per-column fp32 scales, bf16 C: (4096,4096,4096) (597,11008,4096) (16,11008,4096)",
     "mxfp4": "MXFP4 (E2M1, one E8M0 scale per 32 of K), bf16 C: (4096,4096,4096) (597,11008,4096) "
              "(16,11008,4096)",
+    "w4a8": "W4A8 (E4M3 activations, per-row-scaled E2M1 weights), bf16 C: (4096,4096,4096) (597,11008,4096) "
+            "(16,11008,4096) (1,11008,4096)",
     "square256": "bf16 256^3, fp32 C: uniform[-1,1] and integer [-4,4] variants",
     "gpt3xl_train": "GPT-3-XL feed-forward projection, one training step, bf16 C: forward 10240x8192x2048 + bias "
                     "+ GELU; dX = dY W 10240x2048x8192 (W read MN-major); dW = dY^T X 8192x2048x10240 "
@@ -165,6 +167,9 @@ def oracle_band(oracle, lib, c, rows):
     if c.dtype == "mxfp4":
         oracle.mxfp4_gemm(c.A[:rows], c.B, c.sa[:rows], c.sb, lib=lib)
         return
+    if c.dtype == "w4a8":
+        oracle.w4a8_gemm(c.A[:rows], c.B, c.sa[:rows], c.sb, lib=lib)
+        return
     dt = oracle.BF16 if c.dtype == "bf16" else oracle.E4M3
     sa = c.sa[:rows] if c.sa is not None else None
     if c.linear:
@@ -252,7 +257,7 @@ def shape_entry(text):
     m, n, k = (int(v) for v in parts[:3])
     dtype = parts[3] if len(parts) > 3 else "bf16"
     out = parts[4] if len(parts) > 4 else "bf16"
-    return (dtype, m, n, k, out, {"fp8": "fp8", "mxfp4": "mx"}.get(dtype, "normal"))
+    return (dtype, m, n, k, out, {"fp8": "fp8", "mxfp4": "mx", "w4a8": "w4a8"}.get(dtype, "normal"))
 
 
 def workload_text(args):
@@ -337,11 +342,15 @@ def main():
                      ctypes.byref(forced) if forced is not None else None, s_handle)
             fn = lib.dgl_linear
         elif forced is not None:
-            dt = dgl.DTYPE_BF16 if c.dtype == "bf16" else dgl.DTYPE_E4M3
+            dt = {"bf16": dgl.DTYPE_BF16, "fp8": dgl.DTYPE_E4M3, "w4a8": dgl.DTYPE_W4A8}[c.dtype]
             args_ = (dt, A.data_ptr(), B.data_ptr(), sa.data_ptr() if sa is not None else None,
                      sb.data_ptr() if sb is not None else None, C.data_ptr(), c.m, c.n, c.K, c.m, c.n, out_dtype,
                      ctypes.byref(forced), s_handle)
             fn = lib.dgl_gemm_planned
+        elif c.dtype == "w4a8":
+            args_ = (A.data_ptr(), B.data_ptr(), sa.data_ptr(), sb.data_ptr(), C.data_ptr(), c.m, c.n, c.K, c.m,
+                     c.n, out_dtype, s_handle)
+            fn = lib.dgl_gemm_w4a8
         elif c.dtype == "mxfp4":
             args_ = (A.data_ptr(), B.data_ptr(), sa.data_ptr(), sb.data_ptr(), C.data_ptr(), c.m, c.n, c.K, c.m,
                      c.n, out_dtype, s_handle)
@@ -361,7 +370,7 @@ def main():
         return call
 
     calls = [make_call(*o) for o in ops]
-    dtype_ids = {"bf16": dgl.DTYPE_BF16, "fp8": dgl.DTYPE_E4M3, "mxfp4": dgl.DTYPE_MXFP4}
+    dtype_ids = {"bf16": dgl.DTYPE_BF16, "fp8": dgl.DTYPE_E4M3, "mxfp4": dgl.DTYPE_MXFP4, "w4a8": dgl.DTYPE_W4A8}
     plans = [dgl.dgl_plan_linear(dtype_ids[c.dtype], c.m, c.n, c.K,
                                  dgl.OUT_F32 if c.out == "f32" else dgl.OUT_BF16, int(c.gated)) if c.linear else
              dgl.dgl_plan(dtype_ids[c.dtype], c.m, c.n, c.K,
@@ -393,6 +402,10 @@ def main():
             # the GEMM guide's MXFP4 formula (section 8.2), with C at its own element size
             nbytes.append((c.m + c.n) * c.K // 2 + c.m * c.n * o + (c.m + c.n) * (c.K // 32))
             continue
+        if c.dtype == "w4a8":
+            # the guide's 4-bit weight formula (section 8.2): A one byte, B half a byte per element
+            nbytes.append(c.m * c.K + c.n * c.K // 2 + c.m * c.n * o + 4 * (c.m + c.n))
+            continue
         e = 2 if c.dtype == "bf16" else 1
         nbytes.append(c.m * c.K * e + c.b_rows * c.K * e + c.m * c.n * o +
                       (4 * (c.m + c.b_rows) if c.dtype == "fp8" else 0) + (4 * c.b_rows if c.bias is not None else 0))
@@ -408,8 +421,14 @@ def main():
 
     # One step captured as a CUDA graph: the ten calls' host work (argument
     # checks, plan and tensor-map cache look-ups, launch) then leaves the timed
-    # loop, which replays the same launches back to back.
-    step_graph = capture_graph(torch, lambda s: [f(s) for f in calls], stream)
+    # loop, which replays the same launches back to back.  Capture needs a
+    # stream of its own; one step on it first gives a split schedule its
+    # workspace there.  The graph is replayed on the timing stream.
+    cap_stream = torch.cuda.Stream(device=dev)
+    for f in calls:
+        f(cap_stream.cuda_stream)
+    torch.cuda.synchronize()
+    step_graph = capture_graph(torch, lambda s: [f(s) for f in calls], cap_stream)
     launch_mode = "cuda graph of one step" if step_graph is not None else "stream launches"
 
     # ---------------------------------------------------------- device-timed region

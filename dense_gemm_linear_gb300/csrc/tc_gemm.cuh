@@ -175,6 +175,53 @@ __device__ __forceinline__ void store_row_pieces(uint8_t* g, uint32_t s, int lo,
   }
 }
 
+// Stores NW packed words (2 NW bf16 values, value 2i in the low half of w[i])
+// to shared memory so that value j lands at byte a + D + 2 j: a is 16-byte
+// aligned and D (the global row's misalignment) is even and below 16.  The
+// 16-byte words that the values fill completely go out as 16-byte stores;
+// only the partial words at the two ends take 4- and 2-byte stores.  With
+// one thread per staged row and rows 16-byte aligned at an odd multiple of
+// 16 bytes apart, every 8-lane phase of a 16-byte store covers all 32 banks,
+// where 4-byte stores at a common column put four lanes on each bank.
+//   q = D / 4 words of offset, and x[i], the 4 bytes landing at a + 4 q + 4 i,
+//   is w[i] when D % 4 == 0, else the high half of w[i - 1] and the low half
+//   of w[i]; 16-byte word s (16 s .. 16 s + 15) then holds x[4 s - q .. 4 s + 3 - q].
+template <int NW>
+__device__ __forceinline__ void sts_row_shifted(uint32_t a, const uint32_t (&w)[NW], int D) {
+  static_assert(NW % 4 == 0 && NW >= 8, "whole 16-byte words");
+  const int q = D >> 2;
+  const uint32_t sel = (D & 2) ? 0x5432u : 0x7654u;
+  uint32_t x[NW + 1];
+  x[0] = __byte_perm(0u, w[0], sel);
+#pragma unroll
+  for (int i = 1; i < NW; ++i) x[i] = __byte_perm(w[i - 1], w[i], sel);
+  x[NW] = __byte_perm(w[NW - 1], 0u, sel);
+  auto pick = [&](int k) -> uint32_t {  // x[k - q], k a compile-time index >= 3
+    return q == 0 ? x[k] : q == 1 ? x[k - 1] : q == 2 ? x[k - 2] : x[k - 3];
+  };
+  // full words s = 1 .. NW / 4 - 1 (word 0 is full only when D == 0)
+#pragma unroll
+  for (int sw = 1; sw < NW / 4; ++sw)
+    sts_v4(a + 16 * sw, pick(4 * sw), pick(4 * sw + 1), pick(4 * sw + 2), pick(4 * sw + 3));
+  // head: bytes D .. 15 of word 0 are x[0 .. 3 - q] (x[0]'s high half only when D % 4 == 2)
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (i + q <= 3) {
+      const uint32_t addr = a + 4 * (q + i);
+      if (i == 0 && (D & 2))
+        sts_u16(addr + 2, x[0] >> 16);
+      else
+        sts_u32(addr, x[i]);
+    }
+  }
+  // tail: bytes 0 .. D - 1 of word NW / 4 are x[NW - q .. NW - 1], then x[NW]'s low half
+  const uint32_t t0 = a + 4 * NW;
+  if (q >= 1) sts_u32(t0, q == 1 ? x[NW - 1] : q == 2 ? x[NW - 2] : x[NW - 3]);
+  if (q >= 2) sts_u32(t0 + 4, q == 2 ? x[NW - 1] : x[NW - 2]);
+  if (q >= 3) sts_u32(t0 + 8, x[NW - 1]);
+  if (D & 2) sts_u16(t0 + 4 * q, x[NW] & 0xFFFFu);
+}
+
 // Operand tiles in shared memory.  A K-major operand (rows of K contiguous)
 // arrives as one TMA box of BK elements by `rows` rows.  An MN-major operand
 // (stored [K][MN], MN contiguous: the backward-pass layouts) arrives as
@@ -731,16 +778,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[2 * t]), __uint_as_float(v[2 * t + 1]));
             w[t] = *reinterpret_cast<uint32_t*>(&h2);
           }
-          const uint32_t base = srow + 64 * oc;
-          if ((delta & 2) == 0) {
-#pragma unroll
-            for (int t = 0; t < 16; ++t) sts_u32(base + 4 * t, w[t]);
-          } else {
-            sts_u16(base, w[0] & 0xFFFFu);
-#pragma unroll
-            for (int t = 0; t < 15; ++t) sts_u32(base + 2 + 4 * t, __byte_perm(w[t], w[t + 1], 0x5432));
-            sts_u16(base + 62, w[15] >> 16);
-          }
+          sts_row_shifted<16>(srow - delta + 64 * oc, w, delta);
         } else {
           // bf16 chunks alternate between two 2 KB staging tiles, so a chunk's
           // TMA store may still be reading one while the next chunk fills the
@@ -936,8 +974,24 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     apply_act(p.act, __uint_as_float(r[uu][j]) + __shfl_sync(0xffffffffu, b, j)));
             }
           }
+          if constexpr (Cfg::ROWSTG) {
+            // the G chunks are adjacent in the row: stage them as one span,
+            // so only its two ends take narrow stores
+            uint32_t w[16 * G];
 #pragma unroll
-          for (int uu = 0; uu < G; ++uu) emit(r[uu], half * CPW + g0 + uu);
+            for (int uu = 0; uu < G; ++uu) {
+#pragma unroll
+              for (int t = 0; t < 16; ++t) {
+                __nv_bfloat162 h2 =
+                    __floats2bfloat162_rn(__uint_as_float(r[uu][2 * t]), __uint_as_float(r[uu][2 * t + 1]));
+                w[16 * uu + t] = *reinterpret_cast<uint32_t*>(&h2);
+              }
+            }
+            sts_row_shifted<16 * G>(srow - delta + 64 * (half * CPW + g0), w, delta);
+          } else {
+#pragma unroll
+            for (int uu = 0; uu < G; ++uu) emit(r[uu], half * CPW + g0 + uu);
+          }
         }
       }
 
