@@ -25,7 +25,8 @@ cudaError_t set_smem_attr_once(Kernel kern, int bytes, std::atomic<uint64_t>& do
 
 // tcgen05 tile kernel.  out: 0 bf16, 1 fp32.  tile_m: 128 (one CTA per tile)
 // or 256 (a CTA pair per tile, launched as clusters of two), or 64 (passed on
-// to the 64-row variants below; tbh unused).  tile_n: 64, 128 or 256.
+// to the 64-row variants below; tbh unused).  tile_n: 64, 128 or 256, and 224
+// on CTA pairs (plain GEMM only).
 // row_staging (bf16 output only): C rows are not 16-byte aligned, so the
 // epilogue stages whole rows and writes each row's aligned body in bulk.
 // tc: tensor map of C for TMA stores (used when p.c_tma is set).

@@ -37,11 +37,17 @@ struct Rung {
   int tile_m, tile_n;  // tile_m 256 = a CTA pair (cta_group::2), 128 rows per CTA; 64 = one CTA, M = 64 MMAs
   double stage_us;     // per 128-byte k-stage
   double tile_us;      // per tile: accumulator drain, epilogue not hidden
+  int max_kb;          // the planner offers the rung only up to this many k-stages (0: any)
 };
+// The 224-wide pair tile fills 4096 columns with 19 tiles, so 4096 x 4096
+// outputs make exactly four waves of 76 pairs.  Measured (interleaved,
+// L2-rotated): 4095^2 x 1024 28.3 us against 30.9 us on 256 x 256; at K =
+// 4096 its tiles take as long as 256-wide ones (bf16 77.5 against 77.7 us,
+// E4M3 45.1 against 44.5 us), so it is offered for short K only.
 constexpr Rung kLadder[] = {
-    {64, 64, 0.200, 1.0},   {64, 128, 0.230, 1.0},   {64, 256, 0.300, 2.0},
-    {128, 64, 0.260, 1.0},  {128, 128, 0.265, 1.0},  {128, 256, 0.322, 2.6},
-    {256, 128, 0.270, 1.0}, {256, 256, 0.278, 2.2},
+    {64, 64, 0.200, 1.0, 0},   {64, 128, 0.230, 1.0, 0},   {64, 256, 0.300, 2.0, 0},
+    {128, 64, 0.260, 1.0, 0},  {128, 128, 0.265, 1.0, 0},  {128, 256, 0.322, 2.6, 0},
+    {256, 128, 0.270, 1.0, 0}, {256, 224, 0.278, 1.6, 16}, {256, 256, 0.278, 2.2, 0},
 };
 
 // Measured pins: shapes where the screened model's pick is more than 5% off
@@ -337,8 +343,11 @@ void choose_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int 
     }
   }
   const double area = static_cast<double>(m) * static_cast<double>(n);
+  const int64_t nk = (K * (dtype == DGL_DTYPE_E4M3 ? 1 : 2) + 127) / 128;
+  auto offered = [&](const Rung& r) { return r.max_kb == 0 || nk <= r.max_kb; };
   bool any_pass = false;
   for (const Rung& r : kLadder) {
+    if (!offered(r)) continue;
     const double padded = std::ceil(static_cast<double>(m) / r.tile_m) * r.tile_m *
                           std::ceil(static_cast<double>(n) / r.tile_n) * r.tile_n;
     if (padded <= 1.25 * area) any_pass = true;
@@ -346,6 +355,7 @@ void choose_plan(int dtype, int out_dtype, int64_t m, int64_t n, int64_t K, int 
   bool have = false;
   dgl_plan_info best{};
   for (const Rung& r : kLadder) {
+    if (!offered(r)) continue;
     const double padded = std::ceil(static_cast<double>(m) / r.tile_m) * r.tile_m *
                           std::ceil(static_cast<double>(n) / r.tile_n) * r.tile_n;
     if (any_pass && padded > 1.25 * area) continue;

@@ -44,6 +44,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -97,7 +99,10 @@ struct TcConfig {
   static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
   static constexpr int EPI_WARPS = 8;
   static constexpr int CHUNKS = BN / 32;                // 32-column chunks per tile row
-  static constexpr int CHUNKS_PER_WARP = CHUNKS / 2;    // two warps share a lane quarter
+  // two warps share a lane quarter: the first takes chunks [0, CB0), the
+  // second [CB0, CHUNKS) (4 + 3 of a 224-wide tile's 7)
+  static constexpr int CB0 = (CHUNKS + 1) / 2;
+  static constexpr int CHUNKS_PER_WARP = CHUNKS / 2;
   static constexpr int OUT_BYTES = OUT_F32 ? 4 : 2;
   static constexpr int STG_ROW = 32 * OUT_BYTES;        // 32 x 32 staging row: 64 B (bf16) or 128 B (fp32)
   static constexpr int STG_BYTES = 32 * STG_ROW;        // one 32 x 32 staging tile: 2 KB (bf16) or 4 KB (fp32)
@@ -115,7 +120,10 @@ struct TcConfig {
   // fp32 accumulators of BN columns: two, so the epilogue of one tile
   // overlaps the main loop of the next, or one with MX 128 x 256 tiles
   static constexpr int ACC_BUFS = MX && BN == 256 ? 1 : 2;
-  static constexpr int TMEM_COLS = MX ? 512 : 2 * BN;
+  // a 224-wide accumulator is placed 256 columns apart (allocations are
+  // powers of two)
+  static constexpr int ACC_STRIDE = BN == 224 ? 256 : BN;
+  static constexpr int TMEM_COLS = MX ? 512 : 2 * ACC_STRIDE;
   // MX scale ring: slot s holds stage s's scale atoms, 4 columns each
   static constexpr int SCALE_COL0 = ACC_BUFS * BN;
   static constexpr int SCALE_SLOT_COLS = 4 * SCALE_ATOMS;
@@ -128,7 +136,8 @@ struct TcConfig {
   static constexpr int FX_BUFS = FX_WARP_BYTES >= 4096 ? 2 : 1;
   static constexpr int SMEM_BYTES =
       1024 /* alignment slack */ + STAGES * (STAGE_BYTES + SCALE_STAGE_BYTES) + STG_TOTAL + BAR_BYTES;
-  static_assert(BN == 64 || BN == 128 || BN == 256, "tile widths of the ladder");
+  static_assert(BN == 64 || BN == 128 || BN == 256 || (BN == 224 && CG == 2 && !EPI && !MX),
+                "tile widths of the ladder (224: plain GEMM on CTA pairs)");
   static_assert(BM == 128 || (BM == 64 && CG == 1 && !EPI && !MX), "64-row tiles: one CTA, plain GEMM");
   static_assert(STAGES >= 3, "ring too shallow");
   static_assert((ROW_PITCH / 16) % 2 == 1, "row pitch: odd multiple of 16 bytes");
@@ -508,7 +517,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           break;
         }
         tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + acc * BN;
+        const uint32_t d_tmem = tmem_base + acc * Cfg::ACC_STRIDE;
         const uint32_t idesc = sg.half ? idesc_half : idesc_full;  // a half tile: N = BN / 2
         for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
           // (MX: the stage's scales are in shared memory too)
@@ -590,8 +599,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     // ------------------------------------------------------------ epilogue
     const int e = warp - 2;                 // 0..7
     const int q = warp & 3;                 // TMEM lanes 32q .. 32q+31 are reachable from this warp
-    const int half = e >> 2;                // this warp takes chunks [half * CPW, (half + 1) * CPW)
+    const int half = e >> 2;                // this warp takes chunks [c_first, c_first + nc)
     constexpr int CPW = Cfg::CHUNKS_PER_WARP;
+    constexpr bool EVEN = Cfg::CHUNKS % 2 == 0;
+    const int c_first = EVEN ? half * CPW : (half ? Cfg::CB0 : 0);
+    const int nc = EVEN ? CPW : (half ? Cfg::CHUNKS - Cfg::CB0 : Cfg::CB0);
     uint8_t* stg = Cfg::ROWSTG ? sStg + q * 32 * Cfg::ROW_PITCH : sStg + e * 4096;
     const uint32_t stg_addr = smem_u32(stg);
     uint32_t acc = 0, acc_phase = 0, fx_phase = 0;
@@ -619,7 +631,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       tc_fence_after_sync();
       const int row0 = mb * Cfg::TILE_M + static_cast<int>(rank) * BM + q * Cfg::WARP_ROWS;
       const bool row_lane = lane < Cfg::WARP_ROWS;  // this thread holds a row of the tile
-      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * Cfg::ACC_STRIDE;
 
       // ---- stream-K: a segment that does not hold the tile's first k-stage
       // hands its fp32 partial tile over through the workspace; the segment
@@ -633,8 +645,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         const uint32_t fx = Cfg::ROWSTG ? stg_addr + half * Cfg::FX_WARP_BYTES : stg_addr;
         int piece = 0;
 #pragma unroll 1
-        for (int u = 0; u < CPW; ++u) {
-          const int c = half * CPW + u;
+        for (int u = 0; u < nc; ++u) {
+          const int c = c_first + u;
           uint32_t v[32];
           tmem_ld_32x32b_x32(t_row + c * 32, v);
           tmem_ld_wait();
@@ -724,8 +736,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
               if (nonempty(w)) p.flags[w * CG + rank] = 0;
           }
 #pragma unroll 1
-          for (int u = 0; u < CPW; ++u) {
-            const int c = half * CPW + u;
+          for (int u = 0; u < nc; ++u) {
+            const int c = c_first + u;
             uint32_t v[32];
             tmem_ld_32x32b_x32(t_row + c * 32, v);
             tmem_ld_wait();
@@ -936,25 +948,25 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         }
       }
       if (!gated_done) {
-        // The warp's share of the accumulator is read G chunks at a time,
-        // which bounds the registers it holds; the buffer goes back to the MMA
-        // once the last chunk has been read.
-        constexpr int G = CPW > 2 ? 2 : CPW;
+        // The warp's share of the accumulator (chunks c_first .. c_first + nc
+        // - 1) is read two chunks at a time, which bounds the registers it
+        // holds; the buffer goes back to the MMA once the last chunk has been
+        // read.
         const bool epi = Cfg::EPI && (p.act != 0 || p.bias != nullptr);
-#pragma unroll
-        for (int g0 = 0; g0 < CPW; g0 += G) {
+        auto group = [&](auto g_const, int c0, bool last) {
+          constexpr int G = decltype(g_const)::value;
           uint32_t r[G][32];
 #pragma unroll
-          for (int uu = 0; uu < G; ++uu) tmem_ld_32x32b_x32(t_row + (half * CPW + g0 + uu) * 32, r[uu]);
+          for (int uu = 0; uu < G; ++uu) tmem_ld_32x32b_x32(t_row + (c0 + uu) * 32, r[uu]);
           tmem_ld_wait();
 #pragma unroll
           for (int uu = 0; uu < G; ++uu) reg_fence(r[uu]);
-          if (g0 + G == CPW) hand_back();
+          if (last) hand_back();
 
           if constexpr (Cfg::FP8) {
 #pragma unroll
             for (int uu = 0; uu < G; ++uu) {
-              const int col0 = ocol0 + (half * CPW + g0 + uu) * 32;
+              const int col0 = ocol0 + (c0 + uu) * 32;
               const float col_scale = (col0 + lane < p.n) ? p.sb[col0 + lane] : 0.0f;
 #pragma unroll
               for (int j = 0; j < 32; ++j)
@@ -966,7 +978,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             // linear-layer epilogue: bias per column, then the activation
 #pragma unroll
             for (int uu = 0; uu < G; ++uu) {
-              const int col = ocol0 + (half * CPW + g0 + uu) * 32 + lane;
+              const int col = ocol0 + (c0 + uu) * 32 + lane;
               const float b = (p.bias && col < p.n) ? p.bias[col] : 0.0f;
 #pragma unroll
               for (int j = 0; j < 32; ++j)
@@ -987,11 +999,19 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 w[16 * uu + t] = *reinterpret_cast<uint32_t*>(&h2);
               }
             }
-            sts_row_shifted<16 * G>(srow - delta + 64 * (half * CPW + g0), w, delta);
+            sts_row_shifted<16 * G>(srow - delta + 64 * c0, w, delta);
           } else {
 #pragma unroll
-            for (int uu = 0; uu < G; ++uu) emit(r[uu], half * CPW + g0 + uu);
+            for (int uu = 0; uu < G; ++uu) emit(r[uu], c0 + uu);
           }
+        };
+#pragma unroll
+        for (int g0 = 0; g0 < Cfg::CB0; g0 += 2) {
+          if (g0 >= nc) break;
+          if (g0 + 2 <= nc)
+            group(std::integral_constant<int, 2>{}, c_first + g0, g0 + 2 == nc);
+          else
+            group(std::integral_constant<int, 1>{}, c_first + g0, true);
         }
       }
 

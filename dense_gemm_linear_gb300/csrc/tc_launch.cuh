@@ -83,6 +83,9 @@ cudaError_t tc_launch(int out, int tile_m, int tile_n, bool row_staging, const C
   if (tile_m == 256) {
     switch (tile_n) {
       case 128: return tc_launch_bn<128, FP8, 2, EPI>(out, row_staging, ta, tb, tbh, tc, p, grid, stream);
+      case 224:
+        if constexpr (EPI) return cudaErrorInvalidValue;
+        else return tc_launch_bn<224, FP8, 2, EPI>(out, row_staging, ta, tb, tbh, tc, p, grid, stream);
       case 256: return tc_launch_bn<256, FP8, 2, EPI>(out, row_staging, ta, tb, tbh, tc, p, grid, stream);
       default: return cudaErrorInvalidValue;
     }

@@ -96,8 +96,8 @@ typedef enum { DGL_K_MAJOR = 0, DGL_MN_MAJOR = 1 } dgl_major_t;
  */
 typedef struct {
   int32_t path;       /* dgl_path_t */
-  int32_t tile_m;     /* rows of C per tile (tcgen05 path: 128, or 256 for a CTA pair) */
-  int32_t tile_n;     /* columns of C per tile (tcgen05 path: 64, 128 or 256) */
+  int32_t tile_m;     /* rows of C per tile (tcgen05 path: 64, 128, or 256 for a CTA pair) */
+  int32_t tile_n;     /* columns of C per tile (tcgen05 path: 64, 128 or 256; 224 on a CTA pair) */
   int32_t tile_k;     /* K elements per pipeline stage (64 bf16, 128 E4M3) */
   int32_t stages;     /* shared-memory ring depth */
   int32_t cta_group;  /* CTAs sharing one MMA: 1, or 2 (a CTA pair, tile_m 256) */

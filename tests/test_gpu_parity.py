@@ -80,7 +80,7 @@ def test_integer_bit_exact_all_paths(dtype, m):
 # -------------------------------------------------------------- every ladder rung, forced
 LADDER = [(dgl.PATH_TC, 64, 64), (dgl.PATH_TC, 64, 128), (dgl.PATH_TC, 64, 256),
           (dgl.PATH_TC, 128, 64), (dgl.PATH_TC, 128, 128), (dgl.PATH_TC, 128, 256), (dgl.PATH_TC, 256, 128),
-          (dgl.PATH_TC, 256, 256)]
+          (dgl.PATH_TC, 256, 224), (dgl.PATH_TC, 256, 256)]
 
 
 @pytest.mark.parametrize("path,tm,tn", LADDER, ids=lambda v: str(v))
@@ -95,7 +95,8 @@ def test_forced_tile_on_shape_no_tile_divides(path, tm, tn, dtype, out):
 
 @pytest.mark.parametrize("pad,base", [(0, 0), (8, 0), (3, 0), (1, 1), (0, 1), (5, 3)])
 @pytest.mark.parametrize("out", ["bf16", "f32"])
-@pytest.mark.parametrize("tm,tn", [(64, 64), (64, 256), (128, 64), (128, 128), (128, 256), (256, 128), (256, 256)])
+@pytest.mark.parametrize("tm,tn", [(64, 64), (64, 256), (128, 64), (128, 128), (128, 256), (256, 128), (256, 224),
+                                   (256, 256)])
 def test_output_store_paths(pad, base, out, tm, tn):
     """C pitch and base alignment select the TMA-store or the predicated-store
     epilogue; odd pitches alternate row alignment, an odd base shifts every row."""
@@ -114,7 +115,7 @@ def test_persistent_tile_loop_small_grid(tm, grid):
     _full(case, plan=plan)
 
 
-@pytest.mark.parametrize("tm,tn", [(128, 128), (128, 256), (256, 128), (256, 256)])
+@pytest.mark.parametrize("tm,tn", [(128, 128), (128, 256), (256, 128), (256, 224), (256, 256)])
 @pytest.mark.parametrize("m,n,k", [(700, 900, 2048), (300, 520, 4096), (1030, 1000, 1024)])
 @pytest.mark.parametrize("out", ["bf16", "f32"])
 def test_stream_k_split_tiles(tm, tn, m, n, k, out):
@@ -373,3 +374,20 @@ def test_split_k_tail_general_values(out):
     Cbuf, intact = gu.run(case, guard_rows=2, pad_cols=5)
     assert intact
     gu.assert_close_sampled(case, Cbuf, p.tile_m, p.tile_n)
+
+
+# -------------------------------------------------------------- the 224-wide pair tile
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_pair_224_integer_exact_full_waves(dtype, out):
+    """256 x 224 pair tiles: the accumulators sit 256 tensor-memory columns
+    apart and a lane quarter's two warps take 4 + 3 of the 7 chunks.  Exact on
+    integer inputs over several waves, with ragged edges and guard bands."""
+    case = make_case(dtype, 1100, 3000, 512, out=out, dist="int")
+    plan = dgl.PlanInfo(path=dgl.PATH_TC, tile_m=256, tile_n=224)
+    Cbuf, intact = gu.run(case, plan=plan, guard_rows=2, pad_cols=3)
+    assert intact
+    if out == "f32":
+        gu.assert_exact(case, gu.host_valid(case, Cbuf))
+    else:
+        gu.assert_close_full(case, gu.host_valid(case, Cbuf))

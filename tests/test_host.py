@@ -180,7 +180,10 @@ def test_plan_padding_screen(dgl, m, n, k):
     pinned_past_screen = {(597, 11008, 4096), (528, 528, 1024)}
     assert p.path == dgl.PATH_TC
     padded = -(-m // p.tile_m) * p.tile_m * -(-n // p.tile_n) * p.tile_n
+    nk = -(-k * 2 // 128)
     rungs = [(64, 64), (64, 128), (64, 256), (128, 64), (128, 128), (128, 256), (256, 128), (256, 256)]
+    if nk <= 16:
+        rungs.append((256, 224))
     any_ok = any(-(-m // tm) * tm * -(-n // tn) * tn <= 1.25 * m * n for tm, tn in rungs)
     if any_ok and (m, n, k) not in pinned_past_screen:
         assert padded <= 1.25 * m * n
