@@ -434,9 +434,10 @@ def main():
     # ---------------------------------------------------------- device-timed region
     # Pass 1 times whole steps (the reported value): the calls go back to back,
     # so each kernel's launch and set-up can overlap the previous kernel's end
-    # (programmatic dependent launch).  Pass 2 repeats the steps with an event
-    # between calls, which serialises them, for each kernel's own duration
-    # (per-shape times and the roofline).
+    # (programmatic dependent launch).  Pass 2 replays the same steps as a graph
+    # with an event node between calls, which serialises them, for each
+    # kernel's own duration (per-shape times and the roofline); the events sit
+    # in the graph, so the host's launch gaps stay out of those durations.
     K_steps = args.steps
     ncall = len(calls)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(ncall + 1)] for _ in range(K_steps)]
@@ -455,28 +456,32 @@ def main():
                 f()
     t_end.record(stream)
     barrier()
-    t2_start = torch.cuda.Event(enable_timing=True)
-    t2_end = torch.cuda.Event(enable_timing=True)
-    t2_start.record(stream)
-    for s in range(K_steps):
-        ev = evs[s]
-        ev[0].record(stream)
-        for i, f in enumerate(calls):
-            f()
-            ev[i + 1].record(stream)
-    t2_end.record(stream)
+    timing_graph = timed_calls_graph(torch, calls, cap_stream, K_steps)
+    if timing_graph is not None:
+        evs, tg = timing_graph
+        tg.replay()
+    else:
+        for s in range(K_steps):
+            ev = evs[s]
+            ev[0].record(stream)
+            for i, f in enumerate(calls):
+                f()
+                ev[i + 1].record(stream)
+    torch.cuda.synchronize()
     barrier()
     st = lib.dgl_device_status(s_handle)
     if st != 0:
         raise RuntimeError(f"device status after timed region: {dgl.status_string(st)}")
     total_ms = t_start.elapsed_time(t_end)
     ms_per_step = total_ms / K_steps
-    ms_per_step_events = t2_start.elapsed_time(t2_end) / K_steps
     per_call_ms = [0.0] * ncall
     for s in range(K_steps):
         for i in range(ncall):
             per_call_ms[i] += evs[s][i].elapsed_time(evs[s][i + 1])
     per_call_ms = [v / K_steps for v in per_call_ms]
+    ms_per_step_events = sum(per_call_ms)
+    call_timing = "graph with an event node between calls" if timing_graph is not None else \
+        "stream launches with an event between calls"
 
     step_flops = sum(flops)
     ms_max, value = over_ranks(ms_per_step, step_flops, dist, dev)
@@ -654,6 +659,7 @@ def main():
                                       for c in cases})),
             "data": "synthetic (seeded SplitMix64 draws)",
             "config": {"workload": workload_text(args), "gemms_per_step": ncall, "launch": launch_mode,
+                       "per_call_timing": call_timing,
                        "parallelism": "replicas" if world > 1 else "single GPU",
                        "l2": (f"inputs larger than L2: {ws:.0f} MiB per step vs {l2_mb:.0f} MiB")
                              if ws > l2_mb else
@@ -682,6 +688,28 @@ def main():
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def timed_calls_graph(torch, calls, stream, steps):
+    """K steps captured as one CUDA graph with a timing event recorded between
+    consecutive calls (event record nodes), so that each call's duration is
+    read on the device without the host's launch gaps.  Returns (events, graph),
+    or None where events cannot be recorded as graph nodes (the caller then
+    times eager launches)."""
+    try:
+        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(calls) + 1)]
+               for _ in range(steps)]
+    except TypeError:
+        return None
+
+    def body(handle):
+        for ev in evs:
+            ev[0].record()
+            for i, f in enumerate(calls):
+                f(handle)
+                ev[i + 1].record()
+    g = capture_graph(torch, body, stream)
+    return None if g is None else (evs, g)
 
 
 def capture_graph(torch, body, stream=None):

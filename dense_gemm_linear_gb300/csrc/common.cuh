@@ -5,7 +5,8 @@
 
 namespace dgl {
 
-// Bits OR-ed into the device status word when a bounded wait gives up.
+// Bits OR-ed into the device status word when a bounded wait gives up (or a
+// kernel finds its launch unusable and exits without work).
 enum : int {
   STATUS_TIMEOUT_PRODUCER = 1,
   STATUS_TIMEOUT_MMA = 2,
@@ -14,6 +15,7 @@ enum : int {
   STATUS_TMEM_MISMATCH = 16,  // a CTA pair's tensor-memory allocations differ
   STATUS_TIMEOUT_FIXUP = 32,  // a stream-K partial tile never arrived
   STATUS_TIMEOUT_SCALES = 64, // block-scaled kernels: a scale slot was never released
+  STATUS_SMEM_ALIGN = 128,    // dynamic shared memory not 1024-byte aligned: the kernel did nothing
 };
 
 // Persistent tcgen05 tile kernel: problem and schedule.

@@ -182,7 +182,7 @@ int tc_tile_k(int dtype) { return dtype == DGL_DTYPE_E4M3 ? 128 : 64; }
 int tc_stages(int tile_m, int tile_n) {
   const int cg = tile_m == 256 ? 2 : 1;
   const int stage = (tile_m == 64 ? 64 : 128) * 128 + tile_n / cg * 128;
-  const int s = (232448 - 1024 - 32768 - 512) / stage;
+  const int s = (232448 - 32768 - 512) / stage;
   return s < 8 ? s : 8;
 }
 

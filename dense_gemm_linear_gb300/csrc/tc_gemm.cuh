@@ -52,9 +52,10 @@
 namespace dgl {
 
 // Ring depth that fills the 227 KB per-CTA budget left by the epilogue's
-// staging area (at most 8 stages).
+// staging area and the barriers (at most 8 stages).  The dynamic shared
+// memory is declared 1024-byte aligned, so no alignment slack is reserved.
 constexpr int tc_ring_stages(int stage_bytes, int staging_bytes) {
-  const int s = (232448 - 1024 - staging_bytes - 512) / stage_bytes;
+  const int s = (232448 - staging_bytes - 512) / stage_bytes;
   return s < 8 ? s : 8;
 }
 
@@ -135,7 +136,7 @@ struct TcConfig {
   static constexpr int FX_WARP_BYTES = ROWSTG ? 16 * ROW_PITCH : 4096;
   static constexpr int FX_BUFS = FX_WARP_BYTES >= 4096 ? 2 : 1;
   static constexpr int SMEM_BYTES =
-      1024 /* alignment slack */ + STAGES * (STAGE_BYTES + SCALE_STAGE_BYTES) + STG_TOTAL + BAR_BYTES;
+      STAGES * (STAGE_BYTES + SCALE_STAGE_BYTES) + STG_TOTAL + BAR_BYTES;
   static_assert(BN == 64 || BN == 128 || BN == 256 || (BN == 224 && CG == 2 && !EPI && !MX),
                 "tile widths of the ladder (224: plain GEMM on CTA pairs)");
   static_assert(BM == 128 || (BM == 64 && CG == 1 && !EPI && !MX), "64-row tiles: one CTA, plain GEMM");
@@ -325,9 +326,15 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                    const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmC,
                    const TcParams p) {
   constexpr int BM = Cfg::BM, BN = Cfg::BN, STAGES = Cfg::STAGES, CG = Cfg::CG;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = smem;
+  // The 128-byte-swizzled operand tiles need 1024-byte alignment, which the
+  // declaration requests; a launch that did not get it reports and exits
+  // (every CTA of a pair sees the same layout, so both leave together).
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if ((smem_u32(smem_raw) & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicOr(p.status, STATUS_SMEM_ALIGN);
+    return;
+  }
+  uint8_t* sA = smem_raw;
   uint8_t* sB = sA + STAGES * Cfg::A_STAGE_BYTES;
   uint8_t* sSc = sB + STAGES * Cfg::B_STAGE_BYTES;       // MX scale slots (none otherwise)
   uint8_t* sStg = sSc + STAGES * Cfg::SCALE_STAGE_BYTES; // 1024-aligned: stage sizes are multiples of 1 KB
