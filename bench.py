@@ -491,6 +491,23 @@ def main():
     headline = None
     if not args.no_headline and args.shape is None:
         headline = headline_run(torch, dgl, lib, dev, pk)
+
+    # ---------------------------------------------------------- the dominant kernel's GEMMs, back to back
+    # The step's kernel with the largest share of the per-call durations; its
+    # GEMMs are also timed one by one as back-to-back launches (as in the step,
+    # where each launch overlaps its predecessor's end), beside the per-call
+    # durations with an event between calls.
+    by_kernel = {}
+    for i, kn in enumerate(knames):
+        d = by_kernel.setdefault(kn, {"ms": 0.0, "flops": 0.0, "bytes": 0.0, "launches": 0, "calls": []})
+        d["ms"] += per_call_ms[i]
+        d["flops"] += flops[i]
+        d["bytes"] += nbytes[i]
+        d["launches"] += 1
+        d["calls"].append(i)
+    dominant = max(by_kernel, key=lambda k: by_kernel[k]["ms"])
+    dk = by_kernel[dominant]
+    b2b_us = [back_to_back_us(torch, make_call, ops[i], dev) for i in dk["calls"]]
     clocks = sampler.stop()
 
     # ---------------------------------------------------------- context: torch.matmul (cuBLAS), off the measured path
@@ -518,15 +535,10 @@ def main():
             cublas_us[i] = e0.elapsed_time(e1) / 20 * 1e3
 
     # ---------------------------------------------------------- roofline of the dominant kernel
-    by_kernel = {}
-    for i, kn in enumerate(knames):
-        d = by_kernel.setdefault(kn, {"ms": 0.0, "flops": 0.0, "bytes": 0.0, "launches": 0})
-        d["ms"] += per_call_ms[i]
-        d["flops"] += flops[i]
-        d["bytes"] += nbytes[i]
-        d["launches"] += 1
-    dominant = max(by_kernel, key=lambda k: by_kernel[k]["ms"])
-    dk = by_kernel[dominant]
+    b2b_ms = sum(b2b_us) * 1e-3
+    b2b = {"timing": "each of the kernel's GEMMs alone, back-to-back launches over operand copies rotated "
+                     "through more than L2, replayed as one CUDA graph",
+           "avg_launch_us": b2b_ms * 1e3 / dk["launches"], "per_gemm_us": [round(x, 2) for x in b2b_us]}
     if dominant.startswith("tc_gemm"):
         # a contraction's peak: the measured bf16 figure times the nominal dense
         # ratio of its own type (E4M3 4.5 / 2.25 PFLOP/s, FP4 13.5 / 2.25)
@@ -541,6 +553,8 @@ def main():
                     "peak_source": f"{pk_src} bf16 burst" + ratio_txt,
                     "launches_per_step": dk["launches"], "avg_launch_us": dk["ms"] * 1e3 / dk["launches"],
                     "algorithmic_flops_per_launch": dk["flops"] / dk["launches"]}
+        b2b["achieved"] = dk["flops"] / (b2b_ms * 1e-3) / 1e12
+        b2b["frac"] = b2b["achieved"] / peak_tf
     else:
         achieved = dk["bytes"] / (dk["ms"] * 1e-3) / 1e9
         roofline = {"kernel": dominant, "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
@@ -550,6 +564,10 @@ def main():
                     "peak_source": f"{pk_src} hbm copy",
                     "launches_per_step": dk["launches"], "avg_launch_us": dk["ms"] * 1e3 / dk["launches"],
                     "algorithmic_bytes_per_launch": dk["bytes"] / dk["launches"]}
+        b2b["achieved"] = dk["bytes"] / (b2b_ms * 1e-3) / 1e9
+        b2b["frac"] = b2b["achieved"] / pk["hbm_gbs"]
+    roofline["per_call_timing"] = "an event between calls (each launch serialised after its predecessor)"
+    roofline["back_to_back"] = b2b
     kernels = {k: {"launches_per_step": v["launches"], "us_per_step": v["ms"] * 1e3,
                    "share": v["ms"] / sum(x["ms"] for x in by_kernel.values())} for k, v in by_kernel.items()}
     dec = {k: v for k, v in by_kernel.items() if k.startswith("decode")}
@@ -679,6 +697,8 @@ def main():
             line["cpu_baseline"]["sample"] = "first rows of each GEMM of the step"
         line["roofline"] = {k: roofline[k] for k in ("kernel", "bound", "achieved", "peak", "unit", "frac",
                                                       "traffic", "peak_source", "avg_launch_us")}
+        line["roofline"]["back_to_back"] = {k: round(roofline["back_to_back"][k], 4)
+                                            for k in ("achieved", "frac", "avg_launch_us")}
         if roofline_decode:
             line["roofline_decode"] = {"achieved": round(roofline_decode["achieved"], 1),
                                        "frac": round(roofline_decode["frac"], 4)}
@@ -688,6 +708,46 @@ def main():
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def back_to_back_us(torch, make_call, op, dev, launches=48, reps=7):
+    """One GEMM of the step on its own: `launches` back-to-back calls over
+    ceil(3 L2 / (|A| + |B|)) copies of its operands (each with its own C), so
+    every launch reads them from HBM, replayed as one CUDA graph.  Returns the
+    per-launch time of the median replay, in us."""
+    import math
+    c, A, B, sa, sb, C, o, bias = op
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    ab = A.numel() * A.element_size() + B.numel() * B.element_size()
+    copies = max(2, math.ceil(3 * l2 / ab))
+    # the copies stay referenced here: a call holds raw device pointers only
+    bufs = [op] + [(c, A.clone(), B.clone(), sa, sb, torch.empty_like(C), o, bias) for _ in range(copies - 1)]
+    calls = [make_call(*x) for x in bufs]
+    stream = torch.cuda.Stream(device=dev)
+    for f in calls:
+        f(stream.cuda_stream)
+    torch.cuda.synchronize()
+    L = copies * max(1, math.ceil(launches / copies))
+    g = capture_graph(torch, lambda s: [calls[t % copies](s) for t in range(L)], stream)
+    times = []
+    for i in range(reps + 2):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        if g is not None:
+            with torch.cuda.stream(stream):
+                g.replay()
+        else:
+            for t in range(L):
+                calls[t % copies](stream.cuda_stream)
+        e1.record(stream)
+        e1.synchronize()
+        if i >= 2:
+            times.append(e0.elapsed_time(e1) * 1e3 / L)
+    torch.cuda.synchronize()
+    del g, calls, bufs
+    torch.cuda.empty_cache()
+    return statistics.median(times)
 
 
 def timed_calls_graph(torch, calls, stream, steps):
