@@ -894,7 +894,8 @@ dgl_status dgl_device_status(void* stream) {
         return DGL_ERR_CUDA;
     }
     if (cudaDeviceSynchronize() != cudaSuccess) return DGL_ERR_CUDA;
-    return DGL_ERR_TIMEOUT;
+    // a tile kernel that found its shared memory misaligned did nothing
+    return (word & ~STATUS_SMEM_ALIGN) != 0 ? DGL_ERR_TIMEOUT : DGL_ERR_UNSUPPORTED;
   }
   return DGL_OK;
 }

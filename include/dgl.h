@@ -341,8 +341,10 @@ dgl_status dgl_shutdown(void);
  * Synchronise `stream`, then report and clear the current device's status
  * word: DGL_ERR_TIMEOUT if any kernel's bounded wait gave up since the last
  * call (the device is then drained and every partial-tile flag of the
- * library on it cleared), DGL_ERR_CUDA if synchronisation failed, else
- * DGL_OK.
+ * library on it cleared), DGL_ERR_UNSUPPORTED if a tile kernel found its
+ * dynamic shared memory without the 1024-byte alignment it declares and
+ * exited without work (not seen on GB300), DGL_ERR_CUDA if synchronisation
+ * failed, else DGL_OK.
  */
 dgl_status dgl_device_status(void* stream);
 
