@@ -219,6 +219,24 @@ bool encode_operand_map(CUtensorMap* map, const void* base, bool e4m3, int64_t i
   return r == CUDA_SUCCESS;
 }
 
+// 3-D tensor map over a decode call's A ([m][K] row-major, K a whole number
+// of 128-byte steps) as [K steps][m rows][128 bytes]: a box of 16 rows by
+// `steps` K steps lands as `steps` consecutive 2 KB planes of 16 rows, rows
+// past m and steps past K filled with zeros, with the 128-byte swizzle.
+bool encode_decode_a_map(CUtensorMap* map, const void* base, bool e4m3, int64_t K, int64_t m, int steps) {
+  const int64_t esize = e4m3 ? 1 : 2;
+  const int64_t nk = K * esize / 128;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(128 / esize), static_cast<cuuint64_t>(m), static_cast<cuuint64_t>(nk)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(K * esize), 128};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esize), 16, static_cast<cuuint32_t>(steps)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                        const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 2-D tensor map over packed 4-bit codes, [rows][K / 2] bytes (element 2t in
 // the low four bits of byte t), with a box of 128 elements by box_rows rows
 // and the 128-byte swizzle.  The 16U4_ALIGN16B type lands each 16 elements
@@ -276,7 +294,7 @@ struct MapKey {
   const void* base;
   int64_t d0, d1, pitch;
   int box_rows, kind;  // kind: 0 bf16 operand, 1 E4M3 operand, 2 bf16 output, 3 fp32 output, 4 MN-major bf16,
-                       // 5 packed 4-bit operand
+                       // 5 packed 4-bit operand, 6 / 7 a decode call's 3-D bf16 / E4M3 A (box_rows: K steps)
   bool operator==(const MapKey& o) const {
     return base == o.base && d0 == o.d0 && d1 == o.d1 && pitch == o.pitch && box_rows == o.box_rows &&
            kind == o.kind;
@@ -522,6 +540,13 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream, Sta
           decode_stages(rows_hi, want, g) < 2)
         return DGL_ERR_UNSUPPORTED;
       ks = want;
+    }
+    p.a3d = 0;
+    if ((pr.K * esize) % 128 == 0) {
+      const MapKey ak{pr.A, pr.K, pr.m, pr.K, ks, e4m3 ? 7 : 6};
+      if (!cached_map(&ta, ak, [&](CUtensorMap* m) { return encode_decode_a_map(m, pr.A, e4m3, pr.K, pr.m, ks); }))
+        return DGL_ERR_CUDA;
+      p.a3d = 1;
     }
     p.group = g;
     p.ksteps = ks;

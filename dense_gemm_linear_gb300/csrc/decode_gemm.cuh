@@ -10,10 +10,11 @@
 //     rows, at most 128); a CTA walks parts blockIdx.x, +gridDim.x, ...
 //   * warp 0 streams each part through a shared-memory ring of ~192 KB.  A
 //     stage holds `ks` consecutive 128-byte steps of K ("planes"): per plane
-//     one TMA box of the part's B rows and one box of A's m rows (bytes past
-//     K arrive as zeros), both with the 128-byte swizzle.  The planes' loads
-//     go out back to back so adjacent pieces of each B row reach the memory
-//     system together.
+//     one TMA box of the part's B rows, and A's rows for all the stage's
+//     planes in one 3-D box (or, when K ends inside a plane, one box of A's m
+//     rows per plane; bytes past K arrive as zeros), all with the 128-byte
+//     swizzle.  The planes' loads go out back to back so adjacent pieces of
+//     each B row reach the memory system together.
 //   * warp 1 issues tcgen05.mma with the part's B rows as the 128-row operand
 //     and A's 16 rows as the N = 16 operand: D[row of B][row of A] accumulates
 //     in tensor memory (two 16-column buffers, alternating by part).  The MMA
@@ -171,10 +172,19 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
           }
           const int planes = min(ks, nk - kb0);
           uint8_t* sbase = ring + stage * stage_bytes;
-          mbar_arrive_expect_tx(&full[stage], tx * planes);
-          for (int j = 0; j < planes; ++j) {
-            tma_load_2d(sbase + j * DEC_A_BOX_BYTES, &tmA, &full[stage], (kb0 + j) * kstep, 0, pol_a);
-            tma_load_2d(sbase + a_bytes + j * b_plane, mb, &full[stage], (kb0 + j) * kstep, r0, pol_b);
+          if (p.a3d) {
+            // A's box always carries ks planes of 16 rows (zeros past m and K);
+            // a small part's stage then costs one copy for A instead of ks
+            mbar_arrive_expect_tx(&full[stage], ks * DEC_A_BOX_BYTES + planes * (tx - p.m * 128));
+            tma_load_3d(sbase, &tmA, &full[stage], 0, 0, kb0, pol_a);
+            for (int j = 0; j < planes; ++j)
+              tma_load_2d(sbase + a_bytes + j * b_plane, mb, &full[stage], (kb0 + j) * kstep, r0, pol_b);
+          } else {
+            mbar_arrive_expect_tx(&full[stage], tx * planes);
+            for (int j = 0; j < planes; ++j) {
+              tma_load_2d(sbase + j * DEC_A_BOX_BYTES, &tmA, &full[stage], (kb0 + j) * kstep, 0, pol_a);
+              tma_load_2d(sbase + a_bytes + j * b_plane, mb, &full[stage], (kb0 + j) * kstep, r0, pol_b);
+            }
           }
           ++issued;
           if (++stage == static_cast<uint32_t>(stages)) {

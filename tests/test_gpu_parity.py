@@ -181,6 +181,17 @@ def test_decode_every_m(m, out):
     _full(make_case("bf16", m, 1001, 264, out=out), guard_rows=1, pad_cols=3)
 
 
+@pytest.mark.parametrize("m", list(range(1, 17)))
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_decode_every_m_whole_k_steps(m, dtype):
+    """K a whole number of 128-byte steps: each stage's A planes arrive as one
+    3-D box of 16 rows (zeros past m); every m, ragged parts, and a last
+    stage with fewer K steps than the box (zeros past K)."""
+    k = 640 if dtype == "bf16" else 1280   # ten 128-byte steps: stages of 8 and 2
+    case = make_case(dtype, m, 1001, k, out="f32", dist="fp8" if dtype == "fp8" else "normal")
+    _full(case, guard_rows=1, pad_cols=3)
+
+
 @pytest.mark.parametrize("dtype,n,k,g", [("bf16", 1100, 1024, 16), ("bf16", 2000, 512, 8), ("bf16", 4000, 1024, 4),
                                          ("bf16", 9000, 512, 2), ("fp8", 1100, 2048, 16), ("fp8", 4000, 2048, 4)])
 @pytest.mark.parametrize("m,out", [(1, "bf16"), (7, "f32"), (16, "bf16")])
