@@ -98,12 +98,12 @@ struct DecodeParams {
   int act;              // 0 identity, 1 GELU, 2 SiLU
   uint32_t idesc_or;    // bits OR-ed into the MMA instruction descriptor (W4A8: E2M1 B rows)
   int b_tx_shift;       // B boxes' transaction bytes = shared-memory bytes >> b_tx_shift (1: packed 4-bit B)
-  int prefetch_planes;
+  int prefetch_planes;  // K steps of the CTA's first part of B prefetched into L2 before the wait (0: none)
   // 1: A's map is 3-D, [K steps][m rows][128 bytes], with a box of 16 rows
   // (zero past m) by ksteps K steps (zero past K): one copy brings a stage's
   // A planes (K a whole number of 128-byte steps).  0: one 2-D box of m rows
   // per K step.
-  int a3d;  // K steps of the CTA's first part of B prefetched into L2 before the wait (0: none)
+  int a3d;
 };
 
 // The activations of the linear-layer epilogue.
