@@ -164,27 +164,6 @@ __device__ __forceinline__ uint32_t stg_offset(int r, int c16) {
     return static_cast<uint32_t>(r * 128 + ((c16 ^ (r & 7)) << 4));
 }
 
-// Copy bytes [lo, hi) of a staged row to global memory with the widest
-// naturally aligned stores (2, 4 or 8 bytes; the span is under 16 bytes).
-// The staged copy and the global row share their alignment modulo 16.
-__device__ __forceinline__ void store_row_pieces(uint8_t* g, uint32_t s, int lo, int hi) {
-  while (lo < hi) {
-    const uintptr_t ga = reinterpret_cast<uintptr_t>(g + lo);
-    const int left = hi - lo;
-    if ((ga & 7) == 0 && left >= 8) {
-      const uint2 v = lds_v2(s + lo);
-      *reinterpret_cast<uint2*>(g + lo) = v;
-      lo += 8;
-    } else if ((ga & 3) == 0 && left >= 4) {
-      *reinterpret_cast<uint32_t*>(g + lo) = lds_u32(s + lo);
-      lo += 4;
-    } else {
-      *reinterpret_cast<uint16_t*>(g + lo) = static_cast<uint16_t>(lds_u16(s + lo));
-      lo += 2;
-    }
-  }
-}
-
 // Stores NW packed words (2 NW bf16 values, value 2i in the low half of w[i])
 // to shared memory so that value j lands at byte a + D + 2 j: a is 16-byte
 // aligned and D (the global row's misalignment) is even and below 16.  The
@@ -1023,19 +1002,41 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       }
 
       if constexpr (Cfg::ROWSTG) {
+        // Each staged row's 16-byte-aligned body leaves in one bulk copy (the
+        // quarter's first warp, a row per lane); the partial 16-byte units at
+        // its two ends, in 2-byte stores (the second warp).
         fence_proxy_async_shared();
         named_bar_sync(1 + q, 64);
-        if (L > 0) {
-          const int head = min(L, (16 - delta) & 15);
-          const int body = ((L - head) >> 4) << 4;
-          if (half == 0) {
+        if (half == 0) {
+          if (L > 0) {
+            const int head = min(L, (16 - delta) & 15);
+            const int body = ((L - head) >> 4) << 4;
             if (body > 0) {
               bulk_store_1d(rowp + head, srow + head, static_cast<uint32_t>(body));
               bulk_commit();
             }
-          } else {
-            store_row_pieces(rowp, srow, 0, head);
-            store_row_pieces(rowp, srow, head + body, L);
+          }
+        } else {
+          // The quarter's 32 rows have 64 end units.  Eight lanes take one
+          // unit, a bf16 each, so a store instruction writes four units and
+          // each unit's bytes leave as one request (one lane a row, with 2-,
+          // 4- and 8-byte stores, took up to three per unit).
+#pragma unroll 1
+          for (int pass = 0; pass < 16; ++pass) {
+            const int u = 4 * pass + (lane >> 3);  // unit: row u / 2 of the quarter, its head (even) or tail (odd)
+            const int r = u >> 1;
+            const int urow = row0 + r;
+            const int uL = (r < Cfg::WARP_ROWS && urow < p.m) ? 2 * ncols : 0;  // valid bytes of that row
+            uint8_t* up = reinterpret_cast<uint8_t*>(static_cast<__nv_bfloat16*>(p.C) +
+                                                     static_cast<int64_t>(uL > 0 ? urow : 0) * p.ldc + ocol0);
+            const int ud = static_cast<int>(reinterpret_cast<uintptr_t>(up) & 15);
+            const int uhead = min(uL, (16 - ud) & 15);
+            const int ubody = ((uL - uhead) >> 4) << 4;
+            // byte x of the row's segment: the head unit spans x = -ud .. 15 - ud
+            const int x = (u & 1) ? uhead + ubody + 2 * (lane & 7) : 2 * (lane & 7) - ud;
+            if (x >= 0 && x < ((u & 1) ? uL : uhead))
+              *reinterpret_cast<uint16_t*>(up + x) =
+                  static_cast<uint16_t>(lds_u16(stg_addr + r * Cfg::ROW_PITCH + ud + x));
           }
         }
       }
