@@ -31,8 +31,8 @@
 //              For bf16 C whose rows are not 16-byte aligned (N = 50257,
 //              11007, 4095, ...) the quarter's two warps instead stage whole
 //              tile rows, each shifted by its own misalignment, so every row's
-//              16-byte-aligned body leaves in one bulk copy and only its
-//              head and tail bytes take narrow stores.
+//              16-byte-aligned body leaves in one bulk copy and only the
+//              partial 16-byte units at its two ends take 2-byte stores.
 //              The staging transpose is section 7.2's "CShuffle" idea: re-map
 //              threads so each store covers contiguous columns of a row.
 //   warps 10-13 (MXFP4 only) gather each stage's E8M0 scales into shared
