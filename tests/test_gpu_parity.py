@@ -107,6 +107,20 @@ def test_output_store_paths(pad, base, out, tm, tn):
     gu.assert_close_full(case, gu.host_valid(case, Cbuf))
 
 
+@pytest.mark.parametrize("n", [1, 2, 3, 5, 7, 8, 9, 15, 17, 23])
+@pytest.mark.parametrize("base", [0, 1, 3])
+@pytest.mark.parametrize("tm,tn", [(64, 64), (128, 256), (256, 256)])
+def test_row_staging_rows_shorter_than_a_unit(n, base, tm, tn):
+    """bf16 C rows of a few columns at a pitch or base that is not 16-byte
+    aligned: a row's bytes fit in one or two partial 16-byte units (no aligned
+    body), which the end-unit stores write alone."""
+    case = make_case("bf16", 40, n, 64, out="bf16")
+    plan = dgl.PlanInfo(path=dgl.PATH_TC, tile_m=tm, tile_n=tn)
+    Cbuf, intact = gu.run(case, plan=plan, guard_rows=2, pad_cols=3, base_offset=base)
+    assert intact, "wrote outside the valid region"
+    gu.assert_close_full(case, gu.host_valid(case, Cbuf))
+
+
 @pytest.mark.parametrize("tm,grid", [(64, 1), (64, 5), (128, 1), (128, 3), (128, 7), (256, 2), (256, 6)])
 def test_persistent_tile_loop_small_grid(tm, grid):
     """Fewer CTAs (or CTA pairs) than tiles: each walks many tiles through both accumulators."""
