@@ -371,6 +371,34 @@ def main():
 
     calls = [make_call(*o) for o in ops]
     dtype_ids = {"bf16": dgl.DTYPE_BF16, "fp8": dgl.DTYPE_E4M3, "mxfp4": dgl.DTYPE_MXFP4, "w4a8": dgl.DTYPE_W4A8}
+
+    def make_desc(c, A, B, sa, sb, C, out_dtype, bias):
+        """The GEMM as a dgl_gemm_batch item, or None where the batch call has no
+        field for it (linear epilogue, operand layouts, a forced plan)."""
+        if forced is not None or c.linear or c.a_major or c.b_major:
+            return None
+        return dgl.GemmDesc(dtype=dtype_ids[c.dtype], out_dtype=out_dtype, A=A.data_ptr(), B=B.data_ptr(),
+                            scale_a=sa.data_ptr() if sa is not None else None,
+                            scale_b=sb.data_ptr() if sb is not None else None, C=C.data_ptr(),
+                            M=c.m, N=c.n, K=c.K, m_valid=c.m, n_valid=c.n)
+
+    # The step's GEMMs are independent (no GEMM reads another's C), so they go
+    # out as one dgl_gemm_batch: each kernel after the first loads its operands
+    # while the previous one finishes.  Workloads with fused epilogues or
+    # operand layouts the batch call does not take run as single calls.
+    descs = [make_desc(*o) for o in ops]
+    batched = all(d is not None for d in descs)
+    if batched:
+        desc_arr = dgl.gemm_descs(descs)
+
+        def step_call(s=s_handle):
+            st = lib.dgl_gemm_batch(desc_arr, len(desc_arr), s)
+            if st != 0:
+                raise RuntimeError(f"batch failed: {dgl.status_string(st)}")
+    else:
+        def step_call(s=s_handle):
+            for f in calls:
+                f(s)
     plans = [dgl.dgl_plan_linear(dtype_ids[c.dtype], c.m, c.n, c.K,
                                  dgl.OUT_F32 if c.out == "f32" else dgl.OUT_BF16, int(c.gated)) if c.linear else
              dgl.dgl_plan(dtype_ids[c.dtype], c.m, c.n, c.K,
@@ -412,8 +440,7 @@ def main():
 
     # warm-up
     for _ in range(args.warmup):
-        for f in calls:
-            f()
+        step_call()
     torch.cuda.synchronize()
     st = lib.dgl_device_status(s_handle)
     if st != 0:
@@ -425,11 +452,11 @@ def main():
     # stream of its own; one step on it first gives a split schedule its
     # workspace there.  The graph is replayed on the timing stream.
     cap_stream = torch.cuda.Stream(device=dev)
-    for f in calls:
-        f(cap_stream.cuda_stream)
+    step_call(cap_stream.cuda_stream)
     torch.cuda.synchronize()
-    step_graph = capture_graph(torch, lambda s: [f(s) for f in calls], cap_stream)
-    launch_mode = "cuda graph of one step" if step_graph is not None else "stream launches"
+    step_graph = capture_graph(torch, step_call, cap_stream)
+    launch_mode = ("cuda graph of one step" if step_graph is not None else "stream launches") + \
+        (", one dgl_gemm_batch" if batched else ", one call per GEMM")
 
     # ---------------------------------------------------------- device-timed region
     # Pass 1 times whole steps (the reported value): the calls go back to back,
@@ -452,10 +479,23 @@ def main():
         if step_graph is not None:
             step_graph.replay()
         else:
-            for f in calls:
-                f()
+            step_call()
     t_end.record(stream)
     barrier()
+    # the same step as one call per GEMM, for comparison (not the reported value)
+    ms_single_calls = None
+    if batched:
+        single_graph = capture_graph(torch, lambda s: [f(s) for f in calls], cap_stream)
+        if single_graph is not None:
+            u0 = torch.cuda.Event(enable_timing=True)
+            u1 = torch.cuda.Event(enable_timing=True)
+            u0.record(stream)
+            for s in range(K_steps):
+                single_graph.replay()
+            u1.record(stream)
+            torch.cuda.synchronize()
+            ms_single_calls = u0.elapsed_time(u1) / K_steps
+            del single_graph
     timing_graph = timed_calls_graph(torch, calls, cap_stream, K_steps)
     if timing_graph is not None:
         evs, tg = timing_graph
@@ -499,7 +539,8 @@ def main():
     # serialised per-call durations above add up to more (each carries its
     # launch and ramp-up), so the per-kernel figures and the roofline use the
     # back-to-back ones and report the serialised ones beside them.
-    b2b_ms = [back_to_back_us(torch, make_call, op, dev) * 1e-3 for op in ops]
+    b2b_ms = [back_to_back_us(torch, make_call, op, dev, make_desc=make_desc if batched else None, lib=lib) * 1e-3
+              for op in ops]
     clocks = sampler.stop()
     by_kernel = {}
     for i, kn in enumerate(knames):
@@ -568,7 +609,8 @@ def main():
         serial["achieved"] = dk["bytes"] / (dk["ms_serial"] * 1e-3) / 1e9
         serial["frac"] = serial["achieved"] / pk["hbm_gbs"]
     roofline["timing"] = ("each of the kernel's GEMMs alone: 48 back-to-back launches over operand copies rotated "
-                          "through more than L2, replayed as one CUDA graph (CUDA events); the per-GEMM "
+                          "through more than L2" + (", issued as one dgl_gemm_batch as in the step" if batched else "") +
+                          ", replayed as one CUDA graph (CUDA events); the per-GEMM "
                           f"durations of the step add up to {sum(b2b_ms) * 1e3:.1f} us against the "
                           f"{ms_per_step * 1e3:.1f} us step")
     roofline["serialised"] = serial
@@ -693,6 +735,10 @@ def main():
             "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": K_steps * ncall, "clocks": clocks,
             "roofline": roofline,
         }
+        if ms_single_calls is not None:
+            # the same step issued as one call per GEMM (each kernel waits for its
+            # predecessor before loading operands), measured right after it
+            line["ms_per_step_single_calls"] = ms_single_calls
         detail = dict(line)
         detail.update({"roofline_decode": roofline_decode, "kernels": kernels, "per_shape": per_shape,
                        "ms_per_step_with_call_events": ms_per_step_events, "headline": headline})
@@ -717,11 +763,13 @@ def main():
     return 0
 
 
-def back_to_back_us(torch, make_call, op, dev, launches=48, reps=7):
-    """One GEMM of the step on its own: `launches` back-to-back calls over
+def back_to_back_us(torch, make_call, op, dev, launches=48, reps=7, make_desc=None, lib=None):
+    """One GEMM of the step on its own: `launches` back-to-back launches over
     ceil(3 L2 / (|A| + |B|)) copies of its operands (each with its own C), so
-    every launch reads them from HBM, replayed as one CUDA graph.  Returns the
-    per-launch time of the median replay, in us."""
+    every launch reads them from HBM, replayed as one CUDA graph: one
+    dgl_gemm_batch of `launches` items when make_desc is given (as the step
+    runs), else single calls.  Returns the per-launch time of the median
+    replay, in us."""
     import math
     c, A, B, sa, sb, C, o, bias = op
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -735,7 +783,19 @@ def back_to_back_us(torch, make_call, op, dev, launches=48, reps=7):
         f(stream.cuda_stream)
     torch.cuda.synchronize()
     L = copies * max(1, math.ceil(launches / copies))
-    g = capture_graph(torch, lambda s: [calls[t % copies](s) for t in range(L)], stream)
+    if make_desc is not None:
+        import dense_gemm_linear_gb300 as dgl
+        arr = dgl.gemm_descs([make_desc(*bufs[t % copies]) for t in range(L)])
+
+        def body(s):
+            st = lib.dgl_gemm_batch(arr, L, s)
+            if st != 0:
+                raise RuntimeError(f"batch failed: {dgl.status_string(st)}")
+    else:
+        def body(s):
+            for t in range(L):
+                calls[t % copies](s)
+    g = capture_graph(torch, body, stream)
     times = []
     for i in range(reps + 2):
         e0 = torch.cuda.Event(enable_timing=True)
@@ -745,8 +805,7 @@ def back_to_back_us(torch, make_call, op, dev, launches=48, reps=7):
             with torch.cuda.stream(stream):
                 g.replay()
         else:
-            for t in range(L):
-                calls[t % copies](stream.cuda_stream)
+            body(stream.cuda_stream)
         e1.record(stream)
         e1.synchronize()
         if i >= 2:
@@ -811,8 +870,10 @@ NOMINAL_HBM_GBS = 8000.0
 def headline_run(torch, dgl, lib, dev, pk, launches=48, reps=7):
     """Time each HEADLINE shape alone: its operands rotate through
     ceil(3 L2 / (|A| + |B|)) copies, so every launch reads them from HBM, and
-    `launches` back-to-back calls are replayed as one CUDA graph.  Returns
-    {shape: {us, rate, fractions of the nominal and measured peaks}}."""
+    `launches` back-to-back GEMMs, issued as one dgl_gemm_batch, are replayed
+    as one CUDA graph; the same launches as single calls are timed beside them
+    (us_single_calls).  Returns {shape: {us, rate, fractions of the nominal and
+    measured peaks}}."""
     import math
 
     from synthetic import make_workload_case
@@ -855,26 +916,42 @@ def headline_run(torch, dgl, lib, dev, pk, launches=48, reps=7):
             launch(r, cur)
         torch.cuda.synchronize()
         L = copies * max(1, math.ceil(launches / copies))
-        g = capture_graph(torch, lambda s: [launch(t % copies, s) for t in range(L)], stream)
-        times = []
-        for i in range(reps + 2):
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            if g is not None:
-                with torch.cuda.stream(stream):
-                    g.replay()
-            else:
-                for t in range(L):
-                    launch(t % copies, cur)
-            e1.record(stream)
-            e1.synchronize()
-            if i >= 2:
-                times.append(e0.elapsed_time(e1) * 1e3 / L)
-        us = statistics.median(times)
+        # the same L GEMMs as one dgl_gemm_batch: independent, so each kernel
+        # loads its operands while the previous one finishes
+        arr = dgl.gemm_descs([dict(dtype=dgl.DTYPE_BF16 if c.dtype == "bf16" else dgl.DTYPE_E4M3,
+                                   out_dtype=dgl.OUT_BF16, A=As[t % copies].data_ptr(), B=Bs[t % copies].data_ptr(),
+                                   scale_a=sa.data_ptr() if sa is not None else None,
+                                   scale_b=sb.data_ptr() if sb is not None else None, C=Cs[t % copies].data_ptr(),
+                                   M=c.m, N=c.n, K=c.K, m_valid=c.m, n_valid=c.n) for t in range(L)])
+
+        def batch(s):
+            st = lib.dgl_gemm_batch(arr, L, s)
+            if st != 0:
+                raise RuntimeError(f"headline {c.name}: {dgl.status_string(st)}")
+
+        def timed(body):
+            g = capture_graph(torch, body, stream)
+            times = []
+            for i in range(reps + 2):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                if g is not None:
+                    with torch.cuda.stream(stream):
+                        g.replay()
+                else:
+                    body(cur)
+                e1.record(stream)
+                e1.synchronize()
+                if i >= 2:
+                    times.append(e0.elapsed_time(e1) * 1e3 / L)
+            return statistics.median(times)
+
+        us = timed(batch)
+        us_single = timed(lambda s: [launch(t % copies, s) for t in range(L)])
         key = f"{c.m}x{c.n}x{c.K} {'e4m3' if c.dtype == 'fp8' else 'bf16'}"
         plan = dgl.dgl_plan(dgl.DTYPE_BF16 if c.dtype == "bf16" else dgl.DTYPE_E4M3, c.m, c.n, c.K)
-        rec = {"us": round(us, 2), "copies": copies,
+        rec = {"us": round(us, 2), "us_single_calls": round(us_single, 2), "copies": copies,
                "tile": "decode" if plan.path == dgl.PATH_DECODE else f"{plan.tile_m}x{plan.tile_n}"}
         if c.m > 16:
             tf = 2.0 * c.m * c.n * c.K / (us * 1e-6) / 1e12

@@ -42,7 +42,8 @@ MN_MAJOR = 1
 
 EXPORTED = ["dgl_gemm_bf16", "dgl_gemm_fp8", "dgl_gemm_planned", "dgl_plan", "dgl_tile_metrics",
             "dgl_device_status", "dgl_status_string", "dgl_version", "dgl_gemm_noalloc", "dgl_linear",
-            "dgl_plan_linear", "dgl_gemm_bf16_ex", "dgl_gemm_mxfp4", "dgl_shutdown", "dgl_gemm_w4a8"]
+            "dgl_plan_linear", "dgl_gemm_bf16_ex", "dgl_gemm_mxfp4", "dgl_shutdown", "dgl_gemm_w4a8",
+            "dgl_gemm_batch"]
 
 
 class PlanInfo(ctypes.Structure):
@@ -54,6 +55,14 @@ class PlanInfo(ctypes.Structure):
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+class GemmDesc(ctypes.Structure):
+    """One GEMM of dgl_gemm_batch (the C struct dgl_gemm_desc)."""
+    _fields_ = [("dtype", ctypes.c_int32), ("out_dtype", ctypes.c_int32), ("A", ctypes.c_void_p),
+                ("B", ctypes.c_void_p), ("scale_a", ctypes.c_void_p), ("scale_b", ctypes.c_void_p),
+                ("C", ctypes.c_void_p), ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("m_valid", ctypes.c_int64), ("n_valid", ctypes.c_int64)]
 
 
 class DglError(RuntimeError):
@@ -96,6 +105,8 @@ def load_library(path: str | None = None):
     lib.dgl_gemm_w4a8.restype = i32
     lib.dgl_gemm_mxfp4.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i32, vp]
     lib.dgl_gemm_mxfp4.restype = i32
+    lib.dgl_gemm_batch.argtypes = [ctypes.POINTER(GemmDesc), i32, vp]
+    lib.dgl_gemm_batch.restype = i32
     lib.dgl_plan.argtypes = [i32, i64, i64, i64, i32, i32, ctypes.POINTER(PlanInfo)]
     lib.dgl_plan.restype = i32
     lib.dgl_tile_metrics.argtypes = [i64, i64, i32, i32, i32, ctypes.POINTER(PlanInfo)]
@@ -132,6 +143,20 @@ def dgl_gemm_bf16(A, B, C, M, N, K, m_valid=0, n_valid=0, out_dtype=OUT_BF16, st
 
 def dgl_gemm_fp8(A, B, sa, sb, C, M, N, K, m_valid=0, n_valid=0, out_dtype=OUT_BF16, stream=0) -> int:
     return load_library().dgl_gemm_fp8(A, B, sa, sb, C, M, N, K, m_valid, n_valid, out_dtype, stream)
+
+
+def gemm_descs(items):
+    """A ctypes array of GemmDesc from dicts (or GemmDesc instances) for dgl_gemm_batch."""
+    arr = (GemmDesc * len(items))()
+    for i, it in enumerate(items):
+        arr[i] = it if isinstance(it, GemmDesc) else GemmDesc(**it)
+    return arr
+
+
+def dgl_gemm_batch(items, stream=0) -> int:
+    """Independent GEMMs back to back on one stream (see dgl_gemm_batch in dgl.h); items: GemmDesc array or list."""
+    arr = items if isinstance(items, ctypes.Array) else gemm_descs(items)
+    return load_library().dgl_gemm_batch(arr, len(arr), stream)
 
 
 def dgl_gemm_mxfp4(A, B, sfa, sfb, C, M, N, K, m_valid=0, n_valid=0, out_dtype=OUT_BF16, stream=0) -> int:

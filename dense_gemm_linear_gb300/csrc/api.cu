@@ -404,6 +404,8 @@ struct Problem {
   // W4A8 (dgl_gemm_w4a8): dtype E4M3 for A, B holds packed E2M1 codes (K / 2
   // bytes a row)
   int w4 = 0;
+  // programmatic dependent launch mode of the kernel (PDL_*; dgl_gemm_batch)
+  int pdl_mode = PDL_SERIAL;
 };
 
 dgl_status validate(Problem& pr) {
@@ -556,6 +558,7 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream, Sta
     p.status = ds->status;
     p.bias = pr.bias;
     p.act = pr.act;
+    p.pdl_mode = pr.pdl_mode;
     const int grid = forced && forced->grid > 0 ? (forced->grid < parts ? forced->grid : parts)
                                                 : decode_grid(pr.n, ds->num_sms);
     return launch_decode(pr.dtype, pr.out, ta, tb_lo, tb_hi, p, grid, stream) == cudaSuccess ? DGL_OK
@@ -608,6 +611,7 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream, Sta
   p.idesc_or = pr.w4 ? kIdescE2M1 << 10 : 0u;  // E2M1 in the B format field
   p.b_tx_shift = pr.w4 ? 1 : 0;
   p.prefetch_stages = p.num_kb >= 4 * plan.stages ? plan.stages : 0;
+  p.pdl_mode = pr.pdl_mode;
   // A split schedule needs the stream's workspace.  A stream being captured
   // into a CUDA graph cannot have one allocated, so a captured call on a
   // stream without one runs the data-parallel schedule instead.
@@ -676,7 +680,7 @@ dgl_status run(Problem pr, const dgl_plan_info* forced, cudaStream_t stream, Sta
 // Block-scaled FP4 (MXFP4): A and B as byte tensors of K / 2 bytes per row
 // (TMA moves the packed E2M1 codes untouched), E8M0 scales read by the
 // kernel's scale warps, 128 x 256 tiles.
-dgl_status run_mxfp4(Problem pr, const uint8_t* sfa, const uint8_t* sfb, cudaStream_t stream) {
+dgl_status validate_mxfp4(Problem& pr, const uint8_t* sfa, const uint8_t* sfb) {
   if (pr.out != DGL_OUT_BF16 && pr.out != DGL_OUT_F32) return DGL_ERR_ARG;
   if (pr.M < 0 || pr.N < 0 || pr.K < 0 || pr.m < 0 || pr.n < 0) return DGL_ERR_ARG;
   if (pr.m == 0) pr.m = pr.M;
@@ -691,6 +695,13 @@ dgl_status run_mxfp4(Problem pr, const uint8_t* sfa, const uint8_t* sfb, cudaStr
     if (!pr.A || !pr.B || !sfa || !sfb) return DGL_ERR_ARG;
     if (!aligned(pr.A, 16) || !aligned(pr.B, 16)) return DGL_ERR_ALIGN;
   }
+  return DGL_OK;
+}
+
+dgl_status run_mxfp4(Problem pr, const uint8_t* sfa, const uint8_t* sfb, cudaStream_t stream) {
+  const dgl_status vst = validate_mxfp4(pr, sfa, sfb);
+  if (vst != DGL_OK) return vst;
+  if (pr.m == 0 || pr.n == 0) return DGL_OK;
   int dev = 0;
   DeviceState* ds = nullptr;
   dgl_status st = get_device(&dev, &ds);
@@ -733,6 +744,7 @@ dgl_status run_mxfp4(Problem pr, const uint8_t* sfa, const uint8_t* sfb, cudaStr
   p.sfa = sfa;
   p.sfb = sfb;
   p.sf_vec8 = (pr.K % 256 == 0 && aligned(sfa, 8) && aligned(sfb, 8)) ? 1 : 0;
+  p.pdl_mode = pr.pdl_mode;
   const bool row_staging = !c_tma && !f32;
   return launch_tc_mxfp4(pr.out, row_staging, ta, tb, tc, p, grid, stream) == cudaSuccess ? DGL_OK : DGL_ERR_CUDA;
 }
@@ -804,6 +816,49 @@ dgl_status dgl_gemm_mxfp4(const void* A, const void* B, const uint8_t* sfa, cons
                           int64_t N, int64_t K, int64_t m_valid, int64_t n_valid, int32_t out_dtype, void* stream) {
   Problem pr{DGL_DTYPE_MXFP4, out_dtype, A, B, nullptr, nullptr, C, M, N, K, m_valid, n_valid};
   return run_mxfp4(pr, sfa, sfb, static_cast<cudaStream_t>(stream));
+}
+
+dgl_status dgl_gemm_batch(const dgl_gemm_desc* items, int32_t count, void* stream) {
+  if (count < 0 || (count > 0 && !items)) return DGL_ERR_ARG;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto problem = [](const dgl_gemm_desc& d) {
+    const bool e4m3 = d.dtype == DGL_DTYPE_E4M3 || d.dtype == DGL_DTYPE_W4A8;
+    Problem pr{e4m3 ? DGL_DTYPE_E4M3 : d.dtype, d.out_dtype, d.A, d.B,
+               e4m3 ? static_cast<const float*>(d.scale_a) : nullptr,
+               e4m3 ? static_cast<const float*>(d.scale_b) : nullptr, d.C, d.M, d.N, d.K, d.m_valid, d.n_valid};
+    pr.w4 = d.dtype == DGL_DTYPE_W4A8 ? 1 : 0;
+    return pr;
+  };
+  // every item is checked before any is enqueued
+  for (int32_t i = 0; i < count; ++i) {
+    const dgl_gemm_desc& d = items[i];
+    Problem pr = problem(d);
+    dgl_status st = DGL_ERR_ARG;
+    if (d.dtype == DGL_DTYPE_MXFP4)
+      st = validate_mxfp4(pr, static_cast<const uint8_t*>(d.scale_a), static_cast<const uint8_t*>(d.scale_b));
+    else if (d.dtype == DGL_DTYPE_BF16 || d.dtype == DGL_DTYPE_E4M3 || d.dtype == DGL_DTYPE_W4A8)
+      st = validate(pr);
+    if (st != DGL_OK) return st;
+  }
+  // The first kernel waits for the work before the batch and only then lets
+  // the next launch; the later ones read their operands at once and wait for
+  // their predecessor before writing C.  A zero fill (K == 0) is an ordinary
+  // launch, after all earlier work, so it too may head the chain.
+  bool head = true;
+  for (int32_t i = 0; i < count; ++i) {
+    const dgl_gemm_desc& d = items[i];
+    Problem pr = problem(d);
+    const int64_t m = pr.m == 0 ? pr.M : pr.m, n = pr.n == 0 ? pr.N : pr.n;
+    if (m == 0 || n == 0) continue;
+    pr.pdl_mode = head ? PDL_BATCH_HEAD : PDL_BATCH_NEXT;
+    const dgl_status st =
+        d.dtype == DGL_DTYPE_MXFP4
+            ? run_mxfp4(pr, static_cast<const uint8_t*>(d.scale_a), static_cast<const uint8_t*>(d.scale_b), s)
+            : run(pr, nullptr, s);
+    if (st != DGL_OK) return st;
+    head = false;
+  }
+  return DGL_OK;
 }
 
 dgl_status dgl_gemm_planned(int32_t dtype, const void* A, const void* B, const float* sa, const float* sb, void* C,

@@ -18,6 +18,17 @@ enum : int {
   STATUS_SMEM_ALIGN = 128,    // dynamic shared memory not 1024-byte aligned: the kernel did nothing
 };
 
+// Programmatic dependent launch modes.  PDL_SERIAL: let the next kernel on
+// the stream launch, then wait for the previous one to complete before any
+// global access.  PDL_BATCH_HEAD (the first kernel of a batch of GEMMs whose
+// operands were all written before the batch): wait first, then let the next
+// launch, so no later kernel of the batch starts before that earlier work is
+// done.  PDL_BATCH_NEXT (a later kernel of the batch): let the next launch and
+// read operands at once; only the epilogue waits for the previous kernel,
+// before its first global write, so every kernel of the batch completes after
+// the one before it and writes C after it.
+enum : int { PDL_SERIAL = 0, PDL_BATCH_HEAD = 1, PDL_BATCH_NEXT = 2 };
+
 // Persistent tcgen05 tile kernel: problem and schedule.
 struct TcParams {
   void* C;              // output, row pitch ldc elements
@@ -76,6 +87,9 @@ struct TcParams {
   // k-stages of the worker's first tile whose A and B boxes are prefetched
   // into L2 before the wait for the previous kernel (0: none)
   int prefetch_stages;
+  // Programmatic dependent launch (PDL_*): where the kernel waits for the
+  // previous kernel on the stream and when it lets the next one launch
+  int pdl_mode;
 };
 
 // Decode (m <= 16) kernel parameters.  A and B are read through tensor maps.
@@ -104,6 +118,7 @@ struct DecodeParams {
   // A planes (K a whole number of 128-byte steps).  0: one 2-D box of m rows
   // per K step.
   int a3d;
+  int pdl_mode;         // as in TcParams
 };
 
 // The activations of the linear-layer epilogue.

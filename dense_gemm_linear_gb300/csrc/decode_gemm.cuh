@@ -145,8 +145,15 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     const int planes = min(nk, p.prefetch_planes);
     for (int j = 0; j < planes; ++j) tma_prefetch_l2_2d(mb, j * (FP8 ? 128 : 64), first_r0);
   }
-  griddep_launch_dependents();
-  griddep_wait();
+  // a later GEMM of a batch reads its operands at once and waits in the
+  // epilogue (PDL_BATCH_NEXT); see common.cuh
+  if (p.pdl_mode == PDL_BATCH_HEAD) {
+    griddep_wait();
+    griddep_launch_dependents();
+  } else {
+    griddep_launch_dependents();
+    if (p.pdl_mode == PDL_SERIAL) griddep_wait();
+  }
 
   const int ks = p.ksteps;                    // planes per stage
   const int b_plane = p.b_plane_bytes;        // one B box, rows rounded up to 8, x 128 bytes
@@ -261,6 +268,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    // C is written here only
+    if (p.pdl_mode == PDL_BATCH_NEXT) griddep_wait();
     const int q = warp & 3;  // TMEM lanes 32q .. 32q+31: rows 32q .. 32q+31 of the stacked operand
     uint32_t acc = 0, acc_phase = 0, red_phase = 0;
     for (int part = blockIdx.x; part < p.parts; part += gridDim.x) {

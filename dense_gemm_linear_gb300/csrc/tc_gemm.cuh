@@ -307,10 +307,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   constexpr int BM = Cfg::BM, BN = Cfg::BN, STAGES = Cfg::STAGES, CG = Cfg::CG;
   // The 128-byte-swizzled operand tiles need 1024-byte alignment, which the
   // declaration requests; a launch that did not get it reports and exits
-  // (every CTA of a pair sees the same layout, so both leave together).
+  // (every CTA of a pair sees the same layout, so both leave together).  It
+  // still completes only after the previous kernel on the stream, as a kernel
+  // that ran would.
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if ((smem_u32(smem_raw) & 1023u) != 0) {
     if (threadIdx.x == 0) atomicOr(p.status, STATUS_SMEM_ALIGN);
+    griddep_wait();
     return;
   }
   uint8_t* sA = smem_raw;
@@ -394,9 +397,15 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     }
   }
   // set-up touched no global data: let the next kernel launch, then wait for
-  // the previous one before reading operands or writing C
-  griddep_launch_dependents();
-  griddep_wait();
+  // the previous one before reading operands or writing C (a later GEMM of a
+  // batch reads its operands at once and waits in the epilogue)
+  if (p.pdl_mode == PDL_BATCH_HEAD) {
+    griddep_wait();
+    griddep_launch_dependents();
+  } else {
+    griddep_launch_dependents();
+    if (p.pdl_mode == PDL_SERIAL) griddep_wait();
+  }
 
   int fail = 0;
   if constexpr (CG == 2) {
@@ -583,6 +592,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     }
   } else if (warp < 2 + Cfg::EPI_WARPS) {
     // ------------------------------------------------------------ epilogue
+    // C, the split schedule's workspace and its flags are written here only
+    if (p.pdl_mode == PDL_BATCH_NEXT) griddep_wait();
     const int e = warp - 2;                 // 0..7
     const int q = warp & 3;                 // TMEM lanes 32q .. 32q+31 are reachable from this warp
     const int half = e >> 2;                // this warp takes chunks [c_first, c_first + nc)

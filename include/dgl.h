@@ -249,6 +249,52 @@ dgl_status dgl_gemm_noalloc(int32_t dtype, const void* A, const void* B, const f
                             int32_t out_dtype, void* stream);
 
 /*
+ * One GEMM of a batch (dgl_gemm_batch).  The fields are the arguments of
+ * dgl_gemm_bf16 / dgl_gemm_fp8 / dgl_gemm_w4a8 / dgl_gemm_mxfp4, chosen by
+ * dtype (DGL_DTYPE_BF16, _E4M3, _W4A8 or _MXFP4):
+ *   scale_a, scale_b: E4M3 and W4A8: the fp32 per-row scales sa (m_valid
+ *     entries) and sb (n_valid entries); MXFP4: the E8M0 scale bytes sfa
+ *     [m_valid][K / 32] and sfb [n_valid][K / 32]; bf16: unused (NULL).
+ * Layouts, alignment rules and the meaning of M, N, m_valid and n_valid are
+ * those of the matching single call.
+ */
+typedef struct dgl_gemm_desc {
+  int32_t dtype;
+  int32_t out_dtype;
+  const void* A;
+  const void* B;
+  const void* scale_a;
+  const void* scale_b;
+  void* C;
+  int64_t M, N, K, m_valid, n_valid;
+} dgl_gemm_desc;
+
+/*
+ * A batch of GEMMs, enqueued in order on one stream: what `count` single
+ * calls would compute, with the kernels overlapped further.  Each kernel after
+ * the first reads its operands while its predecessor is still running
+ * (programmatic dependent launch) and waits for the predecessor only before
+ * it writes C.  This is the running of independent GEMMs back to back (a
+ * ragged-shape sweep, the projections of a layer that share no output), where
+ * one kernel's operand loads then hide the previous kernel's last tiles.
+ *
+ * Contract: no item's A, B or scales may overlap the C of an earlier item of
+ * the same batch (an item may not consume an earlier item's result).  Items may
+ * share inputs, and may write the same C (the later one wins).  Work enqueued
+ * on the stream before the batch is complete before any item reads its
+ * operands; work enqueued after the batch sees every item's C, as after single
+ * calls.
+ *
+ * items: host array of `count` descriptors, read during the call only.
+ * Every item is checked before any is enqueued: an invalid one returns its
+ * status (DGL_ERR_ARG, _ALIGN, _SHAPE) and nothing is enqueued.  An error while
+ * enqueueing item i (DGL_ERR_CUDA, DGL_ERR_UNSUPPORTED) returns that status,
+ * with items 0 .. i - 1 enqueued.  count == 0 is DGL_OK.  Empty items
+ * (m_valid or n_valid resolving to 0) enqueue nothing; K == 0 items write zeros.
+ */
+dgl_status dgl_gemm_batch(const dgl_gemm_desc* items, int32_t count, void* stream);
+
+/*
  * bf16 GEMM with either operand stored K-major or MN-major and explicit row
  * pitches: the three GEMMs of a linear layer's training step ("GEMM analysis
  * in TraceLens", sections "Backward pass GEMMs" and "How PyTorch calls BLAS"):
