@@ -964,7 +964,7 @@ def headline_run(torch, dgl, lib, dev, pk, launches=48, reps=7):
             rec.update({"GB/s": round(gbs, 1), "of_nominal": round(gbs / NOMINAL_HBM_GBS, 4),
                         "of_measured": round(gbs / pk["hbm_gbs"], 4), "target_of_nominal": 0.60})
         out[key] = rec
-        del g, As, Bs, Cs, A, B
+        del arr, As, Bs, Cs, A, B
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
     return out
