@@ -1030,8 +1030,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         } else {
           // The quarter's 32 rows have 64 end units.  Eight lanes take one
           // unit, a bf16 each, so a store instruction writes four units and
-          // each unit's bytes leave as one request (one lane a row, with 2-,
-          // 4- and 8-byte stores, took up to three per unit).
+          // each unit's bytes leave as one request, where one lane per row
+          // would need up to three 2-, 4- or 8-byte stores per unit.
 #pragma unroll 1
           for (int pass = 0; pass < 16; ++pass) {
             const int u = 4 * pass + (lane >> 3);  // unit: row u / 2 of the quarter, its head (even) or tail (odd)
