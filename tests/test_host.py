@@ -266,3 +266,37 @@ def test_workload_shapes_and_encodings():
     assert ((c8.sa >= 0.5) & (c8.sa < 2)).all()
     ci = make_case("fp8", 4, 4, 16, dist="int")
     assert set(np.unique(ci.sa)) <= {0.5, 1.0, 2.0}
+
+
+def test_batch_descriptor_layout_matches_the_header(tmp_path):
+    """The ctypes GemmDesc has the C struct dgl_gemm_desc's size and field offsets."""
+    import dense_gemm_linear_gb300 as dgl_mod
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    fields = [f for f, _ in dgl_mod.GemmDesc._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text("#include <stddef.h>\n#include <stdio.h>\n#include \"dgl.h\"\nint main(void) {\n"
+                   "  printf(\"%zu\\n\", sizeof(dgl_gemm_desc));\n" +
+                   "".join(f"  printf(\"%zu\\n\", offsetof(dgl_gemm_desc, {f}));\n" for f in fields) +
+                   "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c99", "-I", os.path.join(root, "include"), str(src), "-o", str(exe)], check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    want = [ctypes.sizeof(dgl_mod.GemmDesc)] + [getattr(dgl_mod.GemmDesc, f).offset for f in fields]
+    assert got == want
+
+
+def test_batch_checks_every_item_before_any_device_call(dgl):
+    """dgl_gemm_batch validates all items first: a bad item anywhere returns its
+    status with nothing enqueued (no device is touched here), and a batch of
+    empty items is a no-op."""
+    ok = dict(dtype=dgl.DTYPE_BF16, out_dtype=dgl.OUT_BF16, A=16, B=16, C=16, M=64, N=64, K=64)
+    lib = dgl.load_library()
+    assert dgl.dgl_gemm_batch([ok, dict(ok, K=60)]) == dgl.DGL_ERR_ALIGN          # K * 2 bytes not a multiple of 16
+    assert dgl.dgl_gemm_batch([dict(ok, dtype=9), ok]) == dgl.DGL_ERR_ARG
+    assert dgl.dgl_gemm_batch([ok, dict(ok, m_valid=65)]) == dgl.DGL_ERR_ARG       # m_valid > M
+    assert dgl.dgl_gemm_batch([dict(ok, dtype=dgl.DTYPE_E4M3)]) == dgl.DGL_ERR_ARG  # E4M3 without scales
+    assert dgl.dgl_gemm_batch([dict(ok, dtype=dgl.DTYPE_MXFP4, K=48)]) == dgl.DGL_ERR_ALIGN   # K % 32
+    assert dgl.dgl_gemm_batch([dict(ok, M=0), dict(ok, N=0)]) == dgl.DGL_OK
+    assert dgl.dgl_gemm_batch([]) == dgl.DGL_OK
+    assert lib.dgl_gemm_batch(None, 2, None) == dgl.DGL_ERR_ARG
+    assert lib.dgl_gemm_batch(None, -1, None) == dgl.DGL_ERR_ARG
