@@ -750,17 +750,29 @@ def main():
             line["cpu_baseline"]["sample"] = "first rows of each GEMM of the step"
         line["roofline"] = {k: roofline[k] for k in ("kernel", "bound", "achieved", "peak", "unit", "frac",
                                                       "traffic", "peak_source", "avg_launch_us")}
+        for k in ("achieved", "frac", "avg_launch_us"):
+            line["roofline"][k] = round(line["roofline"][k], 4)
         line["roofline"]["serialised"] = {k: round(roofline["serialised"][k], 4)
                                           for k in ("achieved", "frac", "avg_launch_us")}
         if roofline_decode:
             line["roofline_decode"] = {"achieved": round(roofline_decode["achieved"], 1),
                                        "frac": round(roofline_decode["frac"], 4)}
         line["per_shape_us"] = {f"{c.m}x{c.n}x{c.K}": round(b2b_ms[i] * 1e3, 2) for i, c in enumerate(cases)}
-        line["headline"] = headline
+        line["headline"] = compact_headline(headline)
         print(json.dumps(line, separators=(",", ":")), flush=True)
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def compact_headline(headline):
+    """The headline block as the stdout line carries it: per shape its time, the
+    single-call time, the rate and its fractions of the nominal and measured
+    peaks (the full record on stderr keeps every field)."""
+    if not headline:
+        return headline
+    keep = ("us", "us_single_calls", "TFLOP/s", "GB/s", "of_nominal", "of_measured")
+    return {shape: {k: rec[k] for k in keep if k in rec} for shape, rec in headline.items()}
 
 
 def back_to_back_us(torch, make_call, op, dev, launches=48, reps=7, make_desc=None, lib=None):

@@ -53,3 +53,22 @@ def test_gpu_arm_fails_loudly_without_a_gpu():
     r = _bench("--steps", "1", "--warmup", "3", "--e2e-steps", "0", "--no-cpu-baseline", "--no-context")
     assert r.returncode != 0
     assert not [l for l in r.stdout.splitlines() if l.startswith("{")]
+
+
+def test_compact_headline_keeps_the_rates_and_fractions():
+    """The stdout line's headline block: per shape the times, the rate and both
+    fractions; the full record keeps the rest."""
+    sys.path.insert(0, ROOT)
+    import bench
+    full = {"4096x4096x4096 bf16": {"us": 74.86, "us_single_calls": 86.64, "copies": 7, "tile": "256x256",
+                                    "TFLOP/s": 1836.0, "of_nominal": 0.816, "of_measured": 0.952,
+                                    "target_of_nominal": 0.7},
+            "16x4096x4096 bf16": {"us": 8.82, "us_single_calls": 9.49, "copies": 13, "tile": "decode",
+                                  "GB/s": 3832.9, "of_nominal": 0.4791, "of_measured": 0.5734,
+                                  "target_of_nominal": 0.6}}
+    got = bench.compact_headline(full)
+    assert got == {"4096x4096x4096 bf16": {"us": 74.86, "us_single_calls": 86.64, "TFLOP/s": 1836.0,
+                                           "of_nominal": 0.816, "of_measured": 0.952},
+                   "16x4096x4096 bf16": {"us": 8.82, "us_single_calls": 9.49, "GB/s": 3832.9,
+                                         "of_nominal": 0.4791, "of_measured": 0.5734}}
+    assert bench.compact_headline(None) is None
